@@ -1,0 +1,63 @@
+"""Helpers shared by the GPU parity tests: device copies, error metrics and the
+top-k comparison that tolerates only genuine near-ties."""
+import numpy as np
+import torch
+
+from token_dispatch_gb300 import synth
+
+DEV = "cuda:0"
+TDT = {"f32": torch.float32, "bf16": torch.bfloat16}
+# Tolerances on the normwise relative error max|gpu - ref| / max|ref|:
+# 1e-5 for the fp32 layer, 2e-2 for bf16 storage against the oracle fed the
+# same bf16-rounded inputs.
+TOL = {"f32": 1e-5, "bf16": 2e-2}
+
+
+def dev(stored):
+    return stored.host.to(DEV)
+
+
+def to64(t):
+    return t.detach().to("cpu", torch.float64).numpy() if t.dtype != torch.bfloat16 else \
+        t.detach().to("cpu", torch.float32).numpy().astype(np.float64)
+
+
+def rel_err(gpu, ref):
+    gpu = np.asarray(gpu, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert gpu.shape == ref.shape, (gpu.shape, ref.shape)
+    if ref.size == 0:
+        return 0.0
+    den = np.max(np.abs(ref))
+    num = np.max(np.abs(gpu - ref))
+    return float(num / den) if den > 0 else float(num)
+
+
+def assert_close(gpu, ref, tol, what=""):
+    e = rel_err(gpu, ref)
+    assert e <= tol, f"{what}: normwise relative error {e:.3e} > {tol:.1e}"
+    return e
+
+
+def check_topk(gpu_idx, ref_logits, K, logit_err, max_frac=1e-3):
+    """Rows whose GPU top-K differs from the oracle's must be near-ties: every
+    chosen expert's exact logit is within 2*logit_err of the K-th largest exact
+    logit.  Returns the number of such rows (also bounded by max_frac)."""
+    ref_idx = np.argsort(-ref_logits, axis=1, kind="stable")[:, :K]
+    bad = np.where((gpu_idx != ref_idx).any(axis=1))[0]
+    for t in bad:
+        kth = np.sort(ref_logits[t])[::-1][K - 1]
+        chosen = ref_logits[t, gpu_idx[t]]
+        assert len(set(gpu_idx[t].tolist())) == K
+        assert chosen.min() >= kth - 2 * logit_err - 1e-12, (t, chosen, kth, logit_err)
+        # order inside the row: non-increasing by exact logits up to the bound
+        assert (np.diff(chosen) <= 2 * logit_err + 1e-12).all()
+    assert len(bad) <= max(1, int(max_frac * len(ref_idx))), f"{len(bad)} ambiguous rows"
+    return len(bad)
+
+
+def host_layer_inputs(shape, T=None, seed=0, bias=None):
+    """Small-size inputs drawn on the host (all tensors), as Stored pairs."""
+    x, wr = synth.router_inputs(shape, seed=seed, tokens=T)
+    wg, wu, wd = synth.expert_weights_host(shape, seed=seed)
+    return x, wr, wg, wu, wd

@@ -1,0 +1,385 @@
+"""GPU parity of every libmoe call against the CPU oracle, through the C ABI.
+
+Each call gets the same seeded inputs as the oracle function it is compared
+with.  Integer outputs (top-k indices, cu_seqlens, the permutation, the MoD
+selection) must match exactly; floating-point outputs within the normwise
+relative tolerance of the storage type (1e-5 fp32, 2e-2 bf16).  Sizes span
+several tiles and ragged tails (T not a multiple of the 256-token chunk, H and
+H' not multiples of the GEMM tile widths)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+from token_dispatch_gb300 import _lib as L
+from token_dispatch_gb300 import layer, synth
+from tests.gpu_util import DEV, TDT, TOL, assert_close, check_topk, dev, host_layer_inputs, rel_err, to64
+
+pytestmark = pytest.mark.gpu
+
+S = synth.MoEShape
+SHAPES = [
+    synth.TINY_F32,
+    S("bf16_T1000_H384_E16_K4_Hp320", 1000, 384, 16, 4, 320, "bf16"),
+    S("bf16_T777_H256_E64_K6_Hp192", 777, 256, 64, 6, 192, "bf16"),
+    S("f32_T300_H64_E12_K3_Hp96", 300, 64, 12, 3, 96, "f32"),
+]
+ROUTE_ONLY = [S("bf16_T300_H128_E384_K8", 300, 128, 384, 8, 64, "bf16"),
+              S("f32_T129_H32_E1024_K16", 129, 32, 1024, 16, 32, "f32")]
+CDT = {"f32": L.MOE_F32, "bf16": L.MOE_BF16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from token_dispatch_gb300 import build
+    build.build()
+    assert torch.cuda.is_available()
+
+
+def ids(shapes):
+    return [s.name for s in shapes]
+
+
+def route_gpu(shape, x, wr, bias=None):
+    T, E, K = x.shape[0], shape.E, shape.K
+    logits = torch.empty((T, E), dtype=torch.float32, device=DEV)
+    idx = torch.empty((T, K), dtype=torch.int32, device=DEV)
+    gate = torch.empty((T, K), dtype=torch.float32, device=DEV)
+    b = None if bias is None else torch.from_numpy(bias).to(DEV)
+    L.moe_route(dev(x), dev(wr), b, T, shape.H, E, K, CDT[shape.dtype], logits, idx, gate)
+    torch.cuda.synchronize()
+    return logits.cpu().numpy(), idx.cpu().numpy(), gate.cpu().numpy()
+
+
+@pytest.mark.parametrize("shape", SHAPES + ROUTE_ONLY, ids=ids(SHAPES + ROUTE_ONLY))
+def test_route_matches_oracle(shape):
+    x, wr = synth.router_inputs(shape)
+    bias = synth.expert_bias(shape.E, 0.7, expert=1)
+    logits, idx, gate = route_gpu(shape, x, wr, bias)
+    r_logits, r_p, r_idx, r_gate = O.route(x.ref, wr.ref, shape.K, bias.astype(np.float64))
+    tol = 1e-5 if shape.dtype == "f32" else 1e-5  # fp32 accumulation in both storage types
+    assert_close(logits, r_logits, tol, "logits")
+    logit_err = float(np.max(np.abs(logits - r_logits)))
+    check_topk(idx, r_logits, shape.K, logit_err)
+    same = (idx == r_idx).all(axis=1)
+    assert_close(gate[same], r_gate[same], 1e-5, "gate")
+    # selection on the emitted fp32 logits is exact: redo it in float64 on those values
+    assert np.array_equal(idx, O.topk_experts(logits.astype(np.float64), shape.K))
+
+
+def test_route_ties_pick_lowest_expert():
+    shape = S("f32_ties", 64, 16, 8, 3, 16, "f32")
+    x = synth.store(np.zeros((64, 16)), "f32")
+    wr = synth.store(np.zeros((16, 8)), "f32")
+    bias = np.array([0, 1, 1, 0, 1, 0, 0, 1], np.float32)
+    logits, idx, gate = route_gpu(shape, x, wr, bias)
+    assert (idx == np.array([1, 2, 4])).all()
+    p1 = math.e / (4 * math.e + 4)
+    assert np.allclose(gate, p1, rtol=1e-6)
+
+
+def oracle_idx(shape, T=None):
+    x, wr = synth.router_inputs(shape, tokens=T)
+    return x, wr, O.topk_experts(O.router_logits(x.ref, wr.ref), shape.K)
+
+
+@pytest.mark.parametrize("shape", SHAPES + ROUTE_ONLY, ids=ids(SHAPES + ROUTE_ONLY))
+def test_dispatch_is_bit_exact(shape):
+    x, wr, idx = oracle_idx(shape)
+    T, H, E, K = shape.T, shape.H, shape.E, shape.K
+    cu, dst, src, xs_ref = O.dispatch(x.ref, idx, E)
+    b = layer.MoEBuffers(T, H, E, K, shape.Hp, shape.dtype, DEV, backward=False)
+    L.moe_dispatch(dev(x), torch.from_numpy(idx).to(DEV), T, H, E, K, CDT[shape.dtype], b.cu, b.dst_row,
+                   b.src_tok, b.xs, b.ws_dispatch, b.ws_dispatch_bytes)
+    assert L.moe_last_device_error() == L.MOE_OK
+    assert np.array_equal(b.cu.cpu().numpy(), cu)
+    assert np.array_equal(b.dst_row.cpu().numpy(), dst)
+    assert np.array_equal(b.src_tok.cpu().numpy(), src)
+    assert np.array_equal(to64(b.xs), xs_ref)  # a pure copy: bit-exact
+
+
+def test_dispatch_skewed_all_tokens_to_one_expert():
+    T, H, E, K = 1030, 64, 32, 2
+    idx = np.stack([np.zeros(T, np.int32), 1 + (np.arange(T) % (E - 1))], axis=1).astype(np.int32)
+    x = synth.store(synth.normal(5, 1, T * H).reshape(T, H), "bf16")
+    cu, dst, src, xs_ref = O.dispatch(x.ref, idx, E)
+    b = layer.MoEBuffers(T, H, E, K, 64, "bf16", DEV, backward=False)
+    L.moe_dispatch(dev(x), torch.from_numpy(idx).to(DEV), T, H, E, K, L.MOE_BF16, b.cu, b.dst_row, b.src_tok,
+                   b.xs, b.ws_dispatch, b.ws_dispatch_bytes)
+    assert np.array_equal(b.cu.cpu().numpy(), cu)
+    assert np.array_equal(b.dst_row.cpu().numpy(), dst)
+    assert np.array_equal(to64(b.xs), xs_ref)
+
+
+def test_dispatch_out_of_range_expert_sets_bounds_error():
+    T, H, E, K = 40, 64, 8, 2
+    idx = np.stack([np.arange(T) % E, (np.arange(T) + 1) % E], axis=1).astype(np.int32)
+    idx[7, 1] = E + 3
+    x = synth.store(np.ones((T, H)), "f32")
+    b = layer.MoEBuffers(T, H, E, K, 64, "f32", DEV, backward=False)
+    assert L.moe_last_device_error() == L.MOE_OK
+    L.moe_dispatch(dev(x), torch.from_numpy(idx).to(DEV), T, H, E, K, L.MOE_F32, b.cu, b.dst_row, b.src_tok,
+                   b.xs, b.ws_dispatch, b.ws_dispatch_bytes)
+    assert L.moe_last_device_error() == L.MOE_ERR_DEVICE_BOUNDS
+    assert b.dst_row.cpu().numpy()[15] == -1
+    assert int(b.cu[-1]) == T * K - 1
+    assert L.moe_last_device_error() == L.MOE_OK  # cleared by the read
+
+
+@pytest.mark.parametrize("shape", SHAPES, ids=ids(SHAPES))
+def test_expert_ffn_matches_oracle(shape):
+    x, wr, wg, wu, wd = host_layer_inputs(shape)
+    idx = O.topk_experts(O.router_logits(x.ref, wr.ref), shape.K)
+    cu, dst, src, xs_ref = O.dispatch(x.ref, idx, shape.E)
+    act_ref, h_ref = O.expert_ffn(xs_ref, cu, wg.ref, wu.ref, wd.ref)
+    R, H, Hp = shape.R, shape.H, shape.Hp
+    xs = synth.store(xs_ref, shape.dtype)
+    act = torch.empty((R, Hp), dtype=TDT[shape.dtype], device=DEV)
+    h = torch.empty((R, H), dtype=TDT[shape.dtype], device=DEV)
+    L.moe_expert_ffn(dev(xs), torch.from_numpy(cu).to(DEV), R, dev(wg), dev(wu), dev(wd), shape.E, H, Hp,
+                     CDT[shape.dtype], act, h)
+    torch.cuda.synchronize()
+    assert_close(to64(act), act_ref, TOL[shape.dtype], "act")
+    assert_close(to64(h), h_ref, TOL[shape.dtype], "h")
+
+
+def test_expert_ffn_empty_and_single_row_experts():
+    shape = S("bf16_sparse", 5, 128, 8, 1, 128, "bf16")
+    x = synth.normal_stored(3, 1, (5, 128), 1.0, "bf16")
+    wg, wu, wd = synth.expert_weights_host(shape, seed=3)
+    idx = np.array([[3], [3], [6], [0], [3]], np.int32)  # experts 1,2,4,5,7 empty
+    cu, dst, src, xs_ref = O.dispatch(x.ref, idx, 8)
+    act_ref, h_ref = O.expert_ffn(xs_ref, cu, wg.ref, wu.ref, wd.ref)
+    act = torch.empty((5, 128), dtype=torch.bfloat16, device=DEV)
+    h = torch.empty((5, 128), dtype=torch.bfloat16, device=DEV)
+    L.moe_expert_ffn(dev(synth.store(xs_ref, "bf16")), torch.from_numpy(cu).to(DEV), 5, dev(wg), dev(wu),
+                     dev(wd), 8, 128, 128, L.MOE_BF16, act, h)
+    torch.cuda.synchronize()
+    assert_close(to64(h), h_ref, 2e-2, "h")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("variant", ["plain", "scaled_residual_outrow"])
+def test_combine_matches_oracle(dtype, variant):
+    rng = np.random.default_rng(7)
+    T, K, H = 333, 3, 200 if dtype == "f32" else 256
+    R = T * K
+    h = synth.store(rng.standard_normal((R, H)), dtype)
+    gate = rng.random((T, K)).astype(np.float32)
+    dst = rng.permutation(R).astype(np.int32)
+    kw, gk = {}, {}
+    n_out = T
+    if variant != "plain":
+        n_out = 2 * T
+        scale = rng.standard_normal(T).astype(np.float32)
+        out = np.sort(rng.choice(n_out, T, replace=False)).astype(np.int32)
+        res = synth.store(rng.standard_normal((n_out, H)), dtype)
+        kw = dict(row_scale=scale.astype(np.float64), residual=res.ref, out_row=out, n_out=n_out)
+        gk = dict(row_scale=torch.from_numpy(scale).to(DEV), residual=dev(res), out_row=torch.from_numpy(out).to(DEV))
+    ref = O.combine(h.ref, gate.astype(np.float64), dst, **kw)
+    y = torch.zeros((n_out, H), dtype=TDT[dtype], device=DEV)
+    if variant != "plain":
+        y.copy_(gk["residual"])  # rows not written by any token keep the residual
+    L.moe_combine(dev(h), torch.from_numpy(gate).to(DEV), torch.from_numpy(dst).to(DEV), gk.get("row_scale"),
+                  gk.get("residual"), gk.get("out_row"), T, H, K, CDT[dtype], y)
+    torch.cuda.synchronize()
+    assert_close(to64(y), ref, TOL[dtype], "y")
+
+
+def test_combine_of_dispatch_with_unit_gates_is_K_times_x():
+    for K in (1, 2, 4, 8, 6):
+        T, E, H = 513, 16, 128
+        x = synth.store(synth.normal(11, K, T * H).reshape(T, H), "bf16")
+        idx = np.stack([np.random.default_rng(K).choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)
+        b = layer.MoEBuffers(T, H, E, K, 64, "bf16", DEV, backward=False)
+        L.moe_dispatch(dev(x), torch.from_numpy(idx).to(DEV), T, H, E, K, L.MOE_BF16, b.cu, b.dst_row, b.src_tok,
+                       b.xs, b.ws_dispatch, b.ws_dispatch_bytes)
+        ones = torch.ones((T, K), dtype=torch.float32, device=DEV)
+        y = torch.empty((T, H), dtype=torch.float32, device=DEV)
+        # identity expert: combine the dispatched rows, accumulate in fp32 (f32 view of bf16 rows)
+        xs32 = b.xs.float()
+        L.moe_combine(xs32, ones, b.dst_row, None, None, None, T, H, K, L.MOE_F32, y)
+        torch.cuda.synchronize()
+        want = K * x.ref
+        got = y.cpu().numpy().astype(np.float64)
+        if K in (1, 2, 4, 8):
+            assert np.array_equal(got, want)
+        else:
+            assert np.max(np.abs(got - want) / np.maximum(np.abs(want), 1e-30)) <= 2 ** -22
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_permute_bwd_matches_oracle(dtype):
+    rng = np.random.default_rng(9)
+    T, K, H = 301, 4, 128
+    R, n_out = T * K, 2 * T
+    h = synth.store(rng.standard_normal((R, H)), dtype)
+    dy = synth.store(rng.standard_normal((n_out, H)), dtype)
+    dxs = synth.store(rng.standard_normal((R, H)), dtype)
+    gate = rng.random((T, K)).astype(np.float32)
+    dst = rng.permutation(R).astype(np.int32)
+    scale = rng.standard_normal(T).astype(np.float32)
+    out = rng.choice(n_out, T, replace=False).astype(np.int32)
+    dh_r, dg_r, ds_r, dx_r = O.permute_bwd(dy.ref, h.ref, gate.astype(np.float64), dst, dxs.ref,
+                                           row_scale=scale.astype(np.float64), out_row=out)
+    dh = torch.zeros((R, H), dtype=TDT[dtype], device=DEV)
+    dg = torch.empty((T, K), dtype=torch.float32, device=DEV)
+    ds = torch.empty((T,), dtype=torch.float32, device=DEV)
+    dx = torch.empty((T, H), dtype=TDT[dtype], device=DEV)
+    L.moe_permute_bwd(dev(dy), dev(h), torch.from_numpy(gate).to(DEV), torch.from_numpy(dst).to(DEV),
+                      torch.from_numpy(scale).to(DEV), torch.from_numpy(out).to(DEV), dev(dxs), T, H, K,
+                      CDT[dtype], dh, dg, ds, dx)
+    torch.cuda.synchronize()
+    tol = 1e-5 if dtype == "f32" else 2e-2
+    assert_close(to64(dh), dh_r, tol, "dh")
+    assert_close(dg.cpu().numpy(), dg_r, 1e-5, "d_gate")
+    assert_close(ds.cpu().numpy(), ds_r, 1e-5, "d_scale")
+    assert_close(to64(dx), dx_r, tol, "dx")
+
+
+@pytest.mark.parametrize("shape", SHAPES + ROUTE_ONLY[:1], ids=ids(SHAPES + ROUTE_ONLY[:1]))
+def test_route_bwd_softmax_topk_matches_oracle(shape):
+    T, H, E, K = shape.T, shape.H, shape.E, shape.K
+    x, wr = synth.router_inputs(shape)
+    logits = (x.ref @ wr.ref).astype(np.float32)  # an fp32 logits input shared by both sides
+    idx = O.topk_experts(logits.astype(np.float64), K)
+    d_gate = np.random.default_rng(4).standard_normal((T, K)).astype(np.float32)
+    dl_r, dw_r, dx_r = O.route_bwd_softmax_topk(d_gate.astype(np.float64), logits.astype(np.float64), idx,
+                                                x.ref, wr.ref)
+    dx0 = synth.store(np.random.default_rng(5).standard_normal((T, H)), shape.dtype)
+    dl = torch.empty((T, E), dtype=torch.float32, device=DEV)
+    dw = torch.empty((H, E), dtype=torch.float32, device=DEV)
+    dx = dev(dx0).clone()
+    nbytes = L.moe_workspace_bytes(L.MOE_OP_ROUTE_BWD, T, H, E, K, 0)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    L.moe_route_bwd(L.MOE_ROUTE_SOFTMAX_TOPK, torch.from_numpy(d_gate).to(DEV), torch.from_numpy(logits).to(DEV),
+                    torch.from_numpy(idx).to(DEV), dev(x), dev(wr), T, H, E, K, CDT[shape.dtype], dl, dw, dx, ws,
+                    nbytes)
+    torch.cuda.synchronize()
+    assert_close(dl.cpu().numpy(), dl_r, 1e-5, "d_logits")
+    assert_close(dw.cpu().numpy(), dw_r, 1e-5, "dw_router")
+    assert_close(to64(dx), dx0.ref + dx_r, TOL[shape.dtype], "dx (accumulated)")
+    # overwrite mode
+    L.moe_route_bwd(L.MOE_ROUTE_SOFTMAX_TOPK | L.MOE_ROUTE_DX_WRITE, torch.from_numpy(d_gate).to(DEV),
+                    torch.from_numpy(logits).to(DEV), torch.from_numpy(idx).to(DEV), dev(x), dev(wr), T, H, E, K,
+                    CDT[shape.dtype], None, None, dx, ws, nbytes)
+    torch.cuda.synchronize()
+    assert_close(to64(dx), dx_r, TOL[shape.dtype], "dx (written)")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_route_bwd_linear_matches_oracle(dtype):
+    T, H = 700, 256
+    rng = np.random.default_rng(6)
+    x = synth.store(rng.standard_normal((T, H)), dtype)
+    w = synth.store(rng.standard_normal(H) / 16, dtype)
+    ds = rng.standard_normal(T).astype(np.float32)
+    dw_r, dx_r = O.route_bwd_linear(ds.astype(np.float64), x.ref, w.ref)
+    nbytes = L.moe_workspace_bytes(L.MOE_OP_ROUTE_BWD, T, H, 1, 1, 0)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    dw = torch.empty((H,), dtype=torch.float32, device=DEV)
+    dx = torch.zeros((T, H), dtype=TDT[dtype], device=DEV)
+    L.moe_route_bwd(L.MOE_ROUTE_MOD_LINEAR, torch.from_numpy(ds).to(DEV), None, None, dev(x), dev(w), T, H, 1, 1,
+                    CDT[dtype], None, dw, dx, ws, nbytes)
+    torch.cuda.synchronize()
+    assert_close(dw.cpu().numpy(), dw_r, 1e-5, "dw_mod")
+    assert_close(to64(dx), dx_r, TOL[dtype], "dx")
+
+
+@pytest.mark.parametrize("B,Lseq,C,H,dtype", [(4, 2048, 1024, 128, "bf16"), (3, 1000, 333, 64, "f32"),
+                                              (2, 8192, 100, 64, "bf16"), (1, 7, 7, 64, "f32"),
+                                              (2, 64, 0, 64, "f32")])
+def test_mod_select_matches_oracle(B, Lseq, C, H, dtype):
+    n = B * Lseq
+    x = synth.store(synth.normal(2, 1, n * H).reshape(n, H), dtype)
+    w = synth.store(synth.normal(2, 2, H) / math.sqrt(H), dtype)
+    score = torch.empty(n, dtype=torch.float32, device=DEV)
+    sel = torch.empty(max(B * C, 1), dtype=torch.int32, device=DEV)
+    sel_score = torch.empty(max(B * C, 1), dtype=torch.float32, device=DEV)
+    mask = torch.empty(n, dtype=torch.uint8, device=DEV)
+    x_sel = torch.empty((max(B * C, 1), H), dtype=TDT[dtype], device=DEV)
+    y = torch.full((n, H), float("nan"), dtype=TDT[dtype], device=DEV)
+    L.mod_select(dev(x), dev(w), B, Lseq, H, C, CDT[dtype], score, sel, sel_score, mask, x_sel, y)
+    torch.cuda.synchronize()
+    s_ref = O.mod_scores(x.ref, w.ref)
+    s_gpu = score.cpu().numpy()
+    assert_close(s_gpu, s_ref, 1e-5, "score")
+    # the selection on the emitted fp32 scores is exact
+    sel_o, mask_o = O.mod_select(s_gpu.astype(np.float64), B, Lseq, C)
+    flat_o = (np.arange(B)[:, None] * Lseq + sel_o).reshape(-1)
+    assert np.array_equal(mask.cpu().numpy(), mask_o)
+    if C:
+        assert np.array_equal(sel.cpu().numpy()[:B * C], flat_o)
+        assert np.array_equal(sel_score.cpu().numpy()[:B * C], s_gpu[flat_o])
+        assert np.array_equal(to64(x_sel)[:B * C], x.ref[flat_o])
+    # against the oracle's own fp64 scores: differences only at near-ties
+    sel_r, mask_r = O.mod_select(s_ref, B, Lseq, C)
+    err = float(np.max(np.abs(s_gpu - s_ref)))
+    for b in range(B):
+        diff = set(np.nonzero(mask_o[b * Lseq:(b + 1) * Lseq] != mask_r[b * Lseq:(b + 1) * Lseq])[0])
+        if diff and C:
+            kth = np.sort(s_ref[b * Lseq:(b + 1) * Lseq])[::-1][C - 1]
+            assert all(abs(s_ref[b * Lseq + p] - kth) <= 2 * err + 1e-12 for p in diff)
+    yv = to64(y)
+    keep = mask_o == 0
+    assert np.array_equal(yv[keep], x.ref[keep])
+    assert np.isnan(yv[~keep]).all()  # selected rows are left for the combine
+
+
+def test_tiny_fp32_layer_end_to_end():
+    """The tiny fp32 layer (T=256, H=128, E=8, K=2, H'=256): forward plus the
+    gate/dispatch backward through the C ABI, max relative error <= 1e-5."""
+    shape = synth.TINY_F32
+    T, H, E, K, Hp = shape.T, shape.H, shape.E, shape.K, shape.Hp
+    x, wr, wg, wu, wd = host_layer_inputs(shape)
+    dy = synth.upstream_grad(shape, T, H)
+    dxs = synth.upstream_grad(shape, T * K, H, seed=2, stream=synth.S_DXS)
+    b = layer.MoEBuffers(T, H, E, K, Hp, "f32", DEV)
+    xd, wrd = dev(x), dev(wr)
+    layer.moe_forward(b, xd, wrd, None, dev(wg), dev(wu), dev(wd))
+    layer.moe_backward(b, xd, wrd, dev(dy), dev(dxs))
+    assert L.moe_last_device_error() == L.MOE_OK
+    f = O.moe_forward(x.ref, wr.ref, wg.ref, wu.ref, wd.ref, K)
+    g = O.moe_backward(f, dy.ref, dxs.ref, x.ref, wr.ref)
+    assert np.array_equal(b.idx.cpu().numpy(), f["idx"])
+    assert np.array_equal(b.cu.cpu().numpy(), f["cu"])
+    assert np.array_equal(b.dst_row.cpu().numpy(), f["dst_row"])
+    assert np.array_equal(b.src_tok.cpu().numpy(), f["src_tok"])
+    for name, gpu, ref in [("logits", b.logits, f["logits"]), ("gate", b.gate, f["gate"]), ("act", b.act, f["act"]),
+                           ("h", b.h, f["h"]), ("y", b.y, f["y"]), ("dh", b.dh, g["dh"]),
+                           ("d_gate", b.d_gate, g["d_gate"]), ("d_logits", b.d_logits, g["d_logits"]),
+                           ("dw_router", b.dw_router, g["dw_router"]), ("dx", b.dx, g["dx"])]:
+        assert_close(to64(gpu), ref, 1e-5, name)
+
+
+def test_outputs_are_deterministic():
+    shape = SHAPES[1]
+    x, wr, wg, wu, wd = host_layer_inputs(shape)
+    outs = []
+    for _ in range(2):
+        b = layer.MoEBuffers(shape.T, shape.H, shape.E, shape.K, shape.Hp, shape.dtype, DEV)
+        xd, wrd = dev(x), dev(wr)
+        layer.moe_forward(b, xd, wrd, None, dev(wg), dev(wu), dev(wd))
+        dy = dev(synth.upstream_grad(shape, shape.T, shape.H))
+        dxs = dev(synth.upstream_grad(shape, shape.R, shape.H, seed=2, stream=synth.S_DXS))
+        layer.moe_backward(b, xd, wrd, dy, dxs)
+        torch.cuda.synchronize()
+        outs.append([t.clone() for t in (b.logits, b.idx, b.dst_row, b.xs, b.h, b.y, b.dx, b.dw_router)])
+    for a, c in zip(*outs):
+        assert torch.equal(a.view(torch.uint8) if a.dtype == torch.bfloat16 else a,
+                           c.view(torch.uint8) if c.dtype == torch.bfloat16 else c)
+
+
+def test_zero_tokens_is_a_no_op():
+    E, K, H = 8, 2, 64
+    cu = torch.full((E + 1,), -5, dtype=torch.int32, device=DEV)
+    ws = torch.empty(256, dtype=torch.uint8, device=DEV)
+    w = torch.zeros((E, H, 64), dtype=torch.float32, device=DEV)
+    L.moe_dispatch(None, None, 0, H, E, K, L.MOE_F32, cu, None, None, None, ws, 256)
+    assert (cu.cpu() == 0).all()
+    L.moe_route(None, torch.zeros((H, E), device=DEV), None, 0, H, E, K, L.MOE_F32, None, None, None)
+    L.moe_combine(None, None, None, None, None, None, 0, H, K, L.MOE_F32, None)
+    L.moe_expert_ffn(None, cu, 0, w, w, w, E, H, 64, L.MOE_F32, None, None)
+    assert L.moe_last_device_error() == L.MOE_OK

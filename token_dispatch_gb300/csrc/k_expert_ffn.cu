@@ -1,0 +1,34 @@
+// Grouped SwiGLU expert FFN over contiguous [E, H, H'] weights (MoonEP page,
+// "Step-by-step": one contiguous tensor per projection, experts addressed by row
+// index; T4 bottleneck page, SwiGLU table: three matrix products).
+//
+// The row split per expert is read on the device from cu_seqlens, so no host
+// synchronisation happens between dispatch and the expert GEMMs.
+#include "moe_internal.cuh"
+
+namespace moe {
+
+int launch_expert_ffn(const void* xs, const int32_t* cu, int rows, const void* wg, const void* wu,
+                      const void* wd, int E, int H, int Hp, int dtype, void* act, void* h,
+                      cudaStream_t s) {
+  if (rows == 0) return MOE_OK;
+  // act = silu(xs . Wg[e]) * (xs . Wu[e])
+  SimtGemmArgs a{};
+  a.A = xs; a.a_sm = H; a.a_sk = 1;
+  a.B = wg; a.B2 = wu; a.b_sg = (long long)H * Hp; a.b_sk = Hp; a.b_sn = 1;
+  a.C = act; a.c_sm = Hp;
+  a.cu = cu; a.M = rows; a.N = Hp; a.K = H; a.groups = E;
+  a.epilogue = 0; a.swiglu = true;
+  int st = launch_simt_gemm(a, dtype, dtype, dtype, s);
+  if (st != MOE_OK) return st;
+  // h = act . Wd[e]^T   (Wd[e] stored [H, H'])
+  SimtGemmArgs d{};
+  d.A = act; d.a_sm = Hp; d.a_sk = 1;
+  d.B = wd; d.b_sg = (long long)H * Hp; d.b_sk = 1; d.b_sn = Hp;
+  d.C = h; d.c_sm = H;
+  d.cu = cu; d.M = rows; d.N = H; d.K = Hp; d.groups = E;
+  d.epilogue = 0; d.swiglu = false;
+  return launch_simt_gemm(d, dtype, dtype, dtype, s);
+}
+
+}  // namespace moe
