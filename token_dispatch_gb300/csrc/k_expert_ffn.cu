@@ -8,10 +8,16 @@
 
 namespace moe {
 
+int launch_expert_ffn_tc(const void* xs, const int32_t* cu, int rows, const void* wg, const void* wu,
+                         const void* wd, int E, int H, int Hp, void* act, void* h, cudaStream_t s);
+
+// bf16: tcgen05 grouped GEMMs.  fp32: FFMA grouped GEMMs (a 1e-5 relative error
+// is out of reach of the tf32 tensor-core path).
 int launch_expert_ffn(const void* xs, const int32_t* cu, int rows, const void* wg, const void* wu,
                       const void* wd, int E, int H, int Hp, int dtype, void* act, void* h,
                       cudaStream_t s) {
   if (rows == 0) return MOE_OK;
+  if (dtype == MOE_BF16) return launch_expert_ffn_tc(xs, cu, rows, wg, wu, wd, E, H, Hp, act, h, s);
   // act = silu(xs . Wg[e]) * (xs . Wu[e])
   SimtGemmArgs a{};
   a.A = xs; a.a_sm = H; a.a_sk = 1;

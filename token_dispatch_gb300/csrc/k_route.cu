@@ -161,8 +161,13 @@ size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
 }  // namespace
 
+int launch_router_tc(const void* x, const void* w, const float* bias, int T, int H, int E, float* logits,
+                     cudaStream_t s);
+
+// bf16: tcgen05 GEMM with the bias added in the epilogue.  fp32: FFMA GEMM.
 int launch_router_logits(const void* x, const void* w, const float* bias, int T, int H, int E,
                          int dtype, float* logits, cudaStream_t s) {
+  if (dtype == MOE_BF16) return launch_router_tc(x, w, bias, T, H, E, logits, s);
   SimtGemmArgs a{};
   a.A = x; a.a_sm = H; a.a_sk = 1;
   a.B = w; a.b_sg = 0; a.b_sk = E; a.b_sn = 1;

@@ -93,6 +93,7 @@ int moe_route(const void* x, const void* w_router, const float* logit_bias, int 
   if ((T > 0 && (!x || !logits || !topk_idx || !topk_gate)) || !w_router) return MOE_ERR_INVALID_ARG;
   if (!all_aligned({x, w_router, logit_bias, logits, topk_idx, topk_gate})) return MOE_ERR_MISALIGNED;
   if (H % vec_elems(dtype) != 0 || E % 4 != 0) return MOE_ERR_UNSUPPORTED;
+  if (dtype == MOE_BF16 && E % 8 != 0) return MOE_ERR_UNSUPPORTED;  // 16-byte rows of W_r for TMA
   if (T == 0) return MOE_OK;
   cudaStream_t s = as_stream(stream);
   int st = launch_router_logits(x, w_router, logit_bias, T, H, E, dtype, logits, s);
@@ -125,6 +126,7 @@ int moe_expert_ffn(const void* xs, const int32_t* cu_seqlens, int rows, const vo
     return MOE_ERR_INVALID_ARG;
   if (!all_aligned({xs, cu_seqlens, w_gate, w_up, w_down, act, h})) return MOE_ERR_MISALIGNED;
   if (H % vec_elems(dtype) != 0 || Hp % vec_elems(dtype) != 0) return MOE_ERR_UNSUPPORTED;
+  if (dtype == MOE_BF16 && (H % 64 != 0 || Hp % 64 != 0 || E > 1024)) return MOE_ERR_UNSUPPORTED;
   return launch_expert_ffn(xs, cu_seqlens, rows, w_gate, w_up, w_down, E, H, Hp, dtype, act, h,
                            as_stream(stream));
 }
