@@ -131,25 +131,6 @@ def measured_peaks():
 
 # --------------------------------------------------------------------------- ours
 
-def count_launches(run_step, stream):
-    """Kernels of libmoe launched by one step, counted with the CUDA profiler
-    (outside the timed region).  None if the profiler is unavailable."""
-    import torch
-    try:
-        from torch.profiler import ProfilerActivity, profile
-        with profile(activities=[ProfilerActivity.CUDA]) as prof:
-            with torch.cuda.stream(stream):
-                run_step()
-            torch.cuda.synchronize()
-        n = 0
-        for ev in prof.events():
-            if ev.device_type.name == "CUDA" and "moe::" in ev.name:
-                n += 1
-        return n or None
-    except Exception:
-        return None
-
-
 def run_ours(args, shape, rank, world, local):
     import torch
     from token_dispatch_gb300 import _lib as L
@@ -220,7 +201,6 @@ def run_ours(args, shape, rank, world, local):
 
     counts = np.diff(b.cu.cpu().numpy().astype(np.int64))
     maxvio = float(counts.max() / (R / E) - 1.0)
-    launches_per_step = count_launches(lambda: step(x_d, dy_d, dxs_d), stream)
 
     clocks = Clocks(local)
     clocks.start()
@@ -228,12 +208,14 @@ def run_ours(args, shape, rank, world, local):
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize(dev)
+    launches0 = L.moe_kernel_launches()
     with torch.cuda.stream(stream):
         for i in range(args.steps):
             step(x_d, dy_d, dxs_d, evs[i])
             flush.fill_(1)  # L2 flush between timed steps (outside the step's events)
     torch.cuda.synchronize(dev)
     barrier()
+    launches = L.moe_kernel_launches() - launches0
     step_ms = [evs[i][0].elapsed_time(evs[i][6]) for i in range(args.steps)]
     call_ms = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
                for j, n in enumerate(names)}
@@ -304,7 +286,7 @@ def run_ours(args, shape, rank, world, local):
                      "peak_source": f"{peak_src} bf16_tflops_sustained"},
         "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": None if launches_per_step is None else launches_per_step * args.steps,
+        "gpu_launches": launches,
         "clocks": clk,
     }
     return result, dict(x=x, wr=wr, wg=wg, wu=wu, wd=wd, bias=bias_np, dy=dy_d, dxs=dxs_d, dev=dev)
@@ -390,7 +372,7 @@ def main():
 
     result, inputs = run_ours(args, shape, rank, world, local)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n_tok = args.cpu_sample_tokens or 48
+        n_tok = args.cpu_sample_tokens or 4096
         times = oracle_sample(shape, inputs, n_tok, reps=1)
         result["cpu_baseline"] = {"value": n_tok / times[0], "unit": "tokens/s", "cores": cores(),
                                   "kind": "oracle",

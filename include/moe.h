@@ -76,6 +76,10 @@ MOE_API const char* moe_status_str(int status);
 /* ABI version (major*10000 + minor*100 + patch). */
 MOE_API int moe_version(void);
 
+/* Number of CUDA kernels this library has launched in this process (a host-side
+ * counter; no device work).  Lets a caller count the launches of a region. */
+MOE_API unsigned long long moe_kernel_launches(void);
+
 /* Bytes of device workspace `op` needs for these sizes (0 = none; `ws` may then be
  * NULL).  Sizes not used by `op` are ignored.  Returns 0 for invalid sizes. */
 MOE_API size_t moe_workspace_bytes(int op, int T, int H, int E, int K, int Hp);

@@ -35,7 +35,7 @@ MOE_ROUTE_SOFTMAX_TOPK = 0
 MOE_ROUTE_MOD_LINEAR = 1
 MOE_ROUTE_DX_WRITE = 0x100
 
-EXPORTS = ("moe_status_str", "moe_version", "moe_workspace_bytes", "moe_last_device_error",
+EXPORTS = ("moe_status_str", "moe_version", "moe_kernel_launches", "moe_workspace_bytes", "moe_last_device_error",
            "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_route_bwd",
            "moe_permute_bwd", "mod_select")
 
@@ -55,6 +55,7 @@ _Z = ctypes.c_size_t
 _SIGS = {
     "moe_status_str": (ctypes.c_char_p, [_I]),
     "moe_version": (_I, []),
+    "moe_kernel_launches": (ctypes.c_ulonglong, []),
     "moe_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I]),
     "moe_last_device_error": (_I, [_P]),
     "moe_route": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
@@ -112,6 +113,10 @@ def moe_status_str(status: int) -> str:
 
 def moe_version() -> int:
     return lib().moe_version()
+
+
+def moe_kernel_launches() -> int:
+    return lib().moe_kernel_launches()
 
 
 def moe_workspace_bytes(op: int, T: int, H: int, E: int, K: int, Hp: int) -> int:

@@ -9,6 +9,8 @@ namespace moe {
 // status code here instead of trapping.
 __device__ unsigned g_moe_device_error;
 
+unsigned long long g_kernel_launches = 0;
+
 static unsigned* g_err_ptr[64];
 
 unsigned* device_error_word() {
@@ -60,6 +62,8 @@ const char* moe_status_str(int status) {
 }
 
 int moe_version(void) { return 100; }
+
+unsigned long long moe_kernel_launches(void) { return __atomic_load_n(&g_kernel_launches, __ATOMIC_RELAXED); }
 
 size_t moe_workspace_bytes(int op, int T, int H, int E, int K, int Hp) {
   (void)Hp;

@@ -79,9 +79,15 @@ inline int sm_count() {
   return n > 0 ? n : 1;
 }
 
+// Kernels this library has launched in this process (every launch site is
+// followed by exactly one launch_status()).
+extern unsigned long long g_kernel_launches;
+
 inline int launch_status() {
   cudaError_t e = cudaGetLastError();
-  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  __atomic_fetch_add(&g_kernel_launches, 1ull, __ATOMIC_RELAXED);
+  return MOE_OK;
 }
 
 // ------------------------------------------------------- kernel launchers ---
