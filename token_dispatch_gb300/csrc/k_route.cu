@@ -149,12 +149,184 @@ int rows_grid(long long T) {
   return (int)(ctas < cap ? (ctas > 0 ? ctas : 1) : cap);
 }
 
-int splits_for(int T, int H, int E) {
-  long long by_t = T / 512;
-  long long by_mem = (64ll << 20) / ((long long)H * E * 4);
-  long long s = by_t < by_mem ? by_t : by_mem;
-  if (s > 16) s = 16;
-  return s < 1 ? 1 : (int)s;
+// ---------------------------------------------------------------------------
+// Router weight gradient  dw[h,e] = sum_t x[t,h] dl[t,e].
+// Split over tokens; a thread owns CPT consecutive columns h and EB experts
+// (CPT*EB = 64 fp32 accumulators), reads its x columns with one 16/32-byte load
+// per token and the token's dl values from a shared-memory tile (broadcast).
+// Each split writes its partial [H, E]; a second kernel adds the splits in
+// order, so the result does not depend on scheduling.
+constexpr int DW_THREADS = 256;
+constexpr int DW_TB = 32;  // tokens per shared-memory dl tile
+
+struct DwPlan {
+  int cpt, eb, col_blocks, exp_blocks, splits, rows_per_split;
+};
+
+DwPlan dw_plan(int T, int H, int E) {
+  DwPlan p;
+  p.eb = E <= 8 ? 8 : E <= 16 ? 16 : E <= 32 ? 32 : 64;
+  p.cpt = 64 / p.eb;
+  p.col_blocks = (H + DW_THREADS * p.cpt - 1) / (DW_THREADS * p.cpt);
+  p.exp_blocks = (E + p.eb - 1) / p.eb;
+  long long want = (320 + p.col_blocks * p.exp_blocks - 1) / (p.col_blocks * p.exp_blocks);
+  long long by_t = (T + 15) / 16;
+  long long s = want < by_t ? want : by_t;
+  if (s > 128) s = 128;
+  if (s < 1) s = 1;
+  p.splits = (int)s;
+  p.rows_per_split = (T + p.splits - 1) / p.splits;
+  return p;
+}
+
+template <typename T> __device__ __forceinline__ void load_cols(const T* p, int n, float* v);
+template <> __device__ __forceinline__ void load_cols<bf16>(const bf16* p, int n, float* v) {
+  if (n == 8) {
+    Vec16<bf16>::load(p, v);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) if (j < n) v[j] = __bfloat162float(p[j]);
+  }
+}
+template <> __device__ __forceinline__ void load_cols<float>(const float* p, int n, float* v) {
+  if (n == 8) {
+    Vec16<float>::load(p, v);
+    Vec16<float>::load(p + 4, v + 4);
+  } else if (n == 4) {
+    Vec16<float>::load(p, v);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) if (j < n) v[j] = p[j];
+  }
+}
+
+template <typename T, int CPT, int EB>
+__global__ void __launch_bounds__(DW_THREADS)
+router_dw_partial_kernel(const T* __restrict__ x, const float* __restrict__ dl, int Tn, int H, int E,
+                         int rows_per_split, float* __restrict__ part) {
+  __shared__ float dls[DW_TB][EB];
+  const int h0 = (blockIdx.x * DW_THREADS + threadIdx.x) * CPT;
+  const int e0 = blockIdx.y * EB;
+  const int split = blockIdx.z;
+  const int t_begin = split * rows_per_split;
+  const int t_end = min(Tn, t_begin + rows_per_split);
+  float acc[CPT][EB];
+#pragma unroll
+  for (int j = 0; j < CPT; ++j)
+#pragma unroll
+    for (int e = 0; e < EB; ++e) acc[j][e] = 0.f;
+  const bool col_ok = h0 < H;
+  const int ncol = col_ok ? min(CPT, H - h0) : 0;
+  for (int t0 = t_begin; t0 < t_end; t0 += DW_TB) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < DW_TB * EB; i += DW_THREADS) {
+      const int tt = i / EB, e = i % EB;
+      const int t = t0 + tt, ge = e0 + e;
+      dls[tt][e] = (t < t_end && ge < E) ? __ldg(dl + (long long)t * E + ge) : 0.f;
+    }
+    __syncthreads();
+    const int n_rows = min(DW_TB, t_end - t0);
+    if (col_ok) {
+      for (int tt = 0; tt < n_rows; ++tt) {
+        float xv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        load_cols<T>(x + (long long)(t0 + tt) * H + h0, ncol, xv);
+#pragma unroll
+        for (int j = 0; j < CPT; ++j)
+#pragma unroll
+          for (int e = 0; e < EB; ++e) acc[j][e] = fmaf(xv[j], dls[tt][e], acc[j][e]);
+      }
+    }
+  }
+  if (!col_ok) return;
+  float* out = part + (long long)split * H * E;
+#pragma unroll
+  for (int j = 0; j < CPT; ++j)
+#pragma unroll
+    for (int e = 0; e < EB; ++e)
+      if (j < ncol && e0 + e < E) out[(long long)(h0 + j) * E + e0 + e] = acc[j][e];
+}
+
+// ---------------------------------------------------------------------------
+// Router input gradient  dx[t,h] (+)= sum_e dl[t,e] w[h,e].
+// A CTA covers DX_TR tokens x DX_HB columns; w[h, e-chunk] is staged in shared
+// memory transposed ([e][h], so a warp's 8-column reads are contiguous) together
+// with the tokens' dl chunk; a thread owns 8 consecutive columns of one token.
+constexpr int DX_TR = 32, DX_HB = 256, DX_EC = 32, DX_THREADS = 256;
+// thread (r, c): r = tid / 32 (+ 8 * i), c = tid % 32 -> columns 8c .. 8c+7
+
+template <typename T>
+__global__ void __launch_bounds__(DX_THREADS)
+router_dx_kernel(const float* __restrict__ dl, const T* __restrict__ w, int Tn, int H, int E, bool write,
+                 T* __restrict__ dx) {
+  __shared__ __align__(16) float ws[DX_EC][DX_HB];
+  __shared__ float ds[DX_TR][DX_EC];
+  const int tb = blockIdx.y * DX_TR;
+  const int hb = blockIdx.x * DX_HB;
+  const int c = threadIdx.x & 31;
+  const int r0 = threadIdx.x >> 5;  // 0..7; rows r0, r0+8, r0+16, r0+24
+  float acc[4][8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+  for (int e0 = 0; e0 < E; e0 += DX_EC) {
+    __syncthreads();
+    for (int i = threadIdx.x; i < DX_EC * DX_HB; i += DX_THREADS) {
+      const int h = i % DX_HB, e = i / DX_HB;  // consecutive threads write consecutive h
+      const int gh = hb + h, ge = e0 + e;
+      ws[e][h] = (gh < H && ge < E) ? to_f32(w[(long long)gh * E + ge]) : 0.f;
+    }
+    for (int i = threadIdx.x; i < DX_TR * DX_EC; i += DX_THREADS) {
+      const int r = i / DX_EC, e = i % DX_EC;
+      const int t = tb + r, ge = e0 + e;
+      ds[r][e] = (t < Tn && ge < E) ? __ldg(dl + (long long)t * E + ge) : 0.f;
+    }
+    __syncthreads();
+    const int ne = min(DX_EC, E - e0);
+    for (int e = 0; e < ne; ++e) {
+      float wv[8];
+      const float4 a = *reinterpret_cast<const float4*>(&ws[e][8 * c]);
+      const float4 b = *reinterpret_cast<const float4*>(&ws[e][8 * c + 4]);
+      wv[0] = a.x; wv[1] = a.y; wv[2] = a.z; wv[3] = a.w; wv[4] = b.x; wv[5] = b.y; wv[6] = b.z; wv[7] = b.w;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float d = ds[r0 + 8 * i][e];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(d, wv[j], acc[i][j]);
+      }
+    }
+  }
+  const int h = hb + 8 * c;
+  if (h >= H) return;
+  const int ncol = min(8, H - h);  // 8, or 4 for fp32 rows with H % 8 == 4
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int t = tb + r0 + 8 * i;
+    if (t >= Tn) continue;
+    T* p = dx + (long long)t * H + h;
+    float v[8];
+    if (!write) {
+      float old[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      load_cols<T>(p, ncol, old);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = old[j] + acc[i][j];
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = acc[i][j];
+    }
+    if (ncol == 8) {
+      if (sizeof(T) == 2) {
+        Vec16<T>::store(p, v);
+      } else {
+        Vec16<T>::store(p, v);
+        Vec16<T>::store(p + 4, v + 4);
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        if (j < ncol) p[j] = from_f32<T>(v[j]);
+    }
+  }
 }
 
 size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
@@ -191,23 +363,44 @@ int launch_softmax_topk(const float* logits, int T, int E, int K, int32_t* idx, 
 }
 
 size_t route_bwd_ws_bytes(int T, int H, int E) {
-  int S = splits_for(T, H, E);
-  return align256((size_t)S * H * E * 4) + align256((size_t)T * E * 4);
+  const DwPlan pl = dw_plan(T, H, E);
+  return align256((size_t)pl.splits * H * E * 4) + align256((size_t)T * E * 4);
+}
+
+template <typename T>
+int launch_dw(const T* x, const float* dl, int Tn, int H, int E, float* part, float* dw, cudaStream_t s) {
+  const DwPlan pl = dw_plan(Tn, H, E);
+  dim3 grid(pl.col_blocks, pl.exp_blocks, pl.splits);
+  if (pl.eb == 8) router_dw_partial_kernel<T, 8, 8><<<grid, DW_THREADS, 0, s>>>(x, dl, Tn, H, E, pl.rows_per_split, part);
+  else if (pl.eb == 16) router_dw_partial_kernel<T, 4, 16><<<grid, DW_THREADS, 0, s>>>(x, dl, Tn, H, E, pl.rows_per_split, part);
+  else if (pl.eb == 32) router_dw_partial_kernel<T, 2, 32><<<grid, DW_THREADS, 0, s>>>(x, dl, Tn, H, E, pl.rows_per_split, part);
+  else router_dw_partial_kernel<T, 1, 64><<<grid, DW_THREADS, 0, s>>>(x, dl, Tn, H, E, pl.rows_per_split, part);
+  int st = launch_status();
+  if (st != MOE_OK) return st;
+  const long long n = (long long)H * E;
+  const int rgrid = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  reduce_splits_kernel<<<rgrid, 256, 0, s>>>(part, pl.splits, n, dw);
+  return launch_status();
+}
+
+template <typename T>
+int launch_dx(const float* dl, const T* w, int Tn, int H, int E, bool write, T* dx, cudaStream_t s) {
+  dim3 grid((H + DX_HB - 1) / DX_HB, (Tn + DX_TR - 1) / DX_TR);
+  router_dx_kernel<T><<<grid, DX_THREADS, 0, s>>>(dl, w, Tn, H, E, write, dx);
+  return launch_status();
 }
 
 int launch_route_bwd(int mode, const float* d_gate, const float* logits, const int32_t* idx,
                      const void* x, const void* w, int T, int H, int E, int K, int dtype,
                      float* d_logits, float* dw, void* dx, bool dx_write, void* ws, cudaStream_t s) {
   if (T == 0) {
-    if (dw) {
-      cudaMemsetAsync(dw, 0, (size_t)H * E * 4, s);
-    }
-    return launch_status();
+    if (dw && cudaMemsetAsync(dw, 0, (size_t)H * E * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
   }
-  const int S = splits_for(T, H, E);
+  const DwPlan pl = dw_plan(T, H, E);
   float* part = static_cast<float*>(ws);
   float* dl = d_logits;
-  if (!dl) dl = reinterpret_cast<float*>(static_cast<char*>(ws) + align256((size_t)S * H * E * 4));
+  if (!dl) dl = reinterpret_cast<float*>(static_cast<char*>(ws) + align256((size_t)pl.splits * H * E * 4));
 
   if (mode == MOE_ROUTE_SOFTMAX_TOPK) {
     int grid = rows_grid(T);
@@ -224,39 +417,14 @@ int launch_route_bwd(int mode, const float* d_gate, const float* logits, const i
   if (st != MOE_OK) return st;
 
   if (dw) {
-    // dw[h,e] = sum_t x[t,h] dl[t,e], split over T for parallelism, reduced in order
-    int chunk = (T + S - 1) / S;
-    for (int sp = 0; sp < S; ++sp) {
-      int t0 = sp * chunk;
-      int len = T - t0 < chunk ? T - t0 : chunk;
-      float* out = part + (size_t)sp * H * E;
-      SimtGemmArgs a{};
-      a.A = static_cast<const char*>(x) + (size_t)t0 * H * (dtype == MOE_BF16 ? 2 : 4);
-      a.a_sm = 1; a.a_sk = H;
-      a.B = dl + (size_t)t0 * E; a.b_sg = 0; a.b_sk = E; a.b_sn = 1;
-      a.C = out; a.c_sm = E;
-      a.M = H; a.N = E; a.K = len > 0 ? len : 0; a.groups = 1; a.epilogue = 0;
-      if (len <= 0) {
-        cudaMemsetAsync(out, 0, (size_t)H * E * 4, s);
-        continue;
-      }
-      st = launch_simt_gemm(a, dtype, MOE_F32, MOE_F32, s);
-      if (st != MOE_OK) return st;
-    }
-    long long n = (long long)H * E;
-    int grid = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-    reduce_splits_kernel<<<grid, 256, 0, s>>>(part, S, n, dw);
-    st = launch_status();
+    st = dtype == MOE_BF16 ? launch_dw<bf16>(static_cast<const bf16*>(x), dl, T, H, E, part, dw, s)
+                           : launch_dw<float>(static_cast<const float*>(x), dl, T, H, E, part, dw, s);
     if (st != MOE_OK) return st;
   }
   if (dx) {
-    // dx[t,h] += sum_e dl[t,e] w[h,e]
-    SimtGemmArgs a{};
-    a.A = dl; a.a_sm = E; a.a_sk = 1;
-    a.B = w; a.b_sg = 0; a.b_sk = 1; a.b_sn = E;
-    a.C = dx; a.c_sm = H;
-    a.M = T; a.N = H; a.K = E; a.groups = 1; a.epilogue = dx_write ? 0 : 1;
-    st = launch_simt_gemm(a, MOE_F32, dtype, dtype, s);
+    st = dtype == MOE_BF16
+             ? launch_dx<bf16>(dl, static_cast<const bf16*>(w), T, H, E, dx_write, static_cast<bf16*>(dx), s)
+             : launch_dx<float>(dl, static_cast<const float*>(w), T, H, E, dx_write, static_cast<float*>(dx), s);
     if (st != MOE_OK) return st;
   }
   return MOE_OK;
