@@ -39,6 +39,14 @@ def assert_close(gpu, ref, tol, what=""):
     return e
 
 
+def gate_tol(logit_err):
+    """Bound for the gates given the logits' absolute error d: since
+    d(log p_j)/d(l_i) = [i==j] - p_i, a perturbation of every logit by at most d
+    changes each p_j by at most 2d relative (to first order), so the normwise
+    relative gate error is at most 2d; 1e-6 covers fp32 exp/divide rounding."""
+    return 2.0 * logit_err + 1e-6
+
+
 def check_topk(gpu_idx, ref_logits, K, logit_err, max_frac=1e-3):
     """Rows whose GPU top-K differs from the oracle's must be near-ties: every
     chosen expert's exact logit is within 2*logit_err of the K-th largest exact

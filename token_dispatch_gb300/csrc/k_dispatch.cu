@@ -1,7 +1,6 @@
-// Token dispatch (histogram -> cu_seqlens -> stable permutation -> row gather),
-// combine (gate-weighted gather-sum back to token order) and their backward.
+// Token dispatch: histogram -> cu_seqlens -> stable permutation -> row gather.
 //
-// Dispatch/combine follow the MoE/MoD framework page ("What's in the box":
+// Dispatch follows the MoE/MoD framework page ("What's in the box":
 // a fused kernel moving tokens between experts, reading and writing the buffers
 // directly) and the MoonEP page ("Step-by-step": tokens land in one contiguous
 // expert-sorted buffer whose active rows are described by cu_seqlens).
@@ -151,146 +150,37 @@ dispatch_place_kernel(const int32_t* __restrict__ idx, int T, int E, int K,
   }
 }
 
-// xs[dst_row[t*K+k]] = x[t]: one warp per token, 16-byte vectors, x read once.
+// xs[dst_row[t*K+k]] = x[t]: one warp per token, 16-byte vectors; every x row is
+// read once and written to its K rows, with U vectors per lane in flight.
+template <int KT>
 __global__ void __launch_bounds__(256)
 gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ dst_row, int T, int K,
                    int vec_per_row, uint4* __restrict__ xs) {
+  constexpr int U = 4;
   const int lane = threadIdx.x & 31;
   const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
   for (long long t = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < T; t += nwarps) {
-    int rows[16];
+    int rows[KT];
 #pragma unroll
-    for (int k = 0; k < 16; ++k) rows[k] = (k < K) ? __ldg(dst_row + t * K + k) : -1;
+    for (int k = 0; k < KT; ++k) rows[k] = (k < K) ? __ldg(dst_row + t * K + k) : -1;
     const uint4* src = x + t * vec_per_row;
-    for (int i = lane; i < vec_per_row; i += 64) {
-      uint4 a = __ldg(src + i);
-      bool two = i + 32 < vec_per_row;
-      uint4 b = two ? __ldg(src + i + 32) : make_uint4(0, 0, 0, 0);
+    for (int i0 = lane; i0 < vec_per_row; i0 += 32 * U) {
+      uint4 a[U];
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        if (k < K && rows[k] >= 0) {
-          uint4* dst = xs + (long long)rows[k] * vec_per_row;
-          dst[i] = a;
-          if (two) dst[i + 32] = b;
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + 32 * u;
+        a[u] = (i < vec_per_row) ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int k = 0; k < KT; ++k) {
+        if (rows[k] < 0) continue;
+        uint4* dst = xs + (long long)rows[k] * vec_per_row;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+          const int i = i0 + 32 * u;
+          if (i < vec_per_row) dst[i] = a[u];
         }
       }
-    }
-  }
-}
-
-template <typename T>
-__global__ void __launch_bounds__(256)
-combine_kernel(const T* __restrict__ h, const float* __restrict__ gate,
-               const int32_t* __restrict__ dst_row, const float* __restrict__ scale,
-               const T* __restrict__ residual, const int32_t* __restrict__ out_row,
-               int Tn, int H, int K, T* __restrict__ y) {
-  constexpr int V = Vec16<T>::N;
-  const int lane = threadIdx.x & 31;
-  const int nvec = H / V;
-  const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
-  for (long long t = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < Tn; t += nwarps) {
-    int rows[16];
-    float g[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      rows[k] = (k < K) ? (dst_row ? __ldg(dst_row + t * K + k) : (int)(t * K + k)) : -1;
-      g[k] = (k < K) ? __ldg(gate + t * K + k) : 0.f;
-    }
-    const float s = scale ? __ldg(scale + t) : 1.0f;
-    const long long o = out_row ? (long long)__ldg(out_row + t) : t;
-    for (int i = lane; i < nvec; i += 32) {
-      float acc[V];
-#pragma unroll
-      for (int v = 0; v < V; ++v) acc[v] = 0.f;
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        if (k < K && rows[k] >= 0) {
-          float hv[V];
-          Vec16<T>::load(h + (long long)rows[k] * H + (long long)i * V, hv);
-#pragma unroll
-          for (int v = 0; v < V; ++v) acc[v] = fmaf(g[k], hv[v], acc[v]);
-        }
-      }
-      float out[V];
-      if (residual) {
-        float rv[V];
-        Vec16<T>::load(residual + o * H + (long long)i * V, rv);
-#pragma unroll
-        for (int v = 0; v < V; ++v) out[v] = fmaf(s, acc[v], rv[v]);
-      } else {
-#pragma unroll
-        for (int v = 0; v < V; ++v) out[v] = s * acc[v];
-      }
-      Vec16<T>::store(y + o * H + (long long)i * V, out);
-    }
-  }
-}
-
-template <typename T>
-__global__ void __launch_bounds__(256)
-permute_bwd_kernel(const T* __restrict__ dy, const T* __restrict__ h, const float* __restrict__ gate,
-                   const int32_t* __restrict__ dst_row, const float* __restrict__ scale,
-                   const int32_t* __restrict__ out_row, const T* __restrict__ dxs,
-                   int Tn, int H, int K, T* __restrict__ dh, float* __restrict__ d_gate,
-                   float* __restrict__ d_scale, T* __restrict__ dx) {
-  constexpr int V = Vec16<T>::N;
-  const int lane = threadIdx.x & 31;
-  const int nvec = H / V;
-  const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
-  for (long long t = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < Tn; t += nwarps) {
-    int rows[16];
-    float g[16], dot[16];
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      rows[k] = (k < K) ? (dst_row ? __ldg(dst_row + t * K + k) : (int)(t * K + k)) : -1;
-      g[k] = (k < K) ? __ldg(gate + t * K + k) : 0.f;
-      dot[k] = 0.f;
-    }
-    const float s = scale ? __ldg(scale + t) : 1.0f;
-    const long long o = out_row ? (long long)__ldg(out_row + t) : t;
-    for (int i = lane; i < nvec; i += 32) {
-      float gy[V], ax[V];
-      Vec16<T>::load(dy + o * H + (long long)i * V, gy);
-#pragma unroll
-      for (int v = 0; v < V; ++v) ax[v] = 0.f;
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        if (k < K && rows[k] >= 0) {
-          const long long off = (long long)rows[k] * H + (long long)i * V;
-          if (d_gate || d_scale) {
-            float hv[V];
-            Vec16<T>::load(h + off, hv);
-#pragma unroll
-            for (int v = 0; v < V; ++v) dot[k] = fmaf(gy[v], hv[v], dot[k]);
-          }
-          if (dh) {
-            float d[V];
-            const float c = s * g[k];
-#pragma unroll
-            for (int v = 0; v < V; ++v) d[v] = c * gy[v];
-            Vec16<T>::store(dh + off, d);
-          }
-          if (dx) {
-            float xv[V];
-            Vec16<T>::load(dxs + off, xv);
-#pragma unroll
-            for (int v = 0; v < V; ++v) ax[v] += xv[v];
-          }
-        }
-      }
-      if (dx) Vec16<T>::store(dx + t * H + (long long)i * V, ax);
-    }
-    if (d_gate || d_scale) {
-      float ds = 0.f;
-#pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        if (k < K) {
-          float d = warp_sum(dot[k]);
-          if (lane == 0 && d_gate) d_gate[t * K + k] = s * d;
-          ds = fmaf(g[k], d, ds);
-        }
-      }
-      if (lane == 0 && d_scale) d_scale[t] = ds;
     }
   }
 }
@@ -326,44 +216,15 @@ int launch_dispatch(const void* x, const int32_t* idx, int T, int H, int E, int 
   dispatch_place_kernel<<<C, 32 * CH_WARPS, 0, s>>>(idx, T, E, K, counts, dst_row, src_tok);
   st = launch_status();
   if (st != MOE_OK) return st;
-  const int row_bytes = H * (dtype == MOE_BF16 ? 2 : 4);
-  gather_rows_kernel<<<warp_grid(T), 256, 0, s>>>(static_cast<const uint4*>(x), dst_row, T, K,
-                                                  row_bytes / 16, static_cast<uint4*>(xs));
-  return launch_status();
-}
-
-int launch_combine(const void* h, const float* gate, const int32_t* dst_row, const float* scale,
-                   const void* residual, const int32_t* out_row, int T, int H, int K, int dtype,
-                   void* y, cudaStream_t s) {
-  if (T == 0) return MOE_OK;
-  int grid = warp_grid(T);
-  if (dtype == MOE_BF16)
-    combine_kernel<bf16><<<grid, 256, 0, s>>>(static_cast<const bf16*>(h), gate, dst_row, scale,
-                                              static_cast<const bf16*>(residual), out_row, T, H, K,
-                                              static_cast<bf16*>(y));
-  else
-    combine_kernel<float><<<grid, 256, 0, s>>>(static_cast<const float*>(h), gate, dst_row, scale,
-                                               static_cast<const float*>(residual), out_row, T, H, K,
-                                               static_cast<float*>(y));
-  return launch_status();
-}
-
-int launch_permute_bwd(const void* dy, const void* h, const float* gate, const int32_t* dst_row,
-                       const float* scale, const int32_t* out_row, const void* dxs, int T, int H,
-                       int K, int dtype, void* dh, float* d_gate, float* d_scale, void* dx,
-                       cudaStream_t s) {
-  if (T == 0) return MOE_OK;
-  int grid = warp_grid(T);
-  if (dtype == MOE_BF16)
-    permute_bwd_kernel<bf16><<<grid, 256, 0, s>>>(
-        static_cast<const bf16*>(dy), static_cast<const bf16*>(h), gate, dst_row, scale, out_row,
-        static_cast<const bf16*>(dxs), T, H, K, static_cast<bf16*>(dh), d_gate, d_scale,
-        static_cast<bf16*>(dx));
-  else
-    permute_bwd_kernel<float><<<grid, 256, 0, s>>>(
-        static_cast<const float*>(dy), static_cast<const float*>(h), gate, dst_row, scale, out_row,
-        static_cast<const float*>(dxs), T, H, K, static_cast<float*>(dh), d_gate, d_scale,
-        static_cast<float*>(dx));
+  const int vec = H * (dtype == MOE_BF16 ? 2 : 4) / 16;
+  const uint4* xv = static_cast<const uint4*>(x);
+  uint4* xsv = static_cast<uint4*>(xs);
+  const int grid = warp_grid(T);
+  if (K <= 1) gather_rows_kernel<1><<<grid, 256, 0, s>>>(xv, dst_row, T, K, vec, xsv);
+  else if (K <= 2) gather_rows_kernel<2><<<grid, 256, 0, s>>>(xv, dst_row, T, K, vec, xsv);
+  else if (K <= 4) gather_rows_kernel<4><<<grid, 256, 0, s>>>(xv, dst_row, T, K, vec, xsv);
+  else if (K <= 8) gather_rows_kernel<8><<<grid, 256, 0, s>>>(xv, dst_row, T, K, vec, xsv);
+  else gather_rows_kernel<16><<<grid, 256, 0, s>>>(xv, dst_row, T, K, vec, xsv);
   return launch_status();
 }
 
