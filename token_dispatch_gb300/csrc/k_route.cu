@@ -135,10 +135,12 @@ __global__ void copy_f32_kernel(const float* __restrict__ a, float* __restrict__
 }
 
 // dw[i] = sum_s part[s][i], in split order (deterministic).
-__global__ void reduce_splits_kernel(const float* __restrict__ part, int S, long long n, float* __restrict__ out) {
+__global__ void __launch_bounds__(64) reduce_splits_kernel(const float* __restrict__ part, int S, long long n,
+                                                           float* __restrict__ out) {
   for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
     float acc = 0.f;
-    for (int s = 0; s < S; ++s) acc += part[(long long)s * n + i];
+#pragma unroll 8
+    for (int s = 0; s < S; ++s) acc += __ldg(part + (long long)s * n + i);
     out[i] = acc;
   }
 }
@@ -227,7 +229,24 @@ router_dw_partial_kernel(const T* __restrict__ x, const float* __restrict__ dl, 
     __syncthreads();
     const int n_rows = min(DW_TB, t_end - t0);
     if (col_ok) {
-      for (int tt = 0; tt < n_rows; ++tt) {
+      int tt = 0;
+      // four tokens' x columns are loaded before their FMAs (loads in flight)
+      for (; tt + 4 <= n_rows; tt += 4) {
+        float xv[4][8];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) xv[q][j] = 0.f;
+          load_cols<T>(x + (long long)(t0 + tt + q) * H + h0, ncol, xv[q]);
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+#pragma unroll
+          for (int j = 0; j < CPT; ++j)
+#pragma unroll
+            for (int e = 0; e < EB; ++e) acc[j][e] = fmaf(xv[q][j], dls[tt + q][e], acc[j][e]);
+      }
+      for (; tt < n_rows; ++tt) {
         float xv[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         load_cols<T>(x + (long long)(t0 + tt) * H + h0, ncol, xv);
 #pragma unroll
@@ -254,77 +273,88 @@ router_dw_partial_kernel(const T* __restrict__ x, const float* __restrict__ dl, 
 constexpr int DX_TR = 32, DX_HB = 256, DX_EC = 32, DX_THREADS = 256;
 // thread (r, c): r = tid / 32 (+ 8 * i), c = tid % 32 -> columns 8c .. 8c+7
 
+constexpr int DX_RT = 4;  // row tiles per CTA
+
 template <typename T>
 __global__ void __launch_bounds__(DX_THREADS)
 router_dx_kernel(const float* __restrict__ dl, const T* __restrict__ w, int Tn, int H, int E, bool write,
                  T* __restrict__ dx) {
   __shared__ __align__(16) float ws[DX_EC][DX_HB];
   __shared__ float ds[DX_TR][DX_EC];
-  const int tb = blockIdx.y * DX_TR;
   const int hb = blockIdx.x * DX_HB;
   const int c = threadIdx.x & 31;
-  const int r0 = threadIdx.x >> 5;  // 0..7; rows r0, r0+8, r0+16, r0+24
-  float acc[4][8];
-#pragma unroll
-  for (int i = 0; i < 4; ++i)
-#pragma unroll
-    for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
-  for (int e0 = 0; e0 < E; e0 += DX_EC) {
-    __syncthreads();
-    for (int i = threadIdx.x; i < DX_EC * DX_HB; i += DX_THREADS) {
-      const int h = i % DX_HB, e = i / DX_HB;  // consecutive threads write consecutive h
-      const int gh = hb + h, ge = e0 + e;
-      ws[e][h] = (gh < H && ge < E) ? to_f32(w[(long long)gh * E + ge]) : 0.f;
-    }
-    for (int i = threadIdx.x; i < DX_TR * DX_EC; i += DX_THREADS) {
-      const int r = i / DX_EC, e = i % DX_EC;
-      const int t = tb + r, ge = e0 + e;
-      ds[r][e] = (t < Tn && ge < E) ? __ldg(dl + (long long)t * E + ge) : 0.f;
-    }
-    __syncthreads();
-    const int ne = min(DX_EC, E - e0);
-    for (int e = 0; e < ne; ++e) {
-      float wv[8];
-      const float4 a = *reinterpret_cast<const float4*>(&ws[e][8 * c]);
-      const float4 b = *reinterpret_cast<const float4*>(&ws[e][8 * c + 4]);
-      wv[0] = a.x; wv[1] = a.y; wv[2] = a.z; wv[3] = a.w; wv[4] = b.x; wv[5] = b.y; wv[6] = b.z; wv[7] = b.w;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float d = ds[r0 + 8 * i][e];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(d, wv[j], acc[i][j]);
-      }
-    }
-  }
+  const int r0 = threadIdx.x >> 5;  // 0..7; rows r0, r0+8, r0+16, r0+24 of a tile
   const int h = hb + 8 * c;
-  if (h >= H) return;
-  const int ncol = min(8, H - h);  // 8, or 4 for fp32 rows with H % 8 == 4
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int t = tb + r0 + 8 * i;
-    if (t >= Tn) continue;
-    T* p = dx + (long long)t * H + h;
-    float v[8];
-    if (!write) {
-      float old[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      load_cols<T>(p, ncol, old);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = old[j] + acc[i][j];
-    } else {
-#pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = acc[i][j];
+  const int ncol = h < H ? min(8, H - h) : 0;  // 8, or 4 for fp32 rows with H % 8 == 4
+  const bool one_chunk = E <= DX_EC;
+  auto stage_w = [&](int e0) {
+    const int ne = min(DX_EC, E - e0);
+    for (int i = threadIdx.x; i < ne * DX_HB; i += DX_THREADS) {
+      const int hh = i % DX_HB, e = i / DX_HB;  // consecutive threads write consecutive h
+      const int gh = hb + hh;
+      ws[e][hh] = gh < H ? to_f32(w[(long long)gh * E + e0 + e]) : 0.f;
     }
-    if (ncol == 8) {
-      if (sizeof(T) == 2) {
-        Vec16<T>::store(p, v);
-      } else {
-        Vec16<T>::store(p, v);
-        Vec16<T>::store(p + 4, v + 4);
-      }
-    } else {
+  };
+  if (one_chunk) stage_w(0);
+  for (int rt = 0; rt < DX_RT; ++rt) {
+    const int tb = (blockIdx.y * DX_RT + rt) * DX_TR;
+    if (tb >= Tn) break;
+    float acc[4][8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (j < ncol) p[j] = from_f32<T>(v[j]);
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[i][j] = 0.f;
+    for (int e0 = 0; e0 < E; e0 += DX_EC) {
+      const int ne = min(DX_EC, E - e0);
+      __syncthreads();
+      if (!one_chunk) stage_w(e0);
+      for (int i = threadIdx.x; i < DX_TR * ne; i += DX_THREADS) {
+        const int r = i / ne, e = i % ne;
+        const int t = tb + r;
+        ds[r][e] = t < Tn ? __ldg(dl + (long long)t * E + e0 + e) : 0.f;
+      }
+      __syncthreads();
+      for (int e = 0; e < ne; ++e) {
+        float wv[8];
+        const float4 a = *reinterpret_cast<const float4*>(&ws[e][8 * c]);
+        const float4 b = *reinterpret_cast<const float4*>(&ws[e][8 * c + 4]);
+        wv[0] = a.x; wv[1] = a.y; wv[2] = a.z; wv[3] = a.w; wv[4] = b.x; wv[5] = b.y; wv[6] = b.z; wv[7] = b.w;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float d = ds[r0 + 8 * i][e];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(d, wv[j], acc[i][j]);
+        }
+      }
+    }
+    if (ncol == 0) continue;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int t = tb + r0 + 8 * i;
+      if (t >= Tn) continue;
+      T* p = dx + (long long)t * H + h;
+      float v[8];
+      if (!write) {
+        float old[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        load_cols<T>(p, ncol, old);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = old[j] + acc[i][j];
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = acc[i][j];
+      }
+      if (ncol == 8) {
+        if (sizeof(T) == 2) {
+          Vec16<T>::store(p, v);
+        } else {
+          Vec16<T>::store(p, v);
+          Vec16<T>::store(p + 4, v + 4);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (j < ncol) p[j] = from_f32<T>(v[j]);
+      }
     }
   }
 }
@@ -378,14 +408,14 @@ int launch_dw(const T* x, const float* dl, int Tn, int H, int E, float* part, fl
   int st = launch_status();
   if (st != MOE_OK) return st;
   const long long n = (long long)H * E;
-  const int rgrid = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
-  reduce_splits_kernel<<<rgrid, 256, 0, s>>>(part, pl.splits, n, dw);
+  const int rgrid = (int)((n + 63) / 64 < 8192 ? (n + 63) / 64 : 8192);
+  reduce_splits_kernel<<<rgrid, 64, 0, s>>>(part, pl.splits, n, dw);
   return launch_status();
 }
 
 template <typename T>
 int launch_dx(const float* dl, const T* w, int Tn, int H, int E, bool write, T* dx, cudaStream_t s) {
-  dim3 grid((H + DX_HB - 1) / DX_HB, (Tn + DX_TR - 1) / DX_TR);
+  dim3 grid((H + DX_HB - 1) / DX_HB, (Tn + DX_TR * DX_RT - 1) / (DX_TR * DX_RT));
   router_dx_kernel<T><<<grid, DX_THREADS, 0, s>>>(dl, w, Tn, H, E, write, dx);
   return launch_status();
 }

@@ -150,9 +150,10 @@ EPBENCH_BF16 = MoEShape("epbench_bf16_T8192_H7168_E384_K8_Hp2048", 8192, 7168, 3
 MOD_BF16 = MoEShape("mod_bf16_B4_L2048_C1024_H2048_E16_K2_Hp5632", 4096, 2048, 16, 2, 5632, "bf16",
                     mod_B=4, mod_L=2048, mod_C=1024)
 
-# Same expert GEMM shapes as the Mixtral-shaped layer with 4 experts and half
-# the tokens (1.4 GB of weights): the case the hardware-counter captures run on.
-PROFILE_BF16 = MoEShape("mixtral_profile_bf16_T4096_H4096_E4_K2_Hp14336", 4096, 4096, 4, 2, 14336, "bf16")
+# Same expert GEMM shapes as the Mixtral-shaped layer with a quarter of the
+# tokens (2.8 GB of weights, 0.2 GB of activations): the case the
+# hardware-counter captures run on.
+PROFILE_BF16 = MoEShape("mixtral_profile_bf16_T2048_H4096_E8_K2_Hp14336", 2048, 4096, 8, 2, 14336, "bf16")
 
 WORKLOADS = {s.name: s for s in (TINY_F32, MIXTRAL_BF16, FINEGRAINED_BF16, EPBENCH_BF16, MOD_BF16, PROFILE_BF16)}
 
