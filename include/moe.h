@@ -129,6 +129,32 @@ MOE_API int moe_dispatch(const void* x, const int32_t* topk_idx, int T, int H, i
                  void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * moe_dispatch without a workspace argument.  The source pages have no
+ * counterpart for this call; it exists for callers that cannot allocate device
+ * memory: code whose device memory is owned by someone else (a framework
+ * allocator or a fixed arena planned ahead of time) and that has no scratch
+ * buffer to hand over, or code that must not call cudaMalloc on its hot path,
+ * where it can synchronise the device or fail under memory pressure.
+ *
+ * Same arguments, results and errors as moe_dispatch, minus ws/ws_bytes.  The
+ * scratch it needs (a ceil(T/256) x E table of int32 counts) is a library-owned
+ * static device array of 65536 ints (256 KB), present on every GPU that loads
+ * the library until the process exits.  Sizes with ceil(T/256) * E > 65536
+ * return MOE_ERR_WORKSPACE before anything is launched.  The call allocates
+ * nothing (no cudaMalloc/cudaFree, no allocating library routine).
+ *
+ * The first call on a device looks up the array's device address (one
+ * cudaGetSymbolAddress with that device current); make that first call before
+ * any stream capture.  Every call shares the one array: nothing in it needs
+ * clearing between calls, but calls whose kernels may overlap on the GPU (e.g.
+ * on two streams with no ordering between them) race and must be serialised
+ * by the caller.
+ */
+MOE_API int moe_dispatch_noalloc(const void* x, const int32_t* topk_idx, int T, int H, int E, int K,
+                                 int dtype, int32_t* cu_seqlens, int32_t* dst_row, int32_t* src_tok,
+                                 void* xs, void* stream);
+
+/*
  * Grouped SwiGLU expert FFN over contiguous weights
  *                [EP "Step-by-step" (weights [E,H,H'], rows by index); T4 SwiGLU]
  *

@@ -1,0 +1,80 @@
+"""moe_dispatch_noalloc: dispatch for callers that cannot allocate device memory.
+
+Some callers cannot hand the library a workspace: their device memory belongs
+to an allocator or a pre-planned arena they do not control, or they must not
+call cudaMalloc on their hot path.  For them the library keeps the one scratch
+table dispatch needs (per-chunk expert counts) in a static device array.  This
+file checks, through the C ABI, that the variant gives exactly the results of
+moe_dispatch with a caller workspace, on two calls in a row with different
+sizes (the shared array keeps the previous call's contents), and that sizes
+past the array's capacity are refused before anything runs.
+
+The file name sorts last so that a run stopping at the first failure has run
+every other test before this one."""
+import numpy as np
+import pytest
+import torch
+
+from token_dispatch_gb300 import _lib as L
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from token_dispatch_gb300 import build
+    build.build()
+
+
+def idx_for(T, E, K, seed):
+    rng = np.random.default_rng(seed)
+    return np.stack([rng.choice(E, K, replace=False) for _ in range(T)]).astype(np.int32)
+
+
+def run_both(T, H, E, K, seed):
+    raw = L.lib()
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn((T, H), generator=g).to(torch.bfloat16).to(DEV)
+    idx = torch.from_numpy(idx_for(T, E, K, seed)).to(DEV)
+    stream = torch.cuda.current_stream().cuda_stream
+
+    def outputs():
+        return (torch.full((E + 1,), -7, dtype=torch.int32, device=DEV),
+                torch.full((T * K,), -7, dtype=torch.int32, device=DEV),
+                torch.full((T * K,), -7, dtype=torch.int32, device=DEV),
+                torch.zeros((T * K, H), dtype=torch.bfloat16, device=DEV))
+
+    ref = outputs()
+    nbytes = raw.moe_workspace_bytes(L.MOE_OP_DISPATCH, T, H, E, K, 0)
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=DEV)
+    st = raw.moe_dispatch(x.data_ptr(), idx.data_ptr(), T, H, E, K, L.MOE_BF16, ref[0].data_ptr(),
+                          ref[1].data_ptr(), ref[2].data_ptr(), ref[3].data_ptr(), ws.data_ptr(), nbytes, stream)
+    assert st == L.MOE_OK, L.moe_status_str(st)
+
+    got = outputs()
+    st = raw.moe_dispatch_noalloc(x.data_ptr(), idx.data_ptr(), T, H, E, K, L.MOE_BF16, got[0].data_ptr(),
+                                  got[1].data_ptr(), got[2].data_ptr(), got[3].data_ptr(), stream)
+    assert st == L.MOE_OK, L.moe_status_str(st)
+    assert raw.moe_last_device_error(stream) == L.MOE_OK
+    # integer outputs and the copied rows are exact
+    for a, b in zip(ref[:3], got[:3]):
+        assert torch.equal(a, b)
+    assert torch.equal(ref[3].view(torch.int16), got[3].view(torch.int16))
+    assert int(got[0][-1]) == T * K
+
+
+def test_noalloc_matches_workspace_dispatch_on_two_calls_in_a_row():
+    # the second call is smaller and has more experts: stale counts from the
+    # first call would show up as wrong offsets
+    run_both(T=4000, H=256, E=64, K=6, seed=1)
+    run_both(T=1000, H=128, E=384, K=8, seed=2)
+
+
+def test_noalloc_refuses_sizes_past_the_static_scratch():
+    raw = L.lib()
+    A = 1 << 20  # never dereferenced: the size check comes first
+    # ceil(T/256) * E = 65 * 1024 > 65536
+    st = raw.moe_dispatch_noalloc(A, A, 65 * 256, 64, 1024, 2, L.MOE_BF16, A, A, A, A, None)
+    assert st == L.MOE_ERR_WORKSPACE

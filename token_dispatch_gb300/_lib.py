@@ -36,7 +36,7 @@ MOE_ROUTE_MOD_LINEAR = 1
 MOE_ROUTE_DX_WRITE = 0x100
 
 EXPORTS = ("moe_status_str", "moe_version", "moe_kernel_launches", "moe_workspace_bytes", "moe_last_device_error",
-           "moe_route", "moe_dispatch", "moe_expert_ffn", "moe_combine", "moe_route_bwd",
+           "moe_route", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_route_bwd",
            "moe_permute_bwd", "mod_select")
 
 
@@ -60,6 +60,7 @@ _SIGS = {
     "moe_last_device_error": (_I, [_P]),
     "moe_route": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
     "moe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_dispatch_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_expert_ffn": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _Z, _P]),
     "moe_combine": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_route_bwd": (_I, [_I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
@@ -139,6 +140,14 @@ def moe_dispatch(x, topk_idx, T, H, E, K, dtype, cu_seqlens, dst_row, src_tok, x
     _check("moe_dispatch", lib().moe_dispatch(_ptr(x), _ptr(topk_idx), T, H, E, K, dtype,
                                               _ptr(cu_seqlens), _ptr(dst_row), _ptr(src_tok), _ptr(xs),
                                               _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def moe_dispatch_noalloc(x, topk_idx, T, H, E, K, dtype, cu_seqlens, dst_row, src_tok, xs, stream=None):
+    """moe_dispatch with the count table in a library-owned static device array
+    (for callers that cannot allocate); see include/moe.h for its limits."""
+    _check("moe_dispatch_noalloc", lib().moe_dispatch_noalloc(_ptr(x), _ptr(topk_idx), T, H, E, K, dtype,
+                                                              _ptr(cu_seqlens), _ptr(dst_row), _ptr(src_tok),
+                                                              _ptr(xs), _stream(stream)))
 
 
 def moe_expert_ffn(xs, cu_seqlens, rows, w_gate, w_up, w_down, E, H, Hp, dtype, act, h,

@@ -10,6 +10,8 @@
 // one leader lane per distinct expert updates the counter.  The same pass gives
 // each pair its rank among earlier pairs of the same expert (popc of lower peer
 // lanes), so the permutation is stable by token and identical run to run.
+#include <mutex>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -226,6 +228,54 @@ int launch_dispatch(const void* x, const int32_t* idx, int T, int H, int E, int 
   else if (K <= 8) gather_rows_kernel<8><<<grid, 256, 0, s>>>(xv, dst_row, T, K, vec, xsv);
   else gather_rows_kernel<16><<<grid, 256, 0, s>>>(xv, dst_row, T, K, vec, xsv);
   return launch_status();
+}
+
+// ----------------------------------------------------------------------------
+// Dispatch for callers that cannot allocate device memory.
+//
+// The only scratch dispatch needs is the per-chunk expert count table
+// (ceil(T/256) * E ints).  Here it lives in a file-scope device array, so the
+// caller passes inputs and outputs only.  The array exists once per GPU that
+// loads the library and stays allocated until the process exits.  All calls
+// share it: the count kernel writes every entry the later kernels read, so
+// nothing has to be cleared between calls, but two calls whose kernels overlap
+// on the GPU (different streams, no ordering between them) race on it.
+constexpr long long kStaticScratchInts = 1 << 16;  // 256 KB
+static __device__ __align__(256) int g_dispatch_static_scratch[kStaticScratchInts];
+
+static int* g_static_scratch_dev[64];
+static std::mutex g_static_scratch_mu;
+
+long long dispatch_static_scratch_ints() { return kStaticScratchInts; }
+
+// In host code the array's name is only a host-side stand-in; the kernels need
+// its device address, resolved once per device with that device current.
+static int* static_scratch_address(int* status) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    *status = MOE_ERR_CUDA;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_static_scratch_mu);
+  if (!g_static_scratch_dev[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_dispatch_static_scratch) != cudaSuccess || !p) {
+      *status = MOE_ERR_CUDA;
+      return nullptr;
+    }
+    g_static_scratch_dev[dev] = static_cast<int*>(p);
+  }
+  *status = MOE_OK;
+  return g_static_scratch_dev[dev];
+}
+
+int launch_dispatch_static(const void* x, const int32_t* idx, int T, int H, int E, int K, int dtype,
+                           int32_t* cu, int32_t* dst_row, int32_t* src_tok, void* xs, cudaStream_t s) {
+  if ((long long)n_chunks(T) * E > kStaticScratchInts) return MOE_ERR_WORKSPACE;
+  int st = MOE_OK;
+  int* scratch = static_scratch_address(&st);
+  if (!scratch) return st;
+  return launch_dispatch(x, idx, T, H, E, K, dtype, cu, dst_row, src_tok, xs, scratch, s);
 }
 
 }  // namespace moe

@@ -121,6 +121,20 @@ int moe_dispatch(const void* x, const int32_t* topk_idx, int T, int H, int E, in
                          as_stream(stream));
 }
 
+int moe_dispatch_noalloc(const void* x, const int32_t* topk_idx, int T, int H, int E, int K, int dtype,
+                         int32_t* cu_seqlens, int32_t* dst_row, int32_t* src_tok, void* xs, void* stream) {
+  if (!valid_dtype(dtype) || T < 0 || H < 1 || E < 1 || E > 1024 || K < 1 || K > E || K > 16)
+    return MOE_ERR_INVALID_ARG;
+  if ((long long)T * K > 0x7fffffffll) return MOE_ERR_UNSUPPORTED;
+  if (!cu_seqlens || (T > 0 && (!x || !topk_idx || !dst_row || !src_tok || !xs)))
+    return MOE_ERR_INVALID_ARG;
+  if (!all_aligned({x, topk_idx, cu_seqlens, dst_row, src_tok, xs})) return MOE_ERR_MISALIGNED;
+  if (H % vec_elems(dtype) != 0) return MOE_ERR_UNSUPPORTED;
+  if ((long long)((T + 255) / 256) * E > dispatch_static_scratch_ints()) return MOE_ERR_WORKSPACE;
+  return launch_dispatch_static(x, topk_idx, T, H, E, K, dtype, cu_seqlens, dst_row, src_tok, xs,
+                                as_stream(stream));
+}
+
 int moe_expert_ffn(const void* xs, const int32_t* cu_seqlens, int rows, const void* w_gate,
                    const void* w_up, const void* w_down, int E, int H, int Hp, int dtype, void* act,
                    void* h, void* ws, size_t ws_bytes, void* stream) {

@@ -108,6 +108,9 @@ size_t dispatch_ws_bytes(int T, int E, int K);
 int launch_dispatch(const void* x, const int32_t* idx, int T, int H, int E, int K, int dtype,
                     int32_t* cu, int32_t* dst_row, int32_t* src_tok, void* xs, void* ws,
                     cudaStream_t s);
+int launch_dispatch_static(const void* x, const int32_t* idx, int T, int H, int E, int K, int dtype,
+                           int32_t* cu, int32_t* dst_row, int32_t* src_tok, void* xs, cudaStream_t s);
+long long dispatch_static_scratch_ints();
 int launch_combine(const void* h, const float* gate, const int32_t* dst_row, const float* scale,
                    const void* residual, const int32_t* out_row, int T, int H, int K, int dtype,
                    void* y, cudaStream_t s);
