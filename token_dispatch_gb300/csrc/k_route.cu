@@ -134,14 +134,26 @@ __global__ void copy_f32_kernel(const float* __restrict__ a, float* __restrict__
     b[i] = a[i];
 }
 
-// dw[i] = sum_s part[s][i], in split order (deterministic).
-__global__ void __launch_bounds__(64) reduce_splits_kernel(const float* __restrict__ part, int S, long long n,
-                                                           float* __restrict__ out) {
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+// dw[i] = sum_s part[s][i].  Eight lanes per output: lane q adds splits
+// q, q+8, ... in order, then a fixed shuffle tree adds the eight sums, so the
+// result is the same on every run.
+__global__ void __launch_bounds__(256) reduce_splits_kernel(const float* __restrict__ part, int S, long long n,
+                                                            float* __restrict__ out) {
+  const int q = threadIdx.x & 7;
+  const int grp = (threadIdx.x & 31) >> 3;  // four outputs per warp
+  const long long warp = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long base = warp * 4; base < n; base += nwarps * 4) {  // warp-uniform loop
+    const long long i = base + grp;
     float acc = 0.f;
-#pragma unroll 8
-    for (int s = 0; s < S; ++s) acc += __ldg(part + (long long)s * n + i);
-    out[i] = acc;
+    if (i < n) {
+#pragma unroll 4
+      for (int s = q; s < S; s += 8) acc += __ldg(part + (long long)s * n + i);
+    }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    if (q == 0 && i < n) out[i] = acc;
   }
 }
 
@@ -171,10 +183,12 @@ DwPlan dw_plan(int T, int H, int E) {
   p.cpt = 64 / p.eb;
   p.col_blocks = (H + DW_THREADS * p.cpt - 1) / (DW_THREADS * p.cpt);
   p.exp_blocks = (E + p.eb - 1) / p.eb;
-  long long want = (320 + p.col_blocks * p.exp_blocks - 1) / (p.col_blocks * p.exp_blocks);
-  long long by_t = (T + 15) / 16;
+  // about two CTAs per SM of a 152-SM GPU (a fixed target keeps the workspace
+  // size a function of the shapes alone)
+  long long want = (304 + p.col_blocks * p.exp_blocks - 1) / (p.col_blocks * p.exp_blocks);
+  long long by_t = (T + 7) / 8;
   long long s = want < by_t ? want : by_t;
-  if (s > 128) s = 128;
+  if (s > 256) s = 256;
   if (s < 1) s = 1;
   p.splits = (int)s;
   p.rows_per_split = (T + p.splits - 1) / p.splits;
@@ -199,6 +213,116 @@ template <> __device__ __forceinline__ void load_cols<float>(const float* p, int
   } else {
 #pragma unroll
     for (int j = 0; j < 8; ++j) if (j < n) v[j] = p[j];
+  }
+}
+
+// E <= 8: a thread owns 8 columns x 8 experts and streams its own x columns
+// through a private slot of a DW8_NS-stage shared-memory ring with cp.async
+// (16-byte copies, zero-filled past the tensor), so DW8_NS * DW8_RB tokens per
+// thread are in flight without holding registers.  The slot layout
+// [stage][row][chunk][thread] keeps every access conflict-free, and since no
+// thread reads another's slot no block barrier is needed.
+constexpr int DW8_NS = 3;
+template <typename T> struct Dw8 {
+  static constexpr int CH = sizeof(T) == 2 ? 1 : 2;  // 16-byte chunks per row (8 columns)
+  static constexpr int RB = sizeof(T) == 2 ? 8 : 4;  // rows per stage
+  static constexpr int STAGE = RB * CH * DW_THREADS;  // uint4 per stage
+};
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
+  const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  const int src_size = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(gmem), "r"(src_size) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N> __device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <typename T>
+__global__ void __launch_bounds__(DW_THREADS, 2)
+router_dw8_kernel(const T* __restrict__ x, const float* __restrict__ dl, int Tn, int H, int E,
+                  int rows_per_split, float* __restrict__ part) {
+  using P = Dw8<T>;
+  extern __shared__ uint4 ring[];  // [DW8_NS][RB][CH][DW_THREADS]
+  const int tid = threadIdx.x;
+  const int h0 = (blockIdx.x * DW_THREADS + tid) * 8;
+  const bool col_ok = h0 < H;
+  const int split = blockIdx.z;
+  const int t_begin = split * rows_per_split;
+  const int t_end = min(Tn, t_begin + rows_per_split);
+  const int nb = t_end > t_begin ? (t_end - t_begin + P::RB - 1) / P::RB : 0;
+  auto issue = [&](int blk) {
+    const int stage = blk % DW8_NS;
+#pragma unroll
+    for (int r = 0; r < P::RB; ++r) {
+      const int t = t_begin + blk * P::RB + r;
+      const bool ok = col_ok && blk < nb && t < t_end;
+      const T* src = x + (ok ? (long long)t * H + h0 : 0);
+#pragma unroll
+      for (int c = 0; c < P::CH; ++c) {
+        // chunk c holds columns h0 + c*V .. h0 + (c+1)*V - 1 (V = 16 / sizeof(T))
+        const bool okc = ok && h0 + (c + 1) * (16 / (int)sizeof(T)) <= H;
+        cp_async16(&ring[((stage * P::RB + r) * P::CH + c) * DW_THREADS + tid],
+                   reinterpret_cast<const uint4*>(src) + (okc ? c : 0), okc);
+      }
+    }
+  };
+  float acc[8][8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[j][e] = 0.f;
+#pragma unroll
+  for (int s = 0; s < DW8_NS - 1; ++s) {
+    issue(s);
+    cp_async_commit();
+  }
+  for (int b = 0; b < nb; ++b) {
+    issue(b + DW8_NS - 1);
+    cp_async_commit();
+    cp_async_wait<DW8_NS - 1>();
+    const int stage = b % DW8_NS;
+#pragma unroll
+    for (int r = 0; r < P::RB; ++r) {
+      const int t = t_begin + b * P::RB + r;
+      if (t >= t_end) break;
+      float xv[8];
+      if (sizeof(T) == 2) {
+        Vec16<bf16>::load_raw_unpack(ring[((stage * P::RB + r) * P::CH) * DW_THREADS + tid], xv);
+      } else {
+#pragma unroll
+        for (int c = 0; c < P::CH; ++c) {
+          const uint4 q = ring[((stage * P::RB + r) * P::CH + c) * DW_THREADS + tid];
+          xv[4 * c] = __uint_as_float(q.x); xv[4 * c + 1] = __uint_as_float(q.y);
+          xv[4 * c + 2] = __uint_as_float(q.z); xv[4 * c + 3] = __uint_as_float(q.w);
+        }
+      }
+      float dv[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) dv[e] = e < E ? __ldg(dl + (long long)t * E + e) : 0.f;
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[j][e] = fmaf(xv[j], dv[e], acc[j][e]);
+    }
+  }
+  cp_async_wait<0>();
+  if (!col_ok) return;
+  float* out = part + (long long)split * H * E + (long long)h0 * E;
+  const int ncol = min(8, H - h0);
+  if (E == 8 && ncol == 8) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      reinterpret_cast<float4*>(out)[2 * j] = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
+      reinterpret_cast<float4*>(out)[2 * j + 1] = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        if (j < ncol && e < E) out[j * E + e] = acc[j][e];
   }
 }
 
@@ -275,6 +399,31 @@ constexpr int DX_TR = 32, DX_HB = 256, DX_EC = 32, DX_THREADS = 256;
 
 constexpr int DX_RT = 4;  // row tiles per CTA
 
+// four consecutive values of the storage type (8 bytes of bf16, 16 of fp32);
+// an invalid load yields zeros
+template <typename T> __device__ __forceinline__ void load4(const T* p, bool ok, float* v);
+template <> __device__ __forceinline__ void load4<bf16>(const bf16* p, bool ok, float* v) {
+  uint2 q = ok ? __ldg(reinterpret_cast<const uint2*>(p)) : make_uint2(0, 0);
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+  float2 a = __bfloat1622float2(h[0]), b = __bfloat1622float2(h[1]);
+  v[0] = a.x; v[1] = a.y; v[2] = b.x; v[3] = b.y;
+}
+template <> __device__ __forceinline__ void load4<float>(const float* p, bool ok, float* v) {
+  float4 q = ok ? __ldg(reinterpret_cast<const float4*>(p)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
+}
+template <typename T> __device__ __forceinline__ void store4(T* p, const float* v);
+template <> __device__ __forceinline__ void store4<bf16>(bf16* p, const float* v) {
+  uint2 q;
+  __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&q);
+  h[0] = __floats2bfloat162_rn(v[0], v[1]);
+  h[1] = __floats2bfloat162_rn(v[2], v[3]);
+  *reinterpret_cast<uint2*>(p) = q;
+}
+template <> __device__ __forceinline__ void store4<float>(float* p, const float* v) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+}
+
 template <typename T>
 __global__ void __launch_bounds__(DX_THREADS)
 router_dx_kernel(const float* __restrict__ dl, const T* __restrict__ w, int Tn, int H, int E, bool write,
@@ -284,8 +433,11 @@ router_dx_kernel(const float* __restrict__ dl, const T* __restrict__ w, int Tn, 
   const int hb = blockIdx.x * DX_HB;
   const int c = threadIdx.x & 31;
   const int r0 = threadIdx.x >> 5;  // 0..7; rows r0, r0+8, r0+16, r0+24 of a tile
-  const int h = hb + 8 * c;
-  const int ncol = h < H ? min(8, H - h) : 0;  // 8, or 4 for fp32 rows with H % 8 == 4
+  // a thread owns columns hb+4c..+3 and hb+128+4c..+3: consecutive lanes read
+  // consecutive 16-byte words of ws (no bank conflicts) and a warp's stores of
+  // each 4-column group are contiguous; H % 4 == 0 makes each group all-in or all-out
+  const int ha = hb + 4 * c, hbb = hb + 128 + 4 * c;
+  const bool oka = ha < H, okb = hbb < H;
   const bool one_chunk = E <= DX_EC;
   auto stage_w = [&](int e0) {
     const int ne = min(DX_EC, E - e0);
@@ -316,8 +468,8 @@ router_dx_kernel(const float* __restrict__ dl, const T* __restrict__ w, int Tn, 
       __syncthreads();
       for (int e = 0; e < ne; ++e) {
         float wv[8];
-        const float4 a = *reinterpret_cast<const float4*>(&ws[e][8 * c]);
-        const float4 b = *reinterpret_cast<const float4*>(&ws[e][8 * c + 4]);
+        const float4 a = *reinterpret_cast<const float4*>(&ws[e][4 * c]);
+        const float4 b = *reinterpret_cast<const float4*>(&ws[e][128 + 4 * c]);
         wv[0] = a.x; wv[1] = a.y; wv[2] = a.z; wv[3] = a.w; wv[4] = b.x; wv[5] = b.y; wv[6] = b.z; wv[7] = b.w;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -327,34 +479,25 @@ router_dx_kernel(const float* __restrict__ dl, const T* __restrict__ w, int Tn, 
         }
       }
     }
-    if (ncol == 0) continue;
+    float old[4][8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {  // all read-modify-write loads first
+      const int t = tb + r0 + 8 * i;
+      const bool rok = t < Tn && !write;
+      const T* p = dx + (long long)t * H;
+      load4<T>(p + ha, rok && oka, old[i]);
+      load4<T>(p + hbb, rok && okb, old[i] + 4);
+    }
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const int t = tb + r0 + 8 * i;
       if (t >= Tn) continue;
-      T* p = dx + (long long)t * H + h;
+      T* p = dx + (long long)t * H;
       float v[8];
-      if (!write) {
-        float old[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        load_cols<T>(p, ncol, old);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = old[j] + acc[i][j];
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = acc[i][j];
-      }
-      if (ncol == 8) {
-        if (sizeof(T) == 2) {
-          Vec16<T>::store(p, v);
-        } else {
-          Vec16<T>::store(p, v);
-          Vec16<T>::store(p + 4, v + 4);
-        }
-      } else {
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (j < ncol) p[j] = from_f32<T>(v[j]);
-      }
+      for (int j = 0; j < 8; ++j) v[j] = old[i][j] + acc[i][j];
+      if (oka) store4<T>(p + ha, v);
+      if (okb) store4<T>(p + hbb, v + 4);
     }
   }
 }
@@ -401,15 +544,20 @@ template <typename T>
 int launch_dw(const T* x, const float* dl, int Tn, int H, int E, float* part, float* dw, cudaStream_t s) {
   const DwPlan pl = dw_plan(Tn, H, E);
   dim3 grid(pl.col_blocks, pl.exp_blocks, pl.splits);
-  if (pl.eb == 8) router_dw_partial_kernel<T, 8, 8><<<grid, DW_THREADS, 0, s>>>(x, dl, Tn, H, E, pl.rows_per_split, part);
-  else if (pl.eb == 16) router_dw_partial_kernel<T, 4, 16><<<grid, DW_THREADS, 0, s>>>(x, dl, Tn, H, E, pl.rows_per_split, part);
+  if (pl.eb == 8) {
+    const int smem = DW8_NS * Dw8<T>::STAGE * (int)sizeof(uint4);
+    if (cudaFuncSetAttribute(router_dw8_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    router_dw8_kernel<T><<<grid, DW_THREADS, smem, s>>>(x, dl, Tn, H, E, pl.rows_per_split, part);
+  } else if (pl.eb == 16) router_dw_partial_kernel<T, 4, 16><<<grid, DW_THREADS, 0, s>>>(x, dl, Tn, H, E, pl.rows_per_split, part);
   else if (pl.eb == 32) router_dw_partial_kernel<T, 2, 32><<<grid, DW_THREADS, 0, s>>>(x, dl, Tn, H, E, pl.rows_per_split, part);
   else router_dw_partial_kernel<T, 1, 64><<<grid, DW_THREADS, 0, s>>>(x, dl, Tn, H, E, pl.rows_per_split, part);
   int st = launch_status();
   if (st != MOE_OK) return st;
   const long long n = (long long)H * E;
-  const int rgrid = (int)((n + 63) / 64 < 8192 ? (n + 63) / 64 : 8192);
-  reduce_splits_kernel<<<rgrid, 64, 0, s>>>(part, pl.splits, n, dw);
+  const long long thr = n * 8;
+  const int rgrid = (int)((thr + 255) / 256 < 16384 ? (thr + 255) / 256 : 16384);
+  reduce_splits_kernel<<<rgrid, 256, 0, s>>>(part, pl.splits, n, dw);
   return launch_status();
 }
 

@@ -52,6 +52,14 @@ template <> struct Vec16<bf16> {
       v[2 * i] = f.x; v[2 * i + 1] = f.y;
     }
   }
+  __device__ __forceinline__ static void load_raw_unpack(const uint4& q, float* v) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&q);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 f = __bfloat1622float2(h[i]);
+      v[2 * i] = f.x; v[2 * i + 1] = f.y;
+    }
+  }
   __device__ __forceinline__ static void store(bf16* p, const float* v) {
     uint4 q;
     __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&q);
