@@ -1,27 +1,31 @@
-"""Benchmark of the MoE layer hot path on GB300.
+"""Benchmark of the MoE / MoD layer hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--bias-target MAXVIO]
+                    [--workload NAME] [--bias-target MAXVIO|none]
 
-A step is one pass of the layer on one batch of synthetic input: router GEMM +
-softmax/top-K, dispatch (histogram, cu_seqlens, permutation, gather), grouped
-SwiGLU expert FFN, combine, and the gate/dispatch backward (moe_permute_bwd +
-moe_route_bwd).  The default workload is the Mixtral-shaped bf16 layer
-(4 x 2048 tokens, H=4096, E=8, K=2, H'=14336, uniform router).
+A step is one pass of the layer over one batch of synthetic input:
+  * Mixtral-shaped and fine-grained layers: router GEMM + softmax/top-K,
+    dispatch (histogram, cu_seqlens, permutation, gather), grouped SwiGLU
+    expert FFN, combine, then the gate/dispatch backward (moe_permute_bwd +
+    moe_route_bwd) with a synthetic expert-input gradient;
+  * expert-parallel benchmark shapes (E=384): the forward only;
+  * MoD + MoE: mod_select, the MoE forward on the selected tokens with the
+    score-scaled residual combine, then the route backward of both routers.
+The default workload is the Mixtral-shaped bf16 layer (4 x 2048 tokens, H=4096,
+E=8, K=2, H'=14336) with the router skewed to maxvio 0.2 by an expert-0 logit
+bias from tests/golden/skew_bias.json.
 
 Multi-GPU runs (torchrun) are replicas: every rank processes its own batch with
 no data-path collective; `value` is all ranks' tokens over the slowest rank's
 time ("scaling": "weak").
 
 `--impl reference` times the CPU oracle (float64, numpy) on the host cores on a
-bounded token sample of the same workload per step; under torchrun only rank 0
-runs it.
+bounded sample of the same workload per step; under torchrun only rank 0 runs.
 """
 from __future__ import annotations
 
 import argparse
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -33,8 +37,8 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-METRIC = "MoE layer tokens/s (fwd + gate/dispatch bwd)"
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
+DEFAULT_WORKLOAD = "mixtral_bf16_T8192_H4096_E8_K2_Hp14336"
 
 
 def parse():
@@ -43,30 +47,50 @@ def parse():
     p.add_argument("--steps", type=int, default=50)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="mixtral_bf16_T8192_H4096_E8_K2_Hp14336")
-    p.add_argument("--bias-target", type=float, default=None,
-                   help="router skew target (maxvio) from tests/golden/skew_bias.json")
+    p.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    p.add_argument("--bias-target", default="auto",
+                   help="router skew (maxvio) from tests/golden/skew_bias.json; 'none' for the natural "
+                        "router; 'auto' = 0.2 where the table has it")
     p.add_argument("--cpu-sample-tokens", type=int, default=None)
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
 
 
 def dist_env():
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return rank, world, local
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def mode_of(shape):
+    from token_dispatch_gb300 import synth
+    if shape.mod_B:
+        return "mod"
+    if shape.name == synth.EPBENCH_BF16.name:
+        return "fwd"
+    return "fwd_bwd"
+
+
+METRICS = {"fwd_bwd": "MoE layer tokens/s (fwd + gate/dispatch bwd)",
+           "fwd": "MoE layer tokens/s (fwd)",
+           "mod": "MoD+MoE layer tokens/s (fwd + route bwd)"}
 
 
 def skew_bias(shape, target):
-    if target is None:
-        return None, None
+    """(bias [E] or None, table entry or None, target used)."""
     path = os.path.join(ROOT, "tests", "golden", "skew_bias.json")
     with open(path) as fh:
         table = json.load(fh)
-    entry = table[shape.name][f"{target:g}"]
+    entries = table.get(shape.name, {})
+    if target in (None, "none"):
+        return None, None, None
+    if target == "auto":
+        if "0.2" not in entries:
+            return None, None, None
+        target = "0.2"
+    key = f"{float(target):g}"
+    entry = entries[key]
     from token_dispatch_gb300 import synth
-    return synth.expert_bias(shape.E, entry["beta"], expert=0), entry
+    return synth.expert_bias(shape.E, entry["beta"], expert=0), entry, float(key)
 
 
 class Clocks:
@@ -123,23 +147,33 @@ class Clocks:
 
 def algorithmic_bytes(shape):
     """Minimum HBM bytes each HBM-bound call must move (read + write), from its
-    definition: b = storage bytes, R = T*K rows; indices and gates are 4 bytes."""
+    definition: b = storage bytes, R = T*K rows; indices, gates and scores are 4
+    bytes.  For the MoD workload T is the selected tokens (B*C)."""
     T, H, E, K = shape.T, shape.H, shape.E, shape.K
     R = T * K
     b = 2 if shape.dtype == "bf16" else 4
-    return {
+    out = {
         # x, W_r in; logits, idx, gate out
         "route": T * H * b + H * E * b + T * E * 4 + 2 * T * K * 4,
         # idx in; x in once; xs, dst_row, src_tok, cu out
         "dispatch": T * K * 4 + T * H * b + R * H * b + 2 * R * 4 + (E + 1) * 4,
-        # h, gate, dst_row in; y out
-        "combine": R * H * b + T * K * 4 + R * 4 + T * H * b,
+        # h, gate, dst_row in; y out (MoD: also the score and the residual rows)
+        "combine": R * H * b + T * K * 4 + R * 4 + T * H * b + (T * (H * b + 8) if shape.mod_B else 0),
         # dy, h, dxs, gate, dst_row in; dh, dx, d_gate out
         "permute_bwd": T * H * b + 3 * R * H * b + T * H * b + T * K * 4 + R * 4 + T * K * 4,
         # d_gate, logits, idx, x, W_r in; d_logits, dW out; dx read + written
         "route_bwd": T * K * 4 + T * E * 4 + T * K * 4 + T * H * b + H * E * b + T * E * 4 + H * E * 4
                      + 2 * T * H * b,
     }
+    if shape.mod_B:
+        n = shape.mod_B * shape.mod_L
+        # x read once, w_mod; score, mask, sel, sel_score out; x_sel and the skip rows written
+        out["mod_select"] = n * H * b + H * b + n * 4 + n + 2 * T * 4 + T * H * b + (n - T) * H * b
+        # MoD route backward: dy (selected rows), h in; dh, d_gate, d_score out (no dxs)
+        out["permute_bwd"] = T * H * b + 2 * R * H * b + T * K * 4 + R * 4 + T * K * 4 + T * 4 + T * 4
+        out["route_bwd"] = out["route_bwd"]
+        out["mod_route_bwd"] = T * 4 + T * H * b + H * b + H * 4 + 2 * T * H * b
+    return out
 
 
 def measured_peaks():
@@ -152,10 +186,101 @@ def measured_peaks():
 
 # --------------------------------------------------------------------------- ours
 
+def build_inputs(shape, dev, rank, bias_np):
+    """Routing inputs from the host generator (each rank its own batch), expert
+    weights and the synthetic upstream gradients drawn on the device."""
+    import torch
+    from token_dispatch_gb300 import synth
+    mode = mode_of(shape)
+    n_tok = shape.mod_B * shape.mod_L if shape.mod_B else shape.T
+    tdt = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
+    x, wr = synth.router_inputs(shape, seed=rank, tokens=n_tok)
+    wg, wu, wd = synth.expert_weights_device(shape, dev, seed=0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1000 + rank)
+    inp = dict(x=x, wr=wr, wg=wg, wu=wu, wd=wd, bias=bias_np, mode=mode, n_tok=n_tok)
+    if mode == "fwd_bwd":
+        inp["dy"] = torch.randn((shape.T, shape.H), generator=g, device=dev).to(tdt)
+        inp["dxs"] = torch.randn((shape.R, shape.H), generator=g, device=dev).to(tdt)
+    elif mode == "mod":
+        inp["wmod"] = synth.mod_weight(shape, seed=rank)
+        inp["dy"] = torch.randn((n_tok, shape.H), generator=g, device=dev).to(tdt)
+    return inp
+
+
+def make_step(shape, inp, dev, stream):
+    """(call names, step(x, dy, dxs, marks) -> None, buffers, outputs for the host)."""
+    import torch
+    from token_dispatch_gb300 import _lib as L
+    from token_dispatch_gb300 import layer
+    T, H, E, K, Hp = shape.T, shape.H, shape.E, shape.K, shape.Hp
+    R = T * K
+    mode = inp["mode"]
+    wr_d = inp["wr"].host.to(dev)
+    bias_d = None if inp["bias"] is None else torch.from_numpy(inp["bias"]).to(dev)
+    wg, wu, wd = inp["wg"], inp["wu"], inp["wd"]
+
+    if mode in ("fwd_bwd", "fwd"):
+        b = layer.MoEBuffers(T, H, E, K, Hp, shape.dtype, dev, backward=(mode == "fwd_bwd"))
+        calls = [
+            ("route", lambda xi, dyi, dxsi: L.moe_route(xi, wr_d, bias_d, T, H, E, K, b.cdt, b.logits, b.idx, b.gate,
+                                                       stream=stream)),
+            ("dispatch", lambda xi, dyi, dxsi: L.moe_dispatch(xi, b.idx, T, H, E, K, b.cdt, b.cu, b.dst_row,
+                                                             b.src_tok, b.xs, b.ws_dispatch, b.ws_dispatch_bytes,
+                                                             stream=stream)),
+            ("expert_ffn", lambda xi, dyi, dxsi: L.moe_expert_ffn(b.xs, b.cu, R, wg, wu, wd, E, H, Hp, b.cdt, b.act,
+                                                                 b.h, stream=stream)),
+            ("combine", lambda xi, dyi, dxsi: L.moe_combine(b.h, b.gate, b.dst_row, None, None, None, T, H, K, b.cdt,
+                                                           b.y, stream=stream)),
+        ]
+        outs = [b.y]
+        if mode == "fwd_bwd":
+            calls += [
+                ("permute_bwd", lambda xi, dyi, dxsi: L.moe_permute_bwd(dyi, b.h, b.gate, b.dst_row, None, None,
+                                                                       dxsi, T, H, K, b.cdt, b.dh, b.d_gate, None,
+                                                                       b.dx, stream=stream)),
+                ("route_bwd", lambda xi, dyi, dxsi: L.moe_route_bwd(L.MOE_ROUTE_SOFTMAX_TOPK, b.d_gate, b.logits,
+                                                                   b.idx, xi, wr_d, T, H, E, K, b.cdt, b.d_logits,
+                                                                   b.dw_router, b.dx, b.ws_bwd, b.ws_bwd_bytes,
+                                                                   stream=stream)),
+            ]
+            outs = [b.y, b.dx, b.dw_router]
+        return calls, b, outs, b.cu
+
+    # MoD + MoE
+    Bq, Lq, C = shape.mod_B, shape.mod_L, shape.mod_C
+    m = layer.MoDBuffers(Bq, Lq, C, H, E, K, Hp, shape.dtype, dev)
+    b = m.moe
+    wmod_d = inp["wmod"].host.to(dev)
+    calls = [
+        ("mod_select", lambda xi, dyi, dxsi: L.mod_select(xi, wmod_d, Bq, Lq, H, C, m.cdt, m.score, m.sel,
+                                                         m.sel_score, m.mask, m.x_sel, m.y, stream=stream)),
+        ("route", lambda xi, dyi, dxsi: L.moe_route(m.x_sel, wr_d, bias_d, T, H, E, K, b.cdt, b.logits, b.idx,
+                                                   b.gate, stream=stream)),
+        ("dispatch", lambda xi, dyi, dxsi: L.moe_dispatch(m.x_sel, b.idx, T, H, E, K, b.cdt, b.cu, b.dst_row,
+                                                         b.src_tok, b.xs, b.ws_dispatch, b.ws_dispatch_bytes,
+                                                         stream=stream)),
+        ("expert_ffn", lambda xi, dyi, dxsi: L.moe_expert_ffn(b.xs, b.cu, R, wg, wu, wd, E, H, Hp, b.cdt, b.act,
+                                                             b.h, stream=stream)),
+        ("combine", lambda xi, dyi, dxsi: L.moe_combine(b.h, b.gate, b.dst_row, m.sel_score, xi, m.sel, T, H, K,
+                                                       b.cdt, m.y, stream=stream)),
+        ("permute_bwd", lambda xi, dyi, dxsi: L.moe_permute_bwd(dyi, b.h, b.gate, b.dst_row, m.sel_score, m.sel,
+                                                               None, T, H, K, b.cdt, b.dh, b.d_gate, m.d_score,
+                                                               None, stream=stream)),
+        ("route_bwd", lambda xi, dyi, dxsi: L.moe_route_bwd(L.MOE_ROUTE_SOFTMAX_TOPK | L.MOE_ROUTE_DX_WRITE,
+                                                           b.d_gate, b.logits, b.idx, m.x_sel, wr_d, T, H, E, K,
+                                                           b.cdt, b.d_logits, b.dw_router, b.dx, b.ws_bwd,
+                                                           b.ws_bwd_bytes, stream=stream)),
+        ("mod_route_bwd", lambda xi, dyi, dxsi: L.moe_route_bwd(L.MOE_ROUTE_MOD_LINEAR, m.d_score, None, None,
+                                                               m.x_sel, wmod_d, T, H, 1, 1, b.cdt, None, m.dw_mod,
+                                                               b.dx, m.ws_lin, m.ws_lin_bytes, stream=stream)),
+    ]
+    return calls, m, [m.y, m.dw_mod, b.dw_router], b.cu
+
+
 def run_ours(args, shape, rank, world, local):
     import torch
     from token_dispatch_gb300 import _lib as L
-    from token_dispatch_gb300 import layer, synth
 
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -165,47 +290,25 @@ def run_ours(args, shape, rank, world, local):
 
     T, H, E, K, Hp = shape.T, shape.H, shape.E, shape.K, shape.Hp
     R = T * K
-    tdt = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
-    bias_np, bias_entry = skew_bias(shape, args.bias_target)
-
-    # inputs: routing inputs from the host generator (each rank its own batch),
-    # expert weights and the synthetic upstream gradients drawn on the device
-    x, wr = synth.router_inputs(shape, seed=rank)
-    x_h = x.host.pin_memory()
-    wr_d = wr.host.to(dev)
-    bias_d = None if bias_np is None else torch.from_numpy(bias_np).to(dev)
-    wg, wu, wd = synth.expert_weights_device(shape, dev, seed=0)
-    g = torch.Generator(device=dev)
-    g.manual_seed(1000 + rank)
-    dy_d = torch.randn((T, H), generator=g, device=dev, dtype=torch.float32).to(tdt)
-    dxs_d = torch.randn((R, H), generator=g, device=dev, dtype=torch.float32).to(tdt)
+    bias_np, bias_entry, target = skew_bias(shape, args.bias_target)
+    inp = build_inputs(shape, dev, rank, bias_np)
+    mode = inp["mode"]
+    n_tok = inp["n_tok"]
+    x_h = inp["x"].host.pin_memory()
     x_d = x_h.to(dev)
-    b = layer.MoEBuffers(T, H, E, K, Hp, shape.dtype, dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    dy_d, dxs_d = inp.get("dy"), inp.get("dxs")
     stream = torch.cuda.Stream(device=dev)
+    calls, bufs, outs, cu = make_step(shape, inp, dev, stream)
+    names = [n for n, _ in calls]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
 
-    names = ("route", "dispatch", "expert_ffn", "combine", "permute_bwd", "route_bwd")
-
-    def step(xin, dyin, dxsin, ev=None):
-        def mark(i):
+    def step(xi, dyi, dxsi, ev=None):
+        for j, (_, fn) in enumerate(calls):
             if ev is not None:
-                ev[i].record(stream)
-        mark(0)
-        L.moe_route(xin, wr_d, bias_d, T, H, E, K, b.cdt, b.logits, b.idx, b.gate, stream=stream)
-        mark(1)
-        L.moe_dispatch(xin, b.idx, T, H, E, K, b.cdt, b.cu, b.dst_row, b.src_tok, b.xs, b.ws_dispatch,
-                       b.ws_dispatch_bytes, stream=stream)
-        mark(2)
-        L.moe_expert_ffn(b.xs, b.cu, R, wg, wu, wd, E, H, Hp, b.cdt, b.act, b.h, stream=stream)
-        mark(3)
-        L.moe_combine(b.h, b.gate, b.dst_row, None, None, None, T, H, K, b.cdt, b.y, stream=stream)
-        mark(4)
-        L.moe_permute_bwd(dyin, b.h, b.gate, b.dst_row, None, None, dxsin, T, H, K, b.cdt, b.dh, b.d_gate,
-                          None, b.dx, stream=stream)
-        mark(5)
-        L.moe_route_bwd(L.MOE_ROUTE_SOFTMAX_TOPK, b.d_gate, b.logits, b.idx, xin, wr_d, T, H, E, K, b.cdt,
-                        b.d_logits, b.dw_router, b.dx, b.ws_bwd, b.ws_bwd_bytes, stream=stream)
-        mark(6)
+                ev[j].record(stream)
+            fn(xi, dyi, dxsi)
+        if ev is not None:
+            ev[len(calls)].record(stream)
 
     def barrier():
         if world > 1:
@@ -219,14 +322,14 @@ def run_ours(args, shape, rank, world, local):
     st = L.moe_last_device_error(stream)
     if st != L.MOE_OK:
         raise RuntimeError(f"device error after warm-up: {L.moe_status_str(st)}")
-
-    counts = np.diff(b.cu.cpu().numpy().astype(np.int64))
+    counts = np.diff(cu.cpu().numpy().astype(np.int64))
     maxvio = float(counts.max() / (R / E) - 1.0)
 
     clocks = Clocks(local)
     clocks.start()
     time.sleep(0.3)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(args.steps)]
+    nc = len(calls)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(nc + 1)] for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize(dev)
     launches0 = L.moe_kernel_launches()
@@ -237,41 +340,37 @@ def run_ours(args, shape, rank, world, local):
     torch.cuda.synchronize(dev)
     barrier()
     launches = L.moe_kernel_launches() - launches0
-    step_ms = [evs[i][0].elapsed_time(evs[i][6]) for i in range(args.steps)]
+    step_ms = [evs[i][0].elapsed_time(evs[i][nc]) for i in range(args.steps)]
     call_ms = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
                for j, n in enumerate(names)}
     ms = statistics.mean(step_ms)
 
-    # end to end through the public API: pinned host inputs in, results out, every step
-    dy_h = dy_d.cpu().pin_memory()
-    dxs_h = dxs_d.cpu().pin_memory()
-    y_h = torch.empty((T, H), dtype=tdt).pin_memory()
-    dx_h = torch.empty((T, H), dtype=tdt).pin_memory()
-    dw_h = torch.empty((H, E), dtype=torch.float32).pin_memory()
-    x_in = torch.empty_like(x_d)
-    dy_in = torch.empty_like(dy_d)
-    dxs_in = torch.empty_like(dxs_d)
+    # end to end through the public API: every step copies its inputs from pinned
+    # host memory and its results back
+    host_in = [(x_h, torch.empty_like(x_d))]
+    if dy_d is not None:
+        host_in.append((dy_d.cpu().pin_memory(), torch.empty_like(dy_d)))
+    if dxs_d is not None:
+        host_in.append((dxs_d.cpu().pin_memory(), torch.empty_like(dxs_d)))
+    host_out = [(o, torch.empty(o.shape, dtype=o.dtype).pin_memory()) for o in outs]
     e2e_steps = max(3, min(args.steps, 20))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize(dev)
     with torch.cuda.stream(stream):
         e0.record(stream)
         for _ in range(e2e_steps):
-            x_in.copy_(x_h, non_blocking=True)
-            dy_in.copy_(dy_h, non_blocking=True)
-            dxs_in.copy_(dxs_h, non_blocking=True)
-            step(x_in, dy_in, dxs_in)
-            y_h.copy_(b.y, non_blocking=True)
-            dx_h.copy_(b.dx, non_blocking=True)
-            dw_h.copy_(b.dw_router, non_blocking=True)
+            for h, d in host_in:
+                d.copy_(h, non_blocking=True)
+            step(host_in[0][1], host_in[1][1] if len(host_in) > 1 else None,
+                 host_in[2][1] if len(host_in) > 2 else None)
+            for d, h in host_out:
+                h.copy_(d, non_blocking=True)
         e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     clk = clocks.stop()
-
-    h2d = x_in.numel() * x_in.element_size() + dy_in.numel() * dy_in.element_size() + \
-        dxs_in.numel() * dxs_in.element_size()
-    d2h = y_h.numel() * y_h.element_size() + dx_h.numel() * dx_h.element_size() + dw_h.numel() * 4
+    h2d = sum(d.numel() * d.element_size() for _, d in host_in)
+    d2h = sum(h.numel() * h.element_size() for _, h in host_out)
 
     if world > 1:
         import torch.distributed as dist
@@ -281,18 +380,18 @@ def run_ours(args, shape, rank, world, local):
 
     peaks, peak_src = measured_peaks()
     ffn_flops = 6.0 * R * H * Hp
-    ffn_ms = call_ms["expert_ffn"]
-    tflops = ffn_flops / (ffn_ms * 1e-3) / 1e12
+    tflops = ffn_flops / (call_ms["expert_ffn"] * 1e-3) / 1e12
     # the timed region is well under a second: the burst peak applies
     peak_tf = peaks.get("bf16_tflops", 1900.0) if shape.dtype == "bf16" else None
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
     hbm = {}
     for name, nbytes in algorithmic_bytes(shape).items():
-        gbs = nbytes / (call_ms[name] * 1e-3) / 1e9
-        hbm[name] = {"bytes": nbytes, "GB/s": round(gbs, 1), "frac": round(gbs / hbm_peak, 4)}
+        if name in call_ms:
+            gbs = nbytes / (call_ms[name] * 1e-3) / 1e9
+            hbm[name] = {"bytes": nbytes, "GB/s": round(gbs, 1), "frac": round(gbs / hbm_peak, 4)}
     result = {
-        "metric": METRIC,
-        "value": world * T / (ms * 1e-3),
+        "metric": METRICS[mode],
+        "value": world * n_tok / (ms * 1e-3),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -303,38 +402,48 @@ def run_ours(args, shape, rank, world, local):
         "vs_baseline": None,
         "dtype": shape.dtype,
         "data": "synthetic",
-        "config": {"workload": shape.name, "tokens_per_gpu": T, "H": H, "E": E, "K": K, "Hp": Hp,
-                   "maxvio": round(maxvio, 4), "bias_target": args.bias_target,
+        "config": {"workload": shape.name, "tokens_per_gpu": n_tok, "moe_tokens": T, "H": H, "E": E, "K": K,
+                   "Hp": Hp, "maxvio": round(maxvio, 4), "maxvio_target": target,
+                   "expert0_logit_bias": None if bias_entry is None else bias_entry["beta"],
                    "l2": "flushed between timed steps (512 MB write)", "parallelism": f"replicas{world}"},
         "calls_ms": {k: round(v, 4) for k, v in call_ms.items()},
-        "roofline": {"kernel": "moe_expert_ffn (grouped gate/up+SwiGLU GEMM + down GEMM)",
+        "roofline": {"kernel": "moe_expert_ffn (grouped gate/up+SwiGLU GEMM + down GEMM, tcgen05)",
                      "bound": "tensor", "achieved": tflops, "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": (tflops / peak_tf) if peak_tf else None, "traffic": None,
                      "peak_source": f"{peak_src} bf16_tflops (burst)"},
         "hbm_roofline": {"peak_GB/s": hbm_peak, "peak_source": f"{peak_src} hbm_gbs", "calls": hbm},
-        "e2e": {"value": world * T / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": world * n_tok / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches,
         "clocks": clk,
     }
-    return result, dict(x=x, wr=wr, wg=wg, wu=wu, wd=wd, bias=bias_np, dy=dy_d, dxs=dxs_d, dev=dev)
+    return result, inp
 
 
 # ----------------------------------------------------------------- CPU oracle arm
 
-def oracle_sample(shape, inputs, n_tok, reps=1):
-    """Time the CPU oracle (fwd + gate/dispatch bwd) on the first n_tok tokens."""
-    import torch
+def oracle_sample(shape, inp, n_tok, reps=1):
+    """Time the CPU oracle on a bounded sample of the step: the first n_tok tokens
+    (MoE workloads) or the first sequence (MoD workload).  Returns (times, tokens)."""
     import oracle as O
     from token_dispatch_gb300 import synth
+    mode = inp["mode"]
+    bias = None if inp["bias"] is None else inp["bias"].astype(np.float64)
+    wr64 = inp["wr"].ref
+    if mode == "mod":
+        n_tok = shape.mod_L
+    x64 = inp["x"].ref[:n_tok]
 
-    x64 = inputs["x"].ref[:n_tok]
-    wr64 = inputs["wr"].ref
-    bias = None if inputs["bias"] is None else inputs["bias"].astype(np.float64)
-    idx = O.topk_experts(O.router_logits(x64, wr64, bias), shape.K)
-    experts = sorted(set(idx.reshape(-1).tolist()))
+    # the experts this sample visits, copied to the host in float64
+    if mode == "mod":
+        s = O.mod_scores(x64, inp["wmod"].ref)
+        sel, _ = O.mod_select(s, 1, shape.mod_L, shape.mod_C)
+        xr = x64[sel[0]]
+    else:
+        xr = x64
+    experts = sorted(set(O.topk_experts(O.router_logits(xr, wr64, bias), shape.K).reshape(-1).tolist()))
 
-    class Experts:  # host float64 copies of the experts this sample visits
+    class Experts:
         def __init__(self, w):
             self.shape = tuple(w.shape)
             self.a = dict(zip(experts, synth.weights_to_host(w, experts)))
@@ -342,16 +451,25 @@ def oracle_sample(shape, inputs, n_tok, reps=1):
         def __getitem__(self, e):
             return self.a[e]
 
-    wg, wu, wd = Experts(inputs["wg"]), Experts(inputs["wu"]), Experts(inputs["wd"])
-    dy = inputs["dy"][:n_tok].float().cpu().numpy().astype(np.float64)
-    dxs = inputs["dxs"][:n_tok * shape.K].float().cpu().numpy().astype(np.float64)
+    wg, wu, wd = Experts(inp["wg"]), Experts(inp["wu"]), Experts(inp["wd"])
+    dy = None if "dy" not in inp else inp["dy"][:n_tok].float().cpu().numpy().astype(np.float64)
+    dxs = None if "dxs" not in inp else inp["dxs"][:n_tok * shape.K].float().cpu().numpy().astype(np.float64)
     times = []
     for _ in range(reps):
         t0 = time.perf_counter()
-        f = O.moe_forward(x64, wr64, wg, wu, wd, shape.K, bias)
-        O.moe_backward(f, dy, dxs, x64, wr64)
+        if mode == "mod":
+            f = O.mod_forward(x64, inp["wmod"].ref, wr64, wg, wu, wd, 1, shape.mod_L, shape.mod_C, shape.K)
+            inner = f["inner"]
+            _, d_gate, d_score, _ = O.permute_bwd(dy, inner["h"], inner["gate"], inner["dst_row"],
+                                                  row_scale=f["score"][f["flat"]], out_row=f["flat"])
+            O.route_bwd_softmax_topk(d_gate, inner["logits"], inner["idx"], f["x_sel"], wr64)
+            O.route_bwd_linear(d_score, f["x_sel"], inp["wmod"].ref)
+        else:
+            f = O.moe_forward(x64, wr64, wg, wu, wd, shape.K, bias)
+            if mode == "fwd_bwd":
+                O.moe_backward(f, dy, dxs, x64, wr64)
         times.append(time.perf_counter() - t0)
-    return times
+    return times, n_tok
 
 
 def cores():
@@ -361,51 +479,50 @@ def cores():
         return os.cpu_count()
 
 
+def default_sample(mode):
+    return {"fwd_bwd": 4096, "fwd": 512, "mod": None}[mode]
+
+
 def main():
     args = parse()
     rank, world, local = dist_env()
     from token_dispatch_gb300 import synth
     shape = synth.WORKLOADS[args.workload]
+    mode = mode_of(shape)
 
     if args.impl == "reference":
         if rank != 0:
             return
         import torch
-        # inputs exactly as the GPU arm draws them (expert weights on the device)
-        from token_dispatch_gb300 import synth as S
         dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
-        x, wr = S.router_inputs(shape, seed=0)
-        wg, wu, wd = S.expert_weights_device(shape, dev, seed=0)
-        g = torch.Generator(device=dev)
-        g.manual_seed(1000)
-        tdt = torch.bfloat16 if shape.dtype == "bf16" else torch.float32
-        n_tok = args.cpu_sample_tokens or 32
-        dy = torch.randn((shape.T, shape.H), generator=g, device=dev, dtype=torch.float32).to(tdt)
-        dxs = torch.randn((shape.T * shape.K, shape.H), generator=g, device=dev, dtype=torch.float32).to(tdt)
-        bias_np, _ = skew_bias(shape, args.bias_target)
-        inputs = dict(x=x, wr=wr, wg=wg, wu=wu, wd=wd, bias=bias_np, dy=dy, dxs=dxs)
-        oracle_sample(shape, inputs, n_tok, reps=max(1, args.warmup))
-        times = oracle_sample(shape, inputs, n_tok, reps=args.steps)
+        bias_np, _, target = skew_bias(shape, args.bias_target)
+        inp = build_inputs(shape, dev, 0, bias_np)  # drawn exactly as the GPU arm draws them
+        n_tok = args.cpu_sample_tokens or {"fwd_bwd": 32, "fwd": 8, "mod": None}[mode]
+        oracle_sample(shape, inp, n_tok, reps=1)
+        times, n_tok = oracle_sample(shape, inp, n_tok, reps=args.steps)
         ms = 1e3 * statistics.mean(times)
         val = n_tok / (ms * 1e-3)
-        out = {"metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-               "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        sample = f"first {n_tok} tokens of the batch per step" if mode != "mod" else \
+            "first sequence (2048 tokens, 1024 selected) per step"
+        out = {"metric": METRICS[mode], "value": val, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+               "warmup": 1, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-               "config": {"workload": shape.name, "bias_target": args.bias_target},
+               "config": {"workload": shape.name, "maxvio_target": target},
                "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
-                                "sample": f"first {n_tok} tokens of the batch per step"},
+                                "sample": sample},
                "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(out))
         return
 
-    result, inputs = run_ours(args, shape, rank, world, local)
+    result, inp = run_ours(args, shape, rank, world, local)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n_tok = args.cpu_sample_tokens or 4096
-        times = oracle_sample(shape, inputs, n_tok, reps=1)
+        n_tok = args.cpu_sample_tokens or default_sample(mode)
+        times, n_tok = oracle_sample(shape, inp, n_tok, reps=1)
+        what = "the first sequence (MoD select + MoE on 1024 tokens + route bwd)" if mode == "mod" else \
+            f"first {n_tok} tokens of the batch ({'fwd + gate/dispatch bwd' if mode == 'fwd_bwd' else 'fwd'})"
         result["cpu_baseline"] = {"value": n_tok / times[0], "unit": "tokens/s", "cores": cores(),
                                   "kind": "oracle",
-                                  "sample": f"first {n_tok} tokens of the batch, fwd + gate/dispatch bwd, "
-                                            f"float64 numpy ({times[0]:.1f} s)"}
+                                  "sample": f"{what}, float64 numpy ({times[0]:.1f} s)"}
     if rank == 0:
         print(json.dumps(result))
     if world > 1:
