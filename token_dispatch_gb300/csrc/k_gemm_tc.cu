@@ -5,6 +5,12 @@
 //       act[r, n] = silu(sum_k xs[r,k] Wg[e][k,n]) * (sum_k xs[r,k] Wu[e][k,n])
 //   * down projection  h[r, n] = sum_k act[r,k] Wd[e][n,k]
 //   * router GEMM      logits[t, e] = sum_h x[t,h] W_r[h,e] + bias[e]   (fp32 out)
+//   * router backward  dW_r[h, e] = sum_t x[t,h] dl[t,e]  (A = x^T read MN-major,
+//                      split over t into fp32 partials) and
+//                      dx[t, h] (+)= sum_e dl[t,e] W_r[h,e]
+//     with the fp32 logit gradient dl carried exactly as three bf16 parts
+//     (dl = hi + mid + lo covers fp32's 24-bit significand): the three products
+//     accumulate into the same fp32 TMEM accumulator.
 // The weights are one contiguous [E, H, H'] tensor per projection and experts are
 // addressed by their index (MoonEP page, "Step-by-step"); the rows of expert e
 // are [cu[e], cu[e+1]) of the expert-sorted activation buffer, read on the device
@@ -55,7 +61,14 @@ struct Params {
   const float* bias;
   unsigned* err;
   unsigned long long wait_limit;  // clock64 cycles
+  int ksplit;                     // K split into this many ranges (fp32 partial outputs)
+  long long part_stride;          // elements between the partial outputs of two splits
+  int accumulate;                 // bf16 output: add the existing values
 };
+
+// Waits for copies and MMAs already in flight when a role stops always use
+// this bound, so a kernel that gave up early still leaves nothing running.
+constexpr unsigned long long DRAIN_LIMIT = 4000000000ull;
 
 // ------------------------------------------------------------------ PTX ----
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -162,16 +175,20 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
   return d;
 }
 
-// Instruction descriptor, kind::f16: D fp32, A = B = bf16, A K-major.
-__host__ __device__ constexpr uint32_t instr_desc(int M, int N, bool b_mn_major) {
-  return (1u << 4) | (1u << 7) | (1u << 10) | ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) |
-         ((uint32_t)(M >> 4) << 24);
+// Instruction descriptor, kind::f16: D fp32, A = B = bf16; bit 15 / 16 select
+// MN-major A / B.
+__host__ __device__ constexpr uint32_t instr_desc(int M, int N, bool a_mn_major, bool b_mn_major) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((a_mn_major ? 1u : 0u) << 15) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-template <int BN, int EPI>
+// NA A tiles and NB B tiles per stage; MMA pair p uses A tile min(p, NA-1) and
+// B tile min(p, NB-1), all into one accumulator.
+template <int BN, int EPI, int NA, int NB>
 struct Cfg {
-  static constexpr int B_STAGE_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+  static constexpr int B_TILE_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = NA * A_STAGE_BYTES + NB * B_TILE_BYTES;
+  static constexpr int NP = NA > NB ? NA : NB;
   static constexpr int OUT_BN = (EPI == EPI_SWIGLU) ? BN / 2 : BN;  // output columns per tile
   static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
                                    : (2 * BN <= 256) ? 256 : 512;
@@ -205,11 +222,11 @@ __device__ __forceinline__ TileInfo decode(int t, const int* mt_pre, int G, int 
   return ti;
 }
 
-template <int EPI, bool B_MN, int BN, int STAGES>
+template <int EPI, bool A_MN, bool B_MN, int BN, int STAGES, int NA, int NB>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmB2, const Params p) {
-  using C = Cfg<BN, EPI>;
+  using C = Cfg<BN, EPI, NA, NB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_base = smem;
@@ -275,7 +292,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     if (lane == 0 && p.cu && (p.cu[0] != 0 || p.cu[G] != p.M)) set_error(p.err, DEV_BOUNDS);
     if (lane == 31) {
       mt_pre[G] = incl;
-      total_tiles_s = incl * n_tiles;
+      total_tiles_s = incl * n_tiles * p.ksplit;
     }
   }
   tc_fence_before();
@@ -283,6 +300,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_slot;
   const int total_tiles = total_tiles_s;
+  const int base_tiles = total_tiles / p.ksplit;  // tiles of one K range
+  const int KB_ALL = (p.K + BK - 1) / BK;
+  // k-blocks [kb_lo, kb_hi) of split s (every split non-empty: ksplit <= KB_ALL)
+  auto kb_lo = [&](int s) { return (int)((long long)s * KB_ALL / p.ksplit); };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -291,30 +312,46 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       uint32_t phase = 0;
       int filled_parity[STAGES];
       for (int s = 0; s < STAGES; ++s) filled_parity[s] = -1;
-      const int KB = (p.K + BK - 1) / BK;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-        const TileInfo ti = decode(t, mt_pre, G, n_tiles, p, C::OUT_BN);
-        for (int kb = 0; kb < KB; ++kb) {
+        const int split = t / base_tiles;
+        const TileInfo ti = decode(t - split * base_tiles, mt_pre, G, n_tiles, p, C::OUT_BN);
+        const int kb_end = kb_lo(split + 1);
+        for (int kb = kb_lo(split); kb < kb_end; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, &abort_flag, p)) { ok = false; break; }
           const uint32_t a_dst = smem_u32(stage_base + stage * C::STAGE_BYTES);
-          const uint32_t b_dst = a_dst + A_STAGE_BYTES;
+          const uint32_t b_dst = a_dst + NA * A_STAGE_BYTES;
+          const int k0 = kb * BK;
           mbar_expect_tx(full_bar(stage), C::STAGE_BYTES);
           filled_parity[stage] = (int)phase;
-          tma_load_2d(a_dst, &tmA, full_bar(stage), kb * BK, ti.row0);
-          if (EPI == EPI_SWIGLU) {
 #pragma unroll
-            for (int c = 0; c < BN / 64; ++c) {
-              const CUtensorMap* m = (c < BN / 128) ? &tmB : &tmB2;
-              const int col = ti.n0 + (c % (BN / 128)) * 64;
-              tma_load_3d(b_dst + c * (64 * BK * 2), m, full_bar(stage), col, kb * BK, ti.g);
+          for (int ia = 0; ia < NA; ++ia) {
+            const uint32_t dst = a_dst + ia * A_STAGE_BYTES;
+            if (A_MN) {  // [64 K rows x 64 M] boxes, the two M halves LBO apart
+              tma_load_3d(dst, &tmA, full_bar(stage), ti.row0, k0, ia);
+              tma_load_3d(dst + 64 * BK * 2, &tmA, full_bar(stage), ti.row0 + 64, k0, ia);
+            } else {
+              tma_load_3d(dst, &tmA, full_bar(stage), k0, ti.row0, ia);
             }
-          } else if (B_MN) {
+          }
 #pragma unroll
-            for (int c = 0; c < BN / 64; ++c)
-              tma_load_3d(b_dst + c * (64 * BK * 2), &tmB, full_bar(stage), ti.n0 + c * 64, kb * BK, ti.g);
-          } else {
-            tma_load_3d(b_dst, &tmB, full_bar(stage), kb * BK, ti.n0, ti.g);
+          for (int ib = 0; ib < NB; ++ib) {
+            const uint32_t dst = b_dst + ib * C::B_TILE_BYTES;
+            const int z = NB > 1 ? ib : ti.g;
+            if (EPI == EPI_SWIGLU) {
+#pragma unroll
+              for (int c = 0; c < BN / 64; ++c) {
+                const CUtensorMap* m = (c < BN / 128) ? &tmB : &tmB2;
+                const int col = ti.n0 + (c % (BN / 128)) * 64;
+                tma_load_3d(dst + c * (64 * BK * 2), m, full_bar(stage), col, k0, z);
+              }
+            } else if (B_MN) {
+#pragma unroll
+              for (int c = 0; c < BN / 64; ++c)
+                tma_load_3d(dst + c * (64 * BK * 2), &tmB, full_bar(stage), ti.n0 + c * 64, k0, z);
+            } else {
+              tma_load_3d(dst, &tmB, full_bar(stage), k0, ti.n0, z);
+            }
           }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
@@ -324,17 +361,16 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (filled_parity[s] < 0) continue;
         const long long t0 = clock64();
         while (!mbar_try_wait(full_bar(s), (uint32_t)filled_parity[s])) {
-          if ((unsigned long long)(clock64() - t0) > p.wait_limit) { set_error(p.err, DEV_TIMEOUT); break; }
+          if ((unsigned long long)(clock64() - t0) > DRAIN_LIMIT) { set_error(p.err, DEV_TIMEOUT); break; }
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t IDESC = instr_desc(BM, BN, B_MN);
+      constexpr uint32_t IDESC = instr_desc(BM, BN, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
-      const int KB = (p.K + BK - 1) / BK;
       bool ok = true;
       bool issued = false;
       int i = 0;
@@ -343,17 +379,28 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (!wait_bounded(acce_bar(acc), (((uint32_t)i >> 1) & 1u) ^ 1u, &abort_flag, p)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < KB; ++kb) {
+        const int split = t / base_tiles;
+        const int kb_begin = kb_lo(split), kb_end = kb_lo(split + 1);
+        for (int kb = kb_begin; kb < kb_end; ++kb) {
           if (!wait_bounded(full_bar(stage), phase, &abort_flag, p)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(stage_base + stage * C::STAGE_BYTES);
-          const uint32_t b_addr = a_addr + A_STAGE_BYTES;
+          const uint32_t b_addr = a_addr + NA * A_STAGE_BYTES;
 #pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t adesc = smem_desc(a_addr + k * 32, 16, 1024);
-            const uint64_t bdesc = B_MN ? smem_desc(b_addr + k * 16 * 128, 64 * BK * 2, 1024)
-                                        : smem_desc(b_addr + k * 32, 16, 1024);
-            tc_mma(d_tmem, adesc, bdesc, IDESC, (kb > 0 || k > 0) ? 1u : 0u);
+          for (int pp = 0; pp < C::NP; ++pp) {
+            const uint32_t a_t = a_addr + (pp < NA ? pp : NA - 1) * A_STAGE_BYTES;
+            const uint32_t b_t = b_addr + (pp < NB ? pp : NB - 1) * C::B_TILE_BYTES;
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {
+              // K-major: +32 bytes per 16-element K step inside the 128-byte
+              // swizzle row; MN-major: +16 rows of 128 bytes, 64-wide M/N atoms
+              // 8 KB apart (leading byte offset), 8-row groups 1 KB apart
+              const uint64_t adesc = A_MN ? smem_desc(a_t + k * 16 * 128, 64 * BK * 2, 1024)
+                                          : smem_desc(a_t + k * 32, 16, 1024);
+              const uint64_t bdesc = B_MN ? smem_desc(b_t + k * 16 * 128, 64 * BK * 2, 1024)
+                                          : smem_desc(b_t + k * 32, 16, 1024);
+              tc_mma(d_tmem, adesc, bdesc, IDESC, (kb > kb_begin || pp > 0 || k > 0) ? 1u : 0u);
+            }
           }
           issued = true;
           tc_commit(empty_bar(stage));
@@ -367,7 +414,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         tc_commit(drain_bar);
         const long long t0 = clock64();
         while (!mbar_try_wait(drain_bar, 0)) {
-          if ((unsigned long long)(clock64() - t0) > p.wait_limit) { set_error(p.err, DEV_TIMEOUT); break; }
+          if ((unsigned long long)(clock64() - t0) > DRAIN_LIMIT) { set_error(p.err, DEV_TIMEOUT); break; }
         }
       }
     }
@@ -380,7 +427,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int acc = i & 1;
       if (!wait_bounded(accf_bar(acc), ((uint32_t)i >> 1) & 1u, &abort_flag, p)) break;
       tc_fence_after();
-      const TileInfo ti = decode(t, mt_pre, G, n_tiles, p, C::OUT_BN);
+      const int split = t / base_tiles;
+      const TileInfo ti = decode(t - split * base_tiles, mt_pre, G, n_tiles, p, C::OUT_BN);
       const long long grow = (long long)ti.row0 + r_local;
       const bool row_ok = r_local < ti.rows && grow >= 0 && grow < p.M;
       const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
@@ -414,17 +462,30 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           tmem_ld32(tbase + c * 32, v);
           const int col = ti.n0 + c * 32;
           if (row_ok && col < p.N) {
+            uint4* dst = reinterpret_cast<uint4*>(out + grow * p.ldo + col);
+            if (p.accumulate) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const uint4 o = dst[j];
+                const __nv_bfloat162* oh = reinterpret_cast<const __nv_bfloat162*>(&o);
+#pragma unroll
+                for (int q2 = 0; q2 < 4; ++q2) {
+                  const float2 f = __bfloat1622float2(oh[q2]);
+                  v[8 * j + 2 * q2] += f.x;
+                  v[8 * j + 2 * q2 + 1] += f.y;
+                }
+              }
+            }
             uint4 pk[4];
             __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(pk);
 #pragma unroll
             for (int j = 0; j < 16; ++j) h2[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
-            uint4* dst = reinterpret_cast<uint4*>(out + grow * p.ldo + col);
 #pragma unroll
             for (int j = 0; j < 4; ++j) dst[j] = pk[j];
           }
         }
       } else {
-        float* out = static_cast<float*>(p.out);
+        float* out = static_cast<float*>(p.out) + (long long)split * p.part_stride;
 #pragma unroll 1
         for (int c = 0; c < C::OUT_BN / 32; ++c) {
           float v[32];
@@ -482,12 +543,13 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 
 unsigned long long g_wait_limit = 4000000000ull;  // ~2 s at 2 GHz
 
-template <int EPI, bool B_MN, int BN, int STAGES>
+template <int EPI, bool A_MN, bool B_MN, int BN, int STAGES, int NA, int NB>
 int launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const Params& p,
            long long tiles_upper, cudaStream_t s) {
-  using C = Cfg<BN, EPI>;
+  using C = Cfg<BN, EPI, NA, NB>;
   const size_t smem = (size_t)STAGES * C::STAGE_BYTES + (2 * STAGES + 5) * 8 + 1024;
-  auto k = tc_gemm_kernel<EPI, B_MN, BN, STAGES>;
+  static_assert((size_t)STAGES * C::STAGE_BYTES + (2 * STAGES + 5) * 8 + 1024 <= 227 * 1024, "smem");
+  auto k = tc_gemm_kernel<EPI, A_MN, B_MN, BN, STAGES, NA, NB>;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return MOE_ERR_CUDA;
   long long grid = sm_count();
@@ -495,6 +557,27 @@ int launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, co
   if (grid < 1) return MOE_OK;
   k<<<(unsigned)grid, NUM_THREADS, smem, s>>>(a, b, b2, p);
   return launch_status();
+}
+
+// [rows, inner] bf16 matrix as a 3D map {inner, rows, 1}
+bool map_2d_as_3d(CUtensorMap* m, const void* base, long long inner, long long rows, int box_inner, int box_rows) {
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, 1};
+  cuuint64_t str[2] = {(cuuint64_t)inner * 2, (cuuint64_t)inner * rows * 2};
+  cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows, 1};
+  return make_map(m, base, 3, dims, str, box);
+}
+
+// [depth, rows, inner] bf16 tensor as a 3D map {inner, rows, depth}
+bool map_3d(CUtensorMap* m, const void* base, long long inner, long long rows, long long depth, int box_inner,
+            int box_rows) {
+  cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, (cuuint64_t)depth};
+  cuuint64_t str[2] = {(cuuint64_t)inner * 2, (cuuint64_t)inner * rows * 2};
+  cuuint32_t box[3] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows, 1};
+  return make_map(m, base, 3, dims, str, box);
+}
+
+Params params(const int32_t* cu, int G, int M, int N, int K, void* out, long long ldo, const float* bias) {
+  return Params{cu, G, M, N, K, out, ldo, bias, device_error_word(), g_wait_limit, 1, 0, 0};
 }
 
 }  // namespace tc
@@ -505,37 +588,17 @@ int launch_expert_ffn_tc(const void* xs, const int32_t* cu, int rows, const void
   using namespace tc;
   if (E > 1024) return MOE_ERR_UNSUPPORTED;
   CUtensorMap mA, mG, mU, mA2, mD;
-  {
-    cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)rows};
-    cuuint64_t str[1] = {(cuuint64_t)H * 2};
-    cuuint32_t box[2] = {BK, BM};
-    if (!make_map(&mA, xs, 2, dims, str, box)) return MOE_ERR_CUDA;
-  }
-  {
-    cuuint64_t dims[3] = {(cuuint64_t)Hp, (cuuint64_t)H, (cuuint64_t)E};
-    cuuint64_t str[2] = {(cuuint64_t)Hp * 2, (cuuint64_t)H * Hp * 2};
-    cuuint32_t box[3] = {64, BK, 1};
-    if (!make_map(&mG, wg, 3, dims, str, box)) return MOE_ERR_CUDA;
-    if (!make_map(&mU, wu, 3, dims, str, box)) return MOE_ERR_CUDA;
-  }
-  {
-    cuuint64_t dims[2] = {(cuuint64_t)Hp, (cuuint64_t)rows};
-    cuuint64_t str[1] = {(cuuint64_t)Hp * 2};
-    cuuint32_t box[2] = {BK, BM};
-    if (!make_map(&mA2, act, 2, dims, str, box)) return MOE_ERR_CUDA;
-  }
-  {
-    cuuint64_t dims[3] = {(cuuint64_t)Hp, (cuuint64_t)H, (cuuint64_t)E};
-    cuuint64_t str[2] = {(cuuint64_t)Hp * 2, (cuuint64_t)H * Hp * 2};
-    cuuint32_t box[3] = {BK, 256, 1};
-    if (!make_map(&mD, wd, 3, dims, str, box)) return MOE_ERR_CUDA;
-  }
+  if (!map_2d_as_3d(&mA, xs, H, rows, BK, BM)) return MOE_ERR_CUDA;
+  if (!map_3d(&mG, wg, Hp, H, E, 64, BK)) return MOE_ERR_CUDA;
+  if (!map_3d(&mU, wu, Hp, H, E, 64, BK)) return MOE_ERR_CUDA;
+  if (!map_2d_as_3d(&mA2, act, Hp, rows, BK, BM)) return MOE_ERR_CUDA;
+  if (!map_3d(&mD, wd, Hp, H, E, BK, 256)) return MOE_ERR_CUDA;
   const long long mtiles = (rows + BM - 1) / BM + E;
-  Params p1{cu, E, rows, Hp, H, act, Hp, nullptr, device_error_word(), g_wait_limit};
-  int st = launch<EPI_SWIGLU, true, 256, 4>(mA, mG, mU, p1, mtiles * ((Hp + 127) / 128), s);
+  Params p1 = params(cu, E, rows, Hp, H, act, Hp, nullptr);
+  int st = launch<EPI_SWIGLU, false, true, 256, 4, 1, 1>(mA, mG, mU, p1, mtiles * ((Hp + 127) / 128), s);
   if (st != MOE_OK) return st;
-  Params p2{cu, E, rows, H, Hp, h, H, nullptr, device_error_word(), g_wait_limit};
-  return launch<EPI_BF16, false, 256, 4>(mA2, mD, mD, p2, mtiles * ((H + 255) / 256), s);
+  Params p2 = params(cu, E, rows, H, Hp, h, H, nullptr);
+  return launch<EPI_BF16, false, false, 256, 4, 1, 1>(mA2, mD, mD, p2, mtiles * ((H + 255) / 256), s);
 }
 
 // logits = x W_r + bias  (bf16 inputs, fp32 out); E % 8 == 0, H % 8 == 0
@@ -543,23 +606,52 @@ int launch_router_tc(const void* x, const void* w, const float* bias, int T, int
                      cudaStream_t s) {
   using namespace tc;
   CUtensorMap mA, mB;
-  {
-    cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)T};
-    cuuint64_t str[1] = {(cuuint64_t)H * 2};
-    cuuint32_t box[2] = {BK, BM};
-    if (!make_map(&mA, x, 2, dims, str, box)) return MOE_ERR_CUDA;
-  }
-  {
-    cuuint64_t dims[3] = {(cuuint64_t)E, (cuuint64_t)H, 1};
-    cuuint64_t str[2] = {(cuuint64_t)E * 2, (cuuint64_t)H * E * 2};
-    cuuint32_t box[3] = {64, BK, 1};
-    if (!make_map(&mB, w, 3, dims, str, box)) return MOE_ERR_CUDA;
-  }
-  Params p{nullptr, 1, T, E, H, logits, E, bias, device_error_word(), g_wait_limit};
+  if (!map_2d_as_3d(&mA, x, H, T, BK, BM)) return MOE_ERR_CUDA;
+  if (!map_3d(&mB, w, E, H, 1, 64, BK)) return MOE_ERR_CUDA;
+  Params p = params(nullptr, 1, T, E, H, logits, E, bias);
   const long long mtiles = (T + BM - 1) / BM;
-  if (E <= 64) return launch<EPI_F32_BIAS, true, 64, 8>(mA, mB, mB, p, mtiles, s);
-  if (E <= 128) return launch<EPI_F32_BIAS, true, 128, 6>(mA, mB, mB, p, mtiles, s);
-  return launch<EPI_F32_BIAS, true, 256, 4>(mA, mB, mB, p, mtiles * ((E + 255) / 256), s);
+  if (E <= 64) return launch<EPI_F32_BIAS, false, true, 64, 8, 1, 1>(mA, mB, mB, p, mtiles, s);
+  if (E <= 128) return launch<EPI_F32_BIAS, false, true, 128, 6, 1, 1>(mA, mB, mB, p, mtiles, s);
+  return launch<EPI_F32_BIAS, false, true, 256, 4, 1, 1>(mA, mB, mB, p, mtiles * ((E + 255) / 256), s);
+}
+
+// Split count for the router weight gradient on tensor cores: about one CTA
+// per SM of a 152-SM GPU, at least one 64-token block per split.
+int router_dw_tc_splits(int T, int H, int E) {
+  const long long tiles = ((H + tc::BM - 1) / tc::BM) * (long long)(E <= 64 ? 1 : (E + 127) / 128);
+  long long s = (152 + tiles - 1) / tiles;
+  const long long kb = (T + tc::BK - 1) / tc::BK;
+  if (s > kb) s = kb;
+  if (s > 64) s = 64;
+  return s < 1 ? 1 : (int)s;
+}
+
+// part[s][h][e] = sum over the tokens of split s of x[t,h] (hi+mid+lo)[t,e]
+// x [T,H] bf16; dl3 [3,T,E] bf16 (the exact three-part split of the fp32 dl)
+int launch_router_dw_tc(const void* x, const void* dl3, int T, int H, int E, float* part, cudaStream_t s) {
+  using namespace tc;
+  CUtensorMap mA, mB;
+  if (!map_2d_as_3d(&mA, x, H, T, 64, BK)) return MOE_ERR_CUDA;  // A = x^T, MN-major boxes [64 t x 64 h]
+  if (!map_3d(&mB, dl3, E, T, 3, 64, BK)) return MOE_ERR_CUDA;
+  const int S = router_dw_tc_splits(T, H, E);
+  Params p = params(nullptr, 1, H, E, T, part, E, nullptr);
+  p.ksplit = S;
+  p.part_stride = (long long)H * E;
+  const long long mtiles = (H + BM - 1) / BM;
+  if (E <= 64) return launch<EPI_F32_BIAS, true, true, 64, 5, 1, 3>(mA, mB, mB, p, mtiles * S, s);
+  return launch<EPI_F32_BIAS, true, true, 128, 3, 1, 3>(mA, mB, mB, p, mtiles * ((E + 127) / 128) * S, s);
+}
+
+// dx[t,h] (+)= sum_e (hi+mid+lo)[t,e] W_r[h,e]; dx bf16 [T,H], H % 64 == 0
+int launch_router_dx_tc(const void* dl3, const void* w, int T, int H, int E, bool write, void* dx, cudaStream_t s) {
+  using namespace tc;
+  CUtensorMap mA, mB;
+  if (!map_3d(&mA, dl3, E, T, 3, BK, BM)) return MOE_ERR_CUDA;
+  if (!map_2d_as_3d(&mB, w, E, H, BK, 256)) return MOE_ERR_CUDA;
+  Params p = params(nullptr, 1, T, H, E, dx, H, nullptr);
+  p.accumulate = write ? 0 : 1;
+  const long long tiles = ((T + BM - 1) / BM) * (long long)((H + 255) / 256);
+  return launch<EPI_BF16, false, false, 256, 2, 3, 1>(mA, mB, mB, p, tiles, s);
 }
 
 }  // namespace moe

@@ -77,11 +77,22 @@ softmax_topk_kernel(const float* __restrict__ logits, int T, int E, int K,
 }
 
 // d_logits[t,j] = p_j (G_j - sum_k d_gate[t,k] p[idx[t,k]])
+// Exact split of an fp32 value into three bf16 parts, v = hi + mid + lo: each
+// subtraction is exact in fp32 and each rounding keeps the next 8+ significant
+// bits, so three parts hold the full 24-bit significand.
+__device__ __forceinline__ void split3(float v, bf16& hi, bf16& mid, bf16& lo) {
+  hi = __float2bfloat16_rn(v);
+  const float r1 = v - __bfloat162float(hi);
+  mid = __float2bfloat16_rn(r1);
+  const float r2 = r1 - __bfloat162float(mid);
+  lo = __float2bfloat16_rn(r2);
+}
+
 template <int VPL>
 __global__ void __launch_bounds__(32 * ROWS_PER_CTA)
 softmax_topk_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ idx,
                         const float* __restrict__ d_gate, int T, int E, int K,
-                        float* __restrict__ d_logits) {
+                        float* __restrict__ d_logits, bf16* __restrict__ dl3) {
   const int lane = threadIdx.x & 31;
   const long long nwarps = (long long)gridDim.x * ROWS_PER_CTA;
   for (long long t = (long long)blockIdx.x * ROWS_PER_CTA + (threadIdx.x >> 5); t < T; t += nwarps) {
@@ -124,6 +135,16 @@ softmax_topk_bwd_kernel(const float* __restrict__ logits, const int32_t* __restr
         r.z = p[4 * q + 2] * (G[4 * q + 2] - inner);
         r.w = p[4 * q + 3] * (G[4 * q + 3] - inner);
         *reinterpret_cast<float4*>(out + e4) = r;
+        if (dl3) {
+          const float vv[4] = {r.x, r.y, r.z, r.w};
+          __align__(8) bf16 part[3][4];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) split3(vv[j], part[0][j], part[1][j], part[2][j]);
+          const long long plane = (long long)T * E;
+#pragma unroll
+          for (int s = 0; s < 3; ++s)
+            *reinterpret_cast<uint2*>(dl3 + s * plane + t * E + e4) = *reinterpret_cast<const uint2*>(part[s]);
+        }
       }
     }
   }
@@ -535,9 +556,31 @@ int launch_softmax_topk(const float* logits, int T, int E, int K, int32_t* idx, 
   return launch_status();
 }
 
-size_t route_bwd_ws_bytes(int T, int H, int E) {
+int router_dw_tc_splits(int T, int H, int E);
+int launch_router_dw_tc(const void* x, const void* dl3, int T, int H, int E, float* part, cudaStream_t s);
+int launch_router_dx_tc(const void* dl3, const void* w, int T, int H, int E, bool write, void* dx, cudaStream_t s);
+
+// The tensor-core router backward serves bf16 layers whose W_r rows are
+// 16-byte multiples (E % 8 == 0) and whose dx rows tile by 64 columns.
+static bool route_bwd_on_tensor_cores(int mode, int dtype, int H, int E) {
+  return mode == MOE_ROUTE_SOFTMAX_TOPK && dtype == MOE_BF16 && E % 8 == 0 && H % 64 == 0;
+}
+
+// workspace: [fp32 partials of dW][fp32 dl (when d_logits is not given)][bf16 dl in three parts]
+struct BwdWs {
+  size_t part, dl, dl3;
+};
+static BwdWs bwd_ws(int T, int H, int E) {
   const DwPlan pl = dw_plan(T, H, E);
-  return align256((size_t)pl.splits * H * E * 4) + align256((size_t)T * E * 4);
+  long long splits = pl.splits;
+  const long long tcs = router_dw_tc_splits(T, H, E);
+  if (tcs > splits) splits = tcs;
+  return BwdWs{align256((size_t)splits * H * E * 4), align256((size_t)T * E * 4), align256((size_t)3 * T * E * 2)};
+}
+
+size_t route_bwd_ws_bytes(int T, int H, int E) {
+  const BwdWs w = bwd_ws(T, H, E);
+  return w.part + w.dl + w.dl3;
 }
 
 template <typename T>
@@ -552,12 +595,14 @@ int launch_dw(const T* x, const float* dl, int Tn, int H, int E, float* part, fl
   } else if (pl.eb == 16) router_dw_partial_kernel<T, 4, 16><<<grid, DW_THREADS, 0, s>>>(x, dl, Tn, H, E, pl.rows_per_split, part);
   else if (pl.eb == 32) router_dw_partial_kernel<T, 2, 32><<<grid, DW_THREADS, 0, s>>>(x, dl, Tn, H, E, pl.rows_per_split, part);
   else router_dw_partial_kernel<T, 1, 64><<<grid, DW_THREADS, 0, s>>>(x, dl, Tn, H, E, pl.rows_per_split, part);
-  int st = launch_status();
-  if (st != MOE_OK) return st;
+  return launch_status();
+}
+
+int launch_reduce(const float* part, int S, int H, int E, float* dw, cudaStream_t s) {
   const long long n = (long long)H * E;
   const long long thr = n * 8;
   const int rgrid = (int)((thr + 255) / 256 < 16384 ? (thr + 255) / 256 : 16384);
-  reduce_splits_kernel<<<rgrid, 256, 0, s>>>(part, pl.splits, n, dw);
+  reduce_splits_kernel<<<rgrid, 256, 0, s>>>(part, S, n, dw);
   return launch_status();
 }
 
@@ -575,18 +620,20 @@ int launch_route_bwd(int mode, const float* d_gate, const float* logits, const i
     if (dw && cudaMemsetAsync(dw, 0, (size_t)H * E * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
   }
-  const DwPlan pl = dw_plan(T, H, E);
-  float* part = static_cast<float*>(ws);
-  float* dl = d_logits;
-  if (!dl) dl = reinterpret_cast<float*>(static_cast<char*>(ws) + align256((size_t)pl.splits * H * E * 4));
+  const BwdWs lay = bwd_ws(T, H, E);
+  char* wsb = static_cast<char*>(ws);
+  float* part = reinterpret_cast<float*>(wsb);
+  float* dl = d_logits ? d_logits : reinterpret_cast<float*>(wsb + lay.part);
+  const bool tc = route_bwd_on_tensor_cores(mode, dtype, H, E);
+  bf16* dl3 = tc ? reinterpret_cast<bf16*>(wsb + lay.part + lay.dl) : nullptr;
 
   if (mode == MOE_ROUTE_SOFTMAX_TOPK) {
     int grid = rows_grid(T);
     int vpl = (E + 127) / 128 * 4;
-    if (vpl <= 4) softmax_topk_bwd_kernel<4><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, idx, d_gate, T, E, K, dl);
-    else if (vpl <= 8) softmax_topk_bwd_kernel<8><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, idx, d_gate, T, E, K, dl);
-    else if (vpl <= 16) softmax_topk_bwd_kernel<16><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, idx, d_gate, T, E, K, dl);
-    else softmax_topk_bwd_kernel<32><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, idx, d_gate, T, E, K, dl);
+    if (vpl <= 4) softmax_topk_bwd_kernel<4><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, idx, d_gate, T, E, K, dl, dl3);
+    else if (vpl <= 8) softmax_topk_bwd_kernel<8><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, idx, d_gate, T, E, K, dl, dl3);
+    else if (vpl <= 16) softmax_topk_bwd_kernel<16><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, idx, d_gate, T, E, K, dl, dl3);
+    else softmax_topk_bwd_kernel<32><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, idx, d_gate, T, E, K, dl, dl3);
   } else {
     // linear score: the score gradient is the logit gradient (E = K = 1)
     copy_f32_kernel<<<rows_grid(T), 256, 0, s>>>(d_gate, dl, (long long)T);
@@ -595,14 +642,22 @@ int launch_route_bwd(int mode, const float* d_gate, const float* logits, const i
   if (st != MOE_OK) return st;
 
   if (dw) {
-    st = dtype == MOE_BF16 ? launch_dw<bf16>(static_cast<const bf16*>(x), dl, T, H, E, part, dw, s)
-                           : launch_dw<float>(static_cast<const float*>(x), dl, T, H, E, part, dw, s);
+    if (tc) {
+      st = launch_router_dw_tc(x, dl3, T, H, E, part, s);
+      if (st == MOE_OK) st = launch_reduce(part, router_dw_tc_splits(T, H, E), H, E, dw, s);
+    } else {
+      st = dtype == MOE_BF16 ? launch_dw<bf16>(static_cast<const bf16*>(x), dl, T, H, E, part, dw, s)
+                             : launch_dw<float>(static_cast<const float*>(x), dl, T, H, E, part, dw, s);
+      if (st == MOE_OK) st = launch_reduce(part, dw_plan(T, H, E).splits, H, E, dw, s);
+    }
     if (st != MOE_OK) return st;
   }
   if (dx) {
-    st = dtype == MOE_BF16
-             ? launch_dx<bf16>(dl, static_cast<const bf16*>(w), T, H, E, dx_write, static_cast<bf16*>(dx), s)
-             : launch_dx<float>(dl, static_cast<const float*>(w), T, H, E, dx_write, static_cast<float*>(dx), s);
+    if (tc) st = launch_router_dx_tc(dl3, w, T, H, E, dx_write, dx, s);
+    else
+      st = dtype == MOE_BF16
+               ? launch_dx<bf16>(dl, static_cast<const bf16*>(w), T, H, E, dx_write, static_cast<bf16*>(dx), s)
+               : launch_dx<float>(dl, static_cast<const float*>(w), T, H, E, dx_write, static_cast<float*>(dx), s);
     if (st != MOE_OK) return st;
   }
   return MOE_OK;
