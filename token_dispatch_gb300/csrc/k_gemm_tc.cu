@@ -456,8 +456,22 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
       } else if (EPI == EPI_BF16) {
         bf16* out = static_cast<bf16*>(p.out);
-#pragma unroll 1
-        for (int c = 0; c < C::OUT_BN / 32; ++c) {
+        constexpr int NCH = C::OUT_BN / 32;
+        // accumulate: every old value of this row segment is requested before
+        // any is used, so a thread keeps NCH*64 bytes of reads in flight
+        uint4 old[NCH][4];
+        if (p.accumulate) {
+#pragma unroll
+          for (int c = 0; c < NCH; ++c) {
+            const int col = ti.n0 + c * 32;
+            const bool ok = row_ok && col < p.N;
+            const uint4* src = reinterpret_cast<const uint4*>(out + (ok ? grow * p.ldo + col : 0));
+#pragma unroll
+            for (int j = 0; j < 4; ++j) old[c][j] = ok ? src[j] : make_uint4(0, 0, 0, 0);
+          }
+        }
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
           float v[32];
           tmem_ld32(tbase + c * 32, v);
           const int col = ti.n0 + c * 32;
@@ -466,8 +480,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (p.accumulate) {
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
-                const uint4 o = dst[j];
-                const __nv_bfloat162* oh = reinterpret_cast<const __nv_bfloat162*>(&o);
+                const __nv_bfloat162* oh = reinterpret_cast<const __nv_bfloat162*>(&old[c][j]);
 #pragma unroll
                 for (int q2 = 0; q2 < 4; ++q2) {
                   const float2 f = __bfloat1622float2(oh[q2]);
