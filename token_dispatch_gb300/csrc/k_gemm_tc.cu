@@ -70,9 +70,6 @@ struct Params {
 // this bound, so a kernel that gave up early still leaves nothing running.
 constexpr unsigned long long DRAIN_LIMIT = 4000000000ull;
 
-// k-blocks between a weight tile's L2 prefetch and its shared-memory load
-constexpr int PF = 8;
-
 // ------------------------------------------------------------------ PTX ----
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -129,13 +126,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
-}
-// Bring a tile into L2 ahead of its shared-memory load (no shared memory, no barrier).
-__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int c0, int c1, int c2) {
-  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(c0), "r"(c1), "r"(c2)
-               : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -361,18 +351,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 tma_load_3d(dst + c * (64 * BK * 2), &tmB, full_bar(stage), ti.n0 + c * 64, k0, z);
             } else {
               tma_load_3d(dst, &tmB, full_bar(stage), k0, ti.n0, z);
-            }
-          }
-          // L2 prefetch of the weight tile PF k-blocks ahead (same tile), so the
-          // shared-memory ring only has to cover the L2 latency
-          if (PF > 0 && kb + PF < kb_end) {
-            const int kp = (kb + PF) * BK;
-            if (EPI == EPI_SWIGLU) {
-#pragma unroll
-              for (int c = 0; c < BN / 64; ++c)
-                tma_prefetch_3d((c < BN / 128) ? &tmB : &tmB2, ti.n0 + (c % (BN / 128)) * 64, kp, ti.g);
-            } else if (!B_MN && NB == 1) {
-              tma_prefetch_3d(&tmB, kp, ti.n0, ti.g);
             }
           }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
