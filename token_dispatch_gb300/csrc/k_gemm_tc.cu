@@ -184,21 +184,14 @@ __host__ __device__ constexpr uint32_t instr_desc(int M, int N, bool a_mn_major,
 
 // NA A tiles and NB B tiles per stage; MMA pair p uses A tile min(p, NA-1) and
 // B tile min(p, NB-1), all into one accumulator.
-// MH = 2: a tile is 2 x 128 rows; both M halves use every B tile of a stage
-// (half the B bytes per FLOP) and own one accumulator each.  The accumulators
-// of a tile are double-buffered when they fit twice in the 512 TMEM columns.
-template <int BN, int EPI, int NA, int NB, int MH>
+template <int BN, int EPI, int NA, int NB>
 struct Cfg {
   static constexpr int B_TILE_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = MH * NA * A_STAGE_BYTES + NB * B_TILE_BYTES;
+  static constexpr int STAGE_BYTES = NA * A_STAGE_BYTES + NB * B_TILE_BYTES;
   static constexpr int NP = NA > NB ? NA : NB;
   static constexpr int OUT_BN = (EPI == EPI_SWIGLU) ? BN / 2 : BN;  // output columns per tile
-  static constexpr int BMT = BM * MH;                                // rows per tile
-  static constexpr int ACC_COLS = MH * BN;                           // TMEM columns per tile
-  static constexpr int ACC_BUFS = (2 * ACC_COLS <= 512) ? 2 : 1;
-  static constexpr int USED = ACC_BUFS * ACC_COLS;
-  static constexpr int TMEM_COLS = USED <= 32 ? 32 : USED <= 64 ? 64 : USED <= 128 ? 128 : USED <= 256 ? 256 : 512;
-  static_assert(USED <= 512, "TMEM");
+  static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
+                                   : (2 * BN <= 256) ? 256 : 512;
 };
 
 struct TileInfo {
@@ -207,7 +200,7 @@ struct TileInfo {
 
 // Tile t -> (group, rows, first output column).  mt_pre[g] = m-tiles before g.
 __device__ __forceinline__ TileInfo decode(int t, const int* mt_pre, int G, int n_tiles, const Params& p,
-                                           int out_bn, int bmt) {
+                                           int out_bn) {
   // largest g with mt_pre[g] * n_tiles <= t
   int lo = 0, hi = G - 1;
   while (lo < hi) {
@@ -223,18 +216,17 @@ __device__ __forceinline__ TileInfo decode(int t, const int* mt_pre, int G, int 
   const int end = p.cu ? p.cu[g + 1] : p.M;
   TileInfo ti;
   ti.g = g;
-  ti.row0 = beg + m * bmt;
-  ti.rows = min(bmt, end - ti.row0);
+  ti.row0 = beg + m * BM;
+  ti.rows = min(BM, end - ti.row0);
   ti.n0 = n * out_bn;
   return ti;
 }
 
-template <int EPI, bool A_MN, bool B_MN, int BN, int STAGES, int NA, int NB, int MH>
+template <int EPI, bool A_MN, bool B_MN, int BN, int STAGES, int NA, int NB>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmB2, const Params p) {
-  using C = Cfg<BN, EPI, NA, NB, MH>;
-  static_assert(MH == 1 || !A_MN, "two M halves need a K-major A");
+  using C = Cfg<BN, EPI, NA, NB>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_base = smem;
@@ -262,7 +254,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
-    for (int a = 0; a < C::ACC_BUFS; ++a) {
+    for (int a = 0; a < 2; ++a) {
       mbar_init(accf_bar(a), 1);
       mbar_init(acce_bar(a), 128);
     }
@@ -283,7 +275,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     int sum = 0;
     for (int g = lane * per; g < min(G, lane * per + per); ++g) {
       int rows = p.cu ? max(0, p.cu[g + 1] - p.cu[g]) : p.M;
-      sum += (rows + C::BMT - 1) / C::BMT;
+      sum += (rows + BM - 1) / BM;
     }
     int incl = sum;
 #pragma unroll
@@ -295,7 +287,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     for (int g = lane * per; g < min(G, lane * per + per); ++g) {
       mt_pre[g] = run;
       int rows = p.cu ? max(0, p.cu[g + 1] - p.cu[g]) : p.M;
-      run += (rows + C::BMT - 1) / C::BMT;
+      run += (rows + BM - 1) / BM;
     }
     if (lane == 0 && p.cu && (p.cu[0] != 0 || p.cu[G] != p.M)) set_error(p.err, DEV_BOUNDS);
     if (lane == 31) {
@@ -323,26 +315,23 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       bool ok = true;
       for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
         const int split = t / base_tiles;
-        const TileInfo ti = decode(t - split * base_tiles, mt_pre, G, n_tiles, p, C::OUT_BN, C::BMT);
+        const TileInfo ti = decode(t - split * base_tiles, mt_pre, G, n_tiles, p, C::OUT_BN);
         const int kb_end = kb_lo(split + 1);
         for (int kb = kb_lo(split); kb < kb_end; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, &abort_flag, p)) { ok = false; break; }
           const uint32_t a_dst = smem_u32(stage_base + stage * C::STAGE_BYTES);
-          const uint32_t b_dst = a_dst + MH * NA * A_STAGE_BYTES;
+          const uint32_t b_dst = a_dst + NA * A_STAGE_BYTES;
           const int k0 = kb * BK;
           mbar_expect_tx(full_bar(stage), C::STAGE_BYTES);
           filled_parity[stage] = (int)phase;
 #pragma unroll
-          for (int mh = 0; mh < MH; ++mh) {
-#pragma unroll
-            for (int ia = 0; ia < NA; ++ia) {
-              const uint32_t dst = a_dst + (mh * NA + ia) * A_STAGE_BYTES;
-              if (A_MN) {  // [64 K rows x 64 M] boxes, the two M halves LBO apart
-                tma_load_3d(dst, &tmA, full_bar(stage), ti.row0, k0, ia);
-                tma_load_3d(dst + 64 * BK * 2, &tmA, full_bar(stage), ti.row0 + 64, k0, ia);
-              } else {
-                tma_load_3d(dst, &tmA, full_bar(stage), k0, ti.row0 + mh * BM, ia);
-              }
+          for (int ia = 0; ia < NA; ++ia) {
+            const uint32_t dst = a_dst + ia * A_STAGE_BYTES;
+            if (A_MN) {  // [64 K rows x 64 M] boxes, the two M halves LBO apart
+              tma_load_3d(dst, &tmA, full_bar(stage), ti.row0, k0, ia);
+              tma_load_3d(dst + 64 * BK * 2, &tmA, full_bar(stage), ti.row0 + 64, k0, ia);
+            } else {
+              tma_load_3d(dst, &tmA, full_bar(stage), k0, ti.row0, ia);
             }
           }
 #pragma unroll
@@ -386,35 +375,31 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       bool issued = false;
       int i = 0;
       for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x, ++i) {
-        const int acc = i % C::ACC_BUFS;
-        const uint32_t use = (uint32_t)(i / C::ACC_BUFS) & 1u;
-        if (!wait_bounded(acce_bar(acc), use ^ 1u, &abort_flag, p)) { ok = false; break; }
+        const int acc = i & 1;
+        if (!wait_bounded(acce_bar(acc), (((uint32_t)i >> 1) & 1u) ^ 1u, &abort_flag, p)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + acc * C::ACC_COLS;
+        const uint32_t d_tmem = tmem_base + acc * BN;
         const int split = t / base_tiles;
         const int kb_begin = kb_lo(split), kb_end = kb_lo(split + 1);
         for (int kb = kb_begin; kb < kb_end; ++kb) {
           if (!wait_bounded(full_bar(stage), phase, &abort_flag, p)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(stage_base + stage * C::STAGE_BYTES);
-          const uint32_t b_addr = a_addr + MH * NA * A_STAGE_BYTES;
+          const uint32_t b_addr = a_addr + NA * A_STAGE_BYTES;
 #pragma unroll
-          for (int mh = 0; mh < MH; ++mh) {
+          for (int pp = 0; pp < C::NP; ++pp) {
+            const uint32_t a_t = a_addr + (pp < NA ? pp : NA - 1) * A_STAGE_BYTES;
+            const uint32_t b_t = b_addr + (pp < NB ? pp : NB - 1) * C::B_TILE_BYTES;
 #pragma unroll
-            for (int pp = 0; pp < C::NP; ++pp) {
-              const uint32_t a_t = a_addr + (mh * NA + (pp < NA ? pp : NA - 1)) * A_STAGE_BYTES;
-              const uint32_t b_t = b_addr + (pp < NB ? pp : NB - 1) * C::B_TILE_BYTES;
-#pragma unroll
-              for (int k = 0; k < BK / 16; ++k) {
-                // K-major: +32 bytes per 16-element K step inside the 128-byte
-                // swizzle row; MN-major: +16 rows of 128 bytes, 64-wide M/N atoms
-                // 8 KB apart (leading byte offset), 8-row groups 1 KB apart
-                const uint64_t adesc = A_MN ? smem_desc(a_t + k * 16 * 128, 64 * BK * 2, 1024)
-                                            : smem_desc(a_t + k * 32, 16, 1024);
-                const uint64_t bdesc = B_MN ? smem_desc(b_t + k * 16 * 128, 64 * BK * 2, 1024)
-                                            : smem_desc(b_t + k * 32, 16, 1024);
-                tc_mma(d_tmem + mh * BN, adesc, bdesc, IDESC, (kb > kb_begin || pp > 0 || k > 0) ? 1u : 0u);
-              }
+            for (int k = 0; k < BK / 16; ++k) {
+              // K-major: +32 bytes per 16-element K step inside the 128-byte
+              // swizzle row; MN-major: +16 rows of 128 bytes, 64-wide M/N atoms
+              // 8 KB apart (leading byte offset), 8-row groups 1 KB apart
+              const uint64_t adesc = A_MN ? smem_desc(a_t + k * 16 * 128, 64 * BK * 2, 1024)
+                                          : smem_desc(a_t + k * 32, 16, 1024);
+              const uint64_t bdesc = B_MN ? smem_desc(b_t + k * 16 * 128, 64 * BK * 2, 1024)
+                                          : smem_desc(b_t + k * 32, 16, 1024);
+              tc_mma(d_tmem, adesc, bdesc, IDESC, (kb > kb_begin || pp > 0 || k > 0) ? 1u : 0u);
             }
           }
           issued = true;
@@ -439,17 +424,14 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     const int r_local = q * 32 + lane;
     int i = 0;
     for (int t = blockIdx.x; t < total_tiles; t += gridDim.x, ++i) {
-      const int acc = i % C::ACC_BUFS;
-      if (!wait_bounded(accf_bar(acc), (uint32_t)(i / C::ACC_BUFS) & 1u, &abort_flag, p)) break;
+      const int acc = i & 1;
+      if (!wait_bounded(accf_bar(acc), ((uint32_t)i >> 1) & 1u, &abort_flag, p)) break;
       tc_fence_after();
       const int split = t / base_tiles;
-      const TileInfo ti = decode(t - split * base_tiles, mt_pre, G, n_tiles, p, C::OUT_BN, C::BMT);
-#pragma unroll 1
-      for (int mh = 0; mh < MH; ++mh) {
-      const int r_tile = mh * BM + r_local;
-      const long long grow = (long long)ti.row0 + r_tile;
-      const bool row_ok = r_tile < ti.rows && grow >= 0 && grow < p.M;
-      const uint32_t tbase = tmem_base + acc * C::ACC_COLS + mh * BN + ((uint32_t)(q * 32) << 16);
+      const TileInfo ti = decode(t - split * base_tiles, mt_pre, G, n_tiles, p, C::OUT_BN);
+      const long long grow = (long long)ti.row0 + r_local;
+      const bool row_ok = r_local < ti.rows && grow >= 0 && grow < p.M;
+      const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
       if (EPI == EPI_SWIGLU) {
         bf16* out = static_cast<bf16*>(p.out);
 #pragma unroll 1
@@ -530,7 +512,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
         }
       }
-      }  // M halves
       tc_fence_before();
       mbar_arrive(acce_bar(acc));
     }
@@ -575,13 +556,13 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 
 unsigned long long g_wait_limit = 4000000000ull;  // ~2 s at 2 GHz
 
-template <int EPI, bool A_MN, bool B_MN, int BN, int STAGES, int NA, int NB, int MH = 1>
+template <int EPI, bool A_MN, bool B_MN, int BN, int STAGES, int NA, int NB>
 int launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const Params& p,
            long long tiles_upper, cudaStream_t s) {
-  using C = Cfg<BN, EPI, NA, NB, MH>;
+  using C = Cfg<BN, EPI, NA, NB>;
   const size_t smem = (size_t)STAGES * C::STAGE_BYTES + (2 * STAGES + 5) * 8 + 1024;
   static_assert((size_t)STAGES * C::STAGE_BYTES + (2 * STAGES + 5) * 8 + 1024 <= 227 * 1024, "smem");
-  auto k = tc_gemm_kernel<EPI, A_MN, B_MN, BN, STAGES, NA, NB, MH>;
+  auto k = tc_gemm_kernel<EPI, A_MN, B_MN, BN, STAGES, NA, NB>;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return MOE_ERR_CUDA;
   long long grid = sm_count();
@@ -625,13 +606,12 @@ int launch_expert_ffn_tc(const void* xs, const int32_t* cu, int rows, const void
   if (!map_3d(&mU, wu, Hp, H, E, 64, BK)) return MOE_ERR_CUDA;
   if (!map_2d_as_3d(&mA2, act, Hp, rows, BK, BM)) return MOE_ERR_CUDA;
   if (!map_3d(&mD, wd, Hp, H, E, BK, 256)) return MOE_ERR_CUDA;
-  // 256-row tiles (two M=128 halves sharing each weight tile), 3-stage ring
-  const long long mtiles = (rows + 2 * BM - 1) / (2 * BM) + E;
+  const long long mtiles = (rows + BM - 1) / BM + E;
   Params p1 = params(cu, E, rows, Hp, H, act, Hp, nullptr);
-  int st = launch<EPI_SWIGLU, false, true, 256, 3, 1, 1, 2>(mA, mG, mU, p1, mtiles * ((Hp + 127) / 128), s);
+  int st = launch<EPI_SWIGLU, false, true, 256, 4, 1, 1>(mA, mG, mU, p1, mtiles * ((Hp + 127) / 128), s);
   if (st != MOE_OK) return st;
   Params p2 = params(cu, E, rows, H, Hp, h, H, nullptr);
-  return launch<EPI_BF16, false, false, 256, 3, 1, 1, 2>(mA2, mD, mD, p2, mtiles * ((H + 255) / 256), s);
+  return launch<EPI_BF16, false, false, 256, 4, 1, 1>(mA2, mD, mD, p2, mtiles * ((H + 255) / 256), s);
 }
 
 // logits = x W_r + bias  (bf16 inputs, fp32 out); E % 8 == 0, H % 8 == 0
