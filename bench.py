@@ -345,31 +345,49 @@ def run_ours(args, shape, rank, world, local):
                for j, n in enumerate(names)}
     ms = statistics.mean(step_ms)
 
-    # end to end through the public API: every step copies its inputs from pinned
-    # host memory and its results back
-    host_in = [(x_h, torch.empty_like(x_d))]
-    if dy_d is not None:
-        host_in.append((dy_d.cpu().pin_memory(), torch.empty_like(dy_d)))
-    if dxs_d is not None:
-        host_in.append((dxs_d.cpu().pin_memory(), torch.empty_like(dxs_d)))
+    # End to end through the public API: every step copies its inputs from pinned
+    # host memory and its results back.  Inputs are double-buffered: the next
+    # step's host-to-device copies run on a copy stream while this step computes;
+    # results are copied back on the compute stream right after the step.
+    srcs = [x_h] + ([dy_d.cpu().pin_memory()] if dy_d is not None else []) + \
+        ([dxs_d.cpu().pin_memory()] if dxs_d is not None else [])
+    bufs_in = [[torch.empty_like(h, device=dev) for h in srcs] for _ in range(2)]
     host_out = [(o, torch.empty(o.shape, dtype=o.dtype).pin_memory()) for o in outs]
+    copy_stream = torch.cuda.Stream(device=dev)
     e2e_steps = max(3, min(args.steps, 20))
+    loaded = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize(dev)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for _ in range(e2e_steps):
-            for h, d in host_in:
+
+    def load(i):
+        slot = i % 2
+        with torch.cuda.stream(copy_stream):
+            if i >= 2:
+                copy_stream.wait_event(consumed[slot])  # step i-2 no longer reads this slot
+            for h, d in zip(srcs, bufs_in[slot]):
                 d.copy_(h, non_blocking=True)
-            step(host_in[0][1], host_in[1][1] if len(host_in) > 1 else None,
-                 host_in[2][1] if len(host_in) > 2 else None)
+            loaded[slot].record(copy_stream)
+
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    copy_stream.wait_event(e0)
+    load(0)
+    for i in range(e2e_steps):
+        if i + 1 < e2e_steps:
+            load(i + 1)
+        slot = i % 2
+        stream.wait_event(loaded[slot])
+        with torch.cuda.stream(stream):
+            ins = bufs_in[slot] + [None, None]
+            step(ins[0], ins[1], ins[2])
+            consumed[slot].record(stream)
             for d, h in host_out:
                 h.copy_(d, non_blocking=True)
-        e1.record(stream)
+    e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     clk = clocks.stop()
-    h2d = sum(d.numel() * d.element_size() for _, d in host_in)
+    h2d = sum(h.numel() * h.element_size() for h in srcs)
     d2h = sum(h.numel() * h.element_size() for _, h in host_out)
 
     if world > 1:
