@@ -224,7 +224,7 @@ def make_step(shape, inp, dev, stream):
         b = layer.MoEBuffers(T, H, E, K, Hp, shape.dtype, dev, backward=(mode == "fwd_bwd"))
         calls = [
             ("route", lambda xi, dyi, dxsi: L.moe_route(xi, wr_d, bias_d, T, H, E, K, b.cdt, b.logits, b.idx, b.gate,
-                                                       stream=stream)),
+                                                       b.ws_route, b.ws_route_bytes, stream=stream)),
             ("dispatch", lambda xi, dyi, dxsi: L.moe_dispatch(xi, b.idx, T, H, E, K, b.cdt, b.cu, b.dst_row,
                                                              b.src_tok, b.xs, b.ws_dispatch, b.ws_dispatch_bytes,
                                                              stream=stream)),
@@ -256,7 +256,7 @@ def make_step(shape, inp, dev, stream):
         ("mod_select", lambda xi, dyi, dxsi: L.mod_select(xi, wmod_d, Bq, Lq, H, C, m.cdt, m.score, m.sel,
                                                          m.sel_score, m.mask, m.x_sel, m.y, stream=stream)),
         ("route", lambda xi, dyi, dxsi: L.moe_route(m.x_sel, wr_d, bias_d, T, H, E, K, b.cdt, b.logits, b.idx,
-                                                   b.gate, stream=stream)),
+                                                   b.gate, b.ws_route, b.ws_route_bytes, stream=stream)),
         ("dispatch", lambda xi, dyi, dxsi: L.moe_dispatch(m.x_sel, b.idx, T, H, E, K, b.cdt, b.cu, b.dst_row,
                                                          b.src_tok, b.xs, b.ws_dispatch, b.ws_dispatch_bytes,
                                                          stream=stream)),

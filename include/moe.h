@@ -102,8 +102,10 @@ MOE_API int moe_last_device_error(void* stream);
  *   logit_bias [E]     float, nullable (added before softmax and selection)
  *   logits     [T,E]   float out (kept for moe_route_bwd)
  *   topk_idx   [T,K]   int32 out;  topk_gate [T,K] float out
- *   1 <= K <= E <= 1024, K <= 16.  bf16 needs E % 8 == 0 and H % 64 == 0.
- *   Workspace: none (ws may be NULL).
+ *   1 <= K <= E <= 1024, K <= 16.  bf16 needs E % 8 == 0.
+ *   Workspace: moe_workspace_bytes(MOE_OP_ROUTE, T, H, E, K, 0) bytes (bf16; 0 when
+ *   the token tiles fill the GPU, then ws may be NULL): partial sums of the router
+ *   GEMM over slices of H, added in a fixed order.
  */
 MOE_API int moe_route(const void* x, const void* w_router, const float* logit_bias,
               int T, int H, int E, int K, int dtype,

@@ -48,7 +48,9 @@ def route_gpu(shape, x, wr, bias=None):
     idx = torch.empty((T, K), dtype=torch.int32, device=DEV)
     gate = torch.empty((T, K), dtype=torch.float32, device=DEV)
     b = None if bias is None else torch.from_numpy(bias).to(DEV)
-    L.moe_route(dev(x), dev(wr), b, T, shape.H, E, K, CDT[shape.dtype], logits, idx, gate)
+    nbytes = L.moe_workspace_bytes(L.MOE_OP_ROUTE, T, shape.H, E, K, 0)
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=DEV)
+    L.moe_route(dev(x), dev(wr), b, T, shape.H, E, K, CDT[shape.dtype], logits, idx, gate, ws, nbytes)
     torch.cuda.synchronize()
     return logits.cpu().numpy(), idx.cpu().numpy(), gate.cpu().numpy()
 

@@ -614,18 +614,37 @@ int launch_expert_ffn_tc(const void* xs, const int32_t* cu, int rows, const void
   return launch<EPI_BF16, false, false, 256, 4, 1, 1>(mA2, mD, mD, p2, mtiles * ((H + 255) / 256), s);
 }
 
-// logits = x W_r + bias  (bf16 inputs, fp32 out); E % 8 == 0, H % 8 == 0
-int launch_router_tc(const void* x, const void* w, const float* bias, int T, int H, int E, float* logits,
+static int router_bn(int E) { return E <= 64 ? 64 : E <= 128 ? 128 : 256; }
+
+// Splits of H for the router GEMM: a CTA streams x from DRAM at a limited rate,
+// so when the token tiles alone would occupy fewer than about 100 of the 152
+// SMs the reduction over H is split (fp32 partials summed by the softmax pass).
+int router_tc_splits(int T, int H, int E) {
+  const long long tiles = ((T + tc::BM - 1) / tc::BM) * (long long)((E + router_bn(E) - 1) / router_bn(E));
+  if (tiles >= 100) return 1;
+  long long s = 152 / (tiles > 0 ? tiles : 1);
+  const long long kb = (H + tc::BK - 1) / tc::BK;
+  if (s > kb) s = kb;
+  if (s > 8) s = 8;
+  return s < 1 ? 1 : (int)s;
+}
+
+// out = x W_r (+ bias when S == 1): bf16 inputs, fp32 [T,E]; with S > 1, out
+// holds S partial sums [S][T][E] over consecutive slices of H (no bias).
+// E % 8 == 0, H % 8 == 0.
+int launch_router_tc(const void* x, const void* w, const float* bias, int T, int H, int E, float* out, int S,
                      cudaStream_t s) {
   using namespace tc;
   CUtensorMap mA, mB;
   if (!map_2d_as_3d(&mA, x, H, T, BK, BM)) return MOE_ERR_CUDA;
   if (!map_3d(&mB, w, E, H, 1, 64, BK)) return MOE_ERR_CUDA;
-  Params p = params(nullptr, 1, T, E, H, logits, E, bias);
-  const long long mtiles = (T + BM - 1) / BM;
-  if (E <= 64) return launch<EPI_F32_BIAS, false, true, 64, 8, 1, 1>(mA, mB, mB, p, mtiles, s);
-  if (E <= 128) return launch<EPI_F32_BIAS, false, true, 128, 6, 1, 1>(mA, mB, mB, p, mtiles, s);
-  return launch<EPI_F32_BIAS, false, true, 256, 4, 1, 1>(mA, mB, mB, p, mtiles * ((E + 255) / 256), s);
+  Params p = params(nullptr, 1, T, E, H, out, E, S > 1 ? nullptr : bias);
+  p.ksplit = S;
+  p.part_stride = (long long)T * E;
+  const long long tiles = (T + BM - 1) / BM * (long long)S;
+  if (E <= 64) return launch<EPI_F32_BIAS, false, true, 64, 8, 1, 1>(mA, mB, mB, p, tiles, s);
+  if (E <= 128) return launch<EPI_F32_BIAS, false, true, 128, 6, 1, 1>(mA, mB, mB, p, tiles, s);
+  return launch<EPI_F32_BIAS, false, true, 256, 4, 1, 1>(mA, mB, mB, p, tiles * ((E + 255) / 256), s);
 }
 
 // Split count for the router weight gradient on tensor cores: about one CTA

@@ -34,15 +34,41 @@ __device__ __forceinline__ int slot_expert(int slot, int lane) {
   return ((slot >> 2) * 32 + lane) * 4 + (slot & 3);
 }
 
+// With S > 1 the router GEMM left S partial sums over slices of H in `part`
+// ([S][T][E]); they are added in slice order, the bias added last, and the
+// logits written before the softmax (a fixed order: the same bits every run).
 template <int VPL>
 __global__ void __launch_bounds__(32 * ROWS_PER_CTA)
-softmax_topk_kernel(const float* __restrict__ logits, int T, int E, int K,
+softmax_topk_kernel(float* __restrict__ logits, const float* __restrict__ part, int S,
+                    const float* __restrict__ bias, int T, int E, int K,
                     int32_t* __restrict__ idx, float* __restrict__ gate) {
   const int lane = threadIdx.x & 31;
   const long long nwarps = (long long)gridDim.x * ROWS_PER_CTA;
   for (long long t = (long long)blockIdx.x * ROWS_PER_CTA + (threadIdx.x >> 5); t < T; t += nwarps) {
     float v[VPL];
-    load_row<VPL>(logits + t * E, E, lane, v);
+    if (S > 1) {
+      load_row<VPL>(part + t * E, E, lane, v);
+      for (int s = 1; s < S; ++s) {
+        float w[VPL];
+        load_row<VPL>(part + (long long)s * T * E + t * E, E, lane, w);
+#pragma unroll
+        for (int j = 0; j < VPL; ++j) v[j] += w[j];
+      }
+#pragma unroll
+      for (int q = 0; q < VPL / 4; ++q) {
+        const int e4 = (q * 32 + lane) * 4;
+        if (e4 < E) {
+          if (bias) {
+            const float4 bb = __ldg(reinterpret_cast<const float4*>(bias + e4));
+            v[4 * q] += bb.x; v[4 * q + 1] += bb.y; v[4 * q + 2] += bb.z; v[4 * q + 3] += bb.w;
+          }
+          *reinterpret_cast<float4*>(logits + t * E + e4) = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2],
+                                                                        v[4 * q + 3]);
+        }
+      }
+    } else {
+      load_row<VPL>(logits + t * E, E, lane, v);
+    }
     float m = -INFINITY;
 #pragma unroll
     for (int j = 0; j < VPL; ++j) m = fmaxf(m, v[j]);
@@ -527,32 +553,46 @@ size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
 }  // namespace
 
-int launch_router_tc(const void* x, const void* w, const float* bias, int T, int H, int E, float* logits,
+int launch_router_tc(const void* x, const void* w, const float* bias, int T, int H, int E, float* out, int S,
                      cudaStream_t s);
+int router_tc_splits(int T, int H, int E);
 
-// bf16: tcgen05 GEMM with the bias added in the epilogue.  fp32: FFMA GEMM.
-int launch_router_logits(const void* x, const void* w, const float* bias, int T, int H, int E,
-                         int dtype, float* logits, cudaStream_t s) {
-  if (dtype == MOE_BF16) return launch_router_tc(x, w, bias, T, H, E, logits, s);
-  SimtGemmArgs a{};
-  a.A = x; a.a_sm = H; a.a_sk = 1;
-  a.B = w; a.b_sg = 0; a.b_sk = E; a.b_sn = 1;
-  a.C = logits; a.c_sm = E;
-  a.bias = bias; a.cu = nullptr;
-  a.M = T; a.N = E; a.K = H; a.groups = 1;
-  a.epilogue = 2; a.swiglu = false;
-  return launch_simt_gemm(a, dtype, dtype, MOE_F32, s);
+size_t route_ws_bytes(int T, int H, int E) {
+  const int S = router_tc_splits(T, H, E);
+  return S > 1 ? align256((size_t)S * T * E * 4) : 0;
 }
 
-int launch_softmax_topk(const float* logits, int T, int E, int K, int32_t* idx, float* gate,
-                        cudaStream_t s) {
+// Router forward.  bf16: tcgen05 GEMM, split over H into S partial sums when
+// the token tiles alone would leave SMs idle (the partials, the bias and the
+// softmax/top-k meet in one pass); fp32: FFMA GEMM with the bias in its epilogue.
+int launch_route(const void* x, const void* w, const float* bias, int T, int H, int E, int K, int dtype,
+                 float* logits, int32_t* idx, float* gate, void* ws, cudaStream_t s) {
   if (T == 0) return MOE_OK;
-  int grid = rows_grid(T);
-  int vpl = (E + 127) / 128 * 4;
-  if (vpl <= 4) softmax_topk_kernel<4><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, T, E, K, idx, gate);
-  else if (vpl <= 8) softmax_topk_kernel<8><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, T, E, K, idx, gate);
-  else if (vpl <= 16) softmax_topk_kernel<16><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, T, E, K, idx, gate);
-  else softmax_topk_kernel<32><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, T, E, K, idx, gate);
+  int S = 1;
+  float* part = nullptr;
+  int st;
+  if (dtype == MOE_BF16) {
+    S = router_tc_splits(T, H, E);
+    part = S > 1 ? static_cast<float*>(ws) : nullptr;
+    st = launch_router_tc(x, w, bias, T, H, E, S > 1 ? part : logits, S, s);
+  } else {
+    SimtGemmArgs a{};
+    a.A = x; a.a_sm = H; a.a_sk = 1;
+    a.B = w; a.b_sg = 0; a.b_sk = E; a.b_sn = 1;
+    a.C = logits; a.c_sm = E;
+    a.bias = bias; a.cu = nullptr;
+    a.M = T; a.N = E; a.K = H; a.groups = 1;
+    a.epilogue = 2; a.swiglu = false;
+    st = launch_simt_gemm(a, dtype, dtype, MOE_F32, s);
+  }
+  if (st != MOE_OK) return st;
+  const int grid = rows_grid(T);
+  const int vpl = (E + 127) / 128 * 4;
+  const float* pb = S > 1 ? bias : nullptr;
+  if (vpl <= 4) softmax_topk_kernel<4><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, part, S, pb, T, E, K, idx, gate);
+  else if (vpl <= 8) softmax_topk_kernel<8><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, part, S, pb, T, E, K, idx, gate);
+  else if (vpl <= 16) softmax_topk_kernel<16><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, part, S, pb, T, E, K, idx, gate);
+  else softmax_topk_kernel<32><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, part, S, pb, T, E, K, idx, gate);
   return launch_status();
 }
 

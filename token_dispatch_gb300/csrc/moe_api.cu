@@ -69,6 +69,7 @@ size_t moe_workspace_bytes(int op, int T, int H, int E, int K, int Hp) {
   (void)Hp;
   if (T < 0 || H < 0 || E < 0 || K < 0) return 0;
   switch (op) {
+    case MOE_OP_ROUTE: return (E > 0 && H > 0) ? route_ws_bytes(T, H, E) : 0;
     case MOE_OP_DISPATCH: return E > 0 ? dispatch_ws_bytes(T, E, K) : 0;
     case MOE_OP_ROUTE_BWD: return (E > 0 && H > 0) ? route_bwd_ws_bytes(T, H, E) : 0;
     default: return 0;
@@ -91,18 +92,17 @@ int moe_last_device_error(void* stream) {
 int moe_route(const void* x, const void* w_router, const float* logit_bias, int T, int H, int E,
               int K, int dtype, float* logits, int32_t* topk_idx, float* topk_gate, void* ws,
               size_t ws_bytes, void* stream) {
-  (void)ws; (void)ws_bytes;
   if (!valid_dtype(dtype) || T < 0 || H < 1 || E < 1 || E > 1024 || K < 1 || K > E || K > 16)
     return MOE_ERR_INVALID_ARG;
   if ((T > 0 && (!x || !logits || !topk_idx || !topk_gate)) || !w_router) return MOE_ERR_INVALID_ARG;
-  if (!all_aligned({x, w_router, logit_bias, logits, topk_idx, topk_gate})) return MOE_ERR_MISALIGNED;
+  if (!all_aligned({x, w_router, logit_bias, logits, topk_idx, topk_gate, ws})) return MOE_ERR_MISALIGNED;
   if (H % vec_elems(dtype) != 0 || E % 4 != 0) return MOE_ERR_UNSUPPORTED;
   if (dtype == MOE_BF16 && E % 8 != 0) return MOE_ERR_UNSUPPORTED;  // 16-byte rows of W_r for TMA
   if (T == 0) return MOE_OK;
-  cudaStream_t s = as_stream(stream);
-  int st = launch_router_logits(x, w_router, logit_bias, T, H, E, dtype, logits, s);
-  if (st != MOE_OK) return st;
-  return launch_softmax_topk(logits, T, E, K, topk_idx, topk_gate, s);
+  const size_t need = dtype == MOE_BF16 ? route_ws_bytes(T, H, E) : 0;
+  if (need > 0 && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;
+  return launch_route(x, w_router, logit_bias, T, H, E, K, dtype, logits, topk_idx, topk_gate, ws,
+                      as_stream(stream));
 }
 
 int moe_dispatch(const void* x, const int32_t* topk_idx, int T, int H, int E, int K, int dtype,

@@ -102,10 +102,9 @@ inline int launch_status() {
 // Each returns a moe_status.  Arguments have been validated by the C ABI layer.
 
 // route
-int launch_router_logits(const void* x, const void* w, const float* bias, int T, int H, int E,
-                         int dtype, float* logits, cudaStream_t s);
-int launch_softmax_topk(const float* logits, int T, int E, int K, int32_t* idx, float* gate,
-                        cudaStream_t s);
+size_t route_ws_bytes(int T, int H, int E);
+int launch_route(const void* x, const void* w, const float* bias, int T, int H, int E, int K, int dtype,
+                 float* logits, int32_t* idx, float* gate, void* ws, cudaStream_t s);
 int launch_route_bwd(int mode, const float* d_gate, const float* logits, const int32_t* idx,
                      const void* x, const void* w, int T, int H, int E, int K, int dtype,
                      float* d_logits, float* dw, void* dx, bool dx_write, void* ws, cudaStream_t s);

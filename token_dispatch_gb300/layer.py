@@ -47,6 +47,8 @@ class MoEBuffers:
         self.y = torch.empty((T, H), dtype=tdt, device=dev)
         self.ws_dispatch_bytes = L.moe_workspace_bytes(L.MOE_OP_DISPATCH, T, H, E, K, Hp)
         self.ws_dispatch = _ws(self.ws_dispatch_bytes, dev)
+        self.ws_route_bytes = L.moe_workspace_bytes(L.MOE_OP_ROUTE, T, H, E, K, Hp)
+        self.ws_route = _ws(self.ws_route_bytes, dev)
         if backward:
             self.dh = torch.empty((R, H), dtype=tdt, device=dev)
             self.d_gate = torch.empty((T, K), dtype=f32, device=dev)
@@ -61,7 +63,8 @@ def moe_forward(b: MoEBuffers, x, w_router, logit_bias, w_gate, w_up, w_down, st
                 row_scale=None, residual=None, out_row=None, y=None):
     """One MoE forward pass into the buffers of ``b`` (y defaults to ``b.y``)."""
     T, H, E, K, Hp, dt = b.T, b.H, b.E, b.K, b.Hp, b.cdt
-    L.moe_route(x, w_router, logit_bias, T, H, E, K, dt, b.logits, b.idx, b.gate, stream=stream)
+    L.moe_route(x, w_router, logit_bias, T, H, E, K, dt, b.logits, b.idx, b.gate, b.ws_route, b.ws_route_bytes,
+                stream=stream)
     L.moe_dispatch(x, b.idx, T, H, E, K, dt, b.cu, b.dst_row, b.src_tok, b.xs, b.ws_dispatch,
                    b.ws_dispatch_bytes, stream=stream)
     L.moe_expert_ffn(b.xs, b.cu, T * K, w_gate, w_up, w_down, E, H, Hp, dt, b.act, b.h, stream=stream)
