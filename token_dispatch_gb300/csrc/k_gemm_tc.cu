@@ -222,11 +222,16 @@ __device__ __forceinline__ TileInfo decode(int t, const int* mt_pre, int G, int 
   return ti;
 }
 
-template <int EPI, bool A_MN, bool B_MN, int BN, int STAGES, int NA, int NB>
+// KSUB > 1: the NA = NB = KSUB tile pairs of a stage are consecutive 64-wide
+// slices of K (a stage covers 64*KSUB of K), so each row of a streamed operand
+// is requested as 128*KSUB contiguous bytes at once.
+template <int EPI, bool A_MN, bool B_MN, int BN, int STAGES, int NA, int NB, int KSUB = 1>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmB2, const Params p) {
   using C = Cfg<BN, EPI, NA, NB>;
+  static_assert(KSUB == 1 || (NA == KSUB && NB == KSUB && !A_MN), "k sub-blocks pair A and B slices");
+  constexpr int KSTAGE = BK * KSUB;  // K covered by one stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_base = smem;
@@ -301,7 +306,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const uint32_t tmem_base = tmem_base_slot;
   const int total_tiles = total_tiles_s;
   const int base_tiles = total_tiles / p.ksplit;  // tiles of one K range
-  const int KB_ALL = (p.K + BK - 1) / BK;
+  const int KB_ALL = (p.K + KSTAGE - 1) / KSTAGE;
   // k-blocks [kb_lo, kb_hi) of split s (every split non-empty: ksplit <= KB_ALL)
   auto kb_lo = [&](int s) { return (int)((long long)s * KB_ALL / p.ksplit); };
 
@@ -321,7 +326,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, &abort_flag, p)) { ok = false; break; }
           const uint32_t a_dst = smem_u32(stage_base + stage * C::STAGE_BYTES);
           const uint32_t b_dst = a_dst + NA * A_STAGE_BYTES;
-          const int k0 = kb * BK;
+          const int k0 = kb * KSTAGE;
           mbar_expect_tx(full_bar(stage), C::STAGE_BYTES);
           filled_parity[stage] = (int)phase;
 #pragma unroll
@@ -331,13 +336,15 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
               tma_load_3d(dst, &tmA, full_bar(stage), ti.row0, k0, ia);
               tma_load_3d(dst + 64 * BK * 2, &tmA, full_bar(stage), ti.row0 + 64, k0, ia);
             } else {
-              tma_load_3d(dst, &tmA, full_bar(stage), k0, ti.row0, ia);
+              if (KSUB > 1) tma_load_3d(dst, &tmA, full_bar(stage), k0 + ia * BK, ti.row0, 0);
+              else tma_load_3d(dst, &tmA, full_bar(stage), k0, ti.row0, ia);
             }
           }
 #pragma unroll
           for (int ib = 0; ib < NB; ++ib) {
             const uint32_t dst = b_dst + ib * C::B_TILE_BYTES;
-            const int z = NB > 1 ? ib : ti.g;
+            const int z = (NB > 1 && KSUB == 1) ? ib : ti.g;
+            const int kb0 = KSUB > 1 ? k0 + ib * BK : k0;
             if (EPI == EPI_SWIGLU) {
 #pragma unroll
               for (int c = 0; c < BN / 64; ++c) {
@@ -348,9 +355,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             } else if (B_MN) {
 #pragma unroll
               for (int c = 0; c < BN / 64; ++c)
-                tma_load_3d(dst + c * (64 * BK * 2), &tmB, full_bar(stage), ti.n0 + c * 64, k0, z);
+                tma_load_3d(dst + c * (64 * BK * 2), &tmB, full_bar(stage), ti.n0 + c * 64, kb0, z);
             } else {
-              tma_load_3d(dst, &tmB, full_bar(stage), k0, ti.n0, z);
+              tma_load_3d(dst, &tmB, full_bar(stage), kb0, ti.n0, z);
             }
           }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -556,13 +563,13 @@ bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims
 
 unsigned long long g_wait_limit = 4000000000ull;  // ~2 s at 2 GHz
 
-template <int EPI, bool A_MN, bool B_MN, int BN, int STAGES, int NA, int NB>
+template <int EPI, bool A_MN, bool B_MN, int BN, int STAGES, int NA, int NB, int KSUB = 1>
 int launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const Params& p,
            long long tiles_upper, cudaStream_t s) {
   using C = Cfg<BN, EPI, NA, NB>;
   const size_t smem = (size_t)STAGES * C::STAGE_BYTES + (2 * STAGES + 5) * 8 + 1024;
   static_assert((size_t)STAGES * C::STAGE_BYTES + (2 * STAGES + 5) * 8 + 1024 <= 227 * 1024, "smem");
-  auto k = tc_gemm_kernel<EPI, A_MN, B_MN, BN, STAGES, NA, NB>;
+  auto k = tc_gemm_kernel<EPI, A_MN, B_MN, BN, STAGES, NA, NB, KSUB>;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return MOE_ERR_CUDA;
   long long grid = sm_count();
@@ -623,7 +630,9 @@ int router_tc_splits(int T, int H, int E) {
   const long long tiles = ((T + tc::BM - 1) / tc::BM) * (long long)((E + router_bn(E) - 1) / router_bn(E));
   if (tiles >= 100) return 1;
   long long s = 152 / (tiles > 0 ? tiles : 1);
-  const long long kb = (H + tc::BK - 1) / tc::BK;
+  // every split needs at least one stage of K (64 * k sub-blocks per stage)
+  const int ksub = E <= 64 ? 4 : E <= 128 ? 2 : 1;
+  const long long kb = (H + tc::BK * ksub - 1) / (tc::BK * ksub);
   if (s > kb) s = kb;
   if (s > 8) s = 8;
   return s < 1 ? 1 : (int)s;
@@ -642,8 +651,10 @@ int launch_router_tc(const void* x, const void* w, const float* bias, int T, int
   p.ksplit = S;
   p.part_stride = (long long)T * E;
   const long long tiles = (T + BM - 1) / BM * (long long)S;
-  if (E <= 64) return launch<EPI_F32_BIAS, false, true, 64, 8, 1, 1>(mA, mB, mB, p, tiles, s);
-  if (E <= 128) return launch<EPI_F32_BIAS, false, true, 128, 6, 1, 1>(mA, mB, mB, p, tiles, s);
+  // x is streamed from DRAM once: stages of 4 (2) consecutive 64-wide K slices
+  // request 512 (256) contiguous bytes of every row at a time
+  if (E <= 64) return launch<EPI_F32_BIAS, false, true, 64, 2, 4, 4, 4>(mA, mB, mB, p, tiles, s);
+  if (E <= 128) return launch<EPI_F32_BIAS, false, true, 128, 3, 2, 2, 2>(mA, mB, mB, p, tiles, s);
   return launch<EPI_F32_BIAS, false, true, 256, 4, 1, 1>(mA, mB, mB, p, tiles * ((E + 255) / 256), s);
 }
 
