@@ -24,14 +24,6 @@ constexpr int RF_WARPS = 16;  // 512 threads, one CTA per SM (W_r fills shared m
 constexpr int RF_TPW = 4;     // tokens per warp pass
 
 template <typename T> constexpr int chunk_rows() { return 16 / (int)sizeof(T); }
-
-template <typename T> __device__ __forceinline__ void unpack16(const uint4& q, float* v);
-template <> __device__ __forceinline__ void unpack16<bf16>(const uint4& q, float* v) {
-  Vec16<bf16>::load_raw_unpack(q, v);
-}
-template <> __device__ __forceinline__ void unpack16<float>(const uint4& q, float* v) {
-  v[0] = __uint_as_float(q.x); v[1] = __uint_as_float(q.y); v[2] = __uint_as_float(q.z); v[3] = __uint_as_float(q.w);
-}
 template <int EP, typename T> constexpr int chunk_stride() { return chunk_rows<T>() * EP + 4; }
 
 template <int EP>
@@ -75,17 +67,12 @@ router_fused_kernel(const T* __restrict__ x, const T* __restrict__ w, const floa
   constexpr int CS = chunk_stride<EP, T>();  // padded chunk stride (floats)
   extern __shared__ __align__(16) float wsm[];
   const int nchunk = H / V;
-  // one W_r row (E values) per thread and step
-  for (int h = threadIdx.x; h < H; h += blockDim.x) {
-    float* dst = wsm + (h / V) * CS + (h % V) * EP;
-    const T* src = w + (long long)h * E;
-#pragma unroll
-    for (int e = 0; e < EP; ++e) dst[e] = e < E ? to_f32(src[e]) : 0.f;
+  for (int i = threadIdx.x; i < nchunk * CF; i += blockDim.x) {
+    const int c = i / CF, r = i % CF;
+    const int h = c * V + r / EP, e = r % EP;
+    wsm[c * CS + r] = e < E ? to_f32(w[(long long)h * E + e]) : 0.f;
   }
   __syncthreads();
-  // chunk columns processed per pass: their CU * TPW 16-byte loads are issued
-  // before any arithmetic, so each lane keeps that many reads in flight
-  constexpr int CU = EP <= 8 ? 4 : 2;
   const int lane = threadIdx.x & 31;
   const long long nw = (long long)gridDim.x * RF_WARPS;
   for (long long t0 = ((long long)blockIdx.x * RF_WARPS + (threadIdx.x >> 5)) * RF_TPW; t0 < Tn;
@@ -95,38 +82,30 @@ router_fused_kernel(const T* __restrict__ x, const T* __restrict__ w, const floa
     for (int j = 0; j < RF_TPW; ++j)
 #pragma unroll
       for (int e = 0; e < EP; ++e) acc[j][e] = 0.f;
-    for (int c0 = lane; c0 < nchunk; c0 += 32 * CU) {
-      uint4 raw[CU][RF_TPW];
+    for (int c = lane; c < nchunk; c += 32) {
+      float xv[RF_TPW][V];
 #pragma unroll
-      for (int u = 0; u < CU; ++u) {
-        const int c = c0 + 32 * u;
+      for (int j = 0; j < RF_TPW; ++j) {
+        if (t0 + j < Tn) {
+          Vec16<T>::load(x + (t0 + j) * H + (long long)c * V, xv[j]);
+        } else {
+#pragma unroll
+          for (int v = 0; v < V; ++v) xv[j][v] = 0.f;
+        }
+      }
+      const float* wc = wsm + c * CS;
+#pragma unroll
+      for (int hv = 0; hv < V; ++hv) {
+        float wr[EP];
+#pragma unroll
+        for (int q = 0; q < EP / 4; ++q) {
+          const float4 f = *reinterpret_cast<const float4*>(wc + hv * EP + 4 * q);
+          wr[4 * q] = f.x; wr[4 * q + 1] = f.y; wr[4 * q + 2] = f.z; wr[4 * q + 3] = f.w;
+        }
 #pragma unroll
         for (int j = 0; j < RF_TPW; ++j)
-          raw[u][j] = (c < nchunk && t0 + j < Tn)
-                          ? __ldg(reinterpret_cast<const uint4*>(x + (t0 + j) * H + (long long)c * V))
-                          : make_uint4(0, 0, 0, 0);
-      }
 #pragma unroll
-      for (int u = 0; u < CU; ++u) {
-        const int c = c0 + 32 * u;
-        if (c >= nchunk) break;
-        float xv[RF_TPW][V];
-#pragma unroll
-        for (int j = 0; j < RF_TPW; ++j) unpack16<T>(raw[u][j], xv[j]);
-        const float* wc = wsm + c * CS;
-#pragma unroll
-        for (int hv = 0; hv < V; ++hv) {
-          float wr[EP];
-#pragma unroll
-          for (int q = 0; q < EP / 4; ++q) {
-            const float4 f = *reinterpret_cast<const float4*>(wc + hv * EP + 4 * q);
-            wr[4 * q] = f.x; wr[4 * q + 1] = f.y; wr[4 * q + 2] = f.z; wr[4 * q + 3] = f.w;
-          }
-#pragma unroll
-          for (int j = 0; j < RF_TPW; ++j)
-#pragma unroll
-            for (int e = 0; e < EP; ++e) acc[j][e] = fmaf(xv[j][hv], wr[e], acc[j][e]);
-        }
+          for (int e = 0; e < EP; ++e) acc[j][e] = fmaf(xv[j][hv], wr[e], acc[j][e]);
       }
     }
 #pragma unroll
