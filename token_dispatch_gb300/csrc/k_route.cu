@@ -557,25 +557,17 @@ int launch_router_tc(const void* x, const void* w, const float* bias, int T, int
                      cudaStream_t s);
 int router_tc_splits(int T, int H, int E);
 
-bool router_fused_ok(int H, int E, int dtype);
-int launch_router_fused(const void* x, const void* w, const float* bias, int T, int H, int E, int K, int dtype,
-                        float* logits, int32_t* idx, float* gate, cudaStream_t s);
-
-// bf16 workspace of the tensor-core router (none for the one-launch router)
 size_t route_ws_bytes(int T, int H, int E) {
-  if (router_fused_ok(H, E, MOE_BF16)) return 0;
   const int S = router_tc_splits(T, H, E);
   return S > 1 ? align256((size_t)S * T * E * 4) : 0;
 }
 
-// Router forward.  E <= 16: one streaming launch (GEMV, softmax, top-k).
-// Otherwise bf16: tcgen05 GEMM, split over H into S partial sums when the
-// token tiles alone would leave SMs idle (the partials, the bias and the
+// Router forward.  bf16: tcgen05 GEMM, split over H into S partial sums when
+// the token tiles alone would leave SMs idle (the partials, the bias and the
 // softmax/top-k meet in one pass); fp32: FFMA GEMM with the bias in its epilogue.
 int launch_route(const void* x, const void* w, const float* bias, int T, int H, int E, int K, int dtype,
                  float* logits, int32_t* idx, float* gate, void* ws, cudaStream_t s) {
   if (T == 0) return MOE_OK;
-  if (router_fused_ok(H, E, dtype)) return launch_router_fused(x, w, bias, T, H, E, K, dtype, logits, idx, gate, s);
   int S = 1;
   float* part = nullptr;
   int st;
