@@ -70,7 +70,7 @@ def test_argument_errors_are_reported_before_launch(libmoe):
     # E not a multiple of 4
     assert raw.moe_route(A, A, None, 4, 64, 6, 2, L.MOE_F32, A, A, A, None, 0, None) == L.MOE_ERR_UNSUPPORTED
     # bf16 router with idle SMs needs its partial-sum workspace
-    assert raw.moe_route(A, A, None, 1024, 256, 8, 2, L.MOE_BF16, A, A, A, None, 0, None) == L.MOE_ERR_WORKSPACE
+    assert raw.moe_route(A, A, None, 1024, 2048, 8, 2, L.MOE_BF16, A, A, A, None, 0, None) == L.MOE_ERR_WORKSPACE
     # workspace too small
     need = L.moe_workspace_bytes(L.MOE_OP_DISPATCH, 1000, 64, 8, 2, 0)
     assert raw.moe_dispatch(A, A, 1000, 64, 8, 2, L.MOE_F32, A, A, A, A, A, need - 256, None) == L.MOE_ERR_WORKSPACE
