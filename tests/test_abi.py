@@ -46,9 +46,11 @@ def test_status_strings_and_version(libmoe):
 
 def test_workspace_sizes(libmoe):
     L = libmoe
-    # router: 64 token tiles of 128 leave SMs idle -> partial sums over slices of H
-    r = L.moe_workspace_bytes(L.MOE_OP_ROUTE, 8192, 4096, 8, 2, 14336)
-    assert r >= 2 * 8192 * 8 * 4 and r % 256 == 0
+    # router: 8 or 16 experts stream in one launch without workspace; on the
+    # GEMM path 64 token tiles of 128 leave SMs idle -> partial sums over slices of H
+    assert L.moe_workspace_bytes(L.MOE_OP_ROUTE, 8192, 4096, 8, 2, 14336) == 0
+    r = L.moe_workspace_bytes(L.MOE_OP_ROUTE, 8192, 4096, 32, 2, 14336)
+    assert r >= 2 * 8192 * 32 * 4 and r % 256 == 0
     assert L.moe_workspace_bytes(L.MOE_OP_ROUTE, 16384, 2048, 64, 6, 1408) == 0
     assert L.moe_workspace_bytes(L.MOE_OP_EXPERT_FFN, 8192, 4096, 8, 2, 14336) == 0
     d = L.moe_workspace_bytes(L.MOE_OP_DISPATCH, 8192, 4096, 8, 2, 14336)
@@ -70,7 +72,7 @@ def test_argument_errors_are_reported_before_launch(libmoe):
     # E not a multiple of 4
     assert raw.moe_route(A, A, None, 4, 64, 6, 2, L.MOE_F32, A, A, A, None, 0, None) == L.MOE_ERR_UNSUPPORTED
     # bf16 router with idle SMs needs its partial-sum workspace
-    assert raw.moe_route(A, A, None, 1024, 2048, 8, 2, L.MOE_BF16, A, A, A, None, 0, None) == L.MOE_ERR_WORKSPACE
+    assert raw.moe_route(A, A, None, 1024, 2048, 32, 2, L.MOE_BF16, A, A, A, None, 0, None) == L.MOE_ERR_WORKSPACE
     # workspace too small
     need = L.moe_workspace_bytes(L.MOE_OP_DISPATCH, 1000, 64, 8, 2, 0)
     assert raw.moe_dispatch(A, A, 1000, 64, 8, 2, L.MOE_F32, A, A, A, A, A, need - 256, None) == L.MOE_ERR_WORKSPACE

@@ -28,6 +28,15 @@ SHAPES = [
 ]
 ROUTE_ONLY = [S("bf16_T300_H128_E384_K8", 300, 128, 384, 8, 64, "bf16"),
               S("f32_T129_H32_E1024_K16", 129, 32, 1024, 16, 32, "f32")]
+# bf16 routers with 8 or 16 experts and H a multiple of 512 take the one-launch
+# streaming router: ragged token blocks of 8 to 64 tokens, fewer blocks than
+# SMs, slices of H from 32 to 256 columns per warp
+ROUTE_STREAM = [S("bf16_T2053_H1536_E8_K2", 2053, 1536, 8, 2, 64, "bf16"),
+                S("bf16_T1000_H512_E16_K4", 1000, 512, 16, 4, 64, "bf16"),
+                S("bf16_T5_H4096_E8_K1", 5, 4096, 8, 1, 64, "bf16"),
+                S("bf16_T3001_H4096_E16_K16", 3001, 4096, 16, 16, 64, "bf16"),
+                S("bf16_T4099_H512_E8_K3", 4099, 512, 8, 3, 64, "bf16"),
+                S("bf16_T333_H1024_E8_K2", 333, 1024, 8, 2, 64, "bf16")]
 CDT = {"f32": L.MOE_F32, "bf16": L.MOE_BF16}
 
 
@@ -55,7 +64,7 @@ def route_gpu(shape, x, wr, bias=None):
     return logits.cpu().numpy(), idx.cpu().numpy(), gate.cpu().numpy()
 
 
-@pytest.mark.parametrize("shape", SHAPES + ROUTE_ONLY, ids=ids(SHAPES + ROUTE_ONLY))
+@pytest.mark.parametrize("shape", SHAPES + ROUTE_ONLY + ROUTE_STREAM, ids=ids(SHAPES + ROUTE_ONLY + ROUTE_STREAM))
 def test_route_matches_oracle(shape):
     x, wr = synth.router_inputs(shape)
     bias = synth.expert_bias(shape.E, 0.7, expert=1)
@@ -69,11 +78,12 @@ def test_route_matches_oracle(shape):
     assert_close(gate[same], r_gate[same], gate_tol(logit_err), "gate")
 
 
-@pytest.mark.parametrize("dtype,E,K", [("f32", 8, 2), ("bf16", 16, 4), ("bf16", 384, 8), ("f32", 64, 6)])
-def test_route_integer_inputs_select_exactly(dtype, E, K):
+@pytest.mark.parametrize("dtype,E,K,H", [("f32", 8, 2, 64), ("bf16", 16, 4, 64), ("bf16", 384, 8, 64),
+                                         ("f32", 64, 6, 64), ("bf16", 8, 2, 512), ("bf16", 16, 5, 1024)])
+def test_route_integer_inputs_select_exactly(dtype, E, K, H):
     """Small-integer x and W make every logit exact in fp32 on both sides, with
     many ties: the selection (tie -> lowest expert) must then match exactly."""
-    T, H = 700, 64
+    T = 700
     rng = np.random.default_rng(E)
     x = synth.store(rng.integers(-2, 3, size=(T, H)).astype(np.float64), dtype)
     wr = synth.store(rng.integers(-1, 2, size=(H, E)).astype(np.float64), dtype)

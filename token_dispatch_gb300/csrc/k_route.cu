@@ -558,16 +558,20 @@ int launch_router_tc(const void* x, const void* w, const float* bias, int T, int
 int router_tc_splits(int T, int H, int E);
 
 size_t route_ws_bytes(int T, int H, int E) {
+  if (router_stream_applies(MOE_BF16, H, E)) return 0;
   const int S = router_tc_splits(T, H, E);
   return S > 1 ? align256((size_t)S * T * E * 4) : 0;
 }
 
-// Router forward.  bf16: tcgen05 GEMM, split over H into S partial sums when
-// the token tiles alone would leave SMs idle (the partials, the bias and the
-// softmax/top-k meet in one pass); fp32: FFMA GEMM with the bias in its epilogue.
+// Router forward.  bf16 with 8 or 16 experts: one streaming launch (logits,
+// softmax and top-K); other bf16 shapes: tcgen05 GEMM, split over H into S
+// partial sums when the token tiles alone would leave SMs idle (the partials,
+// the bias and the softmax/top-k meet in one pass); fp32: FFMA GEMM with the
+// bias in its epilogue.
 int launch_route(const void* x, const void* w, const float* bias, int T, int H, int E, int K, int dtype,
                  float* logits, int32_t* idx, float* gate, void* ws, cudaStream_t s) {
   if (T == 0) return MOE_OK;
+  if (router_stream_applies(dtype, H, E)) return launch_router_stream(x, w, bias, T, H, E, K, logits, idx, gate, s);
   int S = 1;
   float* part = nullptr;
   int st;

@@ -103,6 +103,9 @@ inline int launch_status() {
 
 // route
 size_t route_ws_bytes(int T, int H, int E);
+bool router_stream_applies(int dtype, int H, int E);
+int launch_router_stream(const void* x, const void* w, const float* bias, int T, int H, int E, int K,
+                         float* logits, int32_t* idx, float* gate, cudaStream_t s);
 int launch_route(const void* x, const void* w, const float* bias, int T, int H, int E, int K, int dtype,
                  float* logits, int32_t* idx, float* gate, void* ws, cudaStream_t s);
 int launch_route_bwd(int mode, const float* d_gate, const float* logits, const int32_t* idx,
