@@ -38,6 +38,10 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
+# DRAM bytes (read + write) of one moe_expert_ffn call, both GEMM launches, from
+# an ncu capture of the kernels as they stand (profiles/expert_ffn_* give the
+# command); a workload without a capture reports null
+FFN_DRAM_BYTES = {}
 DEFAULT_WORKLOAD = "mixtral_bf16_T8192_H4096_E8_K2_Hp14336"
 
 
@@ -405,10 +409,23 @@ def run_ours(args, shape, rank, world, local):
 
     peaks, peak_src = measured_peaks()
     ffn_flops = 6.0 * R * H * Hp
-    tflops = ffn_flops / (call_ms["expert_ffn"] * 1e-3) / 1e12
+    ffn_s = call_ms["expert_ffn"] * 1e-3
+    b_el = 2 if shape.dtype == "bf16" else 4
+    # the pair's minimum DRAM bytes: every expert's three projections once, xs
+    # read, the SwiGLU output written and read back, h written
+    ffn_bytes = 3 * E * H * Hp * b_el + R * H * b_el + 2 * R * Hp * b_el + R * H * b_el
     # the timed region is well under a second: the burst peak applies
     peak_tf = peaks.get("bf16_tflops", 1900.0) if shape.dtype == "bf16" else None
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
+    if peak_tf and ffn_flops / (peak_tf * 1e12) >= ffn_bytes / (hbm_peak * 1e9):
+        roof = {"bound": "tensor", "achieved": ffn_flops / ffn_s / 1e12, "peak": peak_tf, "unit": "TFLOP/s",
+                "peak_source": f"{peak_src} bf16_tflops (burst)"}
+    else:  # weight streaming bounds the pair (few rows per expert)
+        roof = {"bound": "hbm", "achieved": ffn_bytes / ffn_s / 1e9, "peak": hbm_peak, "unit": "GB/s",
+                "peak_source": f"{peak_src} hbm_gbs"}
+    roof["frac"] = roof["achieved"] / roof["peak"] if roof["peak"] else None
+    roof["traffic"] = FFN_DRAM_BYTES.get(shape.name)
+    roof["algorithmic"] = {"flops": ffn_flops, "bytes": ffn_bytes}
     hbm = {}
     for name, nbytes in algorithmic_bytes(shape).items():
         if name in call_ms:
@@ -432,10 +449,7 @@ def run_ours(args, shape, rank, world, local):
                    "expert0_logit_bias": None if bias_entry is None else bias_entry["beta"],
                    "l2": "flushed between timed steps (512 MB write, then 512 MB read)", "parallelism": f"replicas{world}"},
         "calls_ms": {k: round(v, 4) for k, v in call_ms.items()},
-        "roofline": {"kernel": "moe_expert_ffn (grouped gate/up+SwiGLU GEMM + down GEMM, tcgen05)",
-                     "bound": "tensor", "achieved": tflops, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": (tflops / peak_tf) if peak_tf else None, "traffic": None,
-                     "peak_source": f"{peak_src} bf16_tflops (burst)"},
+        "roofline": {"kernel": "moe_expert_ffn (grouped gate/up+SwiGLU GEMM + down GEMM, tcgen05)", **roof},
         "hbm_roofline": {"peak_GB/s": hbm_peak, "peak_source": f"{peak_src} hbm_gbs", "calls": hbm},
         "e2e": {"value": world * n_tok / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},

@@ -79,7 +79,8 @@ def test_route_matches_oracle(shape):
 
 
 @pytest.mark.parametrize("dtype,E,K,H", [("f32", 8, 2, 64), ("bf16", 16, 4, 64), ("bf16", 384, 8, 64),
-                                         ("f32", 64, 6, 64), ("bf16", 8, 2, 512), ("bf16", 16, 5, 1024)])
+                                         ("f32", 64, 6, 64), ("bf16", 8, 2, 512), ("bf16", 16, 5, 1024),
+                                         ("bf16", 64, 6, 64), ("bf16", 40, 3, 2048)])
 def test_route_integer_inputs_select_exactly(dtype, E, K, H):
     """Small-integer x and W make every logit exact in fp32 on both sides, with
     many ties: the selection (tie -> lowest expert) must then match exactly."""

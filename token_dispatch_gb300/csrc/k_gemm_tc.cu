@@ -51,7 +51,7 @@ constexpr int BK = 64;            // 64 bf16 = 128 bytes: one swizzle row
 constexpr int NUM_THREADS = 192;  // 6 warps
 constexpr int A_STAGE_BYTES = BM * BK * 2;
 
-enum Epi { EPI_SWIGLU = 0, EPI_BF16 = 1, EPI_F32_BIAS = 2 };
+enum Epi { EPI_SWIGLU = 0, EPI_BF16 = 1, EPI_F32_BIAS = 2, EPI_ROUTER = 3 };
 
 struct Params {
   const int32_t* cu;  // nullptr: one group of M rows
@@ -64,6 +64,11 @@ struct Params {
   int ksplit;                     // K split into this many ranges (fp32 partial outputs)
   long long part_stride;          // elements between the partial outputs of two splits
   int accumulate;                 // bf16 output: add the existing values
+  // EPI_ROUTER: the whole expert row sits in one tile; the epilogue also takes
+  // the softmax and the top-k of it
+  int topk = 0;
+  int32_t* topk_idx = nullptr;
+  float* topk_gate = nullptr;
 };
 
 // Waits for copies and MMAs already in flight when a role stops always use
@@ -504,6 +509,43 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             for (int j = 0; j < 4; ++j) dst[j] = pk[j];
           }
         }
+      } else if (EPI == EPI_ROUTER) {
+        // one thread = one token: its BN logits (E valid) come out of TMEM, get
+        // the bias, are stored, and the softmax / top-k are taken in registers
+        // (value descending, lowest expert first on ties)
+        float v[BN];
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) tmem_ld32(tbase + c * 32, *reinterpret_cast<float(*)[32]>(v + c * 32));
+        if (row_ok) {
+          float* out = static_cast<float*>(p.out) + grow * p.ldo;
+#pragma unroll
+          for (int j = 0; j < BN; j += 4) {
+            if (j < p.N) {
+              if (p.bias) {
+                const float4 bb = __ldg(reinterpret_cast<const float4*>(p.bias + j));
+                v[j] += bb.x; v[j + 1] += bb.y; v[j + 2] += bb.z; v[j + 3] += bb.w;
+              }
+              *reinterpret_cast<float4*>(out + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            }
+          }
+          float m = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < BN; ++j) if (j < p.N) m = fmaxf(m, v[j]);
+          float sum = 0.f;
+#pragma unroll
+          for (int j = 0; j < BN; ++j) if (j < p.N) sum += expf(v[j] - m);
+          unsigned long long taken = 0;
+          for (int k = 0; k < p.topk; ++k) {
+            float bv = -INFINITY;
+            int be = -1;
+#pragma unroll
+            for (int j = 0; j < BN; ++j)
+              if (j < p.N && !((taken >> j) & 1ull) && (be < 0 || v[j] > bv)) { bv = v[j]; be = j; }
+            taken |= 1ull << be;
+            p.topk_idx[grow * p.topk + k] = be;
+            p.topk_gate[grow * p.topk + k] = expf(bv - m) / sum;
+          }
+        }
       } else {
         float* out = static_cast<float*>(p.out) + (long long)split * p.part_stride;
 #pragma unroll 1
@@ -640,9 +682,10 @@ int router_tc_splits(int T, int H, int E) {
 
 // out = x W_r (+ bias when S == 1): bf16 inputs, fp32 [T,E]; with S > 1, out
 // holds S partial sums [S][T][E] over consecutive slices of H (no bias).
-// E % 8 == 0, H % 8 == 0.
+// E % 8 == 0, H % 8 == 0.  With idx given (S == 1 and E <= 64 only) the
+// epilogue also writes the top-K experts and gates.
 int launch_router_tc(const void* x, const void* w, const float* bias, int T, int H, int E, float* out, int S,
-                     cudaStream_t s) {
+                     int K, int32_t* idx, float* gate, cudaStream_t s) {
   using namespace tc;
   CUtensorMap mA, mB;
   if (!map_2d_as_3d(&mA, x, H, T, BK, BM)) return MOE_ERR_CUDA;
@@ -651,6 +694,12 @@ int launch_router_tc(const void* x, const void* w, const float* bias, int T, int
   p.ksplit = S;
   p.part_stride = (long long)T * E;
   const long long tiles = (T + BM - 1) / BM * (long long)S;
+  if (idx) {  // S == 1, E <= 64: logits, softmax and top-k in the GEMM's epilogue
+    p.topk = K;
+    p.topk_idx = idx;
+    p.topk_gate = gate;
+    return launch<EPI_ROUTER, false, true, 64, 2, 4, 4, 4>(mA, mB, mB, p, tiles, s);
+  }
   // x is streamed from DRAM once: stages of 4 (2) consecutive 64-wide K slices
   // request 512 (256) contiguous bytes of every row at a time
   if (E <= 64) return launch<EPI_F32_BIAS, false, true, 64, 2, 4, 4, 4>(mA, mB, mB, p, tiles, s);

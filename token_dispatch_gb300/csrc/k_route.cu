@@ -554,7 +554,7 @@ size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 }  // namespace
 
 int launch_router_tc(const void* x, const void* w, const float* bias, int T, int H, int E, float* out, int S,
-                     cudaStream_t s);
+                     int K, int32_t* idx, float* gate, cudaStream_t s);
 int router_tc_splits(int T, int H, int E);
 
 size_t route_ws_bytes(int T, int H, int E) {
@@ -578,7 +578,11 @@ int launch_route(const void* x, const void* w, const float* bias, int T, int H, 
   if (dtype == MOE_BF16) {
     S = router_tc_splits(T, H, E);
     part = S > 1 ? static_cast<float*>(ws) : nullptr;
-    st = launch_router_tc(x, w, bias, T, H, E, S > 1 ? part : logits, S, s);
+    if (S == 1 && E <= 64) {  // the whole expert row is one tile: one launch
+      st = launch_router_tc(x, w, bias, T, H, E, logits, 1, K, idx, gate, s);
+      return st != MOE_OK ? st : launch_status();
+    }
+    st = launch_router_tc(x, w, bias, T, H, E, S > 1 ? part : logits, S, 0, nullptr, nullptr, s);
   } else {
     SimtGemmArgs a{};
     a.A = x; a.a_sm = H; a.a_sk = 1;
