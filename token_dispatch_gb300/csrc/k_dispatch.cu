@@ -71,56 +71,66 @@ dispatch_count_kernel(const int32_t* __restrict__ idx, int T, int E, int K,
   }
 }
 
-// One CTA: per-expert totals over chunks, exclusive scan over experts -> cu,
-// then per-chunk starting rows (written over the counts).
-__global__ void __launch_bounds__(1024)
-dispatch_scan_kernel(int* __restrict__ counts, int C, int E, int32_t* __restrict__ cu) {
-  __shared__ int sc[MAX_E];
-  const int e = threadIdx.x;
-  int total = 0;
-  if (e < E)
-    for (int c = 0; c < C; ++c) total += counts[(long long)c * E + e];
-  sc[e] = total;
-  __syncthreads();
-  // inclusive Hillis-Steele scan over 1024 entries
-  for (int o = 1; o < 1024; o <<= 1) {
-    int v = e >= o ? sc[e - o] : 0;
-    __syncthreads();
-    sc[e] += v;
-    __syncthreads();
-  }
-  int excl = sc[e] - total;
-  if (e < E) {
-    cu[e] = excl;
-    if (e == E - 1) cu[E] = sc[e];
-    int run = excl;
-    for (int c = 0; c < C; ++c) {
-      int n = counts[(long long)c * E + e];
-      counts[(long long)c * E + e] = run;
-      run += n;
-    }
-  }
-}
-
+// One CTA per chunk.  Besides its own per-warp counts, every CTA sums the
+// chunk count table itself: the per-expert totals (an exclusive scan over
+// experts gives cu_seqlens; CTA 0 writes them) and the counts of the chunks
+// before its own.  Integer sums, so every CTA gets the same numbers and the
+// scan needs no launch of its own.
 __global__ void __launch_bounds__(32 * CH_WARPS)
-dispatch_place_kernel(const int32_t* __restrict__ idx, int T, int E, int K,
-                      const int* __restrict__ chunk_off, int32_t* __restrict__ dst_row,
+dispatch_place_kernel(const int32_t* __restrict__ idx, int T, int E, int K, const int* __restrict__ counts,
+                      int C, int32_t* __restrict__ cu, int32_t* __restrict__ dst_row,
                       int32_t* __restrict__ src_tok) {
   __shared__ int hist[CH_WARPS][MAX_E];
-  const int w = threadIdx.x >> 5;
-  for (int i = threadIdx.x; i < CH_WARPS * E; i += blockDim.x) hist[i / E][i % E] = 0;
+  __shared__ int tot[MAX_E], pre[MAX_E];
+  __shared__ int tsum[32 * CH_WARPS];
+  const int tid = threadIdx.x, w = tid >> 5, nth = blockDim.x;
+  for (int i = tid; i < CH_WARPS * E; i += nth) hist[i / E][i % E] = 0;
+  for (int e = tid; e < E; e += nth) tot[e] = pre[e] = 0;
   __syncthreads();
   const int t0 = blockIdx.x * CH_TOK + w * TOK_PER_WARP;
   warp_count(idx, T, E, K, t0, hist[w], nullptr);
+  // totals over all chunks and over the chunks before this one
+  const long long n = (long long)C * E, before = (long long)blockIdx.x * E;
+#pragma unroll 4
+  for (long long i = tid; i < n; i += nth) {
+    const int v = __ldg(counts + i);
+    const int e = (int)(i % E);
+    atomicAdd(&tot[e], v);
+    if (i < before) atomicAdd(&pre[e], v);
+  }
   __syncthreads();
+  // exclusive scan of the totals: thread r owns a run of consecutive experts
+  const int per = (E + nth - 1) / nth;
+  const int e_lo = tid * per, e_hi = min(E, e_lo + per);
+  int run = 0;
+  for (int e = e_lo; e < e_hi; ++e) run += tot[e];
+  tsum[tid] = run;
+  __syncthreads();
+  for (int o = 1; o < nth; o <<= 1) {
+    const int v = tid >= o ? tsum[tid - o] : 0;
+    __syncthreads();
+    tsum[tid] += v;
+    __syncthreads();
+  }
+  int start = tsum[tid] - run;
+  for (int e = e_lo; e < e_hi; ++e) {
+    const int c = tot[e];
+    tot[e] = start;
+    start += c;
+  }
+  __syncthreads();
+  if (blockIdx.x == 0) {
+    for (int e = tid; e < E; e += nth) cu[e] = tot[e];
+    if (tid == nth - 1) cu[E] = tsum[nth - 1];
+  }
   // hist[w][e] <- first row of warp w for expert e
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    int run = chunk_off[(long long)blockIdx.x * E + e];
+  for (int e = tid; e < E; e += nth) {
+    int r = tot[e] + pre[e];
 #pragma unroll
     for (int ww = 0; ww < CH_WARPS; ++ww) {
-      int n = hist[ww][e];
-      hist[ww][e] = run;
-      run += n;
+      const int c = hist[ww][e];
+      hist[ww][e] = r;
+      r += c;
     }
   }
   __syncthreads();
@@ -212,11 +222,10 @@ int launch_dispatch(const void* x, const int32_t* idx, int T, int H, int E, int 
     int st = launch_status();
     if (st != MOE_OK) return st;
   }
-  dispatch_scan_kernel<<<1, 1024, 0, s>>>(counts, C, E, cu);
+  if (T == 0) return cudaMemsetAsync(cu, 0, (size_t)(E + 1) * sizeof(int32_t), s) == cudaSuccess ? MOE_OK
+                                                                                     : MOE_ERR_CUDA;
+  dispatch_place_kernel<<<C, 32 * CH_WARPS, 0, s>>>(idx, T, E, K, counts, C, cu, dst_row, src_tok);
   int st = launch_status();
-  if (st != MOE_OK || T == 0) return st;
-  dispatch_place_kernel<<<C, 32 * CH_WARPS, 0, s>>>(idx, T, E, K, counts, dst_row, src_tok);
-  st = launch_status();
   if (st != MOE_OK) return st;
   const int vec = H * (dtype == MOE_BF16 ? 2 : 4) / 16;
   const uint4* xv = static_cast<const uint4*>(x);
