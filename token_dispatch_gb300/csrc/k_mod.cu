@@ -26,14 +26,29 @@ mod_score_kernel(const T* __restrict__ x, const T* __restrict__ w, long long n_t
   const int nvec = H / V;
   const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
   for (long long t = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); t < n_tok; t += nwarps) {
+    // all U vectors of a lane's share of the row are requested before any is used
+    constexpr int U = 8;
     float acc = 0.f;
-#pragma unroll 8
-    for (int i = lane; i < nvec; i += 32) {
-      float xv[V], wv[V];
-      Vec16<T>::load(x + t * H + (long long)i * V, xv);
-      Vec16<T>::load(w + (long long)i * V, wv);
+    for (int base = 0; base < nvec; base += 32 * U) {
+      uint4 xr[U], wr[U];
 #pragma unroll
-      for (int v = 0; v < V; ++v) acc = fmaf(xv[v], wv[v], acc);
+      for (int u = 0; u < U; ++u) {
+        const int i = base + 32 * u + lane;
+        if (i < nvec) {
+          xr[u] = __ldg(reinterpret_cast<const uint4*>(x + t * H) + i);
+          wr[u] = __ldg(reinterpret_cast<const uint4*>(w) + i);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        if (base + 32 * u + lane < nvec) {
+          float xv[V], wv[V];
+          Vec16<T>::load_raw_unpack(xr[u], xv);
+          Vec16<T>::load_raw_unpack(wr[u], wv);
+#pragma unroll
+          for (int v = 0; v < V; ++v) acc = fmaf(xv[v], wv[v], acc);
+        }
+      }
     }
     acc = warp_sum(acc);
     if (lane == 0) score[t] = acc;

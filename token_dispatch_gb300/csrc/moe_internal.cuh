@@ -37,6 +37,10 @@ template <> struct Vec16<float> {
     float4 q = __ldg(reinterpret_cast<const float4*>(p));
     v[0] = q.x; v[1] = q.y; v[2] = q.z; v[3] = q.w;
   }
+  __device__ __forceinline__ static void load_raw_unpack(const uint4& q, float* v) {
+    v[0] = __uint_as_float(q.x); v[1] = __uint_as_float(q.y);
+    v[2] = __uint_as_float(q.z); v[3] = __uint_as_float(q.w);
+  }
   __device__ __forceinline__ static void store(float* p, const float* v) {
     *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
   }
