@@ -114,8 +114,13 @@ combine_kernel(const uint4* __restrict__ h, const float* __restrict__ gate, cons
 // d_scale[t] = sum_k gate[t,k] <g(t), h[row]>;  dx[t] = sum_k dxs[row].
 // The K rows are taken in groups of KT (a single group unless K > 8); dx is
 // written by the first group and accumulated by later ones.
+// Small CTAs and a register cap of 128 (four CTAs of four warps per SM): with
+// K rows of h and dxs plus dy requested at once per lane, the loads in flight
+// per SM grow with the resident warps.
+constexpr int PB_WARPS = 4;
+
 template <typename T, int KT>
-__global__ void __launch_bounds__(32 * WARPS)
+__global__ void __launch_bounds__(32 * PB_WARPS, 4)
 permute_bwd_kernel(const uint4* __restrict__ dy, const uint4* __restrict__ h, const float* __restrict__ gate,
                    const int32_t* __restrict__ dst_row, const float* __restrict__ scale,
                    const int32_t* __restrict__ out_row, const uint4* __restrict__ dxs, int Tn, int nvec, int K,
@@ -126,8 +131,8 @@ permute_bwd_kernel(const uint4* __restrict__ dy, const uint4* __restrict__ h, co
   const int lane = threadIdx.x & 31;
   const bool want_dot = d_gate || d_scale;
   const int n_groups = (K + KT - 1) / KT;
-  const long long nwarps = (long long)gridDim.x * WARPS;
-  for (long long t = (long long)blockIdx.x * WARPS + (threadIdx.x >> 5); t < Tn; t += nwarps) {
+  const long long nwarps = (long long)gridDim.x * PB_WARPS;
+  for (long long t = (long long)blockIdx.x * PB_WARPS + (threadIdx.x >> 5); t < Tn; t += nwarps) {
     const float s = scale ? __ldg(scale + t) : 1.0f;
     const long long o = out_row ? (long long)__ldg(out_row + t) : t;
     float ds = 0.f;
@@ -224,7 +229,10 @@ template <typename T, int KT>
 void permute_bwd_t(const void* dy, const void* h, const float* gate, const int32_t* dst_row, const float* scale,
                    const int32_t* out_row, const void* dxs, int Tn, int nvec, int K, void* dh, float* d_gate,
                    float* d_scale, void* dx, cudaStream_t s) {
-  permute_bwd_kernel<T, KT><<<warp_grid(Tn), 32 * WARPS, 0, s>>>(
+  long long ctas = (Tn + PB_WARPS - 1) / PB_WARPS;
+  const long long cap = (long long)sm_count() * 32;
+  if (ctas > cap) ctas = cap;
+  permute_bwd_kernel<T, KT><<<(unsigned)(ctas > 0 ? ctas : 1), 32 * PB_WARPS, 0, s>>>(
       static_cast<const uint4*>(dy), static_cast<const uint4*>(h), gate, dst_row, scale, out_row,
       static_cast<const uint4*>(dxs), Tn, nvec, K, static_cast<uint4*>(dh), d_gate, d_scale, static_cast<uint4*>(dx));
 }
