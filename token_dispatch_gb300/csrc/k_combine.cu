@@ -57,7 +57,7 @@ combine_kernel(const uint4* __restrict__ h, const float* __restrict__ gate, cons
                const float* __restrict__ scale, const uint4* __restrict__ residual,
                const int32_t* __restrict__ out_row, int Tn, int nvec, int K, uint4* __restrict__ y) {
   constexpr int V = Raw<T>::V;
-  constexpr int U = KT <= 2 ? 4 : KT <= 4 ? 2 : 1;
+  constexpr int U = KT <= 2 ? 4 : KT <= 8 ? 2 : 1;  // U*KT h rows of 16 bytes per lane in flight
   const int lane = threadIdx.x & 31;
   const long long nwarps = (long long)gridDim.x * WARPS;
   for (long long t = (long long)blockIdx.x * WARPS + (threadIdx.x >> 5); t < Tn; t += nwarps) {
