@@ -197,6 +197,10 @@ struct Cfg {
   static constexpr int OUT_BN = (EPI == EPI_SWIGLU) ? BN / 2 : BN;  // output columns per tile
   static constexpr int TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
                                    : (2 * BN <= 256) ? 256 : 512;
+  // bf16 epilogue: per warp a [32 rows][33] fp32 staging tile, so the global
+  // stores (and the reads of the old values) go out row-contiguous
+  static constexpr int STG_LD = 33;
+  static constexpr int EPI_BYTES = (EPI == EPI_BF16) ? 4 * 32 * STG_LD * 4 : 0;
 };
 
 struct TileInfo {
@@ -240,7 +244,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_base = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES);
+  float* epi_stage = reinterpret_cast<float*>(smem + STAGES * C::STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * C::STAGE_BYTES + C::EPI_BYTES);
   // bars: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain
   __shared__ uint32_t tmem_base_slot;
   __shared__ int abort_flag;
@@ -467,47 +472,61 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
         }
       } else if (EPI == EPI_BF16) {
+        // TMEM row per thread -> this warp's staging tile -> 8 rows x 64 bytes
+        // per store instruction (4 lanes per row segment of 32 columns).  With
+        // accumulate, every old value the warp will add is requested first.
         bf16* out = static_cast<bf16*>(p.out);
         constexpr int NCH = C::OUT_BN / 32;
-        // accumulate: every old value of this row segment is requested before
-        // any is used, so a thread keeps NCH*64 bytes of reads in flight
+        float* stg = epi_stage + q * 32 * C::STG_LD;
+        const int seg = (lane & 3) * 8;
         uint4 old[NCH][4];
         if (p.accumulate) {
 #pragma unroll
           for (int c = 0; c < NCH; ++c) {
-            const int col = ti.n0 + c * 32;
-            const bool ok = row_ok && col < p.N;
-            const uint4* src = reinterpret_cast<const uint4*>(out + (ok ? grow * p.ldo + col : 0));
 #pragma unroll
-            for (int j = 0; j < 4; ++j) old[c][j] = ok ? src[j] : make_uint4(0, 0, 0, 0);
+            for (int ps = 0; ps < 4; ++ps) {
+              const int rr = q * 32 + ps * 8 + (lane >> 2);
+              const long long gr = (long long)ti.row0 + rr;
+              const int col = ti.n0 + c * 32 + seg;
+              const bool ok = rr < ti.rows && gr < p.M && col < p.N;
+              old[c][ps] = ok ? *reinterpret_cast<const uint4*>(out + gr * p.ldo + col) : make_uint4(0, 0, 0, 0);
+            }
           }
         }
 #pragma unroll
         for (int c = 0; c < NCH; ++c) {
           float v[32];
           tmem_ld32(tbase + c * 32, v);
-          const int col = ti.n0 + c * 32;
-          if (row_ok && col < p.N) {
-            uint4* dst = reinterpret_cast<uint4*>(out + grow * p.ldo + col);
-            if (p.accumulate) {
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const __nv_bfloat162* oh = reinterpret_cast<const __nv_bfloat162*>(&old[c][j]);
+          for (int j = 0; j < 32; ++j) stg[lane * C::STG_LD + j] = v[j];
+          __syncwarp();
+#pragma unroll
+          for (int ps = 0; ps < 4; ++ps) {
+            const int rw = ps * 8 + (lane >> 2);
+            const int rr = q * 32 + rw;
+            const long long gr = (long long)ti.row0 + rr;
+            const int col = ti.n0 + c * 32 + seg;
+            if (rr < ti.rows && gr < p.M && col < p.N) {
+              float a[8];
+#pragma unroll
+              for (int j = 0; j < 8; ++j) a[j] = stg[rw * C::STG_LD + seg + j];
+              if (p.accumulate) {
+                const __nv_bfloat162* oh = reinterpret_cast<const __nv_bfloat162*>(&old[c][ps]);
 #pragma unroll
                 for (int q2 = 0; q2 < 4; ++q2) {
                   const float2 f = __bfloat1622float2(oh[q2]);
-                  v[8 * j + 2 * q2] += f.x;
-                  v[8 * j + 2 * q2 + 1] += f.y;
+                  a[2 * q2] += f.x;
+                  a[2 * q2 + 1] += f.y;
                 }
               }
+              uint4 pk;
+              __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&pk);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) h2[j] = __floats2bfloat162_rn(a[2 * j], a[2 * j + 1]);
+              *reinterpret_cast<uint4*>(out + gr * p.ldo + col) = pk;
             }
-            uint4 pk[4];
-            __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(pk);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) h2[j] = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) dst[j] = pk[j];
           }
+          __syncwarp();
         }
       } else if (EPI == EPI_ROUTER) {
         // one thread = one token: its BN logits (E valid) come out of TMEM, get
@@ -609,8 +628,9 @@ template <int EPI, bool A_MN, bool B_MN, int BN, int STAGES, int NA, int NB, int
 int launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const Params& p,
            long long tiles_upper, cudaStream_t s) {
   using C = Cfg<BN, EPI, NA, NB>;
-  const size_t smem = (size_t)STAGES * C::STAGE_BYTES + (2 * STAGES + 5) * 8 + 1024;
-  static_assert((size_t)STAGES * C::STAGE_BYTES + (2 * STAGES + 5) * 8 + 1024 <= 227 * 1024, "smem");
+  const size_t smem = (size_t)STAGES * C::STAGE_BYTES + C::EPI_BYTES + (2 * STAGES + 5) * 8 + 1024;
+  static_assert((size_t)STAGES * C::STAGE_BYTES + C::EPI_BYTES + (2 * STAGES + 5) * 8 + 1024 + 4300 <= 227 * 1024,
+                "smem (dynamic + static)");
   auto k = tc_gemm_kernel<EPI, A_MN, B_MN, BN, STAGES, NA, NB, KSUB>;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -707,15 +727,25 @@ int launch_router_tc(const void* x, const void* w, const float* bias, int T, int
   return launch<EPI_F32_BIAS, false, true, 256, 4, 1, 1>(mA, mB, mB, p, tiles * ((E + 255) / 256), s);
 }
 
-// Split count for the router weight gradient on tensor cores: about one CTA
-// per SM of a 152-SM GPU, at least one 64-token block per split.
+// Split count for the router weight gradient on tensor cores: the (h tile x
+// token split) work items should fill whole waves of the 152-SM GPU; among
+// split counts up to 64 (each split at least one 64-token block) a larger
+// count is taken only when it raises the wave efficiency by more than 2%.
 int router_dw_tc_splits(int T, int H, int E) {
   const long long tiles = ((H + tc::BM - 1) / tc::BM) * (long long)(E <= 64 ? 1 : (E + 127) / 128);
-  long long s = (152 + tiles - 1) / tiles;
   const long long kb = (T + tc::BK - 1) / tc::BK;
-  if (s > kb) s = kb;
-  if (s > 64) s = 64;
-  return s < 1 ? 1 : (int)s;
+  const long long sms = 152;
+  long long best = 1;
+  double best_eff = 0.0;
+  for (long long s = 1; s <= 64 && s <= kb; ++s) {
+    const long long work = tiles * s;
+    const double eff = (double)work / (double)(((work + sms - 1) / sms) * sms);
+    if (eff > best_eff * 1.02) {
+      best = s;
+      best_eff = eff;
+    }
+  }
+  return (int)best;
 }
 
 // part[s][h][e] = sum over the tokens of split s of x[t,h] (hi+mid+lo)[t,e]

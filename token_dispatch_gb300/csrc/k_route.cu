@@ -181,26 +181,23 @@ __global__ void copy_f32_kernel(const float* __restrict__ a, float* __restrict__
     b[i] = a[i];
 }
 
-// dw[i] = sum_s part[s][i].  Eight lanes per output: lane q adds splits
-// q, q+8, ... in order, then a fixed shuffle tree adds the eight sums, so the
-// result is the same on every run.
+// dw[i] = sum_s part[s][i], splits added in order (the same result every run).
+// One thread per output, so a warp's loads of one split are 128 contiguous
+// bytes, and all S loads of a thread are requested before the first add.
 __global__ void __launch_bounds__(256) reduce_splits_kernel(const float* __restrict__ part, int S, long long n,
                                                             float* __restrict__ out) {
-  const int q = threadIdx.x & 7;
-  const int grp = (threadIdx.x & 31) >> 3;  // four outputs per warp
-  const long long warp = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
-  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
-  for (long long base = warp * 4; base < n; base += nwarps * 4) {  // warp-uniform loop
-    const long long i = base + grp;
+  constexpr int U = 8;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += stride) {
     float acc = 0.f;
-    if (i < n) {
-#pragma unroll 4
-      for (int s = q; s < S; s += 8) acc += __ldg(part + (long long)s * n + i);
+    for (int s0 = 0; s0 < S; s0 += U) {
+      float v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) v[u] = s0 + u < S ? __ldg(part + (long long)(s0 + u) * n + i) : 0.f;
+#pragma unroll
+      for (int u = 0; u < U; ++u) acc += v[u];
     }
-    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-    if (q == 0 && i < n) out[i] = acc;
+    out[i] = acc;
   }
 }
 
@@ -648,8 +645,7 @@ int launch_dw(const T* x, const float* dl, int Tn, int H, int E, float* part, fl
 
 int launch_reduce(const float* part, int S, int H, int E, float* dw, cudaStream_t s) {
   const long long n = (long long)H * E;
-  const long long thr = n * 8;
-  const int rgrid = (int)((thr + 255) / 256 < 16384 ? (thr + 255) / 256 : 16384);
+  const int rgrid = (int)((n + 255) / 256 < 16384 ? (n + 255) / 256 : 16384);
   reduce_splits_kernel<<<rgrid, 256, 0, s>>>(part, S, n, dw);
   return launch_status();
 }
