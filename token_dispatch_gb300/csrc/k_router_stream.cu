@@ -67,8 +67,8 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 // the bytes a block streams.
 template <int CH, bool E16>
 struct StreamCfg {
-  static constexpr int NT = CH >= 5 ? 1 : (8 / CH < (E16 ? 4 : 8) ? 8 / CH : (E16 ? 4 : 8));
-  static constexpr int D = 16 / (NT * CH) < 2 ? 2 : 16 / (NT * CH);
+  static constexpr int NT = CH >= 6 ? 2 : CH >= 5 ? 1 : (8 / CH < (E16 ? 4 : 8) ? 8 / CH : (E16 ? 4 : 8));
+  static constexpr int D = NT * CH > 8 ? 1 : (16 / (NT * CH) < 2 ? 2 : 16 / (NT * CH));
   static constexpr int TOK = RS_TOK * NT;                       // tokens per block
   static constexpr int RED_FLOATS = 2 * RS_WARPS * TOK * RS_RED_LD;  // double-buffered partials
 };
