@@ -201,6 +201,28 @@ __global__ void __launch_bounds__(256) reduce_splits_kernel(const float* __restr
   }
 }
 
+// The same sum for many splits: eight lanes per output, lane q adds splits
+// q, q+8, ... in order and a fixed shuffle tree adds the eight sums.
+__global__ void __launch_bounds__(256) reduce_splits_wide_kernel(const float* __restrict__ part, int S, long long n,
+                                                                 float* __restrict__ out) {
+  const int q = threadIdx.x & 7;
+  const int grp = (threadIdx.x & 31) >> 3;  // four outputs per warp
+  const long long warp = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
+  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
+  for (long long base = warp * 4; base < n; base += nwarps * 4) {  // warp-uniform loop
+    const long long i = base + grp;
+    float acc = 0.f;
+    if (i < n) {
+#pragma unroll 4
+      for (int s = q; s < S; s += 8) acc += __ldg(part + (long long)s * n + i);
+    }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    if (q == 0 && i < n) out[i] = acc;
+  }
+}
+
 int rows_grid(long long T) {
   long long ctas = (T + ROWS_PER_CTA - 1) / ROWS_PER_CTA;
   long long cap = (long long)sm_count() * 16;
@@ -645,8 +667,14 @@ int launch_dw(const T* x, const float* dl, int Tn, int H, int E, float* part, fl
 
 int launch_reduce(const float* part, int S, int H, int E, float* dw, cudaStream_t s) {
   const long long n = (long long)H * E;
-  const int rgrid = (int)((n + 255) / 256 < 16384 ? (n + 255) / 256 : 16384);
-  reduce_splits_kernel<<<rgrid, 256, 0, s>>>(part, S, n, dw);
+  if (S > 16) {  // long sums over few outputs: spread each over eight lanes
+    const long long thr = n * 8;
+    const int rgrid = (int)((thr + 255) / 256 < 16384 ? (thr + 255) / 256 : 16384);
+    reduce_splits_wide_kernel<<<rgrid, 256, 0, s>>>(part, S, n, dw);
+  } else {
+    const int rgrid = (int)((n + 255) / 256 < 16384 ? (n + 255) / 256 : 16384);
+    reduce_splits_kernel<<<rgrid, 256, 0, s>>>(part, S, n, dw);
+  }
   return launch_status();
 }
 
