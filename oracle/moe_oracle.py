@@ -72,12 +72,30 @@ def topk_experts(logits, K):
     return order[:, :K].astype(np.int32)
 
 
-def route(x, w_router, K, bias=None):
-    """Router forward: logits, softmax p, top-k idx, gate = p[idx]."""
-    logits = router_logits(x, w_router, bias)
+def route(x, w_router, K, bias=None, renorm=False, bias_select_only=False):
+    """Router forward: logits, softmax p, top-k idx, gate = p[idx].
+
+    Two variants of the gate a drop-in for a Mixtral-style sparse MoE block
+    needs [FW "How it looks in practice": the framework's block replaces the
+    Mixtral one]:
+      renorm            gate[t, k] = p[idx[t,k]] / sum_k' p[idx[t,k']], the top-k
+                        weights rescaled to sum to 1 (the Mixtral block's routing);
+      bias_select_only  the bias shifts only which experts are chosen
+                        (idx = top-K of x W_r + bias); logits, p and the gate stay
+                        those of x W_r (bias-based load balancing without an
+                        auxiliary loss).
+    """
+    if bias_select_only and bias is not None:
+        logits = router_logits(x, w_router)
+        select = logits + np.asarray(bias, np.float64)[None, :]
+    else:
+        logits = router_logits(x, w_router, bias)
+        select = logits
     p = softmax_experts(logits)
-    idx = topk_experts(logits, K)
+    idx = topk_experts(select, K)
     gate = np.take_along_axis(p, idx.astype(np.int64), axis=1)
+    if renorm:
+        gate = gate / gate.sum(axis=1, keepdims=True)
     return logits, p, idx, gate
 
 
@@ -204,20 +222,32 @@ def combine(h, gate, dst_row, row_scale=None, residual=None, out_row=None, n_out
 # ----------------------------------------------------------------------------
 
 
-def route_bwd_softmax_topk(d_gate, logits, idx, x, w_router):
+def route_bwd_softmax_topk(d_gate, logits, idx, x, w_router, renorm=False):
     """Gradient through gate[t,k] = softmax(logits[t])[idx[t,k]].
 
     The selection is piecewise constant (no gradient through it); gradient reaches
     every logit through the softmax:
         dlogit[t, j] = p_j * (G_j - sum_k d_gate[t,k] * p[idx[t,k]]),
         G_j = d_gate[t,k] if j == idx[t,k] else 0.
+    With renorm the gate is q_k = p[idx_k] / sum_k' p[idx_k'], which is the
+    softmax of the chosen logits alone, so only they get a gradient:
+        dlogit[t, idx_k] = q_k * (d_gate[t,k] - sum_k' d_gate[t,k'] * q_k'),
+    and 0 for the other experts.
     Then dW_r = x^T dlogit and dx = dlogit W_r^T (the logit bias gets sum_t dlogit)."""
     p = softmax_experts(logits)
     T, E = logits.shape
-    G = np.zeros((T, E))
-    np.put_along_axis(G, idx.astype(np.int64), d_gate, axis=1)
-    inner = (d_gate * np.take_along_axis(p, idx.astype(np.int64), axis=1)).sum(axis=1, keepdims=True)
-    d_logits = p * (G - inner)
+    ix = idx.astype(np.int64)
+    if renorm:
+        q = np.take_along_axis(p, ix, axis=1)
+        q = q / q.sum(axis=1, keepdims=True)
+        inner = (d_gate * q).sum(axis=1, keepdims=True)
+        d_logits = np.zeros((T, E))
+        np.put_along_axis(d_logits, ix, q * (d_gate - inner), axis=1)
+    else:
+        G = np.zeros((T, E))
+        np.put_along_axis(G, ix, d_gate, axis=1)
+        inner = (d_gate * np.take_along_axis(p, ix, axis=1)).sum(axis=1, keepdims=True)
+        d_logits = p * (G - inner)
     dw = np.asarray(x).T @ d_logits
     dx = d_logits @ np.asarray(w_router).T
     return d_logits, dw, dx

@@ -103,6 +103,60 @@ def test_route_bias_shifts_only_its_expert():
     assert np.allclose(l1[:, 1] - l0[:, 1], 2.5)
 
 
+def test_route_renorm_gates_sum_to_one_and_keep_ratios():
+    """Mixtral-style renormalisation: the K gates of a token sum to 1 and keep
+    the ratios of the chosen probabilities; K = 1 gives 1; K = E changes nothing."""
+    r = np.random.default_rng(701)
+    x, w = r.standard_normal((25, 10)), r.standard_normal((10, 6)) * 0.7
+    _, p, idx, g0 = O.route(x, w, 3)
+    _, _, idx_r, g = O.route(x, w, 3, renorm=True)
+    assert np.array_equal(idx, idx_r)
+    assert np.allclose(g.sum(axis=1), 1.0, rtol=0, atol=1e-14)
+    assert np.allclose(g[:, 0] / g[:, 2], g0[:, 0] / g0[:, 2], rtol=1e-13)
+    assert np.array_equal(O.route(x, w, 1, renorm=True)[3], np.ones((25, 1)))
+    _, p6, i6, g6 = O.route(x, w, 6, renorm=True)
+    assert np.allclose(g6, np.take_along_axis(p6, i6.astype(np.int64), axis=1), rtol=1e-13)
+
+
+def test_route_renorm_ignores_the_experts_not_chosen():
+    """Renormalised gates depend only on the chosen logits: lowering every
+    unchosen logit (keeping it below the K-th) leaves them as they are, while
+    the plain gates grow."""
+    l = np.random.default_rng(702).standard_normal((40, 7))
+    K = 3
+    idx = O.topk_experts(l, K)
+    chosen = np.zeros_like(l, dtype=bool)
+    np.put_along_axis(chosen, idx.astype(np.int64), True, axis=1)
+    l2 = np.where(chosen, l, l - 3.0)
+    x = np.eye(7)
+    a = O.route(l, x, K, renorm=True)
+    b = O.route(l2, x, K, renorm=True)
+    assert np.array_equal(a[2], b[2])
+    assert np.allclose(a[3], b[3], rtol=1e-13)
+    assert (O.route(l2, x, K)[3] > O.route(l, x, K)[3]).all()
+
+
+def test_route_bias_select_only_moves_choice_not_gates():
+    """With the bias used for selection only, idx is the brute-force top-K of
+    logits + bias (ties -> lower expert) while logits and gates are unbiased."""
+    T, E, K = 60, 5, 2
+    r = np.random.default_rng(703)
+    x = r.integers(-2, 3, size=(T, 4)).astype(np.float64)
+    w = r.integers(-1, 2, size=(4, E)).astype(np.float64)
+    b = np.array([0.0, 1.0, -1.0, 2.0, 0.0])
+    logits, p, idx, gate = O.route(x, w, K, b, bias_select_only=True)
+    l0 = x @ w
+    assert np.array_equal(logits, l0)
+    assert np.allclose(p, O.softmax_experts(l0), rtol=1e-14)
+    for t in range(T):
+        sel = l0[t] + b
+        best = max(itertools.combinations(range(E), K),
+                   key=lambda c: (sorted((sel[e] for e in c), reverse=True), [-e for e in c]))
+        order = sorted(best, key=lambda e: (-sel[e], e))
+        assert list(idx[t]) == order
+        assert np.array_equal(gate[t], p[t, order])
+
+
 # ----------------------------------------------- histogram / cu_seqlens ---
 
 def test_histogram_and_cu_seqlens_by_counting():
@@ -289,6 +343,27 @@ def test_route_backward_matches_central_differences(T, H, E, K):
         assert math.isclose(central_diff(loss_w, w, i), dw.reshape(-1)[i], rel_tol=1e-7, abs_tol=1e-9)
     for i in range(x.size):
         assert math.isclose(central_diff(loss_x, x, i), dx.reshape(-1)[i], rel_tol=1e-7, abs_tol=1e-9)
+
+
+@pytest.mark.parametrize("T,E,K", [(6, 5, 2), (4, 8, 3), (5, 4, 4), (3, 6, 1)])
+def test_route_backward_renorm_matches_central_differences(T, E, K):
+    """Renormalised gates: the gradient w.r.t. every logit (chosen or not)."""
+    r = np.random.default_rng(710 + T * E + K)
+    l = r.standard_normal((T, E))
+    d_gate = r.standard_normal((T, K))
+    idx = O.topk_experts(l, K)
+    assert topk_margin(l, K) > 1e-3
+
+    def loss_l(lv):
+        q = np.take_along_axis(O.softmax_experts(lv), idx.astype(np.int64), axis=1)
+        return float((d_gate * q / q.sum(axis=1, keepdims=True)).sum())
+
+    d_logits, _, _ = O.route_bwd_softmax_topk(d_gate, l, idx, np.zeros((T, 1)), np.zeros((1, E)), renorm=True)
+    for i in range(l.size):
+        assert math.isclose(central_diff(loss_l, l, i), d_logits.reshape(-1)[i], rel_tol=1e-7, abs_tol=1e-9)
+    chosen = np.zeros_like(l, dtype=bool)
+    np.put_along_axis(chosen, idx.astype(np.int64), True, axis=1)
+    assert (d_logits[~chosen] == 0).all()
 
 
 def test_route_backward_E_equals_K_is_softmax_jacobian():
