@@ -67,8 +67,13 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 enum { MOE_OP_ROUTE = 0, MOE_OP_DISPATCH = 1, MOE_OP_EXPERT_FFN = 2, MOE_OP_ROUTE_BWD = 3, MOE_OP_MOD_SELECT = 4 };
 
 /* moe_route_bwd modes; MOE_ROUTE_DX_WRITE may be or-ed in to overwrite dx instead
- * of accumulating into it */
-enum { MOE_ROUTE_SOFTMAX_TOPK = 0, MOE_ROUTE_MOD_LINEAR = 1, MOE_ROUTE_DX_WRITE = 0x100 };
+ * of accumulating into it, MOE_ROUTE_GATE_RENORM when the forward renormalised the
+ * gates (moe_route_ex with MOE_ROUTE_RENORM) */
+enum { MOE_ROUTE_SOFTMAX_TOPK = 0, MOE_ROUTE_MOD_LINEAR = 1, MOE_ROUTE_DX_WRITE = 0x100,
+       MOE_ROUTE_GATE_RENORM = 0x200 };
+
+/* moe_route_ex gate options (bit flags) */
+enum { MOE_ROUTE_RENORM = 0x1, MOE_ROUTE_BIAS_SELECT = 0x2 };
 
 /* Human-readable name of a status code (static string, never NULL). */
 MOE_API const char* moe_status_str(int status);
@@ -109,6 +114,26 @@ MOE_API int moe_last_device_error(void* stream);
  */
 MOE_API int moe_route(const void* x, const void* w_router, const float* logit_bias,
               int T, int H, int E, int K, int dtype,
+              float* logits, int32_t* topk_idx, float* topk_gate,
+              void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Router with gate options, for a drop-in replacement of a Mixtral-style sparse
+ * MoE block                              [FW "How it looks in practice"]
+ *
+ * moe_route with `flags`, a bitwise or of
+ *   MOE_ROUTE_RENORM       topk_gate[t,k] = p[t,topk_idx[t,k]] / sum_k' p[t,topk_idx[t,k']]
+ *                          (the K gates of a token sum to 1, as in the Mixtral block);
+ *   MOE_ROUTE_BIAS_SELECT  logit_bias shifts only the selection: topk_idx = the top K of
+ *                          x w_router + logit_bias (same order and ties as above), while
+ *                          logits, p and the gates are those of x w_router alone.
+ * flags = 0 is exactly moe_route; other bits return MOE_ERR_INVALID_ARG.  Arguments,
+ * layouts, workspace and errors as moe_route.  The backward of renormalised gates is
+ * moe_route_bwd with MOE_ROUTE_GATE_RENORM; the selection-only bias needs no flag there
+ * (the stored logits are unbiased).
+ */
+MOE_API int moe_route_ex(const void* x, const void* w_router, const float* logit_bias,
+              int T, int H, int E, int K, int dtype, int flags,
               float* logits, int32_t* topk_idx, float* topk_gate,
               void* ws, size_t ws_bytes, void* stream);
 
@@ -197,6 +222,8 @@ MOE_API int moe_combine(const void* h, const float* gate, const int32_t* dst_row
  *   dw_router[h,e] = sum_t x[t,h] * d_logits[t,e]      (float, nullable)
  *   dx[t,h]       += sum_e d_logits[t,e] * w_router[h,e] (dtype, nullable, accumulated;
  *                   written instead when mode has MOE_ROUTE_DX_WRITE)
+ * with MOE_ROUTE_GATE_RENORM or-ed in (gate[t,k] = q_k = p[topk_idx[t,k]] / sum_k' p[topk_idx[t,k']]):
+ *   d_logits[t,topk_idx[t,k]] = q_k * (d_gate[t,k] - sum_k' d_gate[t,k'] * q_k'), 0 elsewhere
  * mode MOE_ROUTE_MOD_LINEAR (scalar score s[t] = x[t] . w; pass E = K = 1,
  *   w_router = w [H], d_gate = d_score [T], logits/topk_idx unused):
  *   d_logits = d_score (nullable), dw_router[h] = sum_t d_score[t] x[t,h],

@@ -73,6 +73,10 @@ def test_argument_errors_are_reported_before_launch(libmoe):
     assert raw.moe_route(A, A, None, 4, 64, 6, 2, L.MOE_F32, A, A, A, None, 0, None) == L.MOE_ERR_UNSUPPORTED
     # bf16 router with idle SMs needs its partial-sum workspace
     assert raw.moe_route(A, A, None, 1024, 2048, 32, 2, L.MOE_BF16, A, A, A, None, 0, None) == L.MOE_ERR_WORKSPACE
+    # unknown route flags; renormalised-gate backward of the linear score
+    assert raw.moe_route_ex(A, A, None, 4, 64, 8, 2, L.MOE_F32, 4, A, A, A, None, 0, None) == L.MOE_ERR_INVALID_ARG
+    assert raw.moe_route_bwd(L.MOE_ROUTE_MOD_LINEAR | L.MOE_ROUTE_GATE_RENORM, A, None, None, A, A, 4, 64, 1, 1,
+                             L.MOE_F32, None, A, None, A, 1 << 30, None) == L.MOE_ERR_INVALID_ARG
     # workspace too small
     need = L.moe_workspace_bytes(L.MOE_OP_DISPATCH, 1000, 64, 8, 2, 0)
     assert raw.moe_dispatch(A, A, 1000, 64, 8, 2, L.MOE_F32, A, A, A, A, A, need - 256, None) == L.MOE_ERR_WORKSPACE

@@ -78,6 +78,52 @@ def test_route_matches_oracle(shape):
     assert_close(gate[same], r_gate[same], gate_tol(logit_err), "gate")
 
 
+# every router form: streaming (E = 8 / 16), tcgen05 with the fused epilogue
+# (E <= 64, one H range), tcgen05 split over H + softmax kernel (E = 384), FFMA (fp32)
+VARIANT_SHAPES = [S("bf16_T1000_H512_E8_K2", 1000, 512, 8, 2, 64, "bf16"),
+                  S("bf16_T777_H1024_E16_K4", 777, 1024, 16, 4, 64, "bf16"),
+                  S("bf16_T777_H256_E64_K6", 777, 256, 64, 6, 64, "bf16"),
+                  S("bf16_T300_H128_E384_K8", 300, 128, 384, 8, 64, "bf16"),
+                  S("f32_T300_H64_E12_K3", 300, 64, 12, 3, 64, "f32")]
+FLAGS = {"renorm": 1, "bias_select": 2, "both": 3}
+
+
+@pytest.mark.parametrize("flags", list(FLAGS), ids=list(FLAGS))
+@pytest.mark.parametrize("shape", VARIANT_SHAPES, ids=ids(VARIANT_SHAPES))
+def test_route_variants_match_oracle(shape, flags):
+    """Mixtral-style renormalised gates and the selection-only bias, against
+    the oracle's route(renorm=..., bias_select_only=...)."""
+    fl = FLAGS[flags]
+    renorm, select = bool(fl & L.MOE_ROUTE_RENORM), bool(fl & L.MOE_ROUTE_BIAS_SELECT)
+    T, E, K = shape.T, shape.E, shape.K
+    x, wr = synth.router_inputs(shape)
+    bias = (np.random.default_rng(11).standard_normal(E) * 0.5).astype(np.float32)  # shifts every expert
+    logits = torch.empty((T, E), dtype=torch.float32, device=DEV)
+    idx = torch.empty((T, K), dtype=torch.int32, device=DEV)
+    gate = torch.empty((T, K), dtype=torch.float32, device=DEV)
+    nbytes = L.moe_workspace_bytes(L.MOE_OP_ROUTE, T, shape.H, E, K, 0)
+    ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=DEV)
+    L.moe_route_ex(dev(x), dev(wr), torch.from_numpy(bias).to(DEV), T, shape.H, E, K, CDT[shape.dtype], fl, logits,
+                   idx, gate, ws, nbytes)
+    torch.cuda.synchronize()
+    r_logits, r_p, r_idx, r_gate = O.route(x.ref, wr.ref, K, bias.astype(np.float64), renorm=renorm,
+                                           bias_select_only=select)
+    logits, idx, gate = logits.cpu().numpy(), idx.cpu().numpy(), gate.cpu().numpy()
+    assert_close(logits, r_logits, 1e-5, "logits")
+    err = float(np.max(np.abs(logits - r_logits)))
+    r_sel = r_logits + (bias.astype(np.float64)[None, :] if select else 0.0)
+    check_topk(idx, r_sel, K, err)
+    same = (idx == r_idx).all(axis=1)
+    assert_close(gate[same], r_gate[same], gate_tol(err), "gate")
+    if renorm:
+        assert np.allclose(gate.sum(axis=1), 1.0, atol=1e-5)
+    # the gate of every chosen expert, chosen or not by the oracle, is its own probability
+    q = np.take_along_axis(r_p, idx.astype(np.int64), axis=1)
+    if renorm:
+        q = q / q.sum(axis=1, keepdims=True)
+    assert_close(gate, q, gate_tol(err), "gate of the GPU's choice")
+
+
 @pytest.mark.parametrize("dtype,E,K,H", [("f32", 8, 2, 64), ("bf16", 16, 4, 64), ("bf16", 384, 8, 64),
                                          ("f32", 64, 6, 64), ("bf16", 8, 2, 512), ("bf16", 16, 5, 1024),
                                          ("bf16", 64, 6, 64), ("bf16", 40, 3, 2048)])
@@ -294,6 +340,32 @@ def test_route_bwd_softmax_topk_matches_oracle(shape):
                     CDT[shape.dtype], None, None, dx, ws, nbytes)
     torch.cuda.synchronize()
     assert_close(to64(dx), dx_r, TOL[shape.dtype], "dx (written)")
+
+
+@pytest.mark.parametrize("shape", SHAPES + ROUTE_ONLY[:1], ids=ids(SHAPES + ROUTE_ONLY[:1]))
+def test_route_bwd_renorm_matches_oracle(shape):
+    """Backward of renormalised gates: only the chosen logits get a gradient."""
+    T, H, E, K = shape.T, shape.H, shape.E, shape.K
+    x, wr = synth.router_inputs(shape)
+    logits = (x.ref @ wr.ref).astype(np.float32)
+    idx = O.topk_experts(logits.astype(np.float64), K)
+    d_gate = np.random.default_rng(6).standard_normal((T, K)).astype(np.float32)
+    dl_r, dw_r, dx_r = O.route_bwd_softmax_topk(d_gate.astype(np.float64), logits.astype(np.float64), idx,
+                                                x.ref, wr.ref, renorm=True)
+    dl = torch.empty((T, E), dtype=torch.float32, device=DEV)
+    dw = torch.empty((H, E), dtype=torch.float32, device=DEV)
+    dx = torch.empty((T, H), dtype=TDT[shape.dtype], device=DEV)
+    nbytes = L.moe_workspace_bytes(L.MOE_OP_ROUTE_BWD, T, H, E, K, 0)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    L.moe_route_bwd(L.MOE_ROUTE_SOFTMAX_TOPK | L.MOE_ROUTE_GATE_RENORM | L.MOE_ROUTE_DX_WRITE,
+                    torch.from_numpy(d_gate).to(DEV), torch.from_numpy(logits).to(DEV), torch.from_numpy(idx).to(DEV),
+                    dev(x), dev(wr), T, H, E, K, CDT[shape.dtype], dl, dw, dx, ws, nbytes)
+    torch.cuda.synchronize()
+    dl_g = dl.cpu().numpy()
+    assert_close(dl_g, dl_r, 1e-5, "d_logits")
+    assert (dl_g[dl_r == 0] == 0).all()
+    assert_close(dw.cpu().numpy(), dw_r, 1e-5, "dw_router")
+    assert_close(to64(dx), dx_r, TOL[shape.dtype], "dx")
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])

@@ -34,9 +34,13 @@ MOE_OP_MOD_SELECT = 4
 MOE_ROUTE_SOFTMAX_TOPK = 0
 MOE_ROUTE_MOD_LINEAR = 1
 MOE_ROUTE_DX_WRITE = 0x100
+MOE_ROUTE_GATE_RENORM = 0x200
+
+MOE_ROUTE_RENORM = 0x1
+MOE_ROUTE_BIAS_SELECT = 0x2
 
 EXPORTS = ("moe_status_str", "moe_version", "moe_kernel_launches", "moe_workspace_bytes", "moe_last_device_error",
-           "moe_route", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_route_bwd",
+           "moe_route", "moe_route_ex", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_route_bwd",
            "moe_permute_bwd", "mod_select")
 
 
@@ -59,6 +63,7 @@ _SIGS = {
     "moe_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I]),
     "moe_last_device_error": (_I, [_P]),
     "moe_route": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
+    "moe_route_ex": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
     "moe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_dispatch_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_expert_ffn": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _Z, _P]),
@@ -133,6 +138,13 @@ def moe_route(x, w_router, logit_bias, T, H, E, K, dtype, logits, topk_idx, topk
     _check("moe_route", lib().moe_route(_ptr(x), _ptr(w_router), _ptr(logit_bias), T, H, E, K, dtype,
                                         _ptr(logits), _ptr(topk_idx), _ptr(topk_gate), _ptr(ws),
                                         ws_bytes, _stream(stream)))
+
+
+def moe_route_ex(x, w_router, logit_bias, T, H, E, K, dtype, flags, logits, topk_idx, topk_gate,
+                 ws=None, ws_bytes=0, stream=None):
+    _check("moe_route_ex", lib().moe_route_ex(_ptr(x), _ptr(w_router), _ptr(logit_bias), T, H, E, K, dtype, flags,
+                                              _ptr(logits), _ptr(topk_idx), _ptr(topk_gate), _ptr(ws),
+                                              ws_bytes, _stream(stream)))
 
 
 def moe_dispatch(x, topk_idx, T, H, E, K, dtype, cu_seqlens, dst_row, src_tok, xs, ws, ws_bytes,

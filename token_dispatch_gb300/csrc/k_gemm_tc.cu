@@ -69,6 +69,8 @@ struct Params {
   int topk = 0;
   int32_t* topk_idx = nullptr;
   float* topk_gate = nullptr;
+  const float* sel_bias = nullptr;  // added only where experts are chosen
+  int renorm = 0;                   // the K gates rescaled to sum to 1
 };
 
 // Waits for copies and MMAs already in flight when a role stops always use
@@ -553,17 +555,35 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           float sum = 0.f;
 #pragma unroll
           for (int j = 0; j < BN; ++j) if (j < p.N) sum += expf(v[j] - m);
+          // selection values: the logits, plus the selection-only bias when given
+          float sv[BN];
+#pragma unroll
+          for (int j = 0; j < BN; j += 4) {
+            sv[j] = v[j]; sv[j + 1] = v[j + 1]; sv[j + 2] = v[j + 2]; sv[j + 3] = v[j + 3];
+            if (p.sel_bias && j < p.N) {
+              const float4 bb = __ldg(reinterpret_cast<const float4*>(p.sel_bias + j));
+              sv[j] += bb.x; sv[j + 1] += bb.y; sv[j + 2] += bb.z; sv[j + 3] += bb.w;
+            }
+          }
           unsigned long long taken = 0;
+          float chosen = 0.f;
           for (int k = 0; k < p.topk; ++k) {
             float bv = -INFINITY;
             int be = -1;
 #pragma unroll
             for (int j = 0; j < BN; ++j)
-              if (j < p.N && !((taken >> j) & 1ull) && (be < 0 || v[j] > bv)) { bv = v[j]; be = j; }
+              if (j < p.N && !((taken >> j) & 1ull) && (be < 0 || sv[j] > bv)) { bv = sv[j]; be = j; }
             taken |= 1ull << be;
+            float vb = 0.f;
+#pragma unroll
+            for (int j = 0; j < BN; ++j) if (j == be) vb = v[j];
+            const float pk = expf(vb - m) / sum;
+            chosen += pk;
             p.topk_idx[grow * p.topk + k] = be;
-            p.topk_gate[grow * p.topk + k] = expf(bv - m) / sum;
+            p.topk_gate[grow * p.topk + k] = pk;
           }
+          if (p.renorm)
+            for (int k = 0; k < p.topk; ++k) p.topk_gate[grow * p.topk + k] = p.topk_gate[grow * p.topk + k] / chosen;
         }
       } else {
         float* out = static_cast<float*>(p.out) + (long long)split * p.part_stride;
@@ -704,8 +724,8 @@ int router_tc_splits(int T, int H, int E) {
 // holds S partial sums [S][T][E] over consecutive slices of H (no bias).
 // E % 8 == 0, H % 8 == 0.  With idx given (S == 1 and E <= 64 only) the
 // epilogue also writes the top-K experts and gates.
-int launch_router_tc(const void* x, const void* w, const float* bias, int T, int H, int E, float* out, int S,
-                     int K, int32_t* idx, float* gate, cudaStream_t s) {
+int launch_router_tc(const void* x, const void* w, const float* bias, const float* sel_bias, bool renorm, int T,
+                     int H, int E, float* out, int S, int K, int32_t* idx, float* gate, cudaStream_t s) {
   using namespace tc;
   CUtensorMap mA, mB;
   if (!map_2d_as_3d(&mA, x, H, T, BK, BM)) return MOE_ERR_CUDA;
@@ -718,6 +738,8 @@ int launch_router_tc(const void* x, const void* w, const float* bias, int T, int
     p.topk = K;
     p.topk_idx = idx;
     p.topk_gate = gate;
+    p.sel_bias = sel_bias;
+    p.renorm = renorm ? 1 : 0;
     return launch<EPI_ROUTER, false, true, 64, 2, 4, 4, 4>(mA, mB, mB, p, tiles, s);
   }
   // x is streamed from DRAM once: stages of 4 (2) consecutive 64-wide K slices

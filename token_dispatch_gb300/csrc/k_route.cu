@@ -40,8 +40,8 @@ __device__ __forceinline__ int slot_expert(int slot, int lane) {
 template <int VPL>
 __global__ void __launch_bounds__(32 * ROWS_PER_CTA)
 softmax_topk_kernel(float* __restrict__ logits, const float* __restrict__ part, int S,
-                    const float* __restrict__ bias, int T, int E, int K,
-                    int32_t* __restrict__ idx, float* __restrict__ gate) {
+                    const float* __restrict__ bias, const float* __restrict__ sel_bias, int renorm, int T, int E,
+                    int K, int32_t* __restrict__ idx, float* __restrict__ gate) {
   const int lane = threadIdx.x & 31;
   const long long nwarps = (long long)gridDim.x * ROWS_PER_CTA;
   for (long long t = (long long)blockIdx.x * ROWS_PER_CTA + (threadIdx.x >> 5); t < T; t += nwarps) {
@@ -69,6 +69,16 @@ softmax_topk_kernel(float* __restrict__ logits, const float* __restrict__ part, 
     } else {
       load_row<VPL>(logits + t * E, E, lane, v);
     }
+    // selection values: the logits, or the logits plus a selection-only bias
+    float sv[VPL];
+    if (sel_bias) {
+      load_row<VPL>(sel_bias, E, lane, sv);
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) sv[j] += v[j];
+    } else {
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) sv[j] = v[j];
+    }
     float m = -INFINITY;
 #pragma unroll
     for (int j = 0; j < VPL; ++j) m = fmaxf(m, v[j]);
@@ -78,6 +88,7 @@ softmax_topk_kernel(float* __restrict__ logits, const float* __restrict__ part, 
     for (int j = 0; j < VPL; ++j) s += (slot_expert(j, lane) < E) ? expf(v[j] - m) : 0.f;
     s = warp_sum(s);
     unsigned taken = 0;
+    float chosen_sum = 0.f;
     for (int k = 0; k < K; ++k) {
       float bv = -INFINITY;
       int be = 0x7fffffff;
@@ -85,7 +96,7 @@ softmax_topk_kernel(float* __restrict__ logits, const float* __restrict__ part, 
       for (int j = 0; j < VPL; ++j) {
         int e = slot_expert(j, lane);
         bool ok = e < E && !((taken >> j) & 1u);
-        if (ok && (v[j] > bv || (v[j] == bv && e < be))) { bv = v[j]; be = e; }
+        if (ok && (sv[j] > bv || (sv[j] == bv && e < be))) { bv = sv[j]; be = e; }
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
@@ -93,12 +104,23 @@ softmax_topk_kernel(float* __restrict__ logits, const float* __restrict__ part, 
         int oe = __shfl_xor_sync(0xffffffffu, be, o);
         if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
       }
-      if (((be >> 2) & 31) == lane) taken |= 1u << ((be >> 7) * 4 + (be & 3));
+      // the winner's own logit (not its selection value) gives its probability
+      const int owner = (be >> 2) & 31, wslot = (be >> 7) * 4 + (be & 3);
+      float vw = 0.f;
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) if (j == wslot) vw = v[j];
+      vw = __shfl_sync(0xffffffffu, vw, owner);
+      if (owner == lane) taken |= 1u << wslot;
+      const float pk = expf(vw - m) / s;
+      chosen_sum += pk;
       if (lane == 0) {
         idx[t * K + k] = be;
-        gate[t * K + k] = expf(bv - m) / s;
+        gate[t * K + k] = pk;
       }
     }
+    // Mixtral-style renormalisation: the K gates rescaled to sum to 1
+    if (renorm && lane == 0)
+      for (int k = 0; k < K; ++k) gate[t * K + k] = gate[t * K + k] / chosen_sum;
   }
 }
 
@@ -117,7 +139,7 @@ __device__ __forceinline__ void split3(float v, bf16& hi, bf16& mid, bf16& lo) {
 template <int VPL>
 __global__ void __launch_bounds__(32 * ROWS_PER_CTA)
 softmax_topk_bwd_kernel(const float* __restrict__ logits, const int32_t* __restrict__ idx,
-                        const float* __restrict__ d_gate, int T, int E, int K,
+                        const float* __restrict__ d_gate, int renorm, int T, int E, int K,
                         float* __restrict__ d_logits, bf16* __restrict__ dl3) {
   const int lane = threadIdx.x & 31;
   const long long nwarps = (long long)gridDim.x * ROWS_PER_CTA;
@@ -138,7 +160,8 @@ softmax_topk_bwd_kernel(const float* __restrict__ logits, const int32_t* __restr
       p[j] = (slot_expert(j, lane) < E) ? expf(v[j] - m) / s : 0.f;
       G[j] = 0.f;
     }
-    float inner = 0.f;
+    float inner = 0.f, csum = 0.f;
+    unsigned chosen = 0;
     for (int k = 0; k < K; ++k) {
       int e = __ldg(idx + t * K + k);
       float dg = __ldg(d_gate + t * K + k);
@@ -146,10 +169,18 @@ softmax_topk_bwd_kernel(const float* __restrict__ logits, const int32_t* __restr
         int slot = (e >> 7) * 4 + (e & 3);
 #pragma unroll
         for (int j = 0; j < VPL; ++j)
-          if (j == slot) { G[j] = dg; inner += dg * p[j]; }
+          if (j == slot) { G[j] = dg; inner += dg * p[j]; csum += p[j]; chosen |= 1u << j; }
       }
     }
     inner = warp_sum(inner);
+    if (renorm) {
+      // renormalised gates q = p / (sum of the chosen p): only the chosen
+      // logits get a gradient, q_j (G_j - sum_k d_gate_k q_k)
+      csum = warp_sum(csum);
+      inner = inner / csum;
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) p[j] = ((chosen >> j) & 1u) ? p[j] / csum : 0.f;
+    }
     float* out = d_logits + t * E;
 #pragma unroll
     for (int q = 0; q < VPL / 4; ++q) {
@@ -572,8 +603,8 @@ size_t align256(size_t b) { return (b + 255) & ~(size_t)255; }
 
 }  // namespace
 
-int launch_router_tc(const void* x, const void* w, const float* bias, int T, int H, int E, float* out, int S,
-                     int K, int32_t* idx, float* gate, cudaStream_t s);
+int launch_router_tc(const void* x, const void* w, const float* bias, const float* sel_bias, bool renorm, int T,
+                     int H, int E, float* out, int S, int K, int32_t* idx, float* gate, cudaStream_t s);
 int router_tc_splits(int T, int H, int E);
 
 size_t route_ws_bytes(int T, int H, int E) {
@@ -587,10 +618,16 @@ size_t route_ws_bytes(int T, int H, int E) {
 // partial sums when the token tiles alone would leave SMs idle (the partials,
 // the bias and the softmax/top-k meet in one pass); fp32: FFMA GEMM with the
 // bias in its epilogue.
-int launch_route(const void* x, const void* w, const float* bias, int T, int H, int E, int K, int dtype,
+int launch_route(const void* x, const void* w, const float* bias, int T, int H, int E, int K, int dtype, int flags,
                  float* logits, int32_t* idx, float* gate, void* ws, cudaStream_t s) {
   if (T == 0) return MOE_OK;
-  if (router_stream_applies(dtype, H, E)) return launch_router_stream(x, w, bias, T, H, E, K, logits, idx, gate, s);
+  const bool renorm = flags & MOE_ROUTE_RENORM;
+  // a selection-only bias never reaches the GEMM: it is added to copies of the
+  // logits where the experts are chosen
+  const float* sel_bias = (flags & MOE_ROUTE_BIAS_SELECT) ? bias : nullptr;
+  const float* gemm_bias = sel_bias ? nullptr : bias;
+  if (router_stream_applies(dtype, H, E))
+    return launch_router_stream(x, w, gemm_bias, sel_bias, renorm, T, H, E, K, logits, idx, gate, s);
   int S = 1;
   float* part = nullptr;
   int st;
@@ -598,16 +635,17 @@ int launch_route(const void* x, const void* w, const float* bias, int T, int H, 
     S = router_tc_splits(T, H, E);
     part = S > 1 ? static_cast<float*>(ws) : nullptr;
     if (S == 1 && E <= 64) {  // the whole expert row is one tile: one launch
-      st = launch_router_tc(x, w, bias, T, H, E, logits, 1, K, idx, gate, s);
+      st = launch_router_tc(x, w, gemm_bias, sel_bias, renorm, T, H, E, logits, 1, K, idx, gate, s);
       return st != MOE_OK ? st : launch_status();
     }
-    st = launch_router_tc(x, w, bias, T, H, E, S > 1 ? part : logits, S, 0, nullptr, nullptr, s);
+    st = launch_router_tc(x, w, gemm_bias, nullptr, false, T, H, E, S > 1 ? part : logits, S, 0, nullptr, nullptr,
+                          s);
   } else {
     SimtGemmArgs a{};
     a.A = x; a.a_sm = H; a.a_sk = 1;
     a.B = w; a.b_sg = 0; a.b_sk = E; a.b_sn = 1;
     a.C = logits; a.c_sm = E;
-    a.bias = bias; a.cu = nullptr;
+    a.bias = gemm_bias; a.cu = nullptr;
     a.M = T; a.N = E; a.K = H; a.groups = 1;
     a.epilogue = 2; a.swiglu = false;
     st = launch_simt_gemm(a, dtype, dtype, MOE_F32, s);
@@ -615,11 +653,16 @@ int launch_route(const void* x, const void* w, const float* bias, int T, int H, 
   if (st != MOE_OK) return st;
   const int grid = rows_grid(T);
   const int vpl = (E + 127) / 128 * 4;
-  const float* pb = S > 1 ? bias : nullptr;
-  if (vpl <= 4) softmax_topk_kernel<4><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, part, S, pb, T, E, K, idx, gate);
-  else if (vpl <= 8) softmax_topk_kernel<8><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, part, S, pb, T, E, K, idx, gate);
-  else if (vpl <= 16) softmax_topk_kernel<16><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, part, S, pb, T, E, K, idx, gate);
-  else softmax_topk_kernel<32><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, part, S, pb, T, E, K, idx, gate);
+  const float* pb = S > 1 ? gemm_bias : nullptr;
+  const int rn = renorm ? 1 : 0;
+  if (vpl <= 4)
+    softmax_topk_kernel<4><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, part, S, pb, sel_bias, rn, T, E, K, idx, gate);
+  else if (vpl <= 8)
+    softmax_topk_kernel<8><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, part, S, pb, sel_bias, rn, T, E, K, idx, gate);
+  else if (vpl <= 16)
+    softmax_topk_kernel<16><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, part, S, pb, sel_bias, rn, T, E, K, idx, gate);
+  else
+    softmax_topk_kernel<32><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, part, S, pb, sel_bias, rn, T, E, K, idx, gate);
   return launch_status();
 }
 
@@ -687,7 +730,7 @@ int launch_dx(const float* dl, const T* w, int Tn, int H, int E, bool write, T* 
 
 int launch_route_bwd(int mode, const float* d_gate, const float* logits, const int32_t* idx,
                      const void* x, const void* w, int T, int H, int E, int K, int dtype,
-                     float* d_logits, float* dw, void* dx, bool dx_write, void* ws, cudaStream_t s) {
+                     float* d_logits, float* dw, void* dx, bool dx_write, bool renorm, void* ws, cudaStream_t s) {
   if (T == 0) {
     if (dw && cudaMemsetAsync(dw, 0, (size_t)H * E * 4, s) != cudaSuccess) return MOE_ERR_CUDA;
     return MOE_OK;
@@ -702,10 +745,15 @@ int launch_route_bwd(int mode, const float* d_gate, const float* logits, const i
   if (mode == MOE_ROUTE_SOFTMAX_TOPK) {
     int grid = rows_grid(T);
     int vpl = (E + 127) / 128 * 4;
-    if (vpl <= 4) softmax_topk_bwd_kernel<4><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, idx, d_gate, T, E, K, dl, dl3);
-    else if (vpl <= 8) softmax_topk_bwd_kernel<8><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, idx, d_gate, T, E, K, dl, dl3);
-    else if (vpl <= 16) softmax_topk_bwd_kernel<16><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, idx, d_gate, T, E, K, dl, dl3);
-    else softmax_topk_bwd_kernel<32><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, idx, d_gate, T, E, K, dl, dl3);
+    const int rn = renorm ? 1 : 0;
+    if (vpl <= 4)
+      softmax_topk_bwd_kernel<4><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, idx, d_gate, rn, T, E, K, dl, dl3);
+    else if (vpl <= 8)
+      softmax_topk_bwd_kernel<8><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, idx, d_gate, rn, T, E, K, dl, dl3);
+    else if (vpl <= 16)
+      softmax_topk_bwd_kernel<16><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, idx, d_gate, rn, T, E, K, dl, dl3);
+    else
+      softmax_topk_bwd_kernel<32><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, idx, d_gate, rn, T, E, K, dl, dl3);
   } else {
     // linear score: the score gradient is the logit gradient (E = K = 1)
     copy_f32_kernel<<<rows_grid(T), 256, 0, s>>>(d_gate, dl, (long long)T);

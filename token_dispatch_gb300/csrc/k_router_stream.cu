@@ -78,8 +78,8 @@ struct StreamCfg {
 template <int CH, bool E16>
 __global__ void __launch_bounds__(RS_THREADS, 1)
 router_stream_kernel(const bf16* __restrict__ x, const bf16* __restrict__ w, const float* __restrict__ bias,
-                     int T, int H, int E, int K, float* __restrict__ logits, int32_t* __restrict__ idx,
-                     float* __restrict__ gate) {
+                     const float* __restrict__ sel_bias, int renorm, int T, int H, int E, int K,
+                     float* __restrict__ logits, int32_t* __restrict__ idx, float* __restrict__ gate) {
   using C = StreamCfg<CH, E16>;
   constexpr int NF = E16 ? 2 : 1;  // 16-byte fragments per lane per chunk
   constexpr int NT = C::NT, D = C::D, TOK = C::TOK;
@@ -195,10 +195,12 @@ router_stream_kernel(const bf16* __restrict__ x, const bf16* __restrict__ w, con
       float sum = expf(v - m);
 #pragma unroll
       for (int o = E16 ? 8 : 4; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      bool taken = false;
+      // selection value: the logit, plus the selection-only bias when given
+      const float sel = sel_bias ? v + __ldg(sel_bias + e) : v;
+      int my_k = -1;
       for (int k = 0; k < K; ++k) {
-        float bv = taken ? -INFINITY : v;
-        int be = taken ? 0x7fffffff : e;
+        float bv = my_k >= 0 ? -INFINITY : sel;
+        int be = my_k >= 0 ? 0x7fffffff : e;
 #pragma unroll
         for (int o = E16 ? 8 : 4; o > 0; o >>= 1) {
           const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
@@ -206,13 +208,20 @@ router_stream_kernel(const bf16* __restrict__ x, const bf16* __restrict__ w, con
           if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
         }
         if (e == be) {
-          taken = true;
-          if (live) {
-            idx[(long long)tk * K + k] = be;
-            gate[(long long)tk * K + k] = expf(bv - m) / sum;
-          }
+          my_k = k;
+          if (live) idx[(long long)tk * K + k] = be;
         }
       }
+      // each chosen expert's thread writes its gate: its own probability, over
+      // the sum of the chosen probabilities when renormalising
+      const float pe = expf(v - m) / sum;
+      float norm = 1.f;
+      if (renorm) {
+        norm = my_k >= 0 ? pe : 0.f;
+#pragma unroll
+        for (int o = E16 ? 8 : 4; o > 0; o >>= 1) norm += __shfl_xor_sync(0xffffffffu, norm, o);
+      }
+      if (my_k >= 0 && live) gate[(long long)tk * K + my_k] = pe / norm;
     }
   };
 
@@ -224,8 +233,8 @@ router_stream_kernel(const bf16* __restrict__ x, const bf16* __restrict__ w, con
 }
 
 template <int CH>
-int launch_ch(const void* x, const void* w, const float* bias, int T, int H, int E, int K, float* logits,
-              int32_t* idx, float* gate, cudaStream_t s) {
+int launch_ch(const void* x, const void* w, const float* bias, const float* sel_bias, bool renorm, int T, int H,
+              int E, int K, float* logits, int32_t* idx, float* gate, cudaStream_t s) {
   const int tok = E > 8 ? StreamCfg<CH, true>::TOK : StreamCfg<CH, false>::TOK;
   const int red = E > 8 ? StreamCfg<CH, true>::RED_FLOATS : StreamCfg<CH, false>::RED_FLOATS;
   const int nblk = (T + tok - 1) / tok;
@@ -236,14 +245,14 @@ int launch_ch(const void* x, const void* w, const float* bias, int T, int H, int
     auto k = router_stream_kernel<CH, true>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return MOE_ERR_CUDA;
-    k<<<grid, RS_THREADS, smem, s>>>(static_cast<const bf16*>(x), static_cast<const bf16*>(w), bias, T, H, E,
-                                        K, logits, idx, gate);
+    k<<<grid, RS_THREADS, smem, s>>>(static_cast<const bf16*>(x), static_cast<const bf16*>(w), bias, sel_bias,
+                                     renorm ? 1 : 0, T, H, E, K, logits, idx, gate);
   } else {
     auto k = router_stream_kernel<CH, false>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return MOE_ERR_CUDA;
-    k<<<grid, RS_THREADS, smem, s>>>(static_cast<const bf16*>(x), static_cast<const bf16*>(w), bias, T, H, E,
-                                        K, logits, idx, gate);
+    k<<<grid, RS_THREADS, smem, s>>>(static_cast<const bf16*>(x), static_cast<const bf16*>(w), bias, sel_bias,
+                                     renorm ? 1 : 0, T, H, E, K, logits, idx, gate);
   }
   return launch_status();
 }
@@ -254,18 +263,18 @@ bool router_stream_applies(int dtype, int H, int E) {
   return dtype == MOE_BF16 && (E == 8 || E == 16) && H % 512 == 0 && H >= 512 && H <= 4096;
 }
 
-int launch_router_stream(const void* x, const void* w, const float* bias, int T, int H, int E, int K,
-                         float* logits, int32_t* idx, float* gate, cudaStream_t s) {
+int launch_router_stream(const void* x, const void* w, const float* bias, const float* sel_bias, bool renorm,
+                         int T, int H, int E, int K, float* logits, int32_t* idx, float* gate, cudaStream_t s) {
   if (T == 0) return MOE_OK;
   switch (H / 512) {
-    case 1: return launch_ch<1>(x, w, bias, T, H, E, K, logits, idx, gate, s);
-    case 2: return launch_ch<2>(x, w, bias, T, H, E, K, logits, idx, gate, s);
-    case 3: return launch_ch<3>(x, w, bias, T, H, E, K, logits, idx, gate, s);
-    case 4: return launch_ch<4>(x, w, bias, T, H, E, K, logits, idx, gate, s);
-    case 5: return launch_ch<5>(x, w, bias, T, H, E, K, logits, idx, gate, s);
-    case 6: return launch_ch<6>(x, w, bias, T, H, E, K, logits, idx, gate, s);
-    case 7: return launch_ch<7>(x, w, bias, T, H, E, K, logits, idx, gate, s);
-    case 8: return launch_ch<8>(x, w, bias, T, H, E, K, logits, idx, gate, s);
+    case 1: return launch_ch<1>(x, w, bias, sel_bias, renorm, T, H, E, K, logits, idx, gate, s);
+    case 2: return launch_ch<2>(x, w, bias, sel_bias, renorm, T, H, E, K, logits, idx, gate, s);
+    case 3: return launch_ch<3>(x, w, bias, sel_bias, renorm, T, H, E, K, logits, idx, gate, s);
+    case 4: return launch_ch<4>(x, w, bias, sel_bias, renorm, T, H, E, K, logits, idx, gate, s);
+    case 5: return launch_ch<5>(x, w, bias, sel_bias, renorm, T, H, E, K, logits, idx, gate, s);
+    case 6: return launch_ch<6>(x, w, bias, sel_bias, renorm, T, H, E, K, logits, idx, gate, s);
+    case 7: return launch_ch<7>(x, w, bias, sel_bias, renorm, T, H, E, K, logits, idx, gate, s);
+    case 8: return launch_ch<8>(x, w, bias, sel_bias, renorm, T, H, E, K, logits, idx, gate, s);
     default: return MOE_ERR_UNSUPPORTED;
   }
 }

@@ -89,11 +89,12 @@ int moe_last_device_error(void* stream) {
   return (int)v;
 }
 
-int moe_route(const void* x, const void* w_router, const float* logit_bias, int T, int H, int E,
-              int K, int dtype, float* logits, int32_t* topk_idx, float* topk_gate, void* ws,
-              size_t ws_bytes, void* stream) {
+int moe_route_ex(const void* x, const void* w_router, const float* logit_bias, int T, int H, int E, int K,
+                 int dtype, int flags, float* logits, int32_t* topk_idx, float* topk_gate, void* ws,
+                 size_t ws_bytes, void* stream) {
   if (!valid_dtype(dtype) || T < 0 || H < 1 || E < 1 || E > 1024 || K < 1 || K > E || K > 16)
     return MOE_ERR_INVALID_ARG;
+  if (flags & ~(MOE_ROUTE_RENORM | MOE_ROUTE_BIAS_SELECT)) return MOE_ERR_INVALID_ARG;
   if ((T > 0 && (!x || !logits || !topk_idx || !topk_gate)) || !w_router) return MOE_ERR_INVALID_ARG;
   if (!all_aligned({x, w_router, logit_bias, logits, topk_idx, topk_gate, ws})) return MOE_ERR_MISALIGNED;
   if (H % vec_elems(dtype) != 0 || E % 4 != 0) return MOE_ERR_UNSUPPORTED;
@@ -101,8 +102,15 @@ int moe_route(const void* x, const void* w_router, const float* logit_bias, int 
   if (T == 0) return MOE_OK;
   const size_t need = dtype == MOE_BF16 ? route_ws_bytes(T, H, E) : 0;
   if (need > 0 && (!ws || ws_bytes < need)) return MOE_ERR_WORKSPACE;
-  return launch_route(x, w_router, logit_bias, T, H, E, K, dtype, logits, topk_idx, topk_gate, ws,
+  return launch_route(x, w_router, logit_bias, T, H, E, K, dtype, flags, logits, topk_idx, topk_gate, ws,
                       as_stream(stream));
+}
+
+int moe_route(const void* x, const void* w_router, const float* logit_bias, int T, int H, int E,
+              int K, int dtype, float* logits, int32_t* topk_idx, float* topk_gate, void* ws,
+              size_t ws_bytes, void* stream) {
+  return moe_route_ex(x, w_router, logit_bias, T, H, E, K, dtype, 0, logits, topk_idx, topk_gate, ws, ws_bytes,
+                      stream);
 }
 
 int moe_dispatch(const void* x, const int32_t* topk_idx, int T, int H, int E, int K, int dtype,
@@ -167,7 +175,9 @@ int moe_route_bwd(int mode, const float* d_gate, const float* logits, const int3
   if (!valid_dtype(dtype) || T < 0 || H < 1 || E < 1 || E > 1024 || K < 1 || K > E || K > 16)
     return MOE_ERR_INVALID_ARG;
   const bool dx_write = (mode & MOE_ROUTE_DX_WRITE) != 0;
-  mode &= ~MOE_ROUTE_DX_WRITE;
+  const bool renorm = (mode & MOE_ROUTE_GATE_RENORM) != 0;
+  mode &= ~(MOE_ROUTE_DX_WRITE | MOE_ROUTE_GATE_RENORM);
+  if (renorm && mode != MOE_ROUTE_SOFTMAX_TOPK) return MOE_ERR_INVALID_ARG;
   if (mode == MOE_ROUTE_SOFTMAX_TOPK) {
     if (T > 0 && (!logits || !topk_idx)) return MOE_ERR_INVALID_ARG;
     if (E % 4 != 0) return MOE_ERR_UNSUPPORTED;
@@ -185,7 +195,7 @@ int moe_route_bwd(int mode, const float* d_gate, const float* logits, const int3
   size_t need = route_bwd_ws_bytes(T, H, E);
   if (!ws || ws_bytes < need) return MOE_ERR_WORKSPACE;
   return launch_route_bwd(mode, d_gate, logits, topk_idx, x, w_router, T, H, E, K, dtype, d_logits,
-                          dw_router, dx, dx_write, ws, as_stream(stream));
+                          dw_router, dx, dx_write, renorm, ws, as_stream(stream));
 }
 
 int moe_permute_bwd(const void* dy, const void* h, const float* gate, const int32_t* dst_row,

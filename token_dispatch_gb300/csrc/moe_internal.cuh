@@ -108,13 +108,15 @@ inline int launch_status() {
 // route
 size_t route_ws_bytes(int T, int H, int E);
 bool router_stream_applies(int dtype, int H, int E);
-int launch_router_stream(const void* x, const void* w, const float* bias, int T, int H, int E, int K,
-                         float* logits, int32_t* idx, float* gate, cudaStream_t s);
-int launch_route(const void* x, const void* w, const float* bias, int T, int H, int E, int K, int dtype,
+// bias: added to the stored logits; sel_bias: added only where experts are
+// chosen (nullable both); renorm: the K gates rescaled to sum to 1
+int launch_router_stream(const void* x, const void* w, const float* bias, const float* sel_bias, bool renorm,
+                         int T, int H, int E, int K, float* logits, int32_t* idx, float* gate, cudaStream_t s);
+int launch_route(const void* x, const void* w, const float* bias, int T, int H, int E, int K, int dtype, int flags,
                  float* logits, int32_t* idx, float* gate, void* ws, cudaStream_t s);
 int launch_route_bwd(int mode, const float* d_gate, const float* logits, const int32_t* idx,
                      const void* x, const void* w, int T, int H, int E, int K, int dtype,
-                     float* d_logits, float* dw, void* dx, bool dx_write, void* ws, cudaStream_t s);
+                     float* d_logits, float* dw, void* dx, bool dx_write, bool renorm, void* ws, cudaStream_t s);
 size_t route_bwd_ws_bytes(int T, int H, int E);
 
 // dispatch / combine / permute backward
