@@ -59,6 +59,8 @@ def parse():
                    help="router skew (maxvio) from tests/golden/skew_bias.json; 'none' for the natural "
                         "router; 'auto' = 0.2 where the table has it")
     p.add_argument("--cpu-sample-tokens", type=int, default=None)
+    p.add_argument("--route-flags", type=int, default=0,
+                   help="moe_route_ex gate options: 1 renormalise the top-k gates, 2 bias for selection only")
     p.add_argument("--no-cpu-baseline", action="store_true")
     return p.parse_args()
 
@@ -215,11 +217,12 @@ def build_inputs(shape, dev, rank, bias_np):
     return inp
 
 
-def make_step(shape, inp, dev, stream):
+def make_step(shape, inp, dev, stream, route_flags=0):
     """(call names, step(x, dy, dxs, marks) -> None, buffers, outputs for the host)."""
     import torch
     from token_dispatch_gb300 import _lib as L
     from token_dispatch_gb300 import layer
+    bwd_renorm = L.MOE_ROUTE_GATE_RENORM if route_flags & L.MOE_ROUTE_RENORM else 0
     T, H, E, K, Hp = shape.T, shape.H, shape.E, shape.K, shape.Hp
     R = T * K
     mode = inp["mode"]
@@ -230,8 +233,9 @@ def make_step(shape, inp, dev, stream):
     if mode in ("fwd_bwd", "fwd"):
         b = layer.MoEBuffers(T, H, E, K, Hp, shape.dtype, dev, backward=(mode == "fwd_bwd"))
         calls = [
-            ("route", lambda xi, dyi, dxsi: L.moe_route(xi, wr_d, bias_d, T, H, E, K, b.cdt, b.logits, b.idx, b.gate,
-                                                       b.ws_route, b.ws_route_bytes, stream=stream)),
+            ("route", lambda xi, dyi, dxsi: L.moe_route_ex(xi, wr_d, bias_d, T, H, E, K, b.cdt, route_flags, b.logits,
+                                                          b.idx, b.gate, b.ws_route, b.ws_route_bytes,
+                                                          stream=stream)),
             ("dispatch", lambda xi, dyi, dxsi: L.moe_dispatch(xi, b.idx, T, H, E, K, b.cdt, b.cu, b.dst_row,
                                                              b.src_tok, b.xs, b.ws_dispatch, b.ws_dispatch_bytes,
                                                              stream=stream)),
@@ -246,7 +250,8 @@ def make_step(shape, inp, dev, stream):
                 ("permute_bwd", lambda xi, dyi, dxsi: L.moe_permute_bwd(dyi, b.h, b.gate, b.dst_row, None, None,
                                                                        dxsi, T, H, K, b.cdt, b.dh, b.d_gate, None,
                                                                        b.dx, stream=stream)),
-                ("route_bwd", lambda xi, dyi, dxsi: L.moe_route_bwd(L.MOE_ROUTE_SOFTMAX_TOPK, b.d_gate, b.logits,
+                ("route_bwd", lambda xi, dyi, dxsi: L.moe_route_bwd(L.MOE_ROUTE_SOFTMAX_TOPK | bwd_renorm, b.d_gate,
+                                                                   b.logits,
                                                                    b.idx, xi, wr_d, T, H, E, K, b.cdt, b.d_logits,
                                                                    b.dw_router, b.dx, b.ws_bwd, b.ws_bwd_bytes,
                                                                    stream=stream)),
@@ -305,7 +310,7 @@ def run_ours(args, shape, rank, world, local):
     x_d = x_h.to(dev)
     dy_d, dxs_d = inp.get("dy"), inp.get("dxs")
     stream = torch.cuda.Stream(device=dev)
-    calls, bufs, outs, cu = make_step(shape, inp, dev, stream)
+    calls, bufs, outs, cu = make_step(shape, inp, dev, stream, args.route_flags)
     names = [n for n, _ in calls]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_rd = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -455,7 +460,8 @@ def run_ours(args, shape, rank, world, local):
         "config": {"workload": shape.name, "tokens_per_gpu": n_tok, "moe_tokens": T, "H": H, "E": E, "K": K,
                    "Hp": Hp, "maxvio": round(maxvio, 4), "maxvio_target": target,
                    "expert0_logit_bias": None if bias_entry is None else bias_entry["beta"],
-                   "l2": "flushed between timed steps (512 MB write, then 512 MB read)", "parallelism": f"replicas{world}"},
+                   "l2": "flushed between timed steps (512 MB write, then 512 MB read)", "parallelism": f"replicas{world}",
+                   "route_flags": args.route_flags},
         "calls_ms": {k: round(v, 4) for k, v in call_ms.items()},
         "roofline": {"kernel": "moe_expert_ffn (grouped gate/up+SwiGLU GEMM + down GEMM, tcgen05)", **roof},
         "hbm_roofline": {"peak_GB/s": hbm_peak, "peak_source": f"{peak_src} hbm_gbs", "calls": hbm},
@@ -469,7 +475,7 @@ def run_ours(args, shape, rank, world, local):
 
 # ----------------------------------------------------------------- CPU oracle arm
 
-def oracle_sample(shape, inp, n_tok, reps=1):
+def oracle_sample(shape, inp, n_tok, reps=1, route_flags=0):
     """Time the CPU oracle on a bounded sample of the step: the first n_tok tokens
     (MoE workloads) or the first sequence (MoD workload).  Returns (times, tokens)."""
     import oracle as O
@@ -512,9 +518,10 @@ def oracle_sample(shape, inp, n_tok, reps=1):
             O.route_bwd_softmax_topk(d_gate, inner["logits"], inner["idx"], f["x_sel"], wr64)
             O.route_bwd_linear(d_score, f["x_sel"], inp["wmod"].ref)
         else:
-            f = O.moe_forward(x64, wr64, wg, wu, wd, shape.K, bias)
+            f = O.moe_forward(x64, wr64, wg, wu, wd, shape.K, bias, renorm=bool(route_flags & 1),
+                              bias_select_only=bool(route_flags & 2))
             if mode == "fwd_bwd":
-                O.moe_backward(f, dy, dxs, x64, wr64)
+                O.moe_backward(f, dy, dxs, x64, wr64, renorm=bool(route_flags & 1))
         times.append(time.perf_counter() - t0)
     return times, n_tok
 
@@ -545,8 +552,8 @@ def main():
         bias_np, _, target = skew_bias(shape, args.bias_target)
         inp = build_inputs(shape, dev, 0, bias_np)  # drawn exactly as the GPU arm draws them
         n_tok = args.cpu_sample_tokens or {"fwd_bwd": 32, "fwd": 8, "mod": None}[mode]
-        oracle_sample(shape, inp, n_tok, reps=1)
-        times, n_tok = oracle_sample(shape, inp, n_tok, reps=args.steps)
+        oracle_sample(shape, inp, n_tok, reps=1, route_flags=args.route_flags)
+        times, n_tok = oracle_sample(shape, inp, n_tok, reps=args.steps, route_flags=args.route_flags)
         ms = 1e3 * statistics.mean(times)
         val = n_tok / (ms * 1e-3)
         sample = f"first {n_tok} tokens of the batch per step" if mode != "mod" else \
@@ -564,7 +571,7 @@ def main():
     result, inp = run_ours(args, shape, rank, world, local)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         n_tok = args.cpu_sample_tokens or default_sample(mode)
-        times, n_tok = oracle_sample(shape, inp, n_tok, reps=1)
+        times, n_tok = oracle_sample(shape, inp, n_tok, reps=1, route_flags=args.route_flags)
         what = "the first sequence (MoD select + MoE on 1024 tokens + route bwd)" if mode == "mod" else \
             f"first {n_tok} tokens of the batch ({'fwd + gate/dispatch bwd' if mode == 'fwd_bwd' else 'fwd'})"
         result["cpu_baseline"] = {"value": n_tok / times[0], "unit": "tokens/s", "cores": cores(),

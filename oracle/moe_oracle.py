@@ -317,10 +317,10 @@ def mod_select(score, B, L, C):
 # ----------------------------------------------------------------------------
 
 
-def moe_forward(x, w_router, w_gate, w_up, w_down, K, bias=None):
-    """route -> dispatch -> grouped SwiGLU experts -> combine."""
+def moe_forward(x, w_router, w_gate, w_up, w_down, K, bias=None, renorm=False, bias_select_only=False):
+    """route -> dispatch -> grouped SwiGLU experts -> combine (gate options as in route)."""
     E = w_router.shape[1]
-    logits, p, idx, gate = route(x, w_router, K, bias)
+    logits, p, idx, gate = route(x, w_router, K, bias, renorm=renorm, bias_select_only=bias_select_only)
     cu, dst_row, src_tok, xs = dispatch(x, idx, E)
     act, h = expert_ffn(xs, cu, w_gate, w_up, w_down)
     y = combine(h, gate, dst_row)
@@ -328,10 +328,10 @@ def moe_forward(x, w_router, w_gate, w_up, w_down, K, bias=None):
                 src_tok=src_tok, xs=xs, act=act, h=h, y=y)
 
 
-def moe_backward(fwd, dy, dxs, x, w_router):
+def moe_backward(fwd, dy, dxs, x, w_router, renorm=False):
     """Gate and dispatch/combine backward given dy and a dxs for the expert inputs."""
     dh, d_gate, _, dx_disp = permute_bwd(dy, fwd["h"], fwd["gate"], fwd["dst_row"], dxs)
-    d_logits, dw, dx_r = route_bwd_softmax_topk(d_gate, fwd["logits"], fwd["idx"], x, w_router)
+    d_logits, dw, dx_r = route_bwd_softmax_topk(d_gate, fwd["logits"], fwd["idx"], x, w_router, renorm=renorm)
     return dict(dh=dh, d_gate=d_gate, d_logits=d_logits, dw_router=dw, dx=dx_disp + dx_r)
 
 

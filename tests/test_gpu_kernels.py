@@ -459,21 +459,26 @@ def test_mod_select_integer_scores_select_exactly(dtype):
     assert np.array_equal(sel.cpu().numpy(), (np.arange(B)[:, None] * Lseq + sel_r).reshape(-1))
 
 
-def test_tiny_fp32_layer_end_to_end():
+@pytest.mark.parametrize("flags", [0, 1, 3], ids=["plain", "renorm", "renorm_bias_select"])
+def test_tiny_fp32_layer_end_to_end(flags):
     """The tiny fp32 layer (T=256, H=128, E=8, K=2, H'=256): forward plus the
-    gate/dispatch backward through the C ABI, max relative error <= 1e-5."""
+    gate/dispatch backward through the C ABI, max relative error <= 1e-5; also
+    with the Mixtral-style renormalised gates and a selection-only bias."""
     shape = synth.TINY_F32
     T, H, E, K, Hp = shape.T, shape.H, shape.E, shape.K, shape.Hp
     x, wr, wg, wu, wd = host_layer_inputs(shape)
     dy = synth.upstream_grad(shape, T, H)
     dxs = synth.upstream_grad(shape, T * K, H, seed=2, stream=synth.S_DXS)
+    bias = (np.random.default_rng(12).standard_normal(E) * 0.3).astype(np.float32) if flags & 2 else None
     b = layer.MoEBuffers(T, H, E, K, Hp, "f32", DEV)
     xd, wrd = dev(x), dev(wr)
-    layer.moe_forward(b, xd, wrd, None, dev(wg), dev(wu), dev(wd))
-    layer.moe_backward(b, xd, wrd, dev(dy), dev(dxs))
+    bd = None if bias is None else torch.from_numpy(bias).to(DEV)
+    layer.moe_forward(b, xd, wrd, bd, dev(wg), dev(wu), dev(wd), route_flags=flags)
+    layer.moe_backward(b, xd, wrd, dev(dy), dev(dxs), route_flags=flags)
     assert L.moe_last_device_error() == L.MOE_OK
-    f = O.moe_forward(x.ref, wr.ref, wg.ref, wu.ref, wd.ref, K)
-    g = O.moe_backward(f, dy.ref, dxs.ref, x.ref, wr.ref)
+    f = O.moe_forward(x.ref, wr.ref, wg.ref, wu.ref, wd.ref, K, None if bias is None else bias.astype(np.float64),
+                      renorm=bool(flags & 1), bias_select_only=bool(flags & 2))
+    g = O.moe_backward(f, dy.ref, dxs.ref, x.ref, wr.ref, renorm=bool(flags & 1))
     assert np.array_equal(b.idx.cpu().numpy(), f["idx"])
     assert np.array_equal(b.cu.cpu().numpy(), f["cu"])
     assert np.array_equal(b.dst_row.cpu().numpy(), f["dst_row"])

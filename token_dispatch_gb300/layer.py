@@ -60,11 +60,12 @@ class MoEBuffers:
 
 
 def moe_forward(b: MoEBuffers, x, w_router, logit_bias, w_gate, w_up, w_down, stream=None,
-                row_scale=None, residual=None, out_row=None, y=None):
-    """One MoE forward pass into the buffers of ``b`` (y defaults to ``b.y``)."""
+                row_scale=None, residual=None, out_row=None, y=None, route_flags=0):
+    """One MoE forward pass into the buffers of ``b`` (y defaults to ``b.y``);
+    ``route_flags``: MOE_ROUTE_RENORM / MOE_ROUTE_BIAS_SELECT gate options."""
     T, H, E, K, Hp, dt = b.T, b.H, b.E, b.K, b.Hp, b.cdt
-    L.moe_route(x, w_router, logit_bias, T, H, E, K, dt, b.logits, b.idx, b.gate, b.ws_route, b.ws_route_bytes,
-                stream=stream)
+    L.moe_route_ex(x, w_router, logit_bias, T, H, E, K, dt, route_flags, b.logits, b.idx, b.gate, b.ws_route,
+                   b.ws_route_bytes, stream=stream)
     L.moe_dispatch(x, b.idx, T, H, E, K, dt, b.cu, b.dst_row, b.src_tok, b.xs, b.ws_dispatch,
                    b.ws_dispatch_bytes, stream=stream)
     L.moe_expert_ffn(b.xs, b.cu, T * K, w_gate, w_up, w_down, E, H, Hp, dt, b.act, b.h, stream=stream)
@@ -73,13 +74,14 @@ def moe_forward(b: MoEBuffers, x, w_router, logit_bias, w_gate, w_up, w_down, st
 
 
 def moe_backward(b: MoEBuffers, x, w_router, dy, dxs, stream=None, row_scale=None, out_row=None,
-                 d_scale=None):
+                 d_scale=None, route_flags=0):
     """Gate and dispatch/combine backward: dh, d_gate, d_logits, dw_router and
     dx = (adjoint of the gather applied to dxs) + router contribution."""
     T, H, E, K, dt = b.T, b.H, b.E, b.K, b.cdt
     L.moe_permute_bwd(dy, b.h, b.gate, b.dst_row, row_scale, out_row, dxs, T, H, K, dt, b.dh,
                       b.d_gate, d_scale, b.dx, stream=stream)
-    L.moe_route_bwd(L.MOE_ROUTE_SOFTMAX_TOPK, b.d_gate, b.logits, b.idx, x, w_router, T, H, E, K, dt,
+    renorm = L.MOE_ROUTE_GATE_RENORM if route_flags & L.MOE_ROUTE_RENORM else 0
+    L.moe_route_bwd(L.MOE_ROUTE_SOFTMAX_TOPK | renorm, b.d_gate, b.logits, b.idx, x, w_router, T, H, E, K, dt,
                     b.d_logits, b.dw_router, b.dx, b.ws_bwd, b.ws_bwd_bytes, stream=stream)
 
 
