@@ -187,6 +187,41 @@ def expert_ffn(xs, cu, w_gate, w_up, w_down):
     return act, h
 
 
+def expert_swiglu_bwd(xs_rows, wg_e, wu_e, wd_e, dh_rows):
+    """Backward of one expert on its rows, given dh = dL/dh for h = a Wd^T with
+    a = silu(g) * u, g = X Wg, u = X Wu  [T4 "RMSNorm, RoPE, SwiGLU": SwiGLU is
+    three matrix products; FW "What's in the box": the layer trains].
+        da  = dh Wd                       dWd = dh^T a
+        dg  = da * u * silu'(g),          silu'(g) = s(g) (1 + g (1 - s(g))), s = logistic
+        du  = da * silu(g)
+        dX  = dg Wg^T + du Wu^T           dWg = X^T dg,  dWu = X^T du
+    Returns dX, dWg, dWu, dWd."""
+    g = xs_rows @ wg_e
+    u = xs_rows @ wu_e
+    sg = 1.0 / (1.0 + np.exp(-g))
+    a = g * sg * u
+    da = dh_rows @ wd_e
+    dg = da * u * sg * (1.0 + g * (1.0 - sg))
+    du = da * g * sg
+    dx = dg @ wg_e.T + du @ wu_e.T
+    return dx, xs_rows.T @ dg, xs_rows.T @ du, dh_rows.T @ a
+
+
+def expert_ffn_bwd(xs, cu, w_gate, w_up, w_down, dh):
+    """Backward of expert_ffn: dxs [R,H] and the weight gradients dW_gate,
+    dW_up, dW_down [E,H,H'] (zero for experts without rows)."""
+    xs, dh = np.asarray(xs, np.float64), np.asarray(dh, np.float64)
+    E, H, Hp = w_gate.shape
+    dxs = np.zeros_like(xs)
+    dwg, dwu, dwd = np.zeros((E, H, Hp)), np.zeros((E, H, Hp)), np.zeros((E, H, Hp))
+    for e in range(E):
+        lo, hi = int(cu[e]), int(cu[e + 1])
+        if hi > lo:
+            dxs[lo:hi], dwg[e], dwu[e], dwd[e] = expert_swiglu_bwd(xs[lo:hi], w_gate[e], w_up[e], w_down[e],
+                                                                   dh[lo:hi])
+    return dxs, dwg, dwu, dwd
+
+
 def expert_of_row(cu, rows):
     """Expert e with cu[e] <= row < cu[e+1] for each row."""
     cu = np.asarray(cu, np.int64)

@@ -366,6 +366,42 @@ def test_route_backward_renorm_matches_central_differences(T, E, K):
     assert (d_logits[~chosen] == 0).all()
 
 
+def test_expert_ffn_backward_matches_central_differences():
+    """dL/d(xs, Wg, Wu, Wd) for L = sum(dh * h) with h the grouped SwiGLU FFN, on
+    three experts one of which has no rows."""
+    r = np.random.default_rng(720)
+    E, H, Hp = 3, 5, 4
+    cu = np.array([0, 3, 3, 7])
+    xs = r.standard_normal((7, H))
+    wg, wu, wd = r.standard_normal((E, H, Hp)), r.standard_normal((E, H, Hp)), r.standard_normal((E, H, Hp))
+    dh = r.standard_normal((7, H))
+
+    def loss(xs_, wg_, wu_, wd_):
+        return float((dh * O.expert_ffn(xs_, cu, wg_, wu_, wd_)[1]).sum())
+
+    dxs, dwg, dwu, dwd = O.expert_ffn_bwd(xs, cu, wg, wu, wd, dh)
+    assert (dwg[1] == 0).all() and (dwu[1] == 0).all() and (dwd[1] == 0).all()
+    for arr, grad, f in [(xs, dxs, lambda v: loss(v, wg, wu, wd)), (wg, dwg, lambda v: loss(xs, v, wu, wd)),
+                         (wu, dwu, lambda v: loss(xs, wg, v, wd)), (wd, dwd, lambda v: loss(xs, wg, wu, v))]:
+        for i in range(arr.size):
+            assert math.isclose(central_diff(f, arr, i), grad.reshape(-1)[i], rel_tol=1e-6, abs_tol=1e-8)
+
+
+def test_expert_backward_single_row_by_hand():
+    """One row, one expert, H = H' = 1: every gradient written out with scalars."""
+    x, g_w, u_w, d_w, dy = 0.7, -1.3, 0.4, 2.1, -0.6
+    g, u = x * g_w, x * u_w
+    s = 1.0 / (1.0 + math.exp(-g))
+    dsilu = s + g * s * (1.0 - s)  # derivative of g * s(g)
+    da = dy * d_w
+    dxs, dwg, dwu, dwd = O.expert_ffn_bwd(np.array([[x]]), np.array([0, 1]), np.array([[[g_w]]]),
+                                          np.array([[[u_w]]]), np.array([[[d_w]]]), np.array([[dy]]))
+    assert math.isclose(dwd[0, 0, 0], dy * g * s * u, rel_tol=1e-14)
+    assert math.isclose(dwg[0, 0, 0], x * da * u * dsilu, rel_tol=1e-14)
+    assert math.isclose(dwu[0, 0, 0], x * da * g * s, rel_tol=1e-14)
+    assert math.isclose(dxs[0, 0], da * u * dsilu * g_w + da * g * s * u_w, rel_tol=1e-14)
+
+
 def test_route_backward_E_equals_K_is_softmax_jacobian():
     """With every expert selected the gradient is J^T g with J = diag(p) - p p^T."""
     T, E = 7, 5
