@@ -64,7 +64,8 @@ typedef enum {
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
 
 /* operation ids for moe_workspace_bytes */
-enum { MOE_OP_ROUTE = 0, MOE_OP_DISPATCH = 1, MOE_OP_EXPERT_FFN = 2, MOE_OP_ROUTE_BWD = 3, MOE_OP_MOD_SELECT = 4 };
+enum { MOE_OP_ROUTE = 0, MOE_OP_DISPATCH = 1, MOE_OP_EXPERT_FFN = 2, MOE_OP_ROUTE_BWD = 3, MOE_OP_MOD_SELECT = 4,
+       MOE_OP_EXPERT_FFN_BWD = 5 };
 
 /* moe_route_bwd modes; MOE_ROUTE_DX_WRITE may be or-ed in to overwrite dx instead
  * of accumulating into it, MOE_ROUTE_GATE_RENORM when the forward renormalised the
@@ -197,6 +198,41 @@ MOE_API int moe_dispatch_noalloc(const void* x, const int32_t* topk_idx, int T, 
 MOE_API int moe_expert_ffn(const void* xs, const int32_t* cu_seqlens, int rows,
                    const void* w_gate, const void* w_up, const void* w_down,
                    int E, int H, int Hp, int dtype, void* act, void* h,
+                   void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Expert FFN forward that also keeps the SwiGLU pre-activations for the backward
+ *
+ * moe_expert_ffn plus gu [rows, 2*Hp] dtype out (nullable): gu[r, 0:Hp] = g =
+ * xs[r,:] . w_gate[e] and gu[r, Hp:2Hp] = u = xs[r,:] . w_up[e], rounded to dtype.
+ * gu needs bf16 (MOE_ERR_UNSUPPORTED otherwise).  gu = NULL is moe_expert_ffn.
+ */
+MOE_API int moe_expert_ffn_ex(const void* xs, const int32_t* cu_seqlens, int rows,
+                   const void* w_gate, const void* w_up, const void* w_down,
+                   int E, int H, int Hp, int dtype, void* act, void* gu, void* h,
+                   void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Expert FFN backward         [T4 "RMSNorm, RoPE, SwiGLU": SwiGLU = three matrix
+ *                              products; FW "What's in the box": the layer trains]
+ *
+ * Given dh = dL/dh [rows,H] for the forward above (gu and act as the forward wrote
+ * them), for every expert e and its rows:
+ *   da  = dh . w_down[e]                        [rows_e, Hp]
+ *   dg  = da * u * s(g) * (1 + g (1 - s(g)))    du = da * g * s(g)      s = logistic
+ *   dxs = dg . w_gate[e]^T + du . w_up[e]^T     [rows_e, H]   dtype out (nullable)
+ *   dw_gate[e] = xs_e^T dg,  dw_up[e] = xs_e^T du,  dw_down[e] = dh_e^T act_e
+ *                                               [E,H,Hp] float out each (nullable);
+ *                                               zero for experts without rows
+ * bf16 only (MOE_ERR_UNSUPPORTED otherwise), same shape rules as moe_expert_ffn.
+ * Workspace: moe_workspace_bytes(MOE_OP_EXPERT_FFN_BWD, T, H, E, K, Hp) bytes with
+ * T*K = rows (it holds [dg | du], bf16).  Weight gradients are written, not
+ * accumulated, each element reduced over its expert's rows in one fp32 accumulator.
+ */
+MOE_API int moe_expert_ffn_bwd(const void* xs, const int32_t* cu_seqlens, int rows,
+                   const void* w_gate, const void* w_up, const void* w_down,
+                   int E, int H, int Hp, int dtype, const void* gu, const void* act, const void* dh,
+                   void* dxs, float* dw_gate, float* dw_up, float* dw_down,
                    void* ws, size_t ws_bytes, void* stream);
 
 /*

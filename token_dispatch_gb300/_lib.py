@@ -30,6 +30,7 @@ MOE_OP_DISPATCH = 1
 MOE_OP_EXPERT_FFN = 2
 MOE_OP_ROUTE_BWD = 3
 MOE_OP_MOD_SELECT = 4
+MOE_OP_EXPERT_FFN_BWD = 5
 
 MOE_ROUTE_SOFTMAX_TOPK = 0
 MOE_ROUTE_MOD_LINEAR = 1
@@ -40,7 +41,8 @@ MOE_ROUTE_RENORM = 0x1
 MOE_ROUTE_BIAS_SELECT = 0x2
 
 EXPORTS = ("moe_status_str", "moe_version", "moe_kernel_launches", "moe_workspace_bytes", "moe_last_device_error",
-           "moe_route", "moe_route_ex", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn", "moe_combine", "moe_route_bwd",
+           "moe_route", "moe_route_ex", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn",
+           "moe_expert_ffn_ex", "moe_expert_ffn_bwd", "moe_combine", "moe_route_bwd",
            "moe_permute_bwd", "mod_select")
 
 
@@ -67,6 +69,8 @@ _SIGS = {
     "moe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_dispatch_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_expert_ffn": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _Z, _P]),
+    "moe_expert_ffn_ex": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
+    "moe_expert_ffn_bwd": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_combine": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_route_bwd": (_I, [_I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
     "moe_permute_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
@@ -167,6 +171,22 @@ def moe_expert_ffn(xs, cu_seqlens, rows, w_gate, w_up, w_down, E, H, Hp, dtype, 
     _check("moe_expert_ffn", lib().moe_expert_ffn(_ptr(xs), _ptr(cu_seqlens), rows, _ptr(w_gate),
                                                   _ptr(w_up), _ptr(w_down), E, H, Hp, dtype, _ptr(act),
                                                   _ptr(h), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def moe_expert_ffn_ex(xs, cu_seqlens, rows, w_gate, w_up, w_down, E, H, Hp, dtype, act, gu, h,
+                      ws=None, ws_bytes=0, stream=None):
+    _check("moe_expert_ffn_ex", lib().moe_expert_ffn_ex(_ptr(xs), _ptr(cu_seqlens), rows, _ptr(w_gate), _ptr(w_up),
+                                                        _ptr(w_down), E, H, Hp, dtype, _ptr(act), _ptr(gu), _ptr(h),
+                                                        _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def moe_expert_ffn_bwd(xs, cu_seqlens, rows, w_gate, w_up, w_down, E, H, Hp, dtype, gu, act, dh, dxs,
+                       dw_gate, dw_up, dw_down, ws, ws_bytes, stream=None):
+    _check("moe_expert_ffn_bwd", lib().moe_expert_ffn_bwd(_ptr(xs), _ptr(cu_seqlens), rows, _ptr(w_gate),
+                                                          _ptr(w_up), _ptr(w_down), E, H, Hp, dtype, _ptr(gu),
+                                                          _ptr(act), _ptr(dh), _ptr(dxs), _ptr(dw_gate),
+                                                          _ptr(dw_up), _ptr(dw_down), _ptr(ws), ws_bytes,
+                                                          _stream(stream)))
 
 
 def moe_combine(h, gate, dst_row, row_scale, residual, out_row, T, H, K, dtype, y, stream=None):

@@ -51,7 +51,10 @@ constexpr int BK = 64;            // 64 bf16 = 128 bytes: one swizzle row
 constexpr int NUM_THREADS = 192;  // 6 warps
 constexpr int A_STAGE_BYTES = BM * BK * 2;
 
-enum Epi { EPI_SWIGLU = 0, EPI_BF16 = 1, EPI_F32_BIAS = 2, EPI_ROUTER = 3 };
+// EPI_SWIGLU_BWD: the accumulator is da; with g, u read back from p.aux it
+// writes dg and du (bf16) side by side.  EPI_F32_GK: fp32 tile of a grouped-K
+// product (one output slab per group), zeros for a group without rows.
+enum Epi { EPI_SWIGLU = 0, EPI_BF16 = 1, EPI_F32_BIAS = 2, EPI_ROUTER = 3, EPI_SWIGLU_BWD = 4, EPI_F32_GK = 5 };
 
 struct Params {
   const int32_t* cu;  // nullptr: one group of M rows
@@ -71,6 +74,15 @@ struct Params {
   float* topk_gate = nullptr;
   const float* sel_bias = nullptr;  // added only where experts are chosen
   int renorm = 0;                   // the K gates rescaled to sum to 1
+  // EPI_SWIGLU: when set, g and u are also stored (bf16, [g | u] per row of
+  // ld_aux elements); EPI_SWIGLU_BWD: where g and u are read from
+  void* aux = nullptr;
+  long long ld_aux = 0;
+  // K-major B from two tensors along K: k < kcat from tmB, k >= kcat from tmB2
+  int kcat = 0;
+  // grouped K: group g reduces over rows [cu[g], cu[g+1]) of K (M, N fixed)
+  int gk = 0;
+  int b_col_off = 0;  // added to the N coordinate of MN-major B loads
 };
 
 // Waits for copies and MMAs already in flight when a role stops always use
@@ -202,7 +214,7 @@ struct Cfg {
   // bf16 epilogue: per warp a [32 rows][33] fp32 staging tile, so the global
   // stores (and the reads of the old values) go out row-contiguous
   static constexpr int STG_LD = 33;
-  static constexpr int EPI_BYTES = (EPI == EPI_BF16) ? 4 * 32 * STG_LD * 4 : 0;
+  static constexpr int EPI_BYTES = (EPI == EPI_BF16 || EPI == EPI_F32_GK) ? 4 * 32 * STG_LD * 4 : 0;
 };
 
 struct TileInfo {
@@ -279,14 +291,20 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
-    if (EPI == EPI_SWIGLU) prefetch_tmap(&tmB2);
+    if (EPI == EPI_SWIGLU || p.kcat) prefetch_tmap(&tmB2);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base_slot)),
                  "r"((uint32_t)C::TMEM_COLS));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  if (warp == 2) {
+  if (warp == 2 && p.gk) {
+    // grouped K: G x (M tiles) x (N tiles), all groups alike
+    if (lane == 0) {
+      total_tiles_s = G * ((p.M + BM - 1) / BM) * n_tiles;
+      if (p.cu[0] != 0 || p.cu[G] != p.K) set_error(p.err, DEV_BOUNDS);
+    }
+  } else if (warp == 2) {
     // m-tile prefix over groups: each lane owns a contiguous run of groups
     const int per = (G + 31) / 32;
     int sum = 0;
@@ -321,6 +339,40 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int KB_ALL = (p.K + KSTAGE - 1) / KSTAGE;
   // k-blocks [kb_lo, kb_hi) of split s (every split non-empty: ksplit <= KB_ALL)
   auto kb_lo = [&](int s) { return (int)((long long)s * KB_ALL / p.ksplit); };
+  // One work item: its output tile, its k-blocks, the first K row of block 0,
+  // the output slab (split or group) and the valid rows of its last k-block.
+  struct Work {
+    TileInfo ti;
+    int kb_begin, kb_end, k_base, slab, last_valid;
+  };
+  const int gk_mt = (p.M + BM - 1) / BM;
+  auto work = [&](int t) {
+    Work w;
+    if (p.gk) {
+      const int per_g = gk_mt * n_tiles;
+      const int g = t / per_g, rem = t - g * per_g;
+      const int m = rem % gk_mt, n = rem / gk_mt;
+      w.ti.g = g;
+      w.ti.row0 = m * BM;
+      w.ti.rows = min(BM, p.M - w.ti.row0);
+      w.ti.n0 = n * C::OUT_BN;
+      const int beg = p.cu[g], rows = max(0, p.cu[g + 1] - beg);
+      w.kb_begin = 0;
+      w.kb_end = (rows + BK - 1) / BK;
+      w.k_base = beg;
+      w.slab = g;
+      w.last_valid = rows - (w.kb_end - 1) * BK;
+    } else {
+      const int split = t / base_tiles;
+      w.ti = decode(t - split * base_tiles, mt_pre, G, n_tiles, p, C::OUT_BN);
+      w.kb_begin = kb_lo(split);
+      w.kb_end = kb_lo(split + 1);
+      w.k_base = 0;
+      w.slab = split;
+      w.last_valid = BK;
+    }
+    return w;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -331,14 +383,13 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       for (int s = 0; s < STAGES; ++s) filled_parity[s] = -1;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-        const int split = t / base_tiles;
-        const TileInfo ti = decode(t - split * base_tiles, mt_pre, G, n_tiles, p, C::OUT_BN);
-        const int kb_end = kb_lo(split + 1);
-        for (int kb = kb_lo(split); kb < kb_end; ++kb) {
+        const Work wk = work(t);
+        const TileInfo& ti = wk.ti;
+        for (int kb = wk.kb_begin; kb < wk.kb_end; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, &abort_flag, p)) { ok = false; break; }
           const uint32_t a_dst = smem_u32(stage_base + stage * C::STAGE_BYTES);
           const uint32_t b_dst = a_dst + NA * A_STAGE_BYTES;
-          const int k0 = kb * KSTAGE;
+          const int k0 = wk.k_base + kb * KSTAGE;
           mbar_expect_tx(full_bar(stage), C::STAGE_BYTES);
           filled_parity[stage] = (int)phase;
 #pragma unroll
@@ -365,9 +416,12 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 tma_load_3d(dst + c * (64 * BK * 2), m, full_bar(stage), col, k0, z);
               }
             } else if (B_MN) {
+              const int zb = p.gk ? 0 : z;
 #pragma unroll
               for (int c = 0; c < BN / 64; ++c)
-                tma_load_3d(dst + c * (64 * BK * 2), &tmB, full_bar(stage), ti.n0 + c * 64, kb0, z);
+                tma_load_3d(dst + c * (64 * BK * 2), &tmB, full_bar(stage), ti.n0 + c * 64 + p.b_col_off, kb0, zb);
+            } else if (p.kcat && kb0 >= p.kcat) {
+              tma_load_3d(dst, &tmB2, full_bar(stage), kb0 - p.kcat, ti.n0, z);
             } else {
               tma_load_3d(dst, &tmB, full_bar(stage), kb0, ti.n0, z);
             }
@@ -398,13 +452,26 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (!wait_bounded(acce_bar(acc), (((uint32_t)i >> 1) & 1u) ^ 1u, &abort_flag, p)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        const int split = t / base_tiles;
-        const int kb_begin = kb_lo(split), kb_end = kb_lo(split + 1);
+        const Work wk = work(t);
+        const int kb_begin = wk.kb_begin, kb_end = wk.kb_end;
         for (int kb = kb_begin; kb < kb_end; ++kb) {
           if (!wait_bounded(full_bar(stage), phase, &abort_flag, p)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(stage_base + stage * C::STAGE_BYTES);
           const uint32_t b_addr = a_addr + NA * A_STAGE_BYTES;
+          if (A_MN && kb == kb_end - 1 && wk.last_valid < BK) {
+            // grouped K: the last block's rows past the group belong to the next
+            // group; zero them in A (each K row of an MN-major box is one
+            // 128-byte line, so the swizzle does not matter) before the MMAs
+            uint8_t* a_gen = stage_base + stage * C::STAGE_BYTES;
+            for (int bx = 0; bx < 2; ++bx)
+              for (int r = wk.last_valid; r < BK; ++r) {
+                uint4* line = reinterpret_cast<uint4*>(a_gen + bx * (64 * BK * 2) + r * 128);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) line[j] = make_uint4(0, 0, 0, 0);
+              }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          }
 #pragma unroll
           for (int pp = 0; pp < C::NP; ++pp) {
             const uint32_t a_t = a_addr + (pp < NA ? pp : NA - 1) * A_STAGE_BYTES;
@@ -446,8 +513,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int acc = i & 1;
       if (!wait_bounded(accf_bar(acc), ((uint32_t)i >> 1) & 1u, &abort_flag, p)) break;
       tc_fence_after();
-      const int split = t / base_tiles;
-      const TileInfo ti = decode(t - split * base_tiles, mt_pre, G, n_tiles, p, C::OUT_BN);
+      const Work wk = work(t);
+      const TileInfo& ti = wk.ti;
+      const int split = wk.slab;
       const long long grow = (long long)ti.row0 + r_local;
       const bool row_ok = r_local < ti.rows && grow >= 0 && grow < p.M;
       const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
@@ -471,7 +539,96 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             uint4* dst = reinterpret_cast<uint4*>(out + grow * p.ldo + col);
 #pragma unroll
             for (int j = 0; j < 4; ++j) dst[j] = pk[j];
+            if (p.aux) {  // keep g and u for the backward
+              uint4 gp[4], up[4];
+              __nv_bfloat162* g2 = reinterpret_cast<__nv_bfloat162*>(gp);
+              __nv_bfloat162* u2 = reinterpret_cast<__nv_bfloat162*>(up);
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                g2[j] = __floats2bfloat162_rn(gv[2 * j], gv[2 * j + 1]);
+                u2[j] = __floats2bfloat162_rn(uv[2 * j], uv[2 * j + 1]);
+              }
+              bf16* ax = static_cast<bf16*>(p.aux) + grow * p.ld_aux;
+              uint4* gd = reinterpret_cast<uint4*>(ax + col);
+              uint4* ud = reinterpret_cast<uint4*>(ax + p.N + col);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                gd[j] = gp[j];
+                ud[j] = up[j];
+              }
+            }
           }
+        }
+      } else if (EPI == EPI_SWIGLU_BWD) {
+        // da for 32 columns at a time; g and u of the same columns come from
+        // p.aux ([g | u] per row); dg and du go to p.out ([dg | du] per row)
+        //   dg = da * u * s(g) * (1 + g * (1 - s(g))),  du = da * g * s(g)
+        bf16* out = static_cast<bf16*>(p.out);
+        const bf16* ax = static_cast<const bf16*>(p.aux);
+#pragma unroll 1
+        for (int c = 0; c < C::OUT_BN / 32; ++c) {
+          float da[32];
+          tmem_ld32(tbase + c * 32, da);
+          const int col = ti.n0 + c * 32;
+          if (row_ok && col < p.N) {
+            const uint4* gs = reinterpret_cast<const uint4*>(ax + grow * p.ld_aux + col);
+            const uint4* us = reinterpret_cast<const uint4*>(ax + grow * p.ld_aux + p.N + col);
+            uint4 gq[4], uq[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              gq[j] = gs[j];
+              uq[j] = us[j];
+            }
+            uint4 dgp[4], dup[4];
+            const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(gq);
+            const __nv_bfloat162* u2 = reinterpret_cast<const __nv_bfloat162*>(uq);
+            __nv_bfloat162* dg2 = reinterpret_cast<__nv_bfloat162*>(dgp);
+            __nv_bfloat162* du2 = reinterpret_cast<__nv_bfloat162*>(dup);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+              const float2 g = __bfloat1622float2(g2[j]);
+              const float2 u = __bfloat1622float2(u2[j]);
+              const float s0 = 1.0f / (1.0f + __expf(-g.x)), s1 = 1.0f / (1.0f + __expf(-g.y));
+              const float a0 = da[2 * j], a1 = da[2 * j + 1];
+              dg2[j] = __floats2bfloat162_rn(a0 * u.x * s0 * (1.0f + g.x * (1.0f - s0)),
+                                             a1 * u.y * s1 * (1.0f + g.y * (1.0f - s1)));
+              du2[j] = __floats2bfloat162_rn(a0 * g.x * s0, a1 * g.y * s1);
+            }
+            uint4* dgd = reinterpret_cast<uint4*>(out + grow * p.ldo + col);
+            uint4* dud = reinterpret_cast<uint4*>(out + grow * p.ldo + p.N + col);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              dgd[j] = dgp[j];
+              dud[j] = dup[j];
+            }
+          }
+        }
+      } else if (EPI == EPI_F32_GK) {
+        // fp32 tile of group wk.slab through this warp's staging tile: 4 rows x
+        // 128 bytes per store instruction; a group without rows gets zeros
+        float* out = static_cast<float*>(p.out) + (long long)wk.slab * p.part_stride;
+        float* stg = epi_stage + q * 32 * C::STG_LD;
+        const bool empty = wk.kb_end <= wk.kb_begin;
+        const int seg = (lane & 7) * 4;
+#pragma unroll 1
+        for (int c = 0; c < C::OUT_BN / 32; ++c) {
+          float v[32];
+          if (!empty) tmem_ld32(tbase + c * 32, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) stg[lane * C::STG_LD + j] = empty ? 0.f : v[j];
+          __syncwarp();
+#pragma unroll
+          for (int ps = 0; ps < 8; ++ps) {
+            const int rw = ps * 4 + (lane >> 3);
+            const int rr = q * 32 + rw;
+            const long long gr = (long long)ti.row0 + rr;
+            const int col = ti.n0 + c * 32 + seg;
+            if (rr < ti.rows && gr < p.M && col < p.N) {
+              const float* sp = stg + rw * C::STG_LD + seg;
+              *reinterpret_cast<float4*>(out + gr * p.ldo + col) = make_float4(sp[0], sp[1], sp[2], sp[3]);
+            }
+          }
+          __syncwarp();
         }
       } else if (EPI == EPI_BF16) {
         // TMEM row per thread -> this warp's staging tile -> 8 rows x 64 bytes
@@ -686,7 +843,7 @@ Params params(const int32_t* cu, int G, int M, int N, int K, void* out, long lon
 
 // act = silu(xs Wg[e]) * (xs Wu[e]);  h = act Wd[e]^T   (bf16, grouped by cu)
 int launch_expert_ffn_tc(const void* xs, const int32_t* cu, int rows, const void* wg, const void* wu,
-                         const void* wd, int E, int H, int Hp, void* act, void* h, cudaStream_t s) {
+                         const void* wd, int E, int H, int Hp, void* act, void* gu, void* h, cudaStream_t s) {
   using namespace tc;
   if (E > 1024) return MOE_ERR_UNSUPPORTED;
   CUtensorMap mA, mG, mU, mA2, mD;
@@ -697,10 +854,62 @@ int launch_expert_ffn_tc(const void* xs, const int32_t* cu, int rows, const void
   if (!map_3d(&mD, wd, Hp, H, E, BK, 256)) return MOE_ERR_CUDA;
   const long long mtiles = (rows + BM - 1) / BM + E;
   Params p1 = params(cu, E, rows, Hp, H, act, Hp, nullptr);
+  p1.aux = gu;  // nullable: g and u kept for the backward
+  p1.ld_aux = 2LL * Hp;
   int st = launch<EPI_SWIGLU, false, true, 256, 4, 1, 1>(mA, mG, mU, p1, mtiles * ((Hp + 127) / 128), s);
   if (st != MOE_OK) return st;
   Params p2 = params(cu, E, rows, H, Hp, h, H, nullptr);
   return launch<EPI_BF16, false, false, 256, 4, 1, 1>(mA2, mD, mD, p2, mtiles * ((H + 255) / 256), s);
+}
+
+// Backward of the grouped SwiGLU FFN (bf16, tcgen05), given dh [rows, H]:
+//   dgu = [dg | du] from da = dh Wd[e] and the saved [g | u]      (per row group)
+//   dxs = dg Wg[e]^T + du Wu[e]^T                                  (K = 2 H', B switches at H')
+//   dWd[e] = dh_e^T act_e,  dWg[e] = xs_e^T dg_e,  dWu[e] = xs_e^T du_e   (grouped K, fp32)
+int launch_expert_ffn_bwd_tc(const void* xs, const int32_t* cu, int rows, const void* wg, const void* wu,
+                             const void* wd, int E, int H, int Hp, const void* gu, const void* act, const void* dh,
+                             void* dgu, void* dxs, float* dwg, float* dwu, float* dwd, cudaStream_t s) {
+  using namespace tc;
+  if (E > 1024) return MOE_ERR_UNSUPPORTED;
+  const long long mtiles = (rows + BM - 1) / BM + E;
+  int st;
+  {  // dgu: A = dh (K-major, K = H), B = Wd[e] read as [K = H, N = H'] (MN-major)
+    CUtensorMap mA, mB;
+    if (!map_2d_as_3d(&mA, dh, H, rows, BK, BM)) return MOE_ERR_CUDA;
+    if (!map_3d(&mB, wd, Hp, H, E, 64, BK)) return MOE_ERR_CUDA;
+    Params p = params(cu, E, rows, Hp, H, dgu, 2LL * Hp, nullptr);
+    p.aux = const_cast<void*>(gu);
+    p.ld_aux = 2LL * Hp;
+    st = launch<EPI_SWIGLU_BWD, false, true, 256, 4, 1, 1>(mA, mB, mB, p, mtiles * ((Hp + 255) / 256), s);
+    if (st != MOE_OK) return st;
+  }
+  if (dxs) {  // A = dgu (K-major, K = 2H'), B = Wg[e] then Wu[e], each [N = H rows, K = H'] (K-major)
+    CUtensorMap mA, mG, mU;
+    if (!map_2d_as_3d(&mA, dgu, 2LL * Hp, rows, BK, BM)) return MOE_ERR_CUDA;
+    if (!map_3d(&mG, wg, Hp, H, E, BK, 256)) return MOE_ERR_CUDA;
+    if (!map_3d(&mU, wu, Hp, H, E, BK, 256)) return MOE_ERR_CUDA;
+    Params p = params(cu, E, rows, H, 2 * Hp, dxs, H, nullptr);
+    p.kcat = Hp;
+    st = launch<EPI_BF16, false, false, 256, 4, 1, 1>(mA, mG, mU, p, mtiles * ((H + 255) / 256), s);
+    if (st != MOE_OK) return st;
+  }
+  // weight gradients: M = H (A = an [rows, H] matrix read transposed, MN-major),
+  // N = H' (B = an [rows, .] matrix, MN-major), K = the rows of each expert
+  const long long gk_tiles = (long long)E * ((H + BM - 1) / BM) * ((Hp + 255) / 256);
+  auto wgrad = [&](const void* a_rows, const void* b_rows, long long b_ld, int b_off, float* out) {
+    CUtensorMap mA, mB;
+    if (!map_2d_as_3d(&mA, a_rows, H, rows, 64, BK)) return (int)MOE_ERR_CUDA;
+    if (!map_2d_as_3d(&mB, b_rows, b_ld, rows, 64, BK)) return (int)MOE_ERR_CUDA;
+    Params p = params(cu, E, H, Hp, rows, out, Hp, nullptr);
+    p.gk = 1;
+    p.b_col_off = b_off;
+    p.part_stride = (long long)H * Hp;
+    return launch<EPI_F32_GK, true, true, 256, 4, 1, 1>(mA, mB, mB, p, gk_tiles, s);
+  };
+  if (dwd && (st = wgrad(dh, act, Hp, 0, dwd)) != MOE_OK) return st;
+  if (dwg && (st = wgrad(xs, dgu, 2LL * Hp, 0, dwg)) != MOE_OK) return st;
+  if (dwu && (st = wgrad(xs, dgu, 2LL * Hp, Hp, dwu)) != MOE_OK) return st;
+  return MOE_OK;
 }
 
 static int router_bn(int E) { return E <= 64 ? 64 : E <= 128 ? 128 : 256; }

@@ -66,12 +66,12 @@ int moe_version(void) { return 100; }
 unsigned long long moe_kernel_launches(void) { return __atomic_load_n(&g_kernel_launches, __ATOMIC_RELAXED); }
 
 size_t moe_workspace_bytes(int op, int T, int H, int E, int K, int Hp) {
-  (void)Hp;
   if (T < 0 || H < 0 || E < 0 || K < 0) return 0;
   switch (op) {
     case MOE_OP_ROUTE: return (E > 0 && H > 0) ? route_ws_bytes(T, H, E) : 0;
     case MOE_OP_DISPATCH: return E > 0 ? dispatch_ws_bytes(T, E, K) : 0;
     case MOE_OP_ROUTE_BWD: return (E > 0 && H > 0) ? route_bwd_ws_bytes(T, H, E) : 0;
+    case MOE_OP_EXPERT_FFN_BWD: return Hp > 0 ? expert_ffn_bwd_ws_bytes((int)((long long)T * K), Hp) : 0;
     default: return 0;
   }
 }
@@ -143,18 +143,48 @@ int moe_dispatch_noalloc(const void* x, const int32_t* topk_idx, int T, int H, i
                                 as_stream(stream));
 }
 
+static int check_expert_ffn(const void* xs, const int32_t* cu_seqlens, int rows, const void* w_gate,
+                            const void* w_up, const void* w_down, int E, int H, int Hp, int dtype) {
+  if (!valid_dtype(dtype) || rows < 0 || E < 1 || H < 1 || Hp < 1) return MOE_ERR_INVALID_ARG;
+  if (!cu_seqlens || !w_gate || !w_up || !w_down || (rows > 0 && !xs)) return MOE_ERR_INVALID_ARG;
+  if (!all_aligned({xs, cu_seqlens, w_gate, w_up, w_down})) return MOE_ERR_MISALIGNED;
+  if (H % vec_elems(dtype) != 0 || Hp % vec_elems(dtype) != 0) return MOE_ERR_UNSUPPORTED;
+  if (dtype == MOE_BF16 && (H % 64 != 0 || Hp % 64 != 0 || E > 1024)) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int moe_expert_ffn_ex(const void* xs, const int32_t* cu_seqlens, int rows, const void* w_gate, const void* w_up,
+                      const void* w_down, int E, int H, int Hp, int dtype, void* act, void* gu, void* h, void* ws,
+                      size_t ws_bytes, void* stream) {
+  (void)ws; (void)ws_bytes;
+  int st = check_expert_ffn(xs, cu_seqlens, rows, w_gate, w_up, w_down, E, H, Hp, dtype);
+  if (st != MOE_OK) return st;
+  if (rows > 0 && (!act || !h)) return MOE_ERR_INVALID_ARG;
+  if (!all_aligned({act, gu, h})) return MOE_ERR_MISALIGNED;
+  if (gu && dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  return launch_expert_ffn(xs, cu_seqlens, rows, w_gate, w_up, w_down, E, H, Hp, dtype, act, gu, h,
+                           as_stream(stream));
+}
+
 int moe_expert_ffn(const void* xs, const int32_t* cu_seqlens, int rows, const void* w_gate,
                    const void* w_up, const void* w_down, int E, int H, int Hp, int dtype, void* act,
                    void* h, void* ws, size_t ws_bytes, void* stream) {
-  (void)ws; (void)ws_bytes;
-  if (!valid_dtype(dtype) || rows < 0 || E < 1 || H < 1 || Hp < 1) return MOE_ERR_INVALID_ARG;
-  if (!cu_seqlens || !w_gate || !w_up || !w_down || (rows > 0 && (!xs || !act || !h)))
-    return MOE_ERR_INVALID_ARG;
-  if (!all_aligned({xs, cu_seqlens, w_gate, w_up, w_down, act, h})) return MOE_ERR_MISALIGNED;
-  if (H % vec_elems(dtype) != 0 || Hp % vec_elems(dtype) != 0) return MOE_ERR_UNSUPPORTED;
-  if (dtype == MOE_BF16 && (H % 64 != 0 || Hp % 64 != 0 || E > 1024)) return MOE_ERR_UNSUPPORTED;
-  return launch_expert_ffn(xs, cu_seqlens, rows, w_gate, w_up, w_down, E, H, Hp, dtype, act, h,
-                           as_stream(stream));
+  return moe_expert_ffn_ex(xs, cu_seqlens, rows, w_gate, w_up, w_down, E, H, Hp, dtype, act, nullptr, h, ws,
+                           ws_bytes, stream);
+}
+
+int moe_expert_ffn_bwd(const void* xs, const int32_t* cu_seqlens, int rows, const void* w_gate, const void* w_up,
+                       const void* w_down, int E, int H, int Hp, int dtype, const void* gu, const void* act,
+                       const void* dh, void* dxs, float* dw_gate, float* dw_up, float* dw_down, void* ws,
+                       size_t ws_bytes, void* stream) {
+  int st = check_expert_ffn(xs, cu_seqlens, rows, w_gate, w_up, w_down, E, H, Hp, dtype);
+  if (st != MOE_OK) return st;
+  if (dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (rows > 0 && (!gu || !act || !dh)) return MOE_ERR_INVALID_ARG;
+  if (!all_aligned({gu, act, dh, dxs, dw_gate, dw_up, dw_down, ws})) return MOE_ERR_MISALIGNED;
+  if (rows > 0 && (!ws || ws_bytes < expert_ffn_bwd_ws_bytes(rows, Hp))) return MOE_ERR_WORKSPACE;
+  return launch_expert_ffn_bwd(xs, cu_seqlens, rows, w_gate, w_up, w_down, E, H, Hp, gu, act, dh, dxs, dw_gate,
+                               dw_up, dw_down, ws, as_stream(stream));
 }
 
 int moe_combine(const void* h, const float* gate, const int32_t* dst_row, const float* row_scale,

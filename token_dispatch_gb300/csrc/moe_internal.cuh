@@ -137,8 +137,12 @@ int launch_permute_bwd(const void* dy, const void* h, const float* gate, const i
 
 // expert FFN
 int launch_expert_ffn(const void* xs, const int32_t* cu, int rows, const void* wg, const void* wu,
-                      const void* wd, int E, int H, int Hp, int dtype, void* act, void* h,
+                      const void* wd, int E, int H, int Hp, int dtype, void* act, void* gu, void* h,
                       cudaStream_t s);
+int launch_expert_ffn_bwd(const void* xs, const int32_t* cu, int rows, const void* wg, const void* wu,
+                          const void* wd, int E, int H, int Hp, const void* gu, const void* act, const void* dh,
+                          void* dxs, float* dwg, float* dwu, float* dwd, void* ws, cudaStream_t s);
+size_t expert_ffn_bwd_ws_bytes(int rows, int Hp);
 
 // MoD
 int launch_mod_select(const void* x, const void* w, int B, int L, int H, int C, int dtype,
