@@ -92,3 +92,99 @@ def test_expert_ffn_backward_without_rows_zeroes_weight_gradients():
     torch.cuda.synchronize()
     for d in dws:
         assert (d == 0).all()
+
+
+FULL = [synth.MIXTRAL_BF16, synth.FINEGRAINED_BF16]
+
+
+@pytest.mark.parametrize("shape", FULL, ids=[s.name for s in FULL])
+def test_full_workload_training_backward_sampled(shape):
+    """The whole training backward of a full-size layer in the benchmark's launch
+    configuration (layer.moe_forward with g/u kept, layer.moe_train_backward), on
+    the oracle's routing; the oracle recomputes sampled rows of dxs and sampled
+    elements of the three weight gradients one by one."""
+    from token_dispatch_gb300 import layer
+    T, H, E, K, Hp = shape.T, shape.H, shape.E, shape.K, shape.Hp
+    R = T * K
+    rng = np.random.default_rng(3)
+    x, wr = synth.router_inputs(shape)
+    wg, wu, wd = synth.expert_weights_device(shape, DEV)
+    r_idx = O.topk_experts(O.router_logits(x.ref, wr.ref), K)
+    cu, dst, src = O.permutation(r_idx, E)
+    b = layer.MoEBuffers(T, H, E, K, Hp, "bf16", DEV, backward=True, train=True)
+    xd = x.host.to(DEV)
+    # forward on the oracle's choice of experts (gates: the GPU's own)
+    layer.moe_forward(b, xd, wr.host.to(DEV), None, wg, wu, wd)
+    L.moe_dispatch(xd, torch.from_numpy(r_idx).to(DEV), T, H, E, K, L.MOE_BF16, b.cu, b.dst_row, b.src_tok, b.xs,
+                   b.ws_dispatch, b.ws_dispatch_bytes)
+    L.moe_expert_ffn_ex(b.xs, b.cu, R, wg, wu, wd, E, H, Hp, L.MOE_BF16, b.act, b.gu, b.h)
+    dh = synth.upstream_grad(shape, R, H, seed=4)
+    b.dh.copy_(dh.host.to(DEV))
+    L.moe_expert_ffn_bwd(b.xs, b.cu, R, wg, wu, wd, E, H, Hp, L.MOE_BF16, b.gu, b.act, b.dh, b.dxs, b.dw_gate,
+                         b.dw_up, b.dw_down, b.ws_ffn_bwd, b.ws_ffn_bwd_bytes)
+    assert L.moe_last_device_error() == L.MOE_OK
+    assert np.array_equal(b.cu.cpu().numpy(), cu)
+    assert np.array_equal(b.dst_row.cpu().numpy(), dst)
+
+    xs_rows = x.ref[src]  # the oracle's dispatched rows
+    dxs_g = to64(b.dxs)
+    got = {"dg": [], "du": [], "dd": []}
+    ref = {"dg": [], "du": [], "dd": []}
+    dxs_got, dxs_ref = [], []
+    for e in sorted({0, E // 2, E - 1}):
+        lo, hi = int(cu[e]), int(cu[e + 1])
+        if hi == lo:
+            continue
+        wg_e, wu_e, wd_e = (synth.weights_to_host(w, [e])[0] for w in (wg, wu, wd))
+        X, D = xs_rows[lo:hi], dh.ref[lo:hi]
+        # dxs on sampled rows of e
+        rows = np.unique(np.r_[lo, hi - 1, rng.integers(lo, hi, size=6)]) - lo
+        dx_r = O.expert_swiglu_bwd(X[rows], wg_e, wu_e, wd_e, D[rows])[0]
+        dxs_got.append(dxs_g[lo + rows])
+        dxs_ref.append(dx_r)
+        # weight gradients on sampled (h, j): the column j of g, u, da over all rows of e
+        hs, js = rng.integers(0, H, size=12), rng.integers(0, Hp, size=12)
+        for h_, j_ in zip(hs, js):
+            g = X @ wg_e[:, j_]
+            u = X @ wu_e[:, j_]
+            s = 1.0 / (1.0 + np.exp(-g))
+            da = D @ wd_e[:, j_]
+            dg = da * u * s * (1.0 + g * (1.0 - s))
+            du = da * g * s
+            ref["dg"].append(X[:, h_] @ dg)
+            ref["du"].append(X[:, h_] @ du)
+            ref["dd"].append(D[:, h_] @ (g * s * u))
+            got["dg"].append(float(b.dw_gate[e, h_, j_]))
+            got["du"].append(float(b.dw_up[e, h_, j_]))
+            got["dd"].append(float(b.dw_down[e, h_, j_]))
+    assert_close(np.concatenate(dxs_got), np.concatenate(dxs_ref), TOL, "dxs (sampled rows)")
+    for k, name in [("dg", "dw_gate"), ("du", "dw_up"), ("dd", "dw_down")]:
+        assert_close(np.array(got[k]), np.array(ref[k]), TOL, name + " (sampled)")
+
+
+def test_layer_training_step_end_to_end():
+    """layer.moe_forward + layer.moe_train_backward on a small bf16 layer against
+    the oracle chain: forward, permute_bwd (dh, d_gate), expert_ffn_bwd (dxs and
+    the weight gradients), then the dispatch adjoint and the router backward."""
+    from tests.gpu_util import host_layer_inputs
+    from token_dispatch_gb300 import layer
+    shape = synth.MoEShape("bf16_T1000_H384_E16_K4_Hp320", 1000, 384, 16, 4, 320, "bf16")
+    T, H, E, K, Hp = shape.T, shape.H, shape.E, shape.K, shape.Hp
+    x, wr, wg, wu, wd = host_layer_inputs(shape)
+    dy = synth.upstream_grad(shape, T, H)
+    b = layer.MoEBuffers(T, H, E, K, Hp, "bf16", DEV, backward=True, train=True)
+    xd, wrd = dev(x), dev(wr)
+    wgd, wud, wdd = dev(wg), dev(wu), dev(wd)
+    layer.moe_forward(b, xd, wrd, None, wgd, wud, wdd)
+    layer.moe_train_backward(b, xd, wrd, wgd, wud, wdd, dev(dy))
+    assert L.moe_last_device_error() == L.MOE_OK
+    f = O.moe_forward(x.ref, wr.ref, wg.ref, wu.ref, wd.ref, K)
+    assert np.array_equal(b.idx.cpu().numpy(), f["idx"])
+    dh_r, d_gate_r, _, _ = O.permute_bwd(dy.ref, f["h"], f["gate"], f["dst_row"])
+    dxs_r, dwg_r, dwu_r, dwd_r = O.expert_ffn_bwd(f["xs"], f["cu"], wg.ref, wu.ref, wd.ref, dh_r)
+    g = O.moe_backward(f, dy.ref, dxs_r, x.ref, wr.ref)
+    for name, gpu, ref, tol in [("dh", b.dh, dh_r, TOL), ("d_gate", b.d_gate, d_gate_r, TOL),
+                                ("dxs", b.dxs, dxs_r, TOL), ("dw_gate", b.dw_gate, dwg_r, TOL),
+                                ("dw_up", b.dw_up, dwu_r, TOL), ("dw_down", b.dw_down, dwd_r, TOL),
+                                ("dx", b.dx, g["dx"], TOL), ("dw_router", b.dw_router, g["dw_router"], TOL)]:
+        assert_close(to64(gpu), ref, tol, name)

@@ -152,7 +152,7 @@ permute_bwd_kernel(const uint4* __restrict__ dy, const uint4* __restrict__ h, co
 #pragma unroll
         for (int u = 0; u < U; ++u) {
           const int i = i0 + 32 * u;
-          gr[u] = (i < nvec) ? __ldg(dy + o * nvec + i) : zero16();
+          gr[u] = (i < nvec && (dh || want_dot)) ? __ldg(dy + o * nvec + i) : zero16();
           pr[u] = (dx && grp > 0 && i < nvec) ? dx[t * nvec + i] : zero16();
 #pragma unroll
           for (int k = 0; k < KT; ++k) {

@@ -28,7 +28,7 @@ def _ws(nbytes: int, device):
 class MoEBuffers:
     """Device buffers of one MoE layer call (T tokens, H, E, K, Hp)."""
 
-    def __init__(self, T, H, E, K, Hp, dtype: str, device, backward: bool = True):
+    def __init__(self, T, H, E, K, Hp, dtype: str, device, backward: bool = True, train: bool = False):
         self.T, self.H, self.E, self.K, self.Hp, self.dtype = T, H, E, K, Hp, dtype
         self.cdt = _CDT[dtype]
         tdt = _TDT[dtype]
@@ -57,6 +57,15 @@ class MoEBuffers:
             self.dx = torch.empty((T, H), dtype=tdt, device=dev)
             self.ws_bwd_bytes = L.moe_workspace_bytes(L.MOE_OP_ROUTE_BWD, T, H, E, K, Hp)
             self.ws_bwd = _ws(self.ws_bwd_bytes, dev)
+        self.gu = None
+        if train:  # the expert backward: saved [g | u], dxs, fp32 weight gradients
+            self.gu = torch.empty((R, 2 * Hp), dtype=tdt, device=dev)
+            self.dxs = torch.empty((R, H), dtype=tdt, device=dev)
+            self.dw_gate = torch.empty((E, H, Hp), dtype=f32, device=dev)
+            self.dw_up = torch.empty((E, H, Hp), dtype=f32, device=dev)
+            self.dw_down = torch.empty((E, H, Hp), dtype=f32, device=dev)
+            self.ws_ffn_bwd_bytes = L.moe_workspace_bytes(L.MOE_OP_EXPERT_FFN_BWD, T, H, E, K, Hp)
+            self.ws_ffn_bwd = _ws(self.ws_ffn_bwd_bytes, dev)
 
 
 def moe_forward(b: MoEBuffers, x, w_router, logit_bias, w_gate, w_up, w_down, stream=None,
@@ -68,7 +77,7 @@ def moe_forward(b: MoEBuffers, x, w_router, logit_bias, w_gate, w_up, w_down, st
                    b.ws_route_bytes, stream=stream)
     L.moe_dispatch(x, b.idx, T, H, E, K, dt, b.cu, b.dst_row, b.src_tok, b.xs, b.ws_dispatch,
                    b.ws_dispatch_bytes, stream=stream)
-    L.moe_expert_ffn(b.xs, b.cu, T * K, w_gate, w_up, w_down, E, H, Hp, dt, b.act, b.h, stream=stream)
+    L.moe_expert_ffn_ex(b.xs, b.cu, T * K, w_gate, w_up, w_down, E, H, Hp, dt, b.act, b.gu, b.h, stream=stream)
     L.moe_combine(b.h, b.gate, b.dst_row, row_scale, residual, out_row, T, H, K, dt,
                   b.y if y is None else y, stream=stream)
 
@@ -80,6 +89,22 @@ def moe_backward(b: MoEBuffers, x, w_router, dy, dxs, stream=None, row_scale=Non
     T, H, E, K, dt = b.T, b.H, b.E, b.K, b.cdt
     L.moe_permute_bwd(dy, b.h, b.gate, b.dst_row, row_scale, out_row, dxs, T, H, K, dt, b.dh,
                       b.d_gate, d_scale, b.dx, stream=stream)
+    renorm = L.MOE_ROUTE_GATE_RENORM if route_flags & L.MOE_ROUTE_RENORM else 0
+    L.moe_route_bwd(L.MOE_ROUTE_SOFTMAX_TOPK | renorm, b.d_gate, b.logits, b.idx, x, w_router, T, H, E, K, dt,
+                    b.d_logits, b.dw_router, b.dx, b.ws_bwd, b.ws_bwd_bytes, stream=stream)
+
+
+def moe_train_backward(b: MoEBuffers, x, w_router, w_gate, w_up, w_down, dy, stream=None, route_flags=0):
+    """Full backward of the layer (buffers made with train=True, forward run
+    with them): dh and d_gate, the expert backward (dxs and the three weight
+    gradients), dx = sum_k dxs[row(t,k)] plus the router's share, dw_router."""
+    T, H, E, K, Hp, dt = b.T, b.H, b.E, b.K, b.Hp, b.cdt
+    L.moe_permute_bwd(dy, b.h, b.gate, b.dst_row, None, None, None, T, H, K, dt, b.dh, b.d_gate, None, None,
+                      stream=stream)
+    L.moe_expert_ffn_bwd(b.xs, b.cu, T * K, w_gate, w_up, w_down, E, H, Hp, dt, b.gu, b.act, b.dh, b.dxs,
+                         b.dw_gate, b.dw_up, b.dw_down, b.ws_ffn_bwd, b.ws_ffn_bwd_bytes, stream=stream)
+    L.moe_permute_bwd(None, None, b.gate, b.dst_row, None, None, b.dxs, T, H, K, dt, None, None, None, b.dx,
+                      stream=stream)
     renorm = L.MOE_ROUTE_GATE_RENORM if route_flags & L.MOE_ROUTE_RENORM else 0
     L.moe_route_bwd(L.MOE_ROUTE_SOFTMAX_TOPK | renorm, b.d_gate, b.logits, b.idx, x, w_router, T, H, E, K, dt,
                     b.d_logits, b.dw_router, b.dx, b.ws_bwd, b.ws_bwd_bytes, stream=stream)
