@@ -59,6 +59,8 @@ def parse():
                    help="router skew (maxvio) from tests/golden/skew_bias.json; 'none' for the natural "
                         "router; 'auto' = 0.2 where the table has it")
     p.add_argument("--cpu-sample-tokens", type=int, default=None)
+    p.add_argument("--train", action="store_true",
+                   help="time the full training step (expert backward and weight gradients included; bf16)")
     p.add_argument("--route-flags", type=int, default=0,
                    help="moe_route_ex gate options: 1 renormalise the top-k gates, 2 bias for selection only")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -80,6 +82,7 @@ def mode_of(shape):
 
 
 METRICS = {"fwd_bwd": "MoE layer tokens/s (fwd + gate/dispatch bwd)",
+           "train": "MoE layer tokens/s (fwd + full bwd incl. expert weight gradients)",
            "fwd": "MoE layer tokens/s (fwd)",
            "mod": "MoD+MoE layer tokens/s (fwd + route bwd)"}
 
@@ -154,7 +157,7 @@ class Clocks:
                 "samples": len(sm)}
 
 
-def algorithmic_bytes(shape):
+def algorithmic_bytes(shape, mode=None):
     """Minimum HBM bytes each HBM-bound call must move (read + write), from its
     definition: b = storage bytes, R = T*K rows; indices, gates and scores are 4
     bytes.  For the MoD workload T is the selected tokens (B*C)."""
@@ -174,6 +177,10 @@ def algorithmic_bytes(shape):
         "route_bwd": T * K * 4 + T * E * 4 + T * K * 4 + T * H * b + H * E * b + T * E * 4 + H * E * 4
                      + 2 * T * H * b,
     }
+    if mode == "train":
+        # dh, d_gate only (dy, h, gate, dst_row in); then dx = sum_k dxs[row]
+        out["permute_bwd"] = T * H * b + R * H * b + R * H * b + T * K * 4 + R * 4 + T * K * 4
+        out["dispatch_bwd"] = R * H * b + T * H * b + T * K * 4 + R * 4
     if shape.mod_B:
         n = shape.mod_B * shape.mod_L
         # x read once, w_mod; score, mask, sel, sel_score out; x_sel and the skip rows written
@@ -230,8 +237,8 @@ def make_step(shape, inp, dev, stream, route_flags=0):
     bias_d = None if inp["bias"] is None else torch.from_numpy(inp["bias"]).to(dev)
     wg, wu, wd = inp["wg"], inp["wu"], inp["wd"]
 
-    if mode in ("fwd_bwd", "fwd"):
-        b = layer.MoEBuffers(T, H, E, K, Hp, shape.dtype, dev, backward=(mode == "fwd_bwd"))
+    if mode in ("fwd_bwd", "fwd", "train"):
+        b = layer.MoEBuffers(T, H, E, K, Hp, shape.dtype, dev, backward=(mode != "fwd"), train=(mode == "train"))
         calls = [
             ("route", lambda xi, dyi, dxsi: L.moe_route_ex(xi, wr_d, bias_d, T, H, E, K, b.cdt, route_flags, b.logits,
                                                           b.idx, b.gate, b.ws_route, b.ws_route_bytes,
@@ -245,6 +252,26 @@ def make_step(shape, inp, dev, stream, route_flags=0):
                                                            b.y, stream=stream)),
         ]
         outs = [b.y]
+        if mode == "train":
+            calls[2] = ("expert_ffn", lambda xi, dyi, dxsi: L.moe_expert_ffn_ex(b.xs, b.cu, R, wg, wu, wd, E, H, Hp,
+                                                                              b.cdt, b.act, b.gu, b.h,
+                                                                              stream=stream))
+            calls += [
+                ("permute_bwd", lambda xi, dyi, dxsi: L.moe_permute_bwd(dyi, b.h, b.gate, b.dst_row, None, None,
+                                                                       None, T, H, K, b.cdt, b.dh, b.d_gate, None,
+                                                                       None, stream=stream)),
+                ("expert_ffn_bwd", lambda xi, dyi, dxsi: L.moe_expert_ffn_bwd(
+                    b.xs, b.cu, R, wg, wu, wd, E, H, Hp, b.cdt, b.gu, b.act, b.dh, b.dxs, b.dw_gate, b.dw_up,
+                    b.dw_down, b.ws_ffn_bwd, b.ws_ffn_bwd_bytes, stream=stream)),
+                ("dispatch_bwd", lambda xi, dyi, dxsi: L.moe_permute_bwd(None, None, b.gate, b.dst_row, None, None,
+                                                                        b.dxs, T, H, K, b.cdt, None, None, None,
+                                                                        b.dx, stream=stream)),
+                ("route_bwd", lambda xi, dyi, dxsi: L.moe_route_bwd(L.MOE_ROUTE_SOFTMAX_TOPK | bwd_renorm, b.d_gate,
+                                                                   b.logits, b.idx, xi, wr_d, T, H, E, K, b.cdt,
+                                                                   b.d_logits, b.dw_router, b.dx, b.ws_bwd,
+                                                                   b.ws_bwd_bytes, stream=stream)),
+            ]
+            outs = [b.y, b.dx, b.dw_router]
         if mode == "fwd_bwd":
             calls += [
                 ("permute_bwd", lambda xi, dyi, dxsi: L.moe_permute_bwd(dyi, b.h, b.gate, b.dst_row, None, None,
@@ -304,6 +331,11 @@ def run_ours(args, shape, rank, world, local):
     R = T * K
     bias_np, bias_entry, target = skew_bias(shape, args.bias_target)
     inp = build_inputs(shape, dev, rank, bias_np)
+    if args.train:
+        if inp["mode"] not in ("fwd_bwd", "fwd") or shape.dtype != "bf16":
+            raise SystemExit("--train needs a bf16 MoE workload")
+        inp["mode"] = "train"
+        inp.pop("dxs", None)  # the expert backward produces dxs
     mode = inp["mode"]
     n_tok = inp["n_tok"]
     x_h = inp["x"].host.pin_memory()
@@ -422,6 +454,14 @@ def run_ours(args, shape, rank, world, local):
     # the pair's minimum DRAM bytes: every expert's three projections once, xs
     # read, the SwiGLU output written and read back, h written
     ffn_bytes = 3 * E * H * Hp * b_el + R * H * b_el + 2 * R * Hp * b_el + R * H * b_el
+    if mode == "train":
+        # forward also writes [g | u]; backward: 12 R H H' FLOP; reads dh, the
+        # three projections, [g | u], act, xs; writes and reads back [dg | du];
+        # writes dxs and the three fp32 weight gradients
+        ffn_flops += 12.0 * R * H * Hp
+        ffn_s += call_ms["expert_ffn_bwd"] * 1e-3
+        ffn_bytes += 2 * R * Hp * b_el + (R * H * b_el + 3 * E * H * Hp * b_el + 2 * R * Hp * b_el + R * Hp * b_el
+                                          + R * H * b_el + 2 * 2 * R * Hp * b_el + R * H * b_el + 3 * E * H * Hp * 4)
     # the timed region is well under a second: the burst peak applies
     peak_tf = peaks.get("bf16_tflops", 1900.0) if shape.dtype == "bf16" else None
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
@@ -437,10 +477,10 @@ def run_ours(args, shape, rank, world, local):
         roof = {"bound": "hbm", "achieved": ffn_bytes / ffn_s / 1e9, "peak": hbm_peak, "unit": "GB/s",
                 "peak_source": f"{peak_src} hbm_gbs"}
     roof["frac"] = roof["achieved"] / roof["peak"] if roof["peak"] else None
-    roof["traffic"] = FFN_DRAM_BYTES.get(shape.name)
+    roof["traffic"] = None if mode == "train" else FFN_DRAM_BYTES.get(shape.name)
     roof["algorithmic"] = {"flops": ffn_flops, "bytes": ffn_bytes}
     hbm = {}
-    for name, nbytes in algorithmic_bytes(shape).items():
+    for name, nbytes in algorithmic_bytes(shape, mode).items():
         if name in call_ms:
             gbs = nbytes / (call_ms[name] * 1e-3) / 1e9
             hbm[name] = {"bytes": nbytes, "GB/s": round(gbs, 1), "frac": round(gbs / hbm_peak, 4)}
@@ -461,9 +501,11 @@ def run_ours(args, shape, rank, world, local):
                    "Hp": Hp, "maxvio": round(maxvio, 4), "maxvio_target": target,
                    "expert0_logit_bias": None if bias_entry is None else bias_entry["beta"],
                    "l2": "flushed between timed steps (512 MB write, then 512 MB read)", "parallelism": f"replicas{world}",
-                   "route_flags": args.route_flags},
+                   "route_flags": args.route_flags, "train": bool(args.train)},
         "calls_ms": {k: round(v, 4) for k, v in call_ms.items()},
-        "roofline": {"kernel": "moe_expert_ffn (grouped gate/up+SwiGLU GEMM + down GEMM, tcgen05)", **roof},
+        "roofline": {"kernel": ("moe_expert_ffn + moe_expert_ffn_bwd (grouped tcgen05 GEMMs, forward and backward)"
+                                if mode == "train" else
+                                "moe_expert_ffn (grouped gate/up+SwiGLU GEMM + down GEMM, tcgen05)"), **roof},
         "hbm_roofline": {"peak_GB/s": hbm_peak, "peak_source": f"{peak_src} hbm_gbs", "calls": hbm},
         "e2e": {"value": world * n_tok / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
@@ -522,6 +564,14 @@ def oracle_sample(shape, inp, n_tok, reps=1, route_flags=0):
                               bias_select_only=bool(route_flags & 2))
             if mode == "fwd_bwd":
                 O.moe_backward(f, dy, dxs, x64, wr64, renorm=bool(route_flags & 1))
+            elif mode == "train":
+                dh = O.permute_bwd(dy, f["h"], f["gate"], f["dst_row"])[0]
+                dxs_t = np.zeros_like(f["xs"])
+                for e in experts:
+                    lo, hi = int(f["cu"][e]), int(f["cu"][e + 1])
+                    if hi > lo:  # dxs rows and the expert's three weight gradients
+                        dxs_t[lo:hi] = O.expert_swiglu_bwd(f["xs"][lo:hi], wg[e], wu[e], wd[e], dh[lo:hi])[0]
+                O.moe_backward(f, dy, dxs_t, x64, wr64, renorm=bool(route_flags & 1))
         times.append(time.perf_counter() - t0)
     return times, n_tok
 
@@ -534,7 +584,7 @@ def cores():
 
 
 def default_sample(mode):
-    return {"fwd_bwd": 4096, "fwd": 512, "mod": None}[mode]
+    return {"fwd_bwd": 4096, "train": 2048, "fwd": 512, "mod": None}[mode]
 
 
 def main():
@@ -543,6 +593,10 @@ def main():
     from token_dispatch_gb300 import synth
     shape = synth.WORKLOADS[args.workload]
     mode = mode_of(shape)
+    if args.train:
+        if mode not in ("fwd_bwd", "fwd") or shape.dtype != "bf16":
+            raise SystemExit("--train needs a bf16 MoE workload")
+        mode = "train"
 
     if args.impl == "reference":
         if rank != 0:
@@ -551,7 +605,10 @@ def main():
         dev = torch.device("cuda", local) if torch.cuda.is_available() else torch.device("cpu")
         bias_np, _, target = skew_bias(shape, args.bias_target)
         inp = build_inputs(shape, dev, 0, bias_np)  # drawn exactly as the GPU arm draws them
-        n_tok = args.cpu_sample_tokens or {"fwd_bwd": 32, "fwd": 8, "mod": None}[mode]
+        if mode == "train":
+            inp["mode"] = "train"
+            inp.pop("dxs", None)
+        n_tok = args.cpu_sample_tokens or {"fwd_bwd": 32, "train": 32, "fwd": 8, "mod": None}[mode]
         oracle_sample(shape, inp, n_tok, reps=1, route_flags=args.route_flags)
         times, n_tok = oracle_sample(shape, inp, n_tok, reps=args.steps, route_flags=args.route_flags)
         ms = 1e3 * statistics.mean(times)
@@ -561,7 +618,8 @@ def main():
         out = {"metric": METRICS[mode], "value": val, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
                "warmup": 1, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
                "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-               "config": {"workload": shape.name, "maxvio_target": target},
+               "config": {"workload": shape.name, "maxvio_target": target, "route_flags": args.route_flags,
+                          "train": bool(args.train)},
                "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": cores(), "kind": "oracle",
                                 "sample": sample},
                "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -573,7 +631,8 @@ def main():
         n_tok = args.cpu_sample_tokens or default_sample(mode)
         times, n_tok = oracle_sample(shape, inp, n_tok, reps=1, route_flags=args.route_flags)
         what = "the first sequence (MoD select + MoE on 1024 tokens + route bwd)" if mode == "mod" else \
-            f"first {n_tok} tokens of the batch ({'fwd + gate/dispatch bwd' if mode == 'fwd_bwd' else 'fwd'})"
+            f"first {n_tok} tokens of the batch " \
+            f"({ {'fwd_bwd': 'fwd + gate/dispatch bwd', 'train': 'fwd + full bwd', 'fwd': 'fwd'}[mode] })"
         result["cpu_baseline"] = {"value": n_tok / times[0], "unit": "tokens/s", "cores": cores(),
                                   "kind": "oracle",
                                   "sample": f"{what}, float64 numpy ({times[0]:.1f} s)"}
