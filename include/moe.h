@@ -95,6 +95,15 @@ MOE_API size_t moe_workspace_bytes(int op, int T, int H, int E, int K, int Hp);
  * synchronisation itself failed). */
 MOE_API int moe_last_device_error(void* stream);
 
+/* Diagnostic of the device-side failure detection.  Launches one kernel whose
+ * single thread waits, with the same bounded wait every pipelined kernel of this
+ * library uses, on a barrier that nothing ever arrives at.  After `wait_cycles` SM
+ * clock cycles (1 .. 2^31) it gives up and records MOE_ERR_TIMEOUT in the device
+ * error word, as a stalled copy or MMA pipeline would; nothing traps and the
+ * context stays usable.  Returns the launch status (MOE_ERR_INVALID_ARG for
+ * wait_cycles out of range); read the outcome with moe_last_device_error. */
+MOE_API int moe_check_wait_timeout(unsigned long long wait_cycles, void* stream);
+
 /*
  * Router: GEMM, softmax over experts and top-K gate       [FW "What's in the box"]
  *

@@ -77,6 +77,9 @@ def test_argument_errors_are_reported_before_launch(libmoe):
     assert raw.moe_route_ex(A, A, None, 4, 64, 8, 2, L.MOE_F32, 4, A, A, A, None, 0, None) == L.MOE_ERR_INVALID_ARG
     assert raw.moe_route_bwd(L.MOE_ROUTE_MOD_LINEAR | L.MOE_ROUTE_GATE_RENORM, A, None, None, A, A, 4, 64, 1, 1,
                              L.MOE_F32, None, A, None, A, 1 << 30, None) == L.MOE_ERR_INVALID_ARG
+    # failure-detection probe: wait limit out of range
+    assert raw.moe_check_wait_timeout(0, None) == L.MOE_ERR_INVALID_ARG
+    assert raw.moe_check_wait_timeout((1 << 31) + 1, None) == L.MOE_ERR_INVALID_ARG
     # workspace too small
     need = L.moe_workspace_bytes(L.MOE_OP_DISPATCH, 1000, 64, 8, 2, 0)
     assert raw.moe_dispatch(A, A, 1000, 64, 8, 2, L.MOE_F32, A, A, A, A, A, need - 256, None) == L.MOE_ERR_WORKSPACE

@@ -519,3 +519,19 @@ def test_zero_tokens_is_a_no_op():
     L.moe_combine(None, None, None, None, None, None, 0, H, K, L.MOE_F32, None)
     L.moe_expert_ffn(None, cu, 0, w, w, w, E, H, 64, L.MOE_F32, None, None)
     assert L.moe_last_device_error() == L.MOE_OK
+
+
+def test_bounded_wait_times_out_and_the_context_survives():
+    """Failure detection without a fault: a kernel waits on a barrier nothing
+    arrives at; its bounded wait gives up after ~1 ms, the device error word
+    reports MOE_ERR_TIMEOUT, reading it clears it, and the next calls run."""
+    assert L.moe_last_device_error() == L.MOE_OK
+    L.moe_check_wait_timeout(2_000_000)
+    assert L.moe_last_device_error() == L.MOE_ERR_TIMEOUT
+    assert L.moe_last_device_error() == L.MOE_OK
+    shape = SHAPES[1]
+    x, wr = synth.router_inputs(shape)
+    logits, idx, gate = route_gpu(shape, x, wr)
+    r_logits = O.router_logits(x.ref, wr.ref)
+    assert_close(logits, r_logits, 1e-5, "logits after the timeout")
+    assert L.moe_last_device_error() == L.MOE_OK

@@ -41,6 +41,7 @@ MOE_ROUTE_RENORM = 0x1
 MOE_ROUTE_BIAS_SELECT = 0x2
 
 EXPORTS = ("moe_status_str", "moe_version", "moe_kernel_launches", "moe_workspace_bytes", "moe_last_device_error",
+           "moe_check_wait_timeout",
            "moe_route", "moe_route_ex", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn",
            "moe_expert_ffn_ex", "moe_expert_ffn_bwd", "moe_combine", "moe_route_bwd",
            "moe_permute_bwd", "mod_select")
@@ -64,6 +65,7 @@ _SIGS = {
     "moe_kernel_launches": (ctypes.c_ulonglong, []),
     "moe_workspace_bytes": (_Z, [_I, _I, _I, _I, _I, _I]),
     "moe_last_device_error": (_I, [_P]),
+    "moe_check_wait_timeout": (_I, [ctypes.c_ulonglong, _P]),
     "moe_route": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
     "moe_route_ex": (_I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
     "moe_dispatch": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _Z, _P]),
@@ -135,6 +137,10 @@ def moe_workspace_bytes(op: int, T: int, H: int, E: int, K: int, Hp: int) -> int
 
 def moe_last_device_error(stream=None) -> int:
     return lib().moe_last_device_error(_stream(stream))
+
+
+def moe_check_wait_timeout(wait_cycles, stream=None):
+    _check("moe_check_wait_timeout", lib().moe_check_wait_timeout(wait_cycles, _stream(stream)))
 
 
 def moe_route(x, w_router, logit_bias, T, H, E, K, dtype, logits, topk_idx, topk_gate,

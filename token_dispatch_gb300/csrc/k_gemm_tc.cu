@@ -771,6 +771,19 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
 }
 
+// Failure-detection probe: one thread waits on an mbarrier that nothing ever
+// arrives at, with the bounded wait of the pipelined kernels above; it gives up
+// after p.wait_limit cycles and records DEV_TIMEOUT, as a stalled pipeline would.
+__global__ void wait_probe_kernel(const Params p) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  mbar_init(smem_u32(&bar), 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  (void)wait_bounded(smem_u32(&bar), 0, &abort_flag, p);
+}
+
 // ------------------------------------------------------------------ host ----
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -910,6 +923,13 @@ int launch_expert_ffn_bwd_tc(const void* xs, const int32_t* cu, int rows, const 
   if (dwg && (st = wgrad(xs, dgu, 2LL * Hp, 0, dwg)) != MOE_OK) return st;
   if (dwu && (st = wgrad(xs, dgu, 2LL * Hp, Hp, dwu)) != MOE_OK) return st;
   return MOE_OK;
+}
+
+int launch_wait_probe(unsigned long long wait_cycles, cudaStream_t s) {
+  tc::Params p = tc::params(nullptr, 1, 0, 0, 0, nullptr, 0, nullptr);
+  p.wait_limit = wait_cycles;
+  tc::wait_probe_kernel<<<1, 32, 0, s>>>(p);
+  return launch_status();
 }
 
 static int router_bn(int E) { return E <= 64 ? 64 : E <= 128 ? 128 : 256; }

@@ -76,6 +76,11 @@ size_t moe_workspace_bytes(int op, int T, int H, int E, int K, int Hp) {
   }
 }
 
+int moe_check_wait_timeout(unsigned long long wait_cycles, void* stream) {
+  if (wait_cycles == 0 || wait_cycles > (1ull << 31)) return MOE_ERR_INVALID_ARG;
+  return launch_wait_probe(wait_cycles, as_stream(stream));
+}
+
 int moe_last_device_error(void* stream) {
   if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return MOE_ERR_CUDA;
   unsigned* p = device_error_word();

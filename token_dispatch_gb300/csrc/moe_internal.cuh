@@ -144,6 +144,9 @@ int launch_expert_ffn_bwd(const void* xs, const int32_t* cu, int rows, const voi
                           void* dxs, float* dwg, float* dwu, float* dwd, void* ws, cudaStream_t s);
 size_t expert_ffn_bwd_ws_bytes(int rows, int Hp);
 
+// failure-detection probe (a bounded wait that times out)
+int launch_wait_probe(unsigned long long wait_cycles, cudaStream_t s);
+
 // MoD
 int launch_mod_select(const void* x, const void* w, int B, int L, int H, int C, int dtype,
                       float* score, int32_t* sel, float* sel_score, uint8_t* mask, void* x_sel,
