@@ -398,16 +398,23 @@ def run_ours(args, shape, rank, world, local):
 
     # End to end through the public API: every step copies its inputs from pinned
     # host memory and its results back.  Inputs are double-buffered: the next
-    # step's host-to-device copies run on a copy stream while this step computes;
-    # results are copied back on the compute stream right after the step.
+    # step's host-to-device copies run on a copy stream while this step computes.
+    # Results are first copied on the device into a double-buffered staging area
+    # (so the next step may overwrite them), then read back to pinned host memory
+    # on a third stream while the next step computes; the timed region ends when
+    # the last step's results are on the host.
     srcs = [x_h] + ([dy_d.cpu().pin_memory()] if dy_d is not None else []) + \
         ([dxs_d.cpu().pin_memory()] if dxs_d is not None else [])
     bufs_in = [[torch.empty_like(h, device=dev) for h in srcs] for _ in range(2)]
-    host_out = [(o, torch.empty(o.shape, dtype=o.dtype).pin_memory()) for o in outs]
+    stage_out = [[torch.empty_like(o) for o in outs] for _ in range(2)]
+    host_out = [[torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs] for _ in range(2)]
     copy_stream = torch.cuda.Stream(device=dev)
+    d2h_stream = torch.cuda.Stream(device=dev)
     e2e_steps = max(3, min(args.steps, 20))
     loaded = [torch.cuda.Event() for _ in range(2)]
     consumed = [torch.cuda.Event() for _ in range(2)]
+    staged = [torch.cuda.Event() for _ in range(2)]
+    read_back = [torch.cuda.Event() for _ in range(2)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
     def load(i):
@@ -422,6 +429,7 @@ def run_ours(args, shape, rank, world, local):
     torch.cuda.synchronize(dev)
     e0.record(stream)
     copy_stream.wait_event(e0)
+    d2h_stream.wait_event(e0)
     load(0)
     for i in range(e2e_steps):
         if i + 1 < e2e_steps:
@@ -432,14 +440,23 @@ def run_ours(args, shape, rank, world, local):
             ins = bufs_in[slot] + [None, None]
             step(ins[0], ins[1], ins[2])
             consumed[slot].record(stream)
-            for d, h in host_out:
-                h.copy_(d, non_blocking=True)
+            if i >= 2:
+                stream.wait_event(read_back[slot])  # step i-2's results are on the host
+            for d, st in zip(outs, stage_out[slot]):
+                st.copy_(d, non_blocking=True)
+            staged[slot].record(stream)
+        with torch.cuda.stream(d2h_stream):
+            d2h_stream.wait_event(staged[slot])
+            for st, h in zip(stage_out[slot], host_out[slot]):
+                h.copy_(st, non_blocking=True)
+            read_back[slot].record(d2h_stream)
+    stream.wait_event(read_back[(e2e_steps - 1) % 2])
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     clk = clocks.stop()
     h2d = sum(h.numel() * h.element_size() for h in srcs)
-    d2h = sum(h.numel() * h.element_size() for _, h in host_out)
+    d2h = sum(h.numel() * h.element_size() for h in host_out[0])
 
     if world > 1:
         import torch.distributed as dist
