@@ -544,6 +544,7 @@ def oracle_sample(shape, inp, n_tok, reps=1, route_flags=0):
     wr64 = inp["wr"].ref
     if mode == "mod":
         n_tok = shape.mod_L
+    n_tok = min(n_tok, inp["x"].ref.shape[0])  # never more tokens than the batch has
     x64 = inp["x"].ref[:n_tok]
 
     # the experts this sample visits, copied to the host in float64
