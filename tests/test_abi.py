@@ -95,6 +95,14 @@ def test_argument_errors_are_reported_before_launch(libmoe):
     # capacity above the sequence length
     assert raw.mod_select(A, A, 2, 16, 64, 17, L.MOE_F32, A, A, None, A, None, None, None, 0,
                           None) == L.MOE_ERR_INVALID_ARG
+    # expert backward: bf16 only; needs its [dg | du] workspace; g/u output needs bf16
+    assert raw.moe_expert_ffn_bwd(A, A, 8, A, A, A, 2, 64, 64, L.MOE_F32, A, A, A, A, A, A, A, A, 1 << 20,
+                                  None) == L.MOE_ERR_UNSUPPORTED
+    assert raw.moe_expert_ffn_bwd(A, A, 8, A, A, A, 2, 64, 64, L.MOE_BF16, A, A, A, A, A, A, A, None, 0,
+                                  None) == L.MOE_ERR_WORKSPACE
+    assert raw.moe_expert_ffn_ex(A, A, 8, A, A, A, 2, 64, 64, L.MOE_F32, A, A, A, None, 0,
+                                 None) == L.MOE_ERR_UNSUPPORTED
+    assert L.moe_workspace_bytes(L.MOE_OP_EXPERT_FFN_BWD, 8192, 4096, 8, 2, 14336) >= 16384 * 2 * 14336 * 2
     # H not a multiple of the 16-byte vector
     assert raw.moe_expert_ffn(A, A, 8, A, A, A, 2, 60, 64, L.MOE_BF16, A, A, None, 0, None) == L.MOE_ERR_UNSUPPORTED
 
