@@ -118,9 +118,12 @@ MOE_API int moe_check_wait_timeout(unsigned long long wait_cycles, void* stream)
  *   logits     [T,E]   float out (kept for moe_route_bwd)
  *   topk_idx   [T,K]   int32 out;  topk_gate [T,K] float out
  *   1 <= K <= E <= 1024, K <= 16.  bf16 needs E % 8 == 0.
- *   Workspace: moe_workspace_bytes(MOE_OP_ROUTE, T, H, E, K, 0) bytes (bf16; 0 when
- *   the token tiles fill the GPU, then ws may be NULL): partial sums of the router
- *   GEMM over slices of H, added in a fixed order.
+ *   Workspace: moe_workspace_bytes(MOE_OP_ROUTE, T, H, E, K, 0) bytes (bf16 only):
+ *   partial sums of the router GEMM over slices of H, added in a fixed order, for
+ *   shapes whose token tiles alone would leave SMs idle; 0 (ws may be NULL) when the
+ *   token tiles fill the GPU and for E = 8 or 16 with H a multiple of 512 up to 4096
+ *   (those stream x through registers in one launch).  Results are the same bits on
+ *   every run for the same inputs.
  */
 MOE_API int moe_route(const void* x, const void* w_router, const float* logit_bias,
               int T, int H, int E, int K, int dtype,
