@@ -162,9 +162,13 @@ softmax_topk_bwd_kernel(const float* __restrict__ logits, const int32_t* __restr
     }
     float inner = 0.f, csum = 0.f;
     unsigned chosen = 0;
+    // the K (expert, d_gate) pairs of the row: lane k loads pair k (K <= 32), all
+    // loads in flight at once, then each is broadcast
+    const int my_e = lane < K ? __ldg(idx + t * K + lane) : 0;
+    const float my_dg = lane < K ? __ldg(d_gate + t * K + lane) : 0.f;
     for (int k = 0; k < K; ++k) {
-      int e = __ldg(idx + t * K + k);
-      float dg = __ldg(d_gate + t * K + k);
+      const int e = __shfl_sync(0xffffffffu, my_e, k);
+      const float dg = __shfl_sync(0xffffffffu, my_dg, k);
       if (((e >> 2) & 31) == lane) {
         int slot = (e >> 7) * 4 + (e & 3);
 #pragma unroll
