@@ -72,6 +72,22 @@ def dist_env():
         int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def max_over_ranks(times_ms, device):
+    """The slowest rank's times (each rank timed the same number of steps of its
+    own batch): one all-reduce(max) over the process group."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(times_ms, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
+def whole_job_tokens_per_s(tokens_per_rank, world, ms_per_step):
+    """Replicas: every rank processes its own tokens_per_rank tokens per step, so
+    the job's rate is all ranks' tokens over the slowest rank's step time."""
+    return world * tokens_per_rank / (ms_per_step * 1e-3)
+
+
 def mode_of(shape):
     from token_dispatch_gb300 import synth
     if shape.mod_B:
@@ -459,10 +475,7 @@ def run_ours(args, shape, rank, world, local):
     d2h = sum(h.numel() * h.element_size() for h in host_out[0])
 
     if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms, e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e_ms = float(t[0]), float(t[1])
+        ms, e2e_ms = max_over_ranks([ms, e2e_ms], dev)
 
     peaks, peak_src = measured_peaks()
     ffn_flops = 6.0 * R * H * Hp
@@ -503,7 +516,7 @@ def run_ours(args, shape, rank, world, local):
             hbm[name] = {"bytes": nbytes, "GB/s": round(gbs, 1), "frac": round(gbs / hbm_peak, 4)}
     result = {
         "metric": METRICS[mode],
-        "value": world * n_tok / (ms * 1e-3),
+        "value": whole_job_tokens_per_s(n_tok, world, ms),
         "unit": "tokens/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -524,7 +537,7 @@ def run_ours(args, shape, rank, world, local):
                                 if mode == "train" else
                                 "moe_expert_ffn (grouped gate/up+SwiGLU GEMM + down GEMM, tcgen05)"), **roof},
         "hbm_roofline": {"peak_GB/s": hbm_peak, "peak_source": f"{peak_src} hbm_gbs", "calls": hbm},
-        "e2e": {"value": world * n_tok / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+        "e2e": {"value": whole_job_tokens_per_s(n_tok, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches,
         "clocks": clk,
