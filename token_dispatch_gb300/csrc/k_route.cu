@@ -742,7 +742,9 @@ int launch_route_bwd(int mode, const float* d_gate, const float* logits, const i
   const BwdWs lay = bwd_ws(T, H, E);
   char* wsb = static_cast<char*>(ws);
   float* part = reinterpret_cast<float*>(wsb);
-  float* dl = d_logits ? d_logits : reinterpret_cast<float*>(wsb + lay.part);
+  // linear score (E = K = 1): the score gradient is the logit gradient, used as is
+  float* dl = mode == MOE_ROUTE_MOD_LINEAR ? const_cast<float*>(d_gate)
+              : d_logits ? d_logits : reinterpret_cast<float*>(wsb + lay.part);
   const bool tc = route_bwd_on_tensor_cores(mode, dtype, H, E);
   bf16* dl3 = tc ? reinterpret_cast<bf16*>(wsb + lay.part + lay.dl) : nullptr;
 
@@ -758,11 +760,11 @@ int launch_route_bwd(int mode, const float* d_gate, const float* logits, const i
       softmax_topk_bwd_kernel<16><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, idx, d_gate, rn, T, E, K, dl, dl3);
     else
       softmax_topk_bwd_kernel<32><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, idx, d_gate, rn, T, E, K, dl, dl3);
-  } else {
-    // linear score: the score gradient is the logit gradient (E = K = 1)
-    copy_f32_kernel<<<rows_grid(T), 256, 0, s>>>(d_gate, dl, (long long)T);
+  } else if (d_logits) {
+    // the logit gradient output of the linear score is d_score itself
+    copy_f32_kernel<<<rows_grid(T), 256, 0, s>>>(d_gate, d_logits, (long long)T);
   }
-  int st = launch_status();
+  int st = (mode == MOE_ROUTE_SOFTMAX_TOPK || d_logits) ? launch_status() : MOE_OK;
   if (st != MOE_OK) return st;
 
   if (dw) {
