@@ -494,8 +494,14 @@ def run_ours(args, shape, rank, world, local):
         ffn_s += call_ms["expert_ffn_bwd"] * 1e-3
         ffn_bytes += 2 * R * Hp * b_el + (R * H * b_el + 3 * E * H * Hp * b_el + 2 * R * Hp * b_el + R * Hp * b_el
                                           + R * H * b_el + 2 * 2 * R * Hp * b_el + R * H * b_el + 3 * E * H * Hp * 4)
-    # the timed region is well under a second: the burst peak applies
-    peak_tf = peaks.get("bf16_tflops", 1900.0) if shape.dtype == "bf16" else None
+    # The burst bf16 peak applies to a kernel timed alone; when the power cap
+    # engaged during the timed steps the kernel ran inside a long step, and the
+    # sustained peak (measured under the same cap) is the ceiling.  Both
+    # fractions are reported.
+    capped = bool(clk) and "sw_power_cap" in clk.get("reasons", [])
+    peak_burst = peaks.get("bf16_tflops", 1900.0)
+    peak_tf = (peaks.get("bf16_tflops_sustained", 1700.0) if capped else peak_burst) \
+        if shape.dtype == "bf16" else None
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
     if shape.dtype != "bf16":
         # fp32 layers run on FFMA: the peak is 152 SMs x 128 FP32 lanes x 2 FLOP
@@ -504,7 +510,9 @@ def run_ours(args, shape, rank, world, local):
                 "unit": "TFLOP/s", "peak_source": "derived: FP32 FMA lanes x clock"}
     elif ffn_flops / (peak_tf * 1e12) >= ffn_bytes / (hbm_peak * 1e9):
         roof = {"bound": "tensor", "achieved": ffn_flops / ffn_s / 1e12, "peak": peak_tf, "unit": "TFLOP/s",
-                "peak_source": f"{peak_src} bf16_tflops (burst)"}
+                "peak_source": f"{peak_src} bf16_tflops" + ("_sustained (sw_power_cap seen)" if capped else
+                                                            " (burst)"),
+                "frac_of_burst": ffn_flops / ffn_s / 1e12 / peak_burst}
     else:  # weight streaming bounds the pair (few rows per expert)
         roof = {"bound": "hbm", "achieved": ffn_bytes / ffn_s / 1e9, "peak": hbm_peak, "unit": "GB/s",
                 "peak_source": f"{peak_src} hbm_gbs"}
