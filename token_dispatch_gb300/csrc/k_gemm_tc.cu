@@ -222,8 +222,8 @@ struct TileInfo {
 };
 
 // Tile t -> (group, rows, first output column).  mt_pre[g] = m-tiles before g.
-__device__ __forceinline__ TileInfo decode(int t, const int* mt_pre, int G, int n_tiles, const Params& p,
-                                           int out_bn) {
+__device__ __forceinline__ TileInfo decode(int t, const int* mt_pre, const int* cu, int G, int n_tiles,
+                                           const Params& p, int out_bn) {
   // largest g with mt_pre[g] * n_tiles <= t
   int lo = 0, hi = G - 1;
   while (lo < hi) {
@@ -235,8 +235,8 @@ __device__ __forceinline__ TileInfo decode(int t, const int* mt_pre, int G, int 
   const int mt_g = mt_pre[g + 1] - mt_pre[g];
   const int local = t - mt_pre[g] * n_tiles;
   const int m = local % mt_g, n = local / mt_g;
-  const int beg = p.cu ? p.cu[g] : 0;
-  const int end = p.cu ? p.cu[g + 1] : p.M;
+  const int beg = cu ? cu[g] : 0;
+  const int end = cu ? cu[g + 1] : p.M;
   TileInfo ti;
   ti.g = g;
   ti.row0 = beg + m * BM;
@@ -264,6 +264,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   __shared__ uint32_t tmem_base_slot;
   __shared__ int abort_flag;
   __shared__ int mt_pre[1025];
+  __shared__ int cu_s[1025];  // the group boundaries, read once from global memory
   __shared__ int total_tiles_s;
 
   const int warp = threadIdx.x >> 5;
@@ -298,18 +299,36 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                  "r"((uint32_t)C::TMEM_COLS));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
+  if (warp == 2 && p.cu) {
+    // eight loads per lane in flight at a time
+    for (int base = 0; base <= G; base += 32 * 8) {
+      int v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = base + u * 32 + lane;
+        v[u] = i <= G ? p.cu[i] : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = base + u * 32 + lane;
+        if (i <= G) cu_s[i] = v[u];
+      }
+    }
+    __syncwarp();
+  }
+  const int* cu = p.cu ? cu_s : nullptr;
   if (warp == 2 && p.gk) {
     // grouped K: G x (M tiles) x (N tiles), all groups alike
     if (lane == 0) {
       total_tiles_s = G * ((p.M + BM - 1) / BM) * n_tiles;
-      if (p.cu[0] != 0 || p.cu[G] != p.K) set_error(p.err, DEV_BOUNDS);
+      if (cu_s[0] != 0 || cu_s[G] != p.K) set_error(p.err, DEV_BOUNDS);
     }
   } else if (warp == 2) {
     // m-tile prefix over groups: each lane owns a contiguous run of groups
     const int per = (G + 31) / 32;
     int sum = 0;
     for (int g = lane * per; g < min(G, lane * per + per); ++g) {
-      int rows = p.cu ? max(0, p.cu[g + 1] - p.cu[g]) : p.M;
+      int rows = cu ? max(0, cu[g + 1] - cu[g]) : p.M;
       sum += (rows + BM - 1) / BM;
     }
     int incl = sum;
@@ -321,10 +340,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     int run = incl - sum;
     for (int g = lane * per; g < min(G, lane * per + per); ++g) {
       mt_pre[g] = run;
-      int rows = p.cu ? max(0, p.cu[g + 1] - p.cu[g]) : p.M;
+      int rows = cu ? max(0, cu[g + 1] - cu[g]) : p.M;
       run += (rows + BM - 1) / BM;
     }
-    if (lane == 0 && p.cu && (p.cu[0] != 0 || p.cu[G] != p.M)) set_error(p.err, DEV_BOUNDS);
+    if (lane == 0 && cu && (cu[0] != 0 || cu[G] != p.M)) set_error(p.err, DEV_BOUNDS);
     if (lane == 31) {
       mt_pre[G] = incl;
       total_tiles_s = incl * n_tiles * p.ksplit;
@@ -356,7 +375,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       w.ti.row0 = m * BM;
       w.ti.rows = min(BM, p.M - w.ti.row0);
       w.ti.n0 = n * C::OUT_BN;
-      const int beg = p.cu[g], rows = max(0, p.cu[g + 1] - beg);
+      const int beg = cu[g], rows = max(0, cu[g + 1] - beg);
       w.kb_begin = 0;
       w.kb_end = (rows + BK - 1) / BK;
       w.k_base = beg;
@@ -364,7 +383,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       w.last_valid = rows - (w.kb_end - 1) * BK;
     } else {
       const int split = t / base_tiles;
-      w.ti = decode(t - split * base_tiles, mt_pre, G, n_tiles, p, C::OUT_BN);
+      w.ti = decode(t - split * base_tiles, mt_pre, cu, G, n_tiles, p, C::OUT_BN);
       w.kb_begin = kb_lo(split);
       w.kb_end = kb_lo(split + 1);
       w.k_base = 0;
@@ -819,7 +838,7 @@ int launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, co
            long long tiles_upper, cudaStream_t s) {
   using C = Cfg<BN, EPI, NA, NB>;
   const size_t smem = (size_t)STAGES * C::STAGE_BYTES + C::EPI_BYTES + (2 * STAGES + 5) * 8 + 1024;
-  static_assert((size_t)STAGES * C::STAGE_BYTES + C::EPI_BYTES + (2 * STAGES + 5) * 8 + 1024 + 4300 <= 227 * 1024,
+  static_assert((size_t)STAGES * C::STAGE_BYTES + C::EPI_BYTES + (2 * STAGES + 5) * 8 + 1024 + 8500 <= 227 * 1024,
                 "smem (dynamic + static)");
   auto k = tc_gemm_kernel<EPI, A_MN, B_MN, BN, STAGES, NA, NB, KSUB>;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
