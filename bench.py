@@ -1,7 +1,8 @@
 """Benchmark of the MoE / MoD layer hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload NAME] [--bias-target MAXVIO|none]
+                    [--workload NAME] [--bias-target MAXVIO|none] [--train]
+                    [--graph] [--e2e-eager]
 
 A step is one pass of the layer over one batch of synthetic input:
   * Mixtral-shaped and fine-grained layers: router GEMM + softmax/top-K,
@@ -14,6 +15,12 @@ A step is one pass of the layer over one batch of synthetic input:
 The default workload is the Mixtral-shaped bf16 layer (4 x 2048 tokens, H=4096,
 E=8, K=2, H'=14336) with the router skewed to maxvio 0.2 by an expert-0 logit
 bias from tests/golden/skew_bias.json.
+
+`value` and the per-call split come from the calls launched one by one, each
+bracketed by CUDA events (`--graph` times replays of the step captured as one
+CUDA graph instead).  The end-to-end figure replays the step as a CUDA graph
+captured through the same entry points, between the per-step host copies
+(`--e2e-eager` launches it call by call instead).
 
 Multi-GPU runs (torchrun) are replicas: every rank processes its own batch with
 no data-path collective; `value` is all ranks' tokens over the slowest rank's
@@ -60,6 +67,10 @@ def parse():
                    help="router skew (maxvio) from tests/golden/skew_bias.json; 'none' for the natural "
                         "router; 'auto' = 0.2 where the table has it")
     p.add_argument("--cpu-sample-tokens", type=int, default=None)
+    p.add_argument("--graph", action="store_true",
+                   help="time CUDA-graph replays of the step (captured once; the per-call split still eager)")
+    p.add_argument("--e2e-eager", action="store_true",
+                   help="end-to-end loop launches every call from the host instead of replaying a captured graph")
     p.add_argument("--train", action="store_true",
                    help="time the full training step (expert backward and weight gradients included; bf16)")
     p.add_argument("--route-flags", type=int, default=0,
@@ -413,6 +424,34 @@ def run_ours(args, shape, rank, world, local):
     call_ms = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
                for j, n in enumerate(names)}
     ms = statistics.mean(step_ms)
+    eager_ms = ms
+
+    def capture(xi, dyi, dxsi):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+            step(xi, dyi, dxsi)
+        return g
+
+    if args.graph:
+        # the whole step as one CUDA graph: the library's launches are recorded
+        # once (counted here) and replayed with no host work per kernel
+        n0 = L.moe_kernel_launches()
+        graph_main = capture(x_d, dy_d, dxs_d)
+        per_step = L.moe_kernel_launches() - n0
+        gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        barrier()
+        torch.cuda.synchronize(dev)
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                gev[i][0].record(stream)
+                graph_main.replay()
+                gev[i][1].record(stream)
+                flush_l2()
+        torch.cuda.synchronize(dev)
+        barrier()
+        ms = statistics.mean(a.elapsed_time(b) for a, b in gev)
+        launches = per_step * args.steps
 
     # End to end through the public API: every step copies its inputs from pinned
     # host memory and its results back.  Inputs are double-buffered: the next
@@ -429,6 +468,9 @@ def run_ours(args, shape, rank, world, local):
     copy_stream = torch.cuda.Stream(device=dev)
     d2h_stream = torch.cuda.Stream(device=dev)
     e2e_steps = max(3, min(args.steps, 20))
+    # the step's calls are captured once per input slot as a CUDA graph (through
+    # the same public entry points) and replayed: no host launch work per kernel
+    graph_in = None if args.e2e_eager else [capture(*(b + [None, None])[:3]) for b in bufs_in]
     loaded = [torch.cuda.Event() for _ in range(2)]
     consumed = [torch.cuda.Event() for _ in range(2)]
     staged = [torch.cuda.Event() for _ in range(2)]
@@ -456,7 +498,10 @@ def run_ours(args, shape, rank, world, local):
         stream.wait_event(loaded[slot])
         with torch.cuda.stream(stream):
             ins = bufs_in[slot] + [None, None]
-            step(ins[0], ins[1], ins[2])
+            if graph_in:
+                graph_in[slot].replay()
+            else:
+                step(ins[0], ins[1], ins[2])
             consumed[slot].record(stream)
             if i >= 2:
                 stream.wait_event(read_back[slot])  # step i-2's results are on the host
@@ -532,6 +577,7 @@ def run_ours(args, shape, rank, world, local):
         "steps": args.steps,
         "warmup": max(3, args.warmup),
         "ms_per_step": ms,
+        "eager_ms_per_step": eager_ms,
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
@@ -541,14 +587,15 @@ def run_ours(args, shape, rank, world, local):
                    "Hp": Hp, "maxvio": round(maxvio, 4), "maxvio_target": target,
                    "expert0_logit_bias": None if bias_entry is None else bias_entry["beta"],
                    "l2": "flushed between timed steps (512 MB write, then 512 MB read)", "parallelism": f"replicas{world}",
-                   "route_flags": args.route_flags, "train": bool(args.train)},
+                   "route_flags": args.route_flags, "train": bool(args.train), "graph": bool(args.graph)},
         "calls_ms": {k: round(v, 4) for k, v in call_ms.items()},
         "roofline": {"kernel": ("moe_expert_ffn + moe_expert_ffn_bwd (grouped tcgen05 GEMMs, forward and backward)"
                                 if mode == "train" else
                                 "moe_expert_ffn (grouped gate/up+SwiGLU GEMM + down GEMM, tcgen05)"), **roof},
         "hbm_roofline": {"peak_GB/s": hbm_peak, "peak_source": f"{peak_src} hbm_gbs", "calls": hbm},
         "e2e": {"value": whole_job_tokens_per_s(n_tok, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "launch": "host, call by call" if graph_in is None else "CUDA graph of the step, one per input slot"},
         "gpu_launches": launches,
         "clocks": clk,
     }
