@@ -153,6 +153,28 @@ def test_route_ties_pick_lowest_expert():
     assert np.allclose(gate, p1, rtol=1e-6)
 
 
+@pytest.mark.parametrize("E,K", [(300, 7), (384, 8), (1000, 16)])
+def test_route_many_experts_ties_and_infinities(E, K):
+    """Warp top-K over many experts per lane: logits from the bias alone, with
+    runs of equal values, +-0 and -inf entries, so that whole rounds are
+    decided by the lowest expert index and the last picks fall on -inf."""
+    T = 40
+    shape = S(f"f32_T{T}_E{E}_K{K}_ties", T, 16, E, K, 16, "f32")
+    x = synth.store(np.zeros((T, 16)), "f32")
+    wr = synth.store(np.zeros((16, E)), "f32")
+    rng = np.random.default_rng(11)
+    bias = np.full(E, -np.inf, np.float32)
+    n_fin = {300: 4, 384: 12, 1000: 40}[E]  # fewer finite values than K for E=300
+    pos = rng.choice(E, n_fin, replace=False)
+    bias[pos] = rng.choice(np.array([-1.5, 0.0, -0.0, 2.25], np.float32), n_fin)
+    logits, idx, gate = route_gpu(shape, x, wr, bias)
+    ref = np.broadcast_to(bias.astype(np.float64), (T, E))
+    assert np.array_equal(idx, O.topk_experts(ref, K))
+    p = np.exp(ref - ref.max(axis=1, keepdims=True))
+    p /= p.sum(axis=1, keepdims=True)
+    assert np.allclose(gate, np.take_along_axis(p, idx, axis=1), rtol=1e-6, atol=0)
+
+
 def oracle_idx(shape, T=None):
     x, wr = synth.router_inputs(shape, tokens=T)
     return x, wr, O.topk_experts(O.router_logits(x.ref, wr.ref), shape.K)
@@ -385,6 +407,76 @@ def test_route_bwd_linear_matches_oracle(dtype):
     torch.cuda.synchronize()
     assert_close(dw.cpu().numpy(), dw_r, 1e-5, "dw_mod")
     assert_close(to64(dx), dx_r, TOL[dtype], "dx")
+
+
+# bf16 routers with 8 or 16 experts take the one-pass streaming backward:
+# slices of H with idle threads (H=1536), several slices (H=4096, 6144), fewer
+# tokens than CTAs (T=5), several 256-token chunks per CTA (T=40000), ragged
+# token ranges everywhere
+ROUTE_BWD_STREAM = [(2053, 1536, 8, 2), (1000, 512, 16, 4), (5, 4096, 8, 1), (3001, 4096, 16, 16),
+                    (40000, 1024, 8, 2), (777, 6144, 8, 3)]
+
+
+@pytest.mark.parametrize("T,H,E,K", ROUTE_BWD_STREAM, ids=[f"T{t}_H{h}_E{e}_K{k}" for t, h, e, k in ROUTE_BWD_STREAM])
+def test_route_bwd_stream_matches_oracle(T, H, E, K):
+    """All outputs together (dx accumulated), then dx alone (written), then dW
+    alone, with plain and renormalised gates."""
+    shape = S(f"bf16_T{T}_H{H}_E{E}_K{K}", T, H, E, K, 64, "bf16")
+    x, wr = synth.router_inputs(shape)
+    logits = (x.ref @ wr.ref).astype(np.float32)
+    idx = O.topk_experts(logits.astype(np.float64), K)
+    d_gate = np.random.default_rng(7).standard_normal((T, K)).astype(np.float32)
+    dx0 = synth.store(np.random.default_rng(8).standard_normal((T, H)), "bf16")
+    nbytes = L.moe_workspace_bytes(L.MOE_OP_ROUTE_BWD, T, H, E, K, 0)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    g_d, l_d, i_d = (torch.from_numpy(a).to(DEV) for a in (d_gate, logits, idx))
+    x_d, w_d = dev(x), dev(wr)
+    for renorm in (False, True):
+        dl_r, dw_r, dx_r = O.route_bwd_softmax_topk(d_gate.astype(np.float64), logits.astype(np.float64), idx,
+                                                    x.ref, wr.ref, renorm=renorm)
+        flags = L.MOE_ROUTE_SOFTMAX_TOPK | (L.MOE_ROUTE_GATE_RENORM if renorm else 0)
+        dl = torch.empty((T, E), dtype=torch.float32, device=DEV)
+        dw = torch.empty((H, E), dtype=torch.float32, device=DEV)
+        dx = dev(dx0).clone()
+        L.moe_route_bwd(flags, g_d, l_d, i_d, x_d, w_d, T, H, E, K, L.MOE_BF16, dl, dw, dx, ws, nbytes)
+        torch.cuda.synchronize()
+        assert_close(dl.cpu().numpy(), dl_r, 1e-5, "d_logits")
+        assert_close(dw.cpu().numpy(), dw_r, 1e-5, "dw_router")
+        assert_close(to64(dx), dx0.ref + dx_r, TOL["bf16"], "dx (accumulated)")
+        dx.fill_(7)
+        L.moe_route_bwd(flags | L.MOE_ROUTE_DX_WRITE, g_d, l_d, i_d, x_d, w_d, T, H, E, K, L.MOE_BF16, None, None,
+                        dx, ws, nbytes)
+        torch.cuda.synchronize()
+        assert_close(to64(dx), dx_r, TOL["bf16"], "dx (written)")
+        dw.fill_(7)
+        L.moe_route_bwd(flags, g_d, l_d, i_d, x_d, w_d, T, H, E, K, L.MOE_BF16, None, dw, None, ws, nbytes)
+        torch.cuda.synchronize()
+        assert_close(dw.cpu().numpy(), dw_r, 1e-5, "dw_router (alone)")
+    assert L.moe_last_device_error() == L.MOE_OK
+
+
+@pytest.mark.parametrize("T,H", [(20000, 2048), (3, 768), (1000, 4096), (513, 8192)])
+def test_route_bwd_linear_stream_matches_oracle(T, H):
+    """The MoD score backward (E = 1) on the streaming pass: several rows side by
+    side (H=2048), idle threads (H=768), one row per CTA (4096) and two slices
+    (8192)."""
+    rng = np.random.default_rng(9)
+    x = synth.store(rng.standard_normal((T, H)), "bf16")
+    w = synth.store(rng.standard_normal(H) / 16, "bf16")
+    ds = rng.standard_normal(T).astype(np.float32)
+    dx0 = synth.store(rng.standard_normal((T, H)), "bf16")
+    dw_r, dx_r = O.route_bwd_linear(ds.astype(np.float64), x.ref, w.ref)
+    nbytes = L.moe_workspace_bytes(L.MOE_OP_ROUTE_BWD, T, H, 1, 1, 0)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=DEV)
+    dw = torch.empty((H,), dtype=torch.float32, device=DEV)
+    dl = torch.empty((T,), dtype=torch.float32, device=DEV)
+    dx = dev(dx0).clone()
+    L.moe_route_bwd(L.MOE_ROUTE_MOD_LINEAR, torch.from_numpy(ds).to(DEV), None, None, dev(x), dev(w), T, H, 1, 1,
+                    L.MOE_BF16, dl, dw, dx, ws, nbytes)
+    torch.cuda.synchronize()
+    assert np.array_equal(dl.cpu().numpy(), ds)
+    assert_close(dw.cpu().numpy(), dw_r, 1e-5, "dw_mod")
+    assert_close(to64(dx), dx0.ref + dx_r.reshape(T, H), TOL["bf16"], "dx (accumulated)")
 
 
 @pytest.mark.parametrize("B,Lseq,C,H,dtype", [(4, 2048, 1024, 128, "bf16"), (3, 1000, 333, 64, "f32"),

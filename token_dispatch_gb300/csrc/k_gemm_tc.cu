@@ -427,7 +427,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const uint32_t dst = b_dst + ib * C::B_TILE_BYTES;
             const int z = (NB > 1 && KSUB == 1) ? ib : ti.g;
             const int kb0 = KSUB > 1 ? k0 + ib * BK : k0;
-            if (EPI == EPI_SWIGLU) {
+            if constexpr (EPI == EPI_SWIGLU) {
 #pragma unroll
               for (int c = 0; c < BN / 64; ++c) {
                 const CUtensorMap* m = (c < BN / 128) ? &tmB : &tmB2;
@@ -951,7 +951,10 @@ int launch_wait_probe(unsigned long long wait_cycles, cudaStream_t s) {
   return launch_status();
 }
 
-static int router_bn(int E) { return E <= 64 ? 64 : E <= 128 ? 128 : 256; }
+// N tile of the router GEMM: the whole expert row up to 128 experts; beyond,
+// 192-wide tiles when they cover E exactly (E = 384: two tiles, no padded
+// columns), else 256
+static int router_bn(int E) { return E <= 64 ? 64 : E <= 128 ? 128 : E % 192 == 0 ? 192 : 256; }
 
 // Splits of H for the router GEMM: a CTA streams x from DRAM at a limited rate,
 // so when the token tiles alone would occupy fewer than about 100 of the 152
@@ -994,6 +997,7 @@ int launch_router_tc(const void* x, const void* w, const float* bias, const floa
   // request 512 (256) contiguous bytes of every row at a time
   if (E <= 64) return launch<EPI_F32_BIAS, false, true, 64, 2, 4, 4, 4>(mA, mB, mB, p, tiles, s);
   if (E <= 128) return launch<EPI_F32_BIAS, false, true, 128, 3, 2, 2, 2>(mA, mB, mB, p, tiles, s);
+  if (E % 192 == 0) return launch<EPI_F32_BIAS, false, true, 192, 5, 1, 1>(mA, mB, mB, p, tiles * (E / 192), s);
   return launch<EPI_F32_BIAS, false, true, 256, 4, 1, 1>(mA, mB, mB, p, tiles * ((E + 255) / 256), s);
 }
 

@@ -6,6 +6,7 @@
 // loads, max / sum / arg-max are warp-shuffle reductions, and the K winners are
 // taken by K rounds of a (value desc, expert asc) arg-max, which gives the
 // lowest-index tie-break exactly.  Selection is on the fp32 logits themselves.
+#include <climits>
 #include <math.h>
 
 #include "moe_internal.cuh"
@@ -87,30 +88,59 @@ softmax_topk_kernel(float* __restrict__ logits, const float* __restrict__ part, 
 #pragma unroll
     for (int j = 0; j < VPL; ++j) s += (slot_expert(j, lane) < E) ? expf(v[j] - m) : 0.f;
     s = warp_sum(s);
-    unsigned taken = 0;
-    float chosen_sum = 0.f;
-    for (int k = 0; k < K; ++k) {
-      float bv = -INFINITY;
-      int be = 0x7fffffff;
+    // Top-K by selection value, descending, lowest expert first on ties.
+    // A lane's slots hold increasing experts, so scanning them in slot order
+    // with a strict comparison already breaks ties by expert.  Slots past E
+    // and taken slots hold NaN, which no comparison accepts.  Each lane caches
+    // its best two untaken slots (an empty cache still accepts -inf); a round
+    // takes the warp's best cached candidate with two warp reductions (the
+    // largest order-preserving integer key, then the smallest expert among
+    // the lanes holding it); the winning lane promotes its second and scans
+    // again only when its cache ran empty.
+#pragma unroll
+    for (int j = 0; j < VPL; ++j)
+      if (slot_expert(j, lane) >= E) sv[j] = __int_as_float(0x7fffffff);
+    float c1v, c2v, c1r, c2r;
+    int c1j, c2j;
+    auto rescan = [&]() {
+      c1v = c2v = -INFINITY;
+      c1j = c2j = -1;
+      c1r = c2r = 0.f;
 #pragma unroll
       for (int j = 0; j < VPL; ++j) {
-        int e = slot_expert(j, lane);
-        bool ok = e < E && !((taken >> j) & 1u);
-        if (ok && (sv[j] > bv || (sv[j] == bv && e < be))) { bv = sv[j]; be = e; }
+        const float x = sv[j];
+        if (x > c1v || (c1j < 0 && x == x)) {
+          c2v = c1v; c2j = c1j; c2r = c1r;
+          c1v = x; c1j = j; c1r = v[j];
+        } else if (x > c2v || (c2j < 0 && x == x)) {
+          c2v = x; c2j = j; c2r = v[j];
+        }
       }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        int oe = __shfl_xor_sync(0xffffffffu, be, o);
-        if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
-      }
+    };
+    rescan();
+    float chosen_sum = 0.f;
+    for (int k = 0; k < K; ++k) {
+      // order-preserving integer key of the cached value (finite or +-inf);
+      // a lane with nothing left offers the smallest key
+      int key = __float_as_int(c1v);
+      key = key >= 0 ? key : key ^ 0x7fffffff;
+      if (c1v == 0.f) key = 0;  // -0 and +0 are equal values
+      if (c1j < 0) key = INT_MIN;
+      const int kmax = __reduce_max_sync(0xffffffffu, key);
+      const int my_e = (c1j >= 0 && key == kmax) ? slot_expert(c1j, lane) : 0x7fffffff;
+      const int be = __reduce_min_sync(0xffffffffu, (unsigned)my_e);
+      const bool mine = my_e == be && c1j >= 0;
       // the winner's own logit (not its selection value) gives its probability
-      const int owner = (be >> 2) & 31, wslot = (be >> 7) * 4 + (be & 3);
-      float vw = 0.f;
+      const int owner = (be >> 2) & 31;
+      const float vw = __shfl_sync(0xffffffffu, mine ? c1r : 0.f, owner);
+      if (mine) {
 #pragma unroll
-      for (int j = 0; j < VPL; ++j) if (j == wslot) vw = v[j];
-      vw = __shfl_sync(0xffffffffu, vw, owner);
-      if (owner == lane) taken |= 1u << wslot;
+        for (int j = 0; j < VPL; ++j)
+          if (j == c1j) sv[j] = __int_as_float(0x7fffffff);
+        c1v = c2v; c1j = c2j; c1r = c2r;
+        c2v = -INFINITY; c2j = -1;
+        if (c1j < 0) rescan();
+      }
       const float pk = expf(vw - m) / s;
       chosen_sum += pk;
       if (lane == 0) {
@@ -216,45 +246,32 @@ __global__ void copy_f32_kernel(const float* __restrict__ a, float* __restrict__
     b[i] = a[i];
 }
 
-// dw[i] = sum_s part[s][i], splits added in order (the same result every run).
-// One thread per output, so a warp's loads of one split are 128 contiguous
-// bytes, and all S loads of a thread are requested before the first add.
+// dw[i] = sum_s part[s][i] in a fixed order (the same result every run).  A
+// block covers 32 consecutive outputs with 8 warps: warp q adds splits q, q+8,
+// q+16, ... in increasing order for output base + lane, so every load
+// instruction reads 128 contiguous bytes and a thread's loads are independent
+// of one another; the 8 warp sums then meet in shared memory, added in warp
+// order.
 __global__ void __launch_bounds__(256) reduce_splits_kernel(const float* __restrict__ part, int S, long long n,
                                                             float* __restrict__ out) {
-  constexpr int U = 8;
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += stride) {
-    float acc = 0.f;
-    for (int s0 = 0; s0 < S; s0 += U) {
-      float v[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) v[u] = s0 + u < S ? __ldg(part + (long long)(s0 + u) * n + i) : 0.f;
-#pragma unroll
-      for (int u = 0; u < U; ++u) acc += v[u];
-    }
-    out[i] = acc;
-  }
-}
-
-// The same sum for many splits: eight lanes per output, lane q adds splits
-// q, q+8, ... in order and a fixed shuffle tree adds the eight sums.
-__global__ void __launch_bounds__(256) reduce_splits_wide_kernel(const float* __restrict__ part, int S, long long n,
-                                                                 float* __restrict__ out) {
-  const int q = threadIdx.x & 7;
-  const int grp = (threadIdx.x & 31) >> 3;  // four outputs per warp
-  const long long warp = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 5;
-  const long long nwarps = ((long long)gridDim.x * blockDim.x) >> 5;
-  for (long long base = warp * 4; base < n; base += nwarps * 4) {  // warp-uniform loop
-    const long long i = base + grp;
+  __shared__ float red[8][33];
+  const int lane = threadIdx.x & 31, q = threadIdx.x >> 5;
+  for (long long base = blockIdx.x * 32LL; base < n; base += gridDim.x * 32LL) {
+    const long long i = base + lane;
     float acc = 0.f;
     if (i < n) {
-#pragma unroll 4
+#pragma unroll 8
       for (int s = q; s < S; s += 8) acc += __ldg(part + (long long)s * n + i);
     }
-    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-    if (q == 0 && i < n) out[i] = acc;
+    red[q][lane] = acc;
+    __syncthreads();
+    if (q == 0 && i < n) {
+      float t = red[0][lane];
+#pragma unroll
+      for (int j = 1; j < 8; ++j) t += red[j][lane];
+      out[i] = t;
+    }
+    __syncthreads();
   }
 }
 
@@ -663,6 +680,8 @@ int launch_route(const void* x, const void* w, const float* bias, int T, int H, 
     softmax_topk_kernel<4><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, part, S, pb, sel_bias, rn, T, E, K, idx, gate);
   else if (vpl <= 8)
     softmax_topk_kernel<8><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, part, S, pb, sel_bias, rn, T, E, K, idx, gate);
+  else if (vpl <= 12)
+    softmax_topk_kernel<12><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, part, S, pb, sel_bias, rn, T, E, K, idx, gate);
   else if (vpl <= 16)
     softmax_topk_kernel<16><<<grid, 32 * ROWS_PER_CTA, 0, s>>>(logits, part, S, pb, sel_bias, rn, T, E, K, idx, gate);
   else
@@ -689,6 +708,8 @@ static BwdWs bwd_ws(int T, int H, int E) {
   long long splits = pl.splits;
   const long long tcs = router_dw_tc_splits(T, H, E);
   if (tcs > splits) splits = tcs;
+  const long long sts = (E == 1 || E == 8 || E == 16) ? router_bwd_stream_splits(T, H, E) : 0;
+  if (sts > splits) splits = sts;
   return BwdWs{align256((size_t)splits * H * E * 4), align256((size_t)T * E * 4), align256((size_t)3 * T * E * 2)};
 }
 
@@ -714,14 +735,8 @@ int launch_dw(const T* x, const float* dl, int Tn, int H, int E, float* part, fl
 
 int launch_reduce(const float* part, int S, int H, int E, float* dw, cudaStream_t s) {
   const long long n = (long long)H * E;
-  if (S > 16) {  // long sums over few outputs: spread each over eight lanes
-    const long long thr = n * 8;
-    const int rgrid = (int)((thr + 255) / 256 < 16384 ? (thr + 255) / 256 : 16384);
-    reduce_splits_wide_kernel<<<rgrid, 256, 0, s>>>(part, S, n, dw);
-  } else {
-    const int rgrid = (int)((n + 255) / 256 < 16384 ? (n + 255) / 256 : 16384);
-    reduce_splits_kernel<<<rgrid, 256, 0, s>>>(part, S, n, dw);
-  }
+  const long long blocks = (n + 31) / 32;
+  reduce_splits_kernel<<<(int)(blocks < 16384 ? blocks : 16384), 256, 0, s>>>(part, S, n, dw);
   return launch_status();
 }
 
@@ -742,6 +757,12 @@ int launch_route_bwd(int mode, const float* d_gate, const float* logits, const i
   const BwdWs lay = bwd_ws(T, H, E);
   char* wsb = static_cast<char*>(ws);
   float* part = reinterpret_cast<float*>(wsb);
+  if (router_bwd_stream_applies(mode, dtype, H, E, K)) {  // one streaming pass, then the dW_r reduction
+    int st = launch_router_bwd_stream(mode, d_gate, logits, idx, x, w, T, H, E, K, renorm, d_logits,
+                                      dw ? part : nullptr, dx, dx_write, s);
+    if (st == MOE_OK && dw) st = launch_reduce(part, router_bwd_stream_splits(T, H, E), H, E, dw, s);
+    return st;
+  }
   // linear score (E = K = 1): the score gradient is the logit gradient, used as is
   float* dl = mode == MOE_ROUTE_MOD_LINEAR ? const_cast<float*>(d_gate)
               : d_logits ? d_logits : reinterpret_cast<float*>(wsb + lay.part);

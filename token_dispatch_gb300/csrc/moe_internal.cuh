@@ -22,6 +22,12 @@ __device__ __forceinline__ void set_error(unsigned* err, unsigned code) {
 // Address of the current device's error word (resolved once per device).
 unsigned* device_error_word();
 
+// clock64 cycles a bounded wait on a pipeline barrier may take before the
+// kernel records DEV_TIMEOUT and stops
+namespace tc {
+extern unsigned long long g_wait_limit;
+}
+
 // ------------------------------------------------------------ conversions ---
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(bf16 v) { return __bfloat162float(v); }
@@ -118,6 +124,12 @@ int launch_route_bwd(int mode, const float* d_gate, const float* logits, const i
                      const void* x, const void* w, int T, int H, int E, int K, int dtype,
                      float* d_logits, float* dw, void* dx, bool dx_write, bool renorm, void* ws, cudaStream_t s);
 size_t route_bwd_ws_bytes(int T, int H, int E);
+// streaming router backward (bf16; E = 8 or 16 softmax/top-K, E = 1 linear)
+bool router_bwd_stream_applies(int mode, int dtype, int H, int E, int K);
+int router_bwd_stream_splits(int T, int H, int E);
+int launch_router_bwd_stream(int mode, const float* d_gate, const float* logits, const int32_t* idx, const void* x,
+                             const void* w, int T, int H, int E, int K, bool renorm, float* d_logits, float* part,
+                             void* dx, bool dx_write, cudaStream_t s);
 
 // dispatch / combine / permute backward
 size_t dispatch_ws_bytes(int T, int E, int K);
