@@ -22,12 +22,6 @@ __device__ __forceinline__ void set_error(unsigned* err, unsigned code) {
 // Address of the current device's error word (resolved once per device).
 unsigned* device_error_word();
 
-// clock64 cycles a bounded wait on a pipeline barrier may take before the
-// kernel records DEV_TIMEOUT and stops
-namespace tc {
-extern unsigned long long g_wait_limit;
-}
-
 // ------------------------------------------------------------ conversions ---
 __device__ __forceinline__ float to_f32(float v) { return v; }
 __device__ __forceinline__ float to_f32(bf16 v) { return __bfloat162float(v); }
