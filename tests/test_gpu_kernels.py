@@ -610,6 +610,16 @@ def test_zero_tokens_is_a_no_op():
     L.moe_route(None, torch.zeros((H, E), device=DEV), None, 0, H, E, K, L.MOE_F32, None, None, None)
     L.moe_combine(None, None, None, None, None, None, 0, H, K, L.MOE_F32, None)
     L.moe_expert_ffn(None, cu, 0, w, w, w, E, H, 64, L.MOE_F32, None, None)
+    # the router backward of no tokens: dW_r is all zeros, on both bf16 designs
+    # (the one-pass stream for E = 8, the tensor-core GEMMs for E = 64) and fp32
+    for E_, dt in [(8, L.MOE_BF16), (64, L.MOE_BF16), (8, L.MOE_F32)]:
+        nb = L.moe_workspace_bytes(L.MOE_OP_ROUTE_BWD, 0, H, E_, K, 0)
+        wsb = torch.empty(max(nb, 256), dtype=torch.uint8, device=DEV)
+        dw = torch.full((H, E_), 7.0, device=DEV)
+        L.moe_route_bwd(L.MOE_ROUTE_SOFTMAX_TOPK, None, None, None, None, None, 0, H, E_, K, dt, None, dw, None,
+                        wsb, nb)
+        torch.cuda.synchronize()
+        assert (dw.cpu() == 0).all()
     assert L.moe_last_device_error() == L.MOE_OK
 
 
