@@ -46,11 +46,11 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
-# DRAM bytes (read + write) of one moe_expert_ffn call, both GEMM launches, from
-# an ncu capture of the kernels as they stand (profiles/expert_ffn_* give the
-# command); a workload without a capture reports null
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one
+# moe_expert_ffn call, both GEMM launches, from one ncu capture per workload of
+# the kernels as they stand; a workload without a capture reports null
 FFN_DRAM_BYTES = {
-    # profiles/expert_ffn_gemm_mixtral_bf16_T8192.md: 2.472 GB (gate/up) + 2.355 GB (down)
+    # Mixtral-shaped layer, T=8192: 2.472 GB (gate/up) + 2.355 GB (down)
     "mixtral_bf16_T8192_H4096_E8_K2_Hp14336": 4826546944,
 }
 DEFAULT_WORKLOAD = "mixtral_bf16_T8192_H4096_E8_K2_Hp14336"
@@ -549,10 +549,13 @@ def run_ours(args, shape, rank, world, local):
         if shape.dtype == "bf16" else None
     hbm_peak = peaks.get("hbm_gbs", 6800.0)
     if shape.dtype != "bf16":
-        # fp32 layers run on FFMA: the peak is 152 SMs x 128 FP32 lanes x 2 FLOP
-        # x 2.07 GHz (maximum SM clock) = 80.5 TFLOP/s
-        roof = {"bound": "alu", "achieved": ffn_flops / ffn_s / 1e12, "peak": 152 * 128 * 2 * 2.07e9 / 1e12,
-                "unit": "TFLOP/s", "peak_source": "derived: FP32 FMA lanes x clock"}
+        # fp32 layers run on FFMA: the peak is SMs x 128 FP32 lanes x 2 FLOP x the
+        # maximum SM clock (152 x 128 x 2 x 2.07 GHz = 80.5 TFLOP/s on GB300)
+        import torch
+        n_sm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+        sm_hz = peaks.get("sm_max_mhz", 2070.0) * 1e6
+        roof = {"bound": "alu", "achieved": ffn_flops / ffn_s / 1e12, "peak": n_sm * 128 * 2 * sm_hz / 1e12,
+                "unit": "TFLOP/s", "peak_source": f"derived: {n_sm} SMs x 128 FP32 lanes x 2 x max SM clock"}
     elif ffn_flops / (peak_tf * 1e12) >= ffn_bytes / (hbm_peak * 1e9):
         roof = {"bound": "tensor", "achieved": ffn_flops / ffn_s / 1e12, "peak": peak_tf, "unit": "TFLOP/s",
                 "peak_source": f"{peak_src} bf16_tflops" + ("_sustained (sw_power_cap seen)" if capped else

@@ -3,6 +3,7 @@ top-k comparison that tolerates only genuine near-ties."""
 import numpy as np
 import torch
 
+import oracle as O
 from token_dispatch_gb300 import synth
 
 DEV = "cuda:0"
@@ -62,6 +63,30 @@ def check_topk(gpu_idx, ref_logits, K, logit_err, max_frac=1e-3):
         assert (np.diff(chosen) <= 2 * logit_err + 1e-12).all()
     assert len(bad) <= max(1, int(max_frac * len(ref_idx))), f"{len(bad)} ambiguous rows"
     return len(bad)
+
+
+def check_topk_exact(gpu_idx, gpu_logits, K, sel_bias=None, what="top-k"):
+    """Exact index parity on the GPU's own logits: the oracle's top-K (value
+    descending, lowest expert first on ties) run on the fp32 logits the GPU
+    emitted must give the GPU's indices bit for bit.  With a selection-only
+    bias the selection value is the fp32 sum logit + bias, rounded to nearest
+    even exactly as the kernels add it; numpy's float32 add rounds the same way."""
+    key = np.asarray(gpu_logits, np.float32)
+    if sel_bias is not None:
+        key = key + np.asarray(sel_bias, np.float32)[None, :]
+    ref = O.topk_experts(key.astype(np.float64), K)
+    bad = np.nonzero((np.asarray(gpu_idx) != ref).any(axis=1))[0]
+    assert len(bad) == 0, f"{what}: {len(bad)} rows differ from the top-K of the GPU's logits, first {bad[:5]}"
+
+
+def near_tie_rows(ref_logits, K, logit_err):
+    """Rows whose K-th and (K+1)-th exact logits lie within 4x the logit error:
+    the only rows where the fp32 and the fp64 selections may legitimately differ."""
+    E = ref_logits.shape[1]
+    if K >= E:
+        return 0
+    srt = -np.sort(-ref_logits, axis=1)
+    return int(np.count_nonzero(srt[:, K - 1] - srt[:, K] < 4 * logit_err))
 
 
 def host_layer_inputs(shape, T=None, seed=0, bias=None):

@@ -15,7 +15,8 @@ import torch
 import oracle as O
 from token_dispatch_gb300 import _lib as L
 from token_dispatch_gb300 import layer, synth
-from tests.gpu_util import DEV, TDT, TOL, assert_close, check_topk, dev, gate_tol, host_layer_inputs, to64
+from tests.gpu_util import (DEV, TDT, TOL, assert_close, check_topk, check_topk_exact, dev, gate_tol,
+                            host_layer_inputs, to64)
 
 pytestmark = pytest.mark.gpu
 
@@ -73,7 +74,9 @@ def test_route_matches_oracle(shape):
     tol = 1e-5 if shape.dtype == "f32" else 1e-5  # fp32 accumulation in both storage types
     assert_close(logits, r_logits, tol, "logits")
     logit_err = float(np.max(np.abs(logits - r_logits)))
-    check_topk(idx, r_logits, shape.K, logit_err)
+    check_topk_exact(idx, logits, shape.K)
+    n_amb = check_topk(idx, r_logits, shape.K, logit_err)
+    assert n_amb == 0, f"{n_amb} rows differ from the fp64 selection"
     same = (idx == r_idx).all(axis=1)
     assert_close(gate[same], r_gate[same], gate_tol(logit_err), "gate")
 
@@ -112,7 +115,9 @@ def test_route_variants_match_oracle(shape, flags):
     assert_close(logits, r_logits, 1e-5, "logits")
     err = float(np.max(np.abs(logits - r_logits)))
     r_sel = r_logits + (bias.astype(np.float64)[None, :] if select else 0.0)
-    check_topk(idx, r_sel, K, err)
+    check_topk_exact(idx, logits, K, bias if select else None)
+    n_amb = check_topk(idx, r_sel, K, err)
+    assert n_amb == 0, f"{n_amb} rows differ from the fp64 selection"
     same = (idx == r_idx).all(axis=1)
     assert_close(gate[same], r_gate[same], gate_tol(err), "gate")
     if renorm:

@@ -957,12 +957,13 @@ int launch_wait_probe(unsigned long long wait_cycles, cudaStream_t s) {
 static int router_bn(int E) { return E <= 64 ? 64 : E <= 128 ? 128 : E % 192 == 0 ? 192 : 256; }
 
 // Splits of H for the router GEMM: a CTA streams x from DRAM at a limited rate,
-// so when the token tiles alone would occupy fewer than about 100 of the 152
+// so when the token tiles alone would occupy fewer than about two thirds of the
 // SMs the reduction over H is split (fp32 partials summed by the softmax pass).
 int router_tc_splits(int T, int H, int E) {
   const long long tiles = ((T + tc::BM - 1) / tc::BM) * (long long)((E + router_bn(E) - 1) / router_bn(E));
-  if (tiles >= 100) return 1;
-  long long s = 152 / (tiles > 0 ? tiles : 1);
+  const long long sms = sm_count();
+  if (3 * tiles >= 2 * sms) return 1;
+  long long s = sms / (tiles > 0 ? tiles : 1);
   // every split needs at least one stage of K (64 * k sub-blocks per stage)
   const int ksub = E <= 64 ? 4 : E <= 128 ? 2 : 1;
   const long long kb = (H + tc::BK * ksub - 1) / (tc::BK * ksub);
@@ -1002,13 +1003,13 @@ int launch_router_tc(const void* x, const void* w, const float* bias, const floa
 }
 
 // Split count for the router weight gradient on tensor cores: the (h tile x
-// token split) work items should fill whole waves of the 152-SM GPU; among
+// token split) work items should fill whole waves of the GPU's SMs; among
 // split counts up to 64 (each split at least one 64-token block) a larger
 // count is taken only when it raises the wave efficiency by more than 2%.
 int router_dw_tc_splits(int T, int H, int E) {
   const long long tiles = ((H + tc::BM - 1) / tc::BM) * (long long)(E <= 64 ? 1 : (E + 127) / 128);
   const long long kb = (T + tc::BK - 1) / tc::BK;
-  const long long sms = 152;
+  const long long sms = sm_count();
   long long best = 1;
   double best_eff = 0.0;
   for (long long s = 1; s <= 64 && s <= kb; ++s) {

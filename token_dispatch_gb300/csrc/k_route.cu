@@ -301,9 +301,10 @@ DwPlan dw_plan(int T, int H, int E) {
   p.cpt = 64 / p.eb;
   p.col_blocks = (H + DW_THREADS * p.cpt - 1) / (DW_THREADS * p.cpt);
   p.exp_blocks = (E + p.eb - 1) / p.eb;
-  // about two CTAs per SM of a 152-SM GPU (a fixed target keeps the workspace
-  // size a function of the shapes alone)
-  long long want = (304 + p.col_blocks * p.exp_blocks - 1) / (p.col_blocks * p.exp_blocks);
+  // about two CTAs per SM (the workspace size then depends on the current
+  // device's SM count, which moe_workspace_bytes reads the same way)
+  const long long target = 2LL * sm_count();
+  long long want = (target + p.col_blocks * p.exp_blocks - 1) / (p.col_blocks * p.exp_blocks);
   long long by_t = (T + 7) / 8;
   long long s = want < by_t ? want : by_t;
   if (s > 256) s = 256;

@@ -1,6 +1,9 @@
 // The C ABI: argument validation, workspace sizing and launches.
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -11,17 +14,26 @@ __device__ unsigned g_moe_device_error;
 
 unsigned long long g_kernel_launches = 0;
 
-static unsigned* g_err_ptr[64];
+static std::atomic<unsigned*> g_err_ptr[64];
+static std::mutex g_err_mu;
 
+// The device address of the error word, looked up once per device under a lock
+// (two host threads making their first call at the same time both get it);
+// later calls read the published address without locking.
 unsigned* device_error_word() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
-  if (!g_err_ptr[dev]) {
+  unsigned* known = g_err_ptr[dev].load(std::memory_order_acquire);
+  if (known) return known;
+  std::lock_guard<std::mutex> lock(g_err_mu);
+  known = g_err_ptr[dev].load(std::memory_order_relaxed);
+  if (!known) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_moe_device_error) != cudaSuccess) return nullptr;
-    g_err_ptr[dev] = static_cast<unsigned*>(p);
+    known = static_cast<unsigned*>(p);
+    g_err_ptr[dev].store(known, std::memory_order_release);
   }
-  return g_err_ptr[dev];
+  return known;
 }
 
 }  // namespace moe

@@ -84,11 +84,17 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// SMs of the current device.  Without a device to ask (workspace sizes queried
+// on a host with no GPU) the answer is that of GB300, the part this library is
+// built for: 152.
 inline int sm_count() {
   int dev = 0, n = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-  return n > 0 ? n : 1;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+    cudaGetLastError();
+    return 152;
+  }
+  return n;
 }
 
 // Kernels this library has launched in this process (every launch site is
