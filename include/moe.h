@@ -177,10 +177,11 @@ MOE_API int moe_dispatch(const void* x, const int32_t* topk_idx, int T, int H, i
  * where it can synchronise the device or fail under memory pressure.
  *
  * Same arguments, results and errors as moe_dispatch, minus ws/ws_bytes.  The
- * scratch it needs (a ceil(T/256) x E table of int32 counts) is a library-owned
- * static device array of 65536 ints (256 KB), present on every GPU that loads
- * the library until the process exits.  Sizes with ceil(T/256) * E > 65536
- * return MOE_ERR_WORKSPACE before anything is launched.  The call allocates
+ * scratch it needs (a ceil(T/256) x E table of int32 counts and E int32 totals)
+ * is a library-owned static device array of 65536 ints (256 KB), present on
+ * every GPU that loads the library until the process exits.  Sizes with
+ * ceil(T/256) * E + E > 65536 return MOE_ERR_WORKSPACE before anything is
+ * launched.  The call allocates
  * nothing (no cudaMalloc/cudaFree, no allocating library routine).
  *
  * The first call on a device looks up the array's device address (one

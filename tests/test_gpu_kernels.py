@@ -213,6 +213,30 @@ def test_dispatch_skewed_all_tokens_to_one_expert():
     assert np.array_equal(to64(b.xs), xs_ref)
 
 
+@pytest.mark.parametrize("T,E,K", [(65536, 1024, 8), (8192, 384, 8), (16384, 64, 6), (16385, 64, 6),
+                                   (7000, 1024, 16), (300, 1000, 3), (1, 8, 2)])
+def test_dispatch_count_tables_small_and_large(T, E, K):
+    """Both ways the chunk counts are scanned: tables of at most 8192 entries
+    summed by every placing CTA, larger ones (65536 tokens x 1024 experts: a
+    256 x 1024 table) by the column-scan launch.  Skewed (Zipf-like) expert
+    choices, a ragged last chunk; index maps and rows bit-exact."""
+    rng = np.random.default_rng(T + E)
+    w = 1.0 / np.arange(1, E + 1) ** 1.1
+    w /= w.sum()
+    idx = np.stack([rng.choice(E, K, replace=False, p=w) for _ in range(T)]).astype(np.int32)
+    H = 64
+    x = synth.store(rng.standard_normal((T, H)), "bf16")
+    cu, dst, src, xs_ref = O.dispatch(x.ref, idx, E)
+    b = layer.MoEBuffers(T, H, E, K, 64, "bf16", DEV, backward=False)
+    L.moe_dispatch(dev(x), torch.from_numpy(idx).to(DEV), T, H, E, K, L.MOE_BF16, b.cu, b.dst_row, b.src_tok,
+                   b.xs, b.ws_dispatch, b.ws_dispatch_bytes)
+    assert L.moe_last_device_error() == L.MOE_OK
+    assert np.array_equal(b.cu.cpu().numpy(), cu)
+    assert np.array_equal(b.dst_row.cpu().numpy(), dst)
+    assert np.array_equal(b.src_tok.cpu().numpy(), src)
+    assert np.array_equal(to64(b.xs), xs_ref)
+
+
 def test_dispatch_out_of_range_expert_sets_bounds_error():
     T, H, E, K = 40, 64, 8, 2
     idx = np.stack([np.arange(T) % E, (np.arange(T) + 1) % E], axis=1).astype(np.int32)

@@ -22,6 +22,12 @@ from tests.test_gpu_kernels import check_mod_selection
 pytestmark = pytest.mark.gpu
 
 WL = [synth.MIXTRAL_BF16, synth.FINEGRAINED_BF16, synth.EPBENCH_BF16]
+# Rows whose GPU top-K differs from the float64 top-K on these seeds.  The GPU
+# selects exactly on its own fp32 logits (asserted); a row can still differ from
+# the float64 selection where its K-th and (K+1)-th logits lie within the fp32
+# accumulation error.  Over H = 7168 that error reaches 9e-5 and one of the
+# E=384 layer's 8192 rows is such a tie; the other workloads have none.
+AMBIGUOUS_ROWS = {synth.MIXTRAL_BF16.name: 0, synth.FINEGRAINED_BF16.name: 0, synth.EPBENCH_BF16.name: 1}
 BWD = {synth.MIXTRAL_BF16.name, synth.FINEGRAINED_BF16.name}
 
 
@@ -62,9 +68,12 @@ def test_full_workload_forward_and_backward(shape):
     logit_err = float(np.max(np.abs(g_logits - r_logits)))
     check_topk_exact(g_idx, g_logits, K)
     n_amb = check_topk(g_idx, r_logits, K, logit_err)
+    n_near = near_tie_rows(r_logits, K, logit_err)
     print(f"{shape.name}: rows differing from the fp64 selection {n_amb}, "
-          f"near-tie rows (K-th/K+1-th gap < 4x logit error {logit_err:.2e}) {near_tie_rows(r_logits, K, logit_err)}")
-    assert n_amb == 0, f"{n_amb} rows differ from the fp64 selection"
+          f"near-tie rows (K-th/K+1-th gap < 4x logit error {logit_err:.2e}) {n_near}")
+    # every differing row is a genuine near-tie (checked above); their count on
+    # these seeds is pinned so that a change shows
+    assert n_amb == AMBIGUOUS_ROWS[shape.name], f"{n_amb} rows differ from the fp64 selection"
     same = (g_idx == r_idx).all(axis=1)
     assert_close(b.gate.cpu().numpy()[same], r_gate[same], gate_tol(logit_err), "gate")
 
@@ -78,8 +87,11 @@ def test_full_workload_forward_and_backward(shape):
     assert np.array_equal(b2.src_tok.cpu().numpy(), src)
     rows_chk = rng.integers(0, R, size=512)
     assert np.array_equal(to64(b2.xs[torch.from_numpy(rows_chk).to(DEV)]), x.ref[src[rows_chk]])
-    assert np.array_equal(b.cu.cpu().numpy(), cu)
-    assert np.array_equal(b.dst_row.cpu().numpy(), dst)
+    # the layer's own dispatch, of its own indices: bit-exact
+    cu_g, dst_g, src_g = O.permutation(g_idx, E)
+    assert np.array_equal(b.cu.cpu().numpy(), cu_g)
+    assert np.array_equal(b.dst_row.cpu().numpy(), dst_g)
+    assert np.array_equal(b.src_tok.cpu().numpy(), src_g)
 
     # ---- expert FFN on sampled rows of sampled experts (same routing as the oracle)
     L.moe_expert_ffn(b2.xs, b2.cu, R, wg, wu, wd, E, H, Hp, L.MOE_BF16, b2.act, b2.h)

@@ -89,18 +89,20 @@ router_stream_kernel(const bf16* __restrict__ x, const bf16* __restrict__ w, con
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, c = lane & 3;
-  const int nblk = (T + TOK - 1) / TOK;
+  // CTA b streams the contiguous tokens [tb0, tb1), an even share of T (the
+  // last block of a range may be partial), so every SM moves the same bytes
   const int G = gridDim.x;
-  const int my_blocks = (int)blockIdx.x < nblk ? (nblk - 1 - (int)blockIdx.x) / G + 1 : 0;
+  const int tb0 = (int)((long long)blockIdx.x * T / G), tb1 = (int)((long long)(blockIdx.x + 1) * T / G);
+  const int my_blocks = (tb1 - tb0 + TOK - 1) / TOK;
   const bf16* xw = x + warp * (CH * 32) + 8 * c;  // this lane's columns of every chunk
 
-  // loads of block blk into r; rows past the last token are not loaded (their
+  // loads of block i of the range into r; rows past the range are not loaded (their
   // MMA columns hold stale values and are never written out)
-  auto load_block = [&](uint4 (&r)[NT][CH], int blk) {
+  auto load_block = [&](uint4 (&r)[NT][CH], int i) {
 #pragma unroll
     for (int q = 0; q < NT; ++q) {
-      const int tok = blk * TOK + q * RS_TOK + g;
-      const bool ok = blk < nblk && tok < T;
+      const int tok = tb0 + i * TOK + q * RS_TOK + g;
+      const bool ok = i < my_blocks && tok < tb1;
       const bf16* p = xw + (long long)(ok ? tok : 0) * H;
 #pragma unroll
       for (int j = 0; j < CH; ++j) ldg_stream(r[q][j], p + j * 32, ok);
@@ -110,7 +112,7 @@ router_stream_kernel(const bf16* __restrict__ x, const bf16* __restrict__ w, con
   // the first D blocks' loads go out before W_r is staged
   uint4 xr[D][NT][CH] = {};
 #pragma unroll
-  for (int d = 0; d < D; ++d) load_block(xr[d], (int)blockIdx.x + d * G);
+  for (int d = 0; d < D; ++d) load_block(xr[d], d);
 
   // W_r [H, E] row-major -> A fragments: chunk ch, lane (g', c'), row half q,
   // element j = W_r[ch*32 + 8c' + j][g' + 8q].  W_r is read as 16-byte pieces
@@ -147,8 +149,7 @@ router_stream_kernel(const bf16* __restrict__ x, const bf16* __restrict__ w, con
   // top-K
   auto process = [&](uint4 (&r)[NT][CH], int i) {
     const int buf = i & 1;
-    const int blk = (int)blockIdx.x + i * G;
-    const int nxt = blk + D * G;
+    const int nxt = i + D;
     float d[NT][4] = {};
 #pragma unroll
     for (int j = 0; j < CH; ++j) {
@@ -158,8 +159,8 @@ router_stream_kernel(const bf16* __restrict__ x, const bf16* __restrict__ w, con
       for (int q = 0; q < NT; ++q) {
         mma_16816(d[q], a.x, a8.x, a.y, a8.y, r[q][j].x, r[q][j].y);
         mma_16816(d[q], a.z, a8.z, a.w, a8.w, r[q][j].z, r[q][j].w);
-        const int tok = nxt * TOK + q * RS_TOK + g;
-        const bool ok = nxt < nblk && tok < T;
+        const int tok = tb0 + nxt * TOK + q * RS_TOK + g;
+        const bool ok = nxt < my_blocks && tok < tb1;
         ldg_stream(r[q][j], xw + (long long)(ok ? tok : 0) * H + j * 32, ok);
       }
     }
@@ -186,8 +187,8 @@ router_stream_kernel(const bf16* __restrict__ x, const bf16* __restrict__ w, con
 #pragma unroll
       for (int ww = 0; ww < RS_WARPS; ++ww) v += rt[ww * TOK * RS_RED_LD];
       if (bias) v += __ldg(bias + e);
-      const int tk = blk * TOK + t;
-      const bool live = tk < T;
+      const int tk = tb0 + i * TOK + t;
+      const bool live = tk < tb1;
       if (live) logits[(long long)tk * E + e] = v;
       float m = v;
 #pragma unroll

@@ -155,7 +155,7 @@ int moe_dispatch_noalloc(const void* x, const int32_t* topk_idx, int T, int H, i
     return MOE_ERR_INVALID_ARG;
   if (!all_aligned({x, topk_idx, cu_seqlens, dst_row, src_tok, xs})) return MOE_ERR_MISALIGNED;
   if (H % vec_elems(dtype) != 0) return MOE_ERR_UNSUPPORTED;
-  if ((long long)((T + 255) / 256) * E > dispatch_static_scratch_ints()) return MOE_ERR_WORKSPACE;
+  if (dispatch_scratch_ints(T, E) > dispatch_static_scratch_ints()) return MOE_ERR_WORKSPACE;
   return launch_dispatch_static(x, topk_idx, T, H, E, K, dtype, cu_seqlens, dst_row, src_tok, xs,
                                 as_stream(stream));
 }

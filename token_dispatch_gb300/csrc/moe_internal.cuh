@@ -139,6 +139,7 @@ int launch_dispatch(const void* x, const int32_t* idx, int T, int H, int E, int 
 int launch_dispatch_static(const void* x, const int32_t* idx, int T, int H, int E, int K, int dtype,
                            int32_t* cu, int32_t* dst_row, int32_t* src_tok, void* xs, cudaStream_t s);
 long long dispatch_static_scratch_ints();
+long long dispatch_scratch_ints(int T, int E);  // ints of scratch one dispatch call uses
 int launch_combine(const void* h, const float* gate, const int32_t* dst_row, const float* scale,
                    const void* residual, const int32_t* out_row, int T, int H, int K, int dtype,
                    void* y, cudaStream_t s);
