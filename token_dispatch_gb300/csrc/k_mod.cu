@@ -3,19 +3,22 @@
 //
 //   score[t] = x[t] . w_mod                         (one warp per token)
 //   per sequence: the C highest scores are selected, equal scores -> lower
-//   position.  Token i of a sequence is selected iff its rank
+//   position, i.e. token i is selected iff its rank
 //     #{j : s_j > s_i  or  (s_j == s_i and j < i)}
-//   is below C; every token's rank is counted directly against the whole
-//   sequence held in shared memory (L compares per token, all tokens in
-//   parallel across many CTAs).  One CTA per sequence then compacts the
-//   selected positions in order with a block scan, and one launch copies both
-//   the selected rows (the MoE input) and the skipped rows (y = x).
+//   is below C.
+// The selection runs as a radix select on order-preserving integer keys of
+// the scores (-0 folded onto +0, so equal scores are equal keys): four 8-bit
+// passes from the top find the C-th largest key k*; keys above k* are
+// selected, and of the keys equal to k* the first (C - #{key > k*}) by
+// position.  One launch does the select and the row copies: every CTA of a
+// sequence runs the same select on the sequence's scores (identical integer
+// work, identical result), the first CTA writes mask, sel and sel_score, and
+// each CTA copies its share of the rows: the selected ones to the MoE input
+// x_sel in position order, the others to y (y = x for tokens that skip).
 #include "moe_internal.cuh"
 
 namespace moe {
 namespace {
-
-constexpr int SEL_THREADS = 1024;
 
 template <typename T>
 __global__ void __launch_bounds__(256)
@@ -55,106 +58,186 @@ mod_score_kernel(const T* __restrict__ x, const T* __restrict__ w, long long n_t
   }
 }
 
-constexpr int RANK_TOK = 32;    // tokens per rank CTA
-constexpr int RANK_SPLIT = 8;   // threads per token, each counting 1/8 of the sequence
+constexpr int MS_THREADS = 512;
+constexpr int MS_WARPS = MS_THREADS / 32;
+constexpr int MS_MAX_RUN = 16;  // positions per thread: L <= 8192
 
-// mask[b, i] = (rank of token i in sequence b) < C.  grid (ceil(L / RANK_TOK), B).
-// The RANK_SPLIT threads of a token are consecutive lanes; they read
-// consecutive 16-byte words of the shared scores (other tokens of the warp read
-// the same words: broadcasts) and add their counts with shuffles.
-__global__ void __launch_bounds__(RANK_TOK * RANK_SPLIT)
-mod_rank_kernel(const float* __restrict__ score, int L, int C, uint8_t* __restrict__ mask) {
-  extern __shared__ float4 s4[];  // the sequence's scores, padded to a multiple of 4 with -inf
-  float* sv = reinterpret_cast<float*>(s4);
-  const int b = blockIdx.y;
-  const float* s = score + (long long)b * L;
-  const int L4 = (L + 3) / 4;
-  for (int j = threadIdx.x; j < 4 * L4; j += blockDim.x) sv[j] = j < L ? s[j] : -INFINITY;
-  __syncthreads();
-  const int part = threadIdx.x % RANK_SPLIT;
-  const int i = blockIdx.x * RANK_TOK + threadIdx.x / RANK_SPLIT;
-  const int ii = i < L ? i : L - 1;  // rows past L count too (uniform shuffles), nothing is written
-  const float si = sv[ii];
-  int r0 = 0, r1 = 0, r2 = 0, r3 = 0;
-#pragma unroll 4
-  for (int q = part; q < L4; q += RANK_SPLIT) {
-    const float4 v = s4[q];
-    const int j = 4 * q;
-    r0 += (v.x > si) | ((v.x == si) & (j < ii));
-    r1 += (v.y > si) | ((v.y == si) & (j + 1 < ii));
-    r2 += (v.z > si) | ((v.z == si) & (j + 2 < ii));
-    r3 += (v.w > si) | ((v.w == si) & (j + 3 < ii));
-  }
-  int rank = (r0 + r1) + (r2 + r3);
+// Order-preserving key: a > b as floats iff key(a) > key(b); -0 and +0 map to
+// the same key (they are equal scores).
+__device__ __forceinline__ unsigned score_key(float s) {
+  const unsigned u = __float_as_uint(s == 0.f ? 0.f : s);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ unsigned lanemask_lt() {
+  unsigned m;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+  return m;
+}
+
+// Exclusive prefix of v over the CTA's threads in thread order (warp shuffles,
+// then the warp totals); total gets the sum over all threads.
+__device__ __forceinline__ int block_excl_scan(int v, int* wtot, int& total) {
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  int incl = v;
 #pragma unroll
-  for (int o = RANK_SPLIT / 2; o > 0; o >>= 1) rank += __shfl_xor_sync(0xffffffffu, rank, o);
-  if (part == 0 && i < L) mask[(long long)b * L + i] = (uint8_t)(rank < C);
-}
-
-// sel[b, r] = b*L + i for the r-th selected position i of sequence b (and its score)
-__global__ void __launch_bounds__(SEL_THREADS)
-mod_compact_kernel(const float* __restrict__ score, const uint8_t* __restrict__ mask, int L, int C,
-                   int32_t* __restrict__ sel, float* __restrict__ sel_score) {
-  __shared__ int part[SEL_THREADS];
-  const int b = blockIdx.x;
-  const uint8_t* m = mask + (long long)b * L;
-  // each thread owns a run of positions
-  const int per = (L + SEL_THREADS - 1) / SEL_THREADS;
-  const int lo = threadIdx.x * per, hi = min(L, lo + per);
-  int cnt = 0;
-  for (int i = lo; i < hi; ++i) cnt += m[i];
-  part[threadIdx.x] = cnt;
+  for (int o = 1; o < 32; o <<= 1) {
+    const int u = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += u;
+  }
+  __syncthreads();  // wtot may still be read by a previous scan
+  if (lane == 31) wtot[w] = incl;
   __syncthreads();
-  for (int o = 1; o < SEL_THREADS; o <<= 1) {
-    const int v = threadIdx.x >= o ? part[threadIdx.x - o] : 0;
-    __syncthreads();
-    part[threadIdx.x] += v;
-    __syncthreads();
+  int before = incl - v;
+  total = 0;
+#pragma unroll
+  for (int ww = 0; ww < MS_WARPS; ++ww) {
+    before += ww < w ? wtot[ww] : 0;
+    total += wtot[ww];
   }
-  int r = part[threadIdx.x] - cnt;
-  for (int i = lo; i < hi; ++i) {
-    if (m[i] && r < C) {
-      sel[(long long)b * C + r] = b * L + i;
-      if (sel_score) sel_score[(long long)b * C + r] = score[(long long)b * L + i];
-      ++r;
-    }
-  }
+  return before;
 }
 
-// Row copies in one launch, one warp per item, U 16-byte vectors per lane in
-// flight: items [0, n_sel) gather x_sel[j] = x[sel[j]] (sel holds flat token
-// indices); items [n_sel, n_sel + n_tok) copy y[t] = x[t] for the tokens that
-// skip the layer.
-__global__ void __launch_bounds__(256)
-mod_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ sel, long long n_sel,
-                const uint8_t* __restrict__ mask, long long n_tok, int vec_per_row, uint4* __restrict__ x_sel,
-                uint4* __restrict__ y_skip) {
-  constexpr int U = 4;
-  const int lane = threadIdx.x & 31;
-  const long long nwarps = (long long)gridDim.x * (blockDim.x >> 5);
-  for (long long it = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < n_sel + n_tok;
-       it += nwarps) {
-    long long src, dst;
-    uint4* out;
-    if (it < n_sel) {
-      src = __ldg(sel + it);
-      dst = it;
-      out = x_sel;
-    } else {
-      src = dst = it - n_sel;
-      if (mask[src]) continue;
-      out = y_skip;
+// grid (R, B): CTA r of sequence b.  Dynamic shared memory: L ints (the keys,
+// then the row map: selected position -> rank among the selected, else -1).
+__global__ void __launch_bounds__(MS_THREADS)
+mod_select_rows_kernel(const float* __restrict__ score, int L, int C, const uint4* __restrict__ x,
+                       int vec_per_row, int32_t* __restrict__ sel, float* __restrict__ sel_score,
+                       uint8_t* __restrict__ mask, uint4* __restrict__ x_sel, uint4* __restrict__ y_skip) {
+  extern __shared__ unsigned keys[];
+  __shared__ int hist[256];
+  __shared__ int wtot[MS_WARPS];
+  __shared__ int s_bin, s_need;
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int b = blockIdx.y, R = gridDim.x, r = blockIdx.x;
+  const float* s = score + (long long)b * L;
+  for (int i = tid; i < L; i += MS_THREADS) keys[i] = score_key(__ldg(s + i));
+  __syncthreads();
+
+  // radix select of the C-th largest key: after the pass at `shift`, the bits
+  // of `prefix` under `pmask` are fixed and `need` keys are still to be taken
+  // among the keys that match them
+  unsigned prefix = 0, pmask = 0;
+  int need = C;
+  const bool partial = C > 0 && C < L;
+  if (partial) {
+    for (int shift = 24; shift >= 0; shift -= 8) {
+      if (tid < 256) hist[tid] = 0;
+      __syncthreads();
+      for (int i0 = 0; i0 < L; i0 += MS_THREADS) {
+        const int i = i0 + tid;
+        const unsigned k = i < L ? keys[i] : 0u;
+        const int d = (i < L && (k & pmask) == prefix) ? (int)((k >> shift) & 255u) : -1;
+        // lanes with the same digit add once (the lowest of them)
+        const unsigned peers = __match_any_sync(0xffffffffu, d);
+        if (d >= 0 && (peers & lanemask_lt()) == 0) atomicAdd(&hist[d], __popc(peers));
+      }
+      __syncthreads();
+      if (w == 0) {
+        // lane l owns digits 255 - 8l - j, j = 0..7 (descending); the digit
+        // where the count from the top reaches `need` holds the C-th key
+        int c[8], local = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          c[j] = hist[255 - 8 * lane - j];
+          local += c[j];
+        }
+        int incl = local;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int u = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += u;
+        }
+        const int before = incl - local;
+        if (before < need && need <= incl) {
+          int run = before;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            if (run + c[j] >= need) {
+              s_bin = 255 - 8 * lane - j;
+              s_need = need - run;
+              break;
+            }
+            run += c[j];
+          }
+        }
+      }
+      __syncthreads();
+      prefix |= (unsigned)s_bin << shift;
+      pmask |= 255u << shift;
+      need = s_need;
     }
-    const uint4* in = x + src * vec_per_row;
-    uint4* o = out + dst * vec_per_row;
+  }
+  const unsigned kth = prefix;  // the C-th largest key (when 0 < C < L)
+
+  // each thread owns a run of consecutive positions: selection flags with the
+  // tie rule (equal keys taken by position), then ranks among the selected
+  const int per = (L + MS_THREADS - 1) / MS_THREADS;
+  const int lo = min(L, tid * per), hi = min(L, lo + per);
+  int n_eq = 0;
+  for (int i = lo; i < hi; ++i) n_eq += (partial && keys[i] == kth) ? 1 : 0;
+  int tot;
+  int eq_before = block_excl_scan(n_eq, wtot, tot);
+  unsigned flags = 0;
+  int n_sel = 0;
+  for (int i = lo; i < hi; ++i) {
+    const unsigned k = keys[i];
+    bool take;
+    if (!partial) {
+      take = C >= L;
+    } else if (k > kth) {
+      take = true;
+    } else if (k == kth) {
+      take = eq_before < need;
+      ++eq_before;
+    } else {
+      take = false;
+    }
+    if (take) {
+      flags |= 1u << (i - lo);
+      ++n_sel;
+    }
+  }
+  int pos = block_excl_scan(n_sel, wtot, tot);
+  // the row map replaces the keys (each thread rewrites only its own run)
+  for (int i = lo; i < hi; ++i) {
+    const bool take = (flags >> (i - lo)) & 1u;
+    const long long t = (long long)b * L + i;
+    if (r == 0) {
+      mask[t] = take ? 1 : 0;
+      if (take) {
+        sel[(long long)b * C + pos] = (int32_t)t;
+        if (sel_score) sel_score[(long long)b * C + pos] = __ldg(s + i);
+      }
+    }
+    keys[i] = take ? (unsigned)pos : 0xffffffffu;
+    pos += take ? 1 : 0;
+  }
+  __syncthreads();
+
+  // this CTA's rows: one warp per row, 16-byte vectors, all of a lane's
+  // vectors of the row in flight before the first store
+  const int r_lo = (int)((long long)L * r / R), r_hi = (int)((long long)L * (r + 1) / R);
+  for (int i = r_lo + w; i < r_hi; i += MS_WARPS) {
+    const int m = (int)keys[i];
+    uint4* dst;
+    if (m >= 0) {
+      if (!x_sel) continue;
+      dst = x_sel + ((long long)b * C + m) * vec_per_row;
+    } else {
+      if (!y_skip) continue;
+      dst = y_skip + ((long long)b * L + i) * vec_per_row;
+    }
+    const uint4* src = x + ((long long)b * L + i) * vec_per_row;
+    constexpr int U = 8;
     for (int i0 = lane; i0 < vec_per_row; i0 += 32 * U) {
       uint4 a[U];
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        if (i0 + 32 * u < vec_per_row) a[u] = __ldg(in + i0 + 32 * u);
+        if (i0 + 32 * u < vec_per_row) a[u] = __ldg(src + i0 + 32 * u);
 #pragma unroll
       for (int u = 0; u < U; ++u)
-        if (i0 + 32 * u < vec_per_row) o[i0 + 32 * u] = a[u];
+        if (i0 + 32 * u < vec_per_row) dst[i0 + 32 * u] = a[u];
     }
   }
 }
@@ -173,6 +256,7 @@ int launch_mod_select(const void* x, const void* w, int B, int L, int H, int C, 
                       void* y_skip, cudaStream_t s) {
   const long long n_tok = (long long)B * L;
   if (n_tok == 0) return MOE_OK;
+  if (L > MS_THREADS * MS_MAX_RUN) return MOE_ERR_UNSUPPORTED;
   if (dtype == MOE_BF16)
     mod_score_kernel<bf16><<<warp_grid(n_tok), 256, 0, s>>>(static_cast<const bf16*>(x),
                                                             static_cast<const bf16*>(w), n_tok, H, score);
@@ -182,25 +266,19 @@ int launch_mod_select(const void* x, const void* w, int B, int L, int H, int C, 
   int st = launch_status();
   if (st != MOE_OK) return st;
   const int vec = H * (dtype == MOE_BF16 ? 2 : 4) / 16;
-  const size_t smem = (size_t)((L + 3) / 4) * 16;
-  mod_rank_kernel<<<dim3((L + RANK_TOK - 1) / RANK_TOK, B), RANK_TOK * RANK_SPLIT, smem, s>>>(score, L, C,
-                                                                                            mask);
-  st = launch_status();
-  if (st != MOE_OK) return st;
-  if (C > 0) {
-    mod_compact_kernel<<<B, SEL_THREADS, 0, s>>>(score, mask, L, C, sel, sel_score);
-    st = launch_status();
-    if (st != MOE_OK) return st;
-  }
-  const long long n_sel = x_sel ? (long long)B * C : 0;
-  const long long n_skip = y_skip ? n_tok : 0;
-  if (n_sel + n_skip > 0) {
-    mod_rows_kernel<<<warp_grid(n_sel + n_skip), 256, 0, s>>>(static_cast<const uint4*>(x), sel, n_sel, mask,
-                                                              n_skip, vec, static_cast<uint4*>(x_sel),
-                                                              static_cast<uint4*>(y_skip));
-    st = launch_status();
-  }
-  return st;
+  // about two CTAs per SM over all sequences, at least 8 rows each
+  long long R = (2LL * sm_count() + B - 1) / B;
+  if (R > (L + 7) / 8) R = (L + 7) / 8;
+  if (R < 1) R = 1;
+  const size_t smem = (size_t)L * sizeof(unsigned);
+  if (smem > 48 * 1024 &&
+      cudaFuncSetAttribute(mod_select_rows_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess)
+    return MOE_ERR_CUDA;
+  mod_select_rows_kernel<<<dim3((unsigned)R, B), MS_THREADS, smem, s>>>(
+      score, L, C, static_cast<const uint4*>(x), vec, sel, sel_score, mask, static_cast<uint4*>(x_sel),
+      static_cast<uint4*>(y_skip));
+  return launch_status();
 }
 
 }  // namespace moe
