@@ -319,6 +319,32 @@ MOE_API int mod_select(const void* x, const void* w_mod, int B, int L, int H, in
                float* score, int32_t* sel, float* sel_score, uint8_t* mask,
                void* x_sel, void* y_skip, void* ws, size_t ws_bytes, void* stream);
 
+/*
+ * Expert-parallel dispatch plan (host only)      [EP "Step-by-step": the S x K
+ *                      rows per rank invariant, the preload pool of B slots,
+ *                      the [E+B, H, H'] weights addressed by row index]
+ *
+ *   R ranks, E experts (E % R == 0; rank r owns experts [rG, rG+G), G = E/R),
+ *   S tokens per rank, K experts per token, B preload slots per rank.
+ *   counts [R][E] int32: pairs that source rank s routes to expert e; every row
+ *   must sum to S*K (MOE_ERR_INVALID_ARG otherwise).
+ *   Outputs (caller-owned host arrays):
+ *     piece_count [R][R][E], piece_offset [R][R][E]: destination rank d
+ *       processes pairs [offset, offset + count) of source s's pairs for expert
+ *       e (in the source's (t, k) order);
+ *     slot_expert [R][B]: the expert whose weights slot j of rank d holds, or -1;
+ *     local_counts [R][G + B]: rows of each local expert (home experts, then
+ *       the slots) -- the local cu_seqlens is their exclusive scan;
+ *     remote_reads [R]: rows of remote experts left without a slot (weights
+ *       read from the home rank).
+ *   Every destination gets exactly S*K rows.  The plan depends on the counts
+ *   only (deterministic), so every rank computes the same plan from gathered
+ *   counts.  No device work; returns MOE_OK or an argument error.
+ */
+MOE_API int moe_ep_plan(int R, int E, int S, int K, int B, const int32_t* counts, int32_t* piece_count,
+                        int32_t* piece_offset, int32_t* slot_expert, int32_t* local_counts,
+                        int32_t* remote_reads);
+
 #ifdef __cplusplus
 }
 #endif

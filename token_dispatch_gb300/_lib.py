@@ -44,7 +44,7 @@ EXPORTS = ("moe_status_str", "moe_version", "moe_kernel_launches", "moe_workspac
            "moe_check_wait_timeout",
            "moe_route", "moe_route_ex", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn",
            "moe_expert_ffn_ex", "moe_expert_ffn_bwd", "moe_combine", "moe_route_bwd",
-           "moe_permute_bwd", "mod_select")
+           "moe_permute_bwd", "mod_select", "moe_ep_plan")
 
 
 class MoEError(RuntimeError):
@@ -77,6 +77,7 @@ _SIGS = {
     "moe_route_bwd": (_I, [_I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
     "moe_permute_bwd": (_I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "mod_select": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
+    "moe_ep_plan": (_I, [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P]),
 }
 
 
@@ -222,3 +223,23 @@ def mod_select(x, w_mod, B, L, H, C, dtype, score, sel, sel_score, mask, x_sel, 
     _check("mod_select", lib().mod_select(_ptr(x), _ptr(w_mod), B, L, H, C, dtype, _ptr(score),
                                           _ptr(sel), _ptr(sel_score), _ptr(mask), _ptr(x_sel),
                                           _ptr(y_skip), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def moe_ep_plan(R, E, S, K, B, counts):
+    """Host-side expert-parallel plan from the gathered per-rank expert counts
+    (int32 [R, E]).  Returns numpy arrays: piece_count and piece_offset
+    [R dst, R src, E], slot_expert [R, B], local_counts [R, E/R + B],
+    remote_reads [R]."""
+    import numpy as np
+    counts = np.ascontiguousarray(counts, dtype=np.int32)
+    G = E // R if R > 0 and E % R == 0 else 0
+    pc = np.zeros((R, R, E), np.int32)
+    po = np.zeros((R, R, E), np.int32)
+    se = np.zeros((R, max(B, 0)), np.int32)
+    lc = np.zeros((R, G + max(B, 0)), np.int32)
+    rr = np.zeros(R, np.int32)
+
+    def a(x):
+        return x.ctypes.data_as(ctypes.c_void_p) if x.size else None
+    _check("moe_ep_plan", lib().moe_ep_plan(R, E, S, K, B, a(counts), a(pc), a(po), a(se), a(lc), a(rr)))
+    return pc, po, se, lc, rr

@@ -328,6 +328,7 @@ bool router_bwd_stream_applies(int mode, int dtype, int H, int E, int K) {
 // partial sums of dW_r the kernel leaves in the workspace (one per token range
 // and row lane)
 int router_bwd_stream_splits(int T, int H, int E) {
+  if (router_bwd_mma_applies(MOE_ROUTE_SOFTMAX_TOPK, MOE_BF16, H, E, 1)) return router_bwd_mma_splits(T, H);
   const RbGeom q = rb_geom(T, H, E);
   return q.g * q.rpi;
 }
@@ -335,6 +336,9 @@ int router_bwd_stream_splits(int T, int H, int E) {
 int launch_router_bwd_stream(int mode, const float* d_gate, const float* logits, const int32_t* idx, const void* x,
                              const void* w, int T, int H, int E, int K, bool renorm, float* d_logits, float* part,
                              void* dx, bool dx_write, cudaStream_t s) {
+  // 8 or 16 experts with whole 512-column slices: both products on the warp MMA
+  if (router_bwd_mma_applies(mode, MOE_BF16, H, E, K))
+    return launch_router_bwd_mma(d_gate, logits, idx, x, w, T, H, E, K, renorm, d_logits, part, dx, dx_write, s);
   const RbGeom q = rb_geom(T, H, E);
   const int grid = q.g * q.ns;
   const int lin = mode == MOE_ROUTE_MOD_LINEAR ? 1 : 0;

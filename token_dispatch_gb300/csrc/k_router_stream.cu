@@ -15,7 +15,10 @@
 //     (8 tokens), so one 128-bit load of x feeds two MMAs;
 //   * W_r sits in shared memory once per persistent CTA, pre-arranged in the
 //     MMA's A-fragment order (one conflict-free 128-bit load per lane per 32
-//     values of H);
+//     values of H); each thread loads 8 whole rows of W_r and writes their
+//     fragments with an in-register 8 x 8 transpose (byte permutes), so the
+//     staging costs a few instructions per 16 bytes instead of one store per
+//     element;
 //   * the 16 warps of a CTA own 16 consecutive slices of H; their partial
 //     logits meet in shared memory in warp order (fixed: the same bits every
 //     run) and get the bias; the E threads of a token then take the softmax
@@ -49,6 +52,10 @@ __device__ __forceinline__ void ldg_stream(uint4& v, const bf16* p, bool ok) {
       " @q ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%5];\n}"
       : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
       : "r"((int)ok), "l"(p));
+}
+
+__device__ __forceinline__ unsigned word4(const uint4& v, int i) {
+  return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
 }
 
 // D += A B, m16n8k16, bf16 inputs, fp32 accumulate.
@@ -109,37 +116,43 @@ router_stream_kernel(const bf16* __restrict__ x, const bf16* __restrict__ w, con
     }
   };
 
-  // the first D blocks' loads go out before W_r is staged
-  uint4 xr[D][NT][CH] = {};
-#pragma unroll
-  for (int d = 0; d < D; ++d) load_block(xr[d], d);
-
   // W_r [H, E] row-major -> A fragments: chunk ch, lane (g', c'), row half q,
-  // element j = W_r[ch*32 + 8c' + j][g' + 8q].  W_r is read as 16-byte pieces
-  // (8 experts of one row), up to eight per thread in flight at once.
+  // element j = W_r[ch*32 + 8c' + j][g' + 8q].  Thread u owns the 8
+  // consecutive rows 8u .. 8u+7 (128 or 256 contiguous bytes, loaded at once)
+  // and transposes each 8 x 8 block of bf16 in registers with byte permutes:
+  // word a of the fragment of column g' is (row 2a, row 2a+1) of that column.
+  uint4 xr[D][NT][CH] = {};
   {
-    uint16_t* wf = reinterpret_cast<uint16_t*>(wfrag);
-    const uint4* wsrc = reinterpret_cast<const uint4*>(w);
-    const int n16 = H * E / 8;
-    for (int base = 0; base < n16; base += 8 * RS_THREADS) {
-      uint4 v[8];
+    const bool has_unit = tid < H / 8;  // H <= 4096: at most one unit per thread
+    uint4 wv[NF][8];
+    if (has_unit) {
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = base + u * RS_THREADS + tid;
-        if (i < n16) v[u] = __ldg(wsrc + i);
-      }
+      for (int j = 0; j < 8; ++j)
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int i = base + u * RS_THREADS + tid;
-        if (i < n16) {
-          const int h = (i * 8) / E, q = E16 ? (i & 1) : 0;  // experts 8q .. 8q+7 of row h
-          const int ch = h >> 5, cc = (h >> 3) & 3, j = h & 7;
-          const uint16_t* pv = reinterpret_cast<const uint16_t*>(&v[u]);
-#pragma unroll
-          for (int e = 0; e < 8; ++e) wf[((ch * 32 + ((e << 2) | cc)) * NF + q) * 8 + j] = pv[e];
-        }
-      }
+        for (int q = 0; q < NF; ++q) wv[q][j] = __ldg(reinterpret_cast<const uint4*>(w + (size_t)(8 * tid + j) * E) + q);
     }
+    if (has_unit) {
+      const int ch = tid >> 2, cc = tid & 3;
+      // two halves (rows 0-3, rows 4-7): 8-byte stores, fewer live registers
+#pragma unroll
+      for (int q = 0; q < NF; ++q)
+#pragma unroll
+        for (int half = 0; half < 2; ++half)
+#pragma unroll
+          for (int gg = 0; gg < 8; ++gg) {
+            const unsigned sel = (gg & 1) ? 0x7632u : 0x5410u;
+            uint2 o;
+            o.x = __byte_perm(word4(wv[q][4 * half], gg >> 1), word4(wv[q][4 * half + 1], gg >> 1), sel);
+            o.y = __byte_perm(word4(wv[q][4 * half + 2], gg >> 1), word4(wv[q][4 * half + 3], gg >> 1), sel);
+            reinterpret_cast<uint2*>(wfrag + (ch * 32 + 4 * gg + cc) * NF + q)[half] = o;
+          }
+    }
+    // the first D blocks of x go out once the fragments are written: issued
+    // earlier, the x loads (16 per thread) fill the load queues and the W_r
+    // loads wait behind them (measured: 4.5 us of staging instead of 6 us)
+    asm volatile("" ::: "memory");
+#pragma unroll
+    for (int d = 0; d < D; ++d) load_block(xr[d], d);
   }
   __syncthreads();
 

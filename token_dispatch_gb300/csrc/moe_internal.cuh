@@ -127,6 +127,12 @@ size_t route_bwd_ws_bytes(int T, int H, int E);
 // streaming router backward (bf16; E = 8 or 16 softmax/top-K, E = 1 linear)
 bool router_bwd_stream_applies(int mode, int dtype, int H, int E, int K);
 int router_bwd_stream_splits(int T, int H, int E);
+// the same pass with both products on the warp-level MMA (8 or 16 experts, H % 512 == 0)
+bool router_bwd_mma_applies(int mode, int dtype, int H, int E, int K);
+int router_bwd_mma_splits(int T, int H);
+int launch_router_bwd_mma(const float* d_gate, const float* logits, const int32_t* idx, const void* x,
+                          const void* w, int T, int H, int E, int K, bool renorm, float* d_logits, float* part,
+                          void* dx, bool dx_write, cudaStream_t s);
 int launch_router_bwd_stream(int mode, const float* d_gate, const float* logits, const int32_t* idx, const void* x,
                              const void* w, int T, int H, int E, int K, bool renorm, float* d_logits, float* part,
                              void* dx, bool dx_write, cudaStream_t s);
