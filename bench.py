@@ -50,8 +50,9 @@ L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
 # moe_expert_ffn call, both GEMM launches, from one ncu capture per workload of
 # the kernels as they stand; a workload without a capture reports null
 FFN_DRAM_BYTES = {
-    # Mixtral-shaped layer, T=8192: 2.472 GB (gate/up) + 2.355 GB (down)
-    "mixtral_bf16_T8192_H4096_E8_K2_Hp14336": 4826546944,
+    # (workload, rows gathered by the FFN): bytes
+    # Mixtral-shaped layer, T=8192, rows read from xs: 2.472 GB (gate/up) + 2.355 GB (down)
+    ("mixtral_bf16_T8192_H4096_E8_K2_Hp14336", False): 4826546944,
 }
 DEFAULT_WORKLOAD = "mixtral_bf16_T8192_H4096_E8_K2_Hp14336"
 
@@ -76,6 +77,9 @@ def parse():
     p.add_argument("--route-flags", type=int, default=0,
                    help="moe_route_ex gate options: 1 renormalise the top-k gates, 2 bias for selection only")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--fused-gather", action="store_true",
+                   help="the forward's dispatch writes only the index maps and the gate/up GEMM gathers the rows "
+                        "of x itself (moe_expert_ffn_gather) instead of reading the rows dispatch wrote")
     return p.parse_args()
 
 
@@ -198,6 +202,8 @@ def algorithmic_bytes(shape, mode=None):
         "route": T * H * b + H * E * b + T * E * 4 + 2 * T * K * 4,
         # idx in; x in once; xs, dst_row, src_tok, cu out
         "dispatch": T * K * 4 + T * H * b + R * H * b + 2 * R * 4 + (E + 1) * 4,
+        # the same without the rows (the expert FFN gathers them): latency-bound
+        "dispatch_maps": T * K * 4 + 2 * R * 4 + (E + 1) * 4,
         # h, gate, dst_row in; y out (MoD: also the score and the residual rows)
         "combine": R * H * b + T * K * 4 + R * 4 + T * H * b + (T * (H * b + 8) if shape.mod_B else 0),
         # dy, h, dxs, gate, dst_row in; dh, dx, d_gate out
@@ -253,8 +259,11 @@ def build_inputs(shape, dev, rank, bias_np):
     return inp
 
 
-def make_step(shape, inp, dev, stream, route_flags=0):
-    """(call names, step(x, dy, dxs, marks) -> None, buffers, outputs for the host)."""
+def make_step(shape, inp, dev, stream, route_flags=0, fused=True):
+    """(call names, step(x, dy, dxs, marks) -> None, buffers, outputs for the host).
+    fused: the forward's dispatch writes only the index maps and the expert FFN
+    gathers the rows of x in its gate/up operand load (not for the training
+    step, whose expert backward reads the expert-sorted rows)."""
     import torch
     from token_dispatch_gb300 import _lib as L
     from token_dispatch_gb300 import layer
@@ -272,11 +281,15 @@ def make_step(shape, inp, dev, stream, route_flags=0):
             ("route", lambda xi, dyi, dxsi: L.moe_route_ex(xi, wr_d, bias_d, T, H, E, K, b.cdt, route_flags, b.logits,
                                                           b.idx, b.gate, b.ws_route, b.ws_route_bytes,
                                                           stream=stream)),
-            ("dispatch", lambda xi, dyi, dxsi: L.moe_dispatch(xi, b.idx, T, H, E, K, b.cdt, b.cu, b.dst_row,
-                                                             b.src_tok, b.xs, b.ws_dispatch, b.ws_dispatch_bytes,
-                                                             stream=stream)),
-            ("expert_ffn", lambda xi, dyi, dxsi: L.moe_expert_ffn(b.xs, b.cu, R, wg, wu, wd, E, H, Hp, b.cdt, b.act,
-                                                                 b.h, stream=stream)),
+            ("dispatch_maps" if fused else "dispatch",
+             lambda xi, dyi, dxsi: L.moe_dispatch(xi, b.idx, T, H, E, K, b.cdt, b.cu, b.dst_row, b.src_tok,
+                                                  None if fused else b.xs, b.ws_dispatch, b.ws_dispatch_bytes,
+                                                  stream=stream)),
+            ("expert_ffn", (lambda xi, dyi, dxsi: L.moe_expert_ffn_gather(xi, b.src_tok, T, b.cu, R, wg, wu, wd, E, H,
+                                                                         Hp, b.cdt, b.act, None, b.h, stream=stream))
+             if fused else
+             (lambda xi, dyi, dxsi: L.moe_expert_ffn(b.xs, b.cu, R, wg, wu, wd, E, H, Hp, b.cdt, b.act, b.h,
+                                                     stream=stream))),
             ("combine", lambda xi, dyi, dxsi: L.moe_combine(b.h, b.gate, b.dst_row, None, None, None, T, H, K, b.cdt,
                                                            b.y, stream=stream)),
         ]
@@ -325,11 +338,15 @@ def make_step(shape, inp, dev, stream, route_flags=0):
                                                          m.sel_score, m.mask, m.x_sel, m.y, stream=stream)),
         ("route", lambda xi, dyi, dxsi: L.moe_route(m.x_sel, wr_d, bias_d, T, H, E, K, b.cdt, b.logits, b.idx,
                                                    b.gate, b.ws_route, b.ws_route_bytes, stream=stream)),
-        ("dispatch", lambda xi, dyi, dxsi: L.moe_dispatch(m.x_sel, b.idx, T, H, E, K, b.cdt, b.cu, b.dst_row,
-                                                         b.src_tok, b.xs, b.ws_dispatch, b.ws_dispatch_bytes,
-                                                         stream=stream)),
-        ("expert_ffn", lambda xi, dyi, dxsi: L.moe_expert_ffn(b.xs, b.cu, R, wg, wu, wd, E, H, Hp, b.cdt, b.act,
-                                                             b.h, stream=stream)),
+        ("dispatch_maps" if fused else "dispatch",
+         lambda xi, dyi, dxsi: L.moe_dispatch(m.x_sel, b.idx, T, H, E, K, b.cdt, b.cu, b.dst_row, b.src_tok,
+                                              None if fused else b.xs, b.ws_dispatch, b.ws_dispatch_bytes,
+                                              stream=stream)),
+        ("expert_ffn", (lambda xi, dyi, dxsi: L.moe_expert_ffn_gather(m.x_sel, b.src_tok, T, b.cu, R, wg, wu, wd, E,
+                                                                     H, Hp, b.cdt, b.act, None, b.h, stream=stream))
+         if fused else
+         (lambda xi, dyi, dxsi: L.moe_expert_ffn(b.xs, b.cu, R, wg, wu, wd, E, H, Hp, b.cdt, b.act, b.h,
+                                                 stream=stream))),
         ("combine", lambda xi, dyi, dxsi: L.moe_combine(b.h, b.gate, b.dst_row, m.sel_score, xi, m.sel, T, H, K,
                                                        b.cdt, m.y, stream=stream)),
         ("permute_bwd", lambda xi, dyi, dxsi: L.moe_permute_bwd(dyi, b.h, b.gate, b.dst_row, m.sel_score, m.sel,
@@ -371,7 +388,8 @@ def run_ours(args, shape, rank, world, local):
     x_d = x_h.to(dev)
     dy_d, dxs_d = inp.get("dy"), inp.get("dxs")
     stream = torch.cuda.Stream(device=dev)
-    calls, bufs, outs, cu = make_step(shape, inp, dev, stream, args.route_flags)
+    fused = args.fused_gather and mode != "train"
+    calls, bufs, outs, cu = make_step(shape, inp, dev, stream, args.route_flags, fused)
     names = [n for n, _ in calls]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_rd = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -425,6 +443,25 @@ def run_ours(args, shape, rank, world, local):
                for j, n in enumerate(names)}
     ms = statistics.mean(step_ms)
     eager_ms = ms
+
+    if fused:
+        # the step's dispatch writes index maps only; the row-materialising
+        # dispatch (what a caller without the fused FFN runs) is timed on its
+        # own, on the step's routing, for its HBM roofline
+        b_moe = bufs.moe if hasattr(bufs, "moe") else bufs
+        d_in = bufs.x_sel if hasattr(bufs, "moe") else x_d
+        dev_ = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                for _ in range(args.steps)]
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                dev_[i][0].record(stream)
+                L.moe_dispatch(d_in, b_moe.idx, b_moe.T, b_moe.H, b_moe.E, b_moe.K, b_moe.cdt, b_moe.cu,
+                               b_moe.dst_row, b_moe.src_tok, b_moe.xs, b_moe.ws_dispatch, b_moe.ws_dispatch_bytes,
+                               stream=stream)
+                dev_[i][1].record(stream)
+                flush_l2()
+        torch.cuda.synchronize(dev)
+        call_ms["dispatch"] = statistics.mean(a.elapsed_time(c) for a, c in dev_)
 
     def capture(xi, dyi, dxsi):
         g = torch.cuda.CUDAGraph()
@@ -530,7 +567,7 @@ def run_ours(args, shape, rank, world, local):
     b_el = 2 if shape.dtype == "bf16" else 4
     # the pair's minimum DRAM bytes: every expert's three projections once, xs
     # read, the SwiGLU output written and read back, h written
-    ffn_bytes = 3 * E * H * Hp * b_el + R * H * b_el + 2 * R * Hp * b_el + R * H * b_el
+    ffn_bytes = 3 * E * H * Hp * b_el + (T if fused else R) * H * b_el + 2 * R * Hp * b_el + R * H * b_el
     if mode == "train":
         # forward also writes [g | u]; backward: 12 R H H' FLOP; reads dh, the
         # three projections, [g | u], act, xs; writes and reads back [dg | du];
@@ -565,7 +602,7 @@ def run_ours(args, shape, rank, world, local):
         roof = {"bound": "hbm", "achieved": ffn_bytes / ffn_s / 1e9, "peak": hbm_peak, "unit": "GB/s",
                 "peak_source": f"{peak_src} hbm_gbs"}
     roof["frac"] = roof["achieved"] / roof["peak"] if roof["peak"] else None
-    roof["traffic"] = None if mode == "train" else FFN_DRAM_BYTES.get(shape.name)
+    roof["traffic"] = None if mode == "train" else FFN_DRAM_BYTES.get((shape.name, fused))
     roof["algorithmic"] = {"flops": ffn_flops, "bytes": ffn_bytes}
     hbm = {}
     for name, nbytes in algorithmic_bytes(shape, mode).items():
@@ -590,10 +627,13 @@ def run_ours(args, shape, rank, world, local):
                    "Hp": Hp, "maxvio": round(maxvio, 4), "maxvio_target": target,
                    "expert0_logit_bias": None if bias_entry is None else bias_entry["beta"],
                    "l2": "flushed between timed steps (512 MB write, then 512 MB read)", "parallelism": f"replicas{world}",
-                   "route_flags": args.route_flags, "train": bool(args.train), "graph": bool(args.graph)},
+                   "route_flags": args.route_flags, "train": bool(args.train), "graph": bool(args.graph),
+                   "fused_gather": fused},
         "calls_ms": {k: round(v, 4) for k, v in call_ms.items()},
         "roofline": {"kernel": ("moe_expert_ffn + moe_expert_ffn_bwd (grouped tcgen05 GEMMs, forward and backward)"
                                 if mode == "train" else
+                                "moe_expert_ffn_gather (grouped gate/up+SwiGLU GEMM gathering the rows of x, "
+                                "+ down GEMM, tcgen05)" if fused else
                                 "moe_expert_ffn (grouped gate/up+SwiGLU GEMM + down GEMM, tcgen05)"), **roof},
         "hbm_roofline": {"peak_GB/s": hbm_peak, "peak_source": f"{peak_src} hbm_gbs", "calls": hbm},
         "e2e": {"value": whole_job_tokens_per_s(n_tok, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,

@@ -160,7 +160,9 @@ MOE_API int moe_route_ex(const void* x, const void* w_router, const float* logit
  *   dst_row[t*K+k] = row of pair (t,k);  src_tok[row] = t;  xs[row,:] = x[t,:].
  *
  *   x [T,H] dtype; topk_idx [T,K] int32 with distinct experts per token in [0,E)
- *   cu_seqlens [E+1], dst_row [T*K], src_tok [T*K] int32 out; xs [T*K,H] dtype out.
+ *   cu_seqlens [E+1], dst_row [T*K], src_tok [T*K] int32 out; xs [T*K,H] dtype out,
+ *   nullable: without xs only the index maps are written (x may then be NULL)
+ *   and moe_expert_ffn_gather reads the rows of x itself.
  *   An expert id outside [0,E) sets MOE_ERR_DEVICE_BOUNDS; its pair is dropped.
  *   Workspace: moe_workspace_bytes(MOE_OP_DISPATCH, T, 0, E, K, 0) bytes.
  */
@@ -212,6 +214,24 @@ MOE_API int moe_expert_ffn(const void* xs, const int32_t* cu_seqlens, int rows,
                    const void* w_gate, const void* w_up, const void* w_down,
                    int E, int H, int Hp, int dtype, void* act, void* h,
                    void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Grouped SwiGLU expert FFN with the dispatch gather fused into its input load
+ *                      [FW "What's in the box": dispatch reads the buffers
+ *                       directly; EP "Step-by-step": rows addressed by index]
+ *
+ *   moe_expert_ffn_ex with xs[r,:] = x[src_tok[r],:] read straight from x: the
+ *   gate/up GEMM's producer copies the rows of each 128-row tile from x by
+ *   src_tok (as written by moe_dispatch) into its operand stages, so the
+ *   expert-sorted copy of the input is never written or read.
+ *   x [T,H] dtype; src_tok [rows] int32 in [0,T) (an index outside sets
+ *   MOE_ERR_DEVICE_BOUNDS and reads row 0); the rest as moe_expert_ffn_ex.
+ *   Workspace: none.
+ */
+MOE_API int moe_expert_ffn_gather(const void* x, const int32_t* src_tok, int T, const int32_t* cu_seqlens,
+                                  int rows, const void* w_gate, const void* w_up, const void* w_down, int E,
+                                  int H, int Hp, int dtype, void* act, void* gu, void* h, void* ws,
+                                  size_t ws_bytes, void* stream);
 
 /*
  * Expert FFN forward that also keeps the SwiGLU pre-activations for the backward

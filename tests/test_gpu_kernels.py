@@ -269,6 +269,64 @@ def test_expert_ffn_matches_oracle(shape):
     assert_close(to64(h), h_ref, TOL[shape.dtype], "h")
 
 
+GATHER_SHAPES = [S("bf16_T1000_H384_E16_K4_Hp320", 1000, 384, 16, 4, 320, "bf16"),
+                 S("bf16_T777_H256_E64_K6_Hp192", 777, 256, 64, 6, 192, "bf16"),
+                 S("bf16_T3_H128_E8_K2_Hp64", 3, 128, 8, 2, 64, "bf16"),
+                 S("f32_T300_H64_E12_K3_Hp96", 300, 64, 12, 3, 96, "f32")]
+
+
+@pytest.mark.parametrize("shape", GATHER_SHAPES, ids=ids(GATHER_SHAPES))
+def test_expert_ffn_gather_equals_ffn_on_dispatched_rows(shape):
+    """The gate/up GEMM reading the rows of x by src_tok gives bit for bit what
+    the FFN gives on the expert-sorted rows dispatch writes (the same operands
+    in the same order), and matches the oracle; dispatch without xs writes the
+    same index maps.  Ragged experts and tiles (T not a multiple of 128, some
+    experts without rows for T=3)."""
+    x, wr, wg, wu, wd = host_layer_inputs(shape)
+    T, H, E, K, Hp, R = shape.T, shape.H, shape.E, shape.K, shape.Hp, shape.R
+    idx = O.topk_experts(O.router_logits(x.ref, wr.ref), K)
+    cu, dst, src, xs_ref = O.dispatch(x.ref, idx, E)
+    act_ref, h_ref = O.expert_ffn(xs_ref, cu, wg.ref, wu.ref, wd.ref)
+    b = layer.MoEBuffers(T, H, E, K, Hp, shape.dtype, DEV, backward=False)
+    xd, idx_d = dev(x), torch.from_numpy(idx).to(DEV)
+    L.moe_dispatch(xd, idx_d, T, H, E, K, CDT[shape.dtype], b.cu, b.dst_row, b.src_tok, b.xs, b.ws_dispatch,
+                   b.ws_dispatch_bytes)
+    act1 = torch.empty((R, Hp), dtype=TDT[shape.dtype], device=DEV)
+    h1 = torch.empty((R, H), dtype=TDT[shape.dtype], device=DEV)
+    L.moe_expert_ffn(b.xs, b.cu, R, dev(wg), dev(wu), dev(wd), E, H, Hp, CDT[shape.dtype], act1, h1)
+    cu2 = torch.full_like(b.cu, -9)
+    dst2 = torch.full_like(b.dst_row, -9)
+    src2 = torch.full_like(b.src_tok, -9)
+    L.moe_dispatch(None, idx_d, T, H, E, K, CDT[shape.dtype], cu2, dst2, src2, None, b.ws_dispatch,
+                   b.ws_dispatch_bytes)
+    act2 = torch.empty_like(act1)
+    h2 = torch.empty_like(h1)
+    L.moe_expert_ffn_gather(xd, src2, T, cu2, R, dev(wg), dev(wu), dev(wd), E, H, Hp, CDT[shape.dtype], act2, None,
+                            h2)
+    torch.cuda.synchronize()
+    assert L.moe_last_device_error() == L.MOE_OK
+    for a_, b_ in ((b.cu, cu2), (b.dst_row, dst2), (b.src_tok, src2)):
+        assert torch.equal(a_, b_)
+    assert torch.equal(act1, act2) and torch.equal(h1, h2)
+    assert_close(to64(act2), act_ref, TOL[shape.dtype], "act")
+    assert_close(to64(h2), h_ref, TOL[shape.dtype], "h")
+
+
+def test_expert_ffn_gather_out_of_range_row_sets_bounds_error():
+    shape = S("bf16_T40_H128_E8_K2_Hp64", 40, 128, 8, 2, 64, "bf16")
+    x, wr, wg, wu, wd = host_layer_inputs(shape)
+    T, H, E, K, Hp, R = shape.T, shape.H, shape.E, shape.K, shape.Hp, shape.R
+    cu = torch.from_numpy(np.array([0, R] + [R] * (E - 1), np.int32)).to(DEV)
+    src = torch.arange(R, dtype=torch.int32, device=DEV) % T
+    src[5] = T + 100
+    act = torch.empty((R, Hp), dtype=torch.bfloat16, device=DEV)
+    h = torch.empty((R, H), dtype=torch.bfloat16, device=DEV)
+    assert L.moe_last_device_error() == L.MOE_OK
+    L.moe_expert_ffn_gather(dev(x), src, T, cu, R, dev(wg), dev(wu), dev(wd), E, H, Hp, L.MOE_BF16, act, None, h)
+    assert L.moe_last_device_error() == L.MOE_ERR_DEVICE_BOUNDS
+    assert L.moe_last_device_error() == L.MOE_OK
+
+
 def test_expert_ffn_empty_and_single_row_experts():
     shape = S("bf16_sparse", 5, 128, 8, 1, 128, "bf16")
     x = synth.normal_stored(3, 1, (5, 128), 1.0, "bf16")
@@ -623,7 +681,7 @@ def test_outputs_are_deterministic():
         dxs = dev(synth.upstream_grad(shape, shape.R, shape.H, seed=2, stream=synth.S_DXS))
         layer.moe_backward(b, xd, wrd, dy, dxs)
         torch.cuda.synchronize()
-        outs.append([t.clone() for t in (b.logits, b.idx, b.dst_row, b.xs, b.h, b.y, b.dx, b.dw_router)])
+        outs.append([t.clone() for t in (b.logits, b.idx, b.dst_row, b.act, b.h, b.y, b.dx, b.dw_router)])
     for a, c in zip(*outs):
         assert torch.equal(a.view(torch.uint8) if a.dtype == torch.bfloat16 else a,
                            c.view(torch.uint8) if c.dtype == torch.bfloat16 else c)

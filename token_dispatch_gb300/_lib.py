@@ -43,7 +43,7 @@ MOE_ROUTE_BIAS_SELECT = 0x2
 EXPORTS = ("moe_status_str", "moe_version", "moe_kernel_launches", "moe_workspace_bytes", "moe_last_device_error",
            "moe_check_wait_timeout",
            "moe_route", "moe_route_ex", "moe_dispatch", "moe_dispatch_noalloc", "moe_expert_ffn",
-           "moe_expert_ffn_ex", "moe_expert_ffn_bwd", "moe_combine", "moe_route_bwd",
+           "moe_expert_ffn_ex", "moe_expert_ffn_gather", "moe_expert_ffn_bwd", "moe_combine", "moe_route_bwd",
            "moe_permute_bwd", "mod_select", "moe_ep_plan")
 
 
@@ -72,6 +72,7 @@ _SIGS = {
     "moe_dispatch_noalloc": (_I, [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P]),
     "moe_expert_ffn": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _Z, _P]),
     "moe_expert_ffn_ex": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
+    "moe_expert_ffn_gather": (_I, [_P, _P, _I, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
     "moe_expert_ffn_bwd": (_I, [_P, _P, _I, _P, _P, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _Z, _P]),
     "moe_combine": (_I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _P, _P]),
     "moe_route_bwd": (_I, [_I, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _Z, _P]),
@@ -185,6 +186,13 @@ def moe_expert_ffn_ex(xs, cu_seqlens, rows, w_gate, w_up, w_down, E, H, Hp, dtyp
     _check("moe_expert_ffn_ex", lib().moe_expert_ffn_ex(_ptr(xs), _ptr(cu_seqlens), rows, _ptr(w_gate), _ptr(w_up),
                                                         _ptr(w_down), E, H, Hp, dtype, _ptr(act), _ptr(gu), _ptr(h),
                                                         _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def moe_expert_ffn_gather(x, src_tok, T, cu_seqlens, rows, w_gate, w_up, w_down, E, H, Hp, dtype, act, gu, h,
+                          ws=None, ws_bytes=0, stream=None):
+    _check("moe_expert_ffn_gather", lib().moe_expert_ffn_gather(
+        _ptr(x), _ptr(src_tok), T, _ptr(cu_seqlens), rows, _ptr(w_gate), _ptr(w_up), _ptr(w_down), E, H, Hp, dtype,
+        _ptr(act), _ptr(gu), _ptr(h), _ptr(ws), ws_bytes, _stream(stream)))
 
 
 def moe_expert_ffn_bwd(xs, cu_seqlens, rows, w_gate, w_up, w_down, E, H, Hp, dtype, gu, act, dh, dxs,

@@ -380,6 +380,7 @@ int launch_dispatch(const void* x, const int32_t* idx, int T, int H, int E, int 
   dispatch_place_kernel<<<C, CH_THREADS, 0, s>>>(idx, T, E, K, counts, C, scanned ? tot : nullptr, cu, dst_row,
                                                   src_tok);
   if ((st = launch_status()) != MOE_OK) return st;
+  if (!xs) return MOE_OK;  // index maps only: the rows are gathered by the expert FFN's operand load
   const int vec = H * (dtype == MOE_BF16 ? 2 : 4) / 16;
   const uint4* xv = static_cast<const uint4*>(x);
   uint4* xsv = static_cast<uint4*>(xs);

@@ -9,7 +9,8 @@
 namespace moe {
 
 int launch_expert_ffn_tc(const void* xs, const int32_t* cu, int rows, const void* wg, const void* wu,
-                         const void* wd, int E, int H, int Hp, void* act, void* gu, void* h, cudaStream_t s);
+                         const void* wd, int E, int H, int Hp, void* act, void* gu, void* h, cudaStream_t s,
+                         const int32_t* gather, int gather_n);
 int launch_expert_ffn_bwd_tc(const void* xs, const int32_t* cu, int rows, const void* wg, const void* wu,
                              const void* wd, int E, int H, int Hp, const void* gu, const void* act, const void* dh,
                              void* dgu, void* dxs, float* dwg, float* dwu, float* dwd, cudaStream_t s);
@@ -18,12 +19,14 @@ int launch_expert_ffn_bwd_tc(const void* xs, const int32_t* cu, int rows, const 
 // is out of reach of the tf32 tensor-core path).
 int launch_expert_ffn(const void* xs, const int32_t* cu, int rows, const void* wg, const void* wu,
                       const void* wd, int E, int H, int Hp, int dtype, void* act, void* gu, void* h,
-                      cudaStream_t s) {
+                      cudaStream_t s, const int32_t* gather, int gather_n) {
   if (rows == 0) return MOE_OK;
-  if (dtype == MOE_BF16) return launch_expert_ffn_tc(xs, cu, rows, wg, wu, wd, E, H, Hp, act, gu, h, s);
+  if (dtype == MOE_BF16)
+    return launch_expert_ffn_tc(xs, cu, rows, wg, wu, wd, E, H, Hp, act, gu, h, s, gather, gather_n);
   // act = silu(xs . Wg[e]) * (xs . Wu[e])
   SimtGemmArgs a{};
   a.A = xs; a.a_sm = H; a.a_sk = 1;
+  a.a_rows = gather;
   a.B = wg; a.B2 = wu; a.b_sg = (long long)H * Hp; a.b_sk = Hp; a.b_sn = 1;
   a.C = act; a.c_sm = Hp;
   a.cu = cu; a.M = rows; a.N = Hp; a.K = H; a.groups = E;

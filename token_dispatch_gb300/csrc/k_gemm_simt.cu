@@ -46,7 +46,10 @@ __global__ void __launch_bounds__(NT) simt_gemm_kernel(SimtGemmArgs a) {
       long long gm = m0 + m;
       int gk = k0 + k;
       float v = 0.f;
-      if (gm < row_hi && gk < a.K) v = to_f32(A[gm * a.a_sm + (long long)gk * a.a_sk]);
+      if (gm < row_hi && gk < a.K) {
+        const long long am = a.a_rows ? (long long)__ldg(a.a_rows + gm) : gm;
+        v = to_f32(A[am * a.a_sm + (long long)gk * a.a_sk]);
+      }
       As[k][m] = v;
     }
 #pragma unroll

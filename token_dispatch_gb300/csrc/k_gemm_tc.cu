@@ -83,6 +83,12 @@ struct Params {
   // grouped K: group g reduces over rows [cu[g], cu[g+1]) of K (M, N fixed)
   int gk = 0;
   int b_col_off = 0;  // added to the N coordinate of MN-major B loads
+  // K-major A rows gathered from another matrix: row r of A is row gather[r]
+  // of the source [gather_n, K] (bf16) that tmA maps with a 64 x 1 box; the
+  // producer warp loads them with four-row TMA gathers (the dispatch gather
+  // fused into the operand load)
+  const int32_t* gather = nullptr;
+  int gather_n = 0;
 };
 
 // Waits for copies and MMAs already in flight when a role stops always use
@@ -144,6 +150,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+// Four rows of a 2D map (box: 64 columns x 1 row) into four consecutive
+// 128-byte rows of shared memory, swizzled like a 4-row box
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int r0,
+                                            int r1, int r2, int r3) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
       : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
@@ -270,6 +285,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = p.G;
+  // A rows gathered by the producer warp (the gate/up GEMM only)
+  constexpr bool CAN_GATHER = EPI == EPI_SWIGLU && NA == 1 && NB == 1 && KSUB == 1 && !A_MN;
+  const bool gathered = CAN_GATHER && p.gather != nullptr;
   const int n_tiles = (p.N + C::OUT_BN - 1) / C::OUT_BN;
 
   auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
@@ -393,7 +411,65 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     return w;
   };
 
-  if (warp == 0) {
+  if (warp == 0 && gathered) {
+    // ------------------------------------------------ producer, gathered A
+    // Lane 0 waits for free stages, sets the stage's byte count and loads B;
+    // lane l gathers rows 4l .. 4l+3 of the A tile with one four-row TMA
+    // gather (a 64-column, one-row box of the source rows, swizzled as a
+    // 4-row box).  Rows past the matrix read row 0 (their outputs are masked).
+    int stage = 0;
+    uint32_t phase = 0;
+    int filled_parity[STAGES];
+    for (int s = 0; s < STAGES; ++s) filled_parity[s] = -1;
+    bool ok = true;
+    for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+      const Work wk = work(t);
+      const TileInfo& ti = wk.ti;
+      int src[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int r = ti.row0 + 4 * lane + i;
+        int v = r < p.M ? __ldg(p.gather + r) : 0;
+        if (v < 0 || v >= p.gather_n) {
+          set_error(p.err, DEV_BOUNDS);
+          v = 0;
+        }
+        src[i] = v;
+      }
+      for (int kb = wk.kb_begin; kb < wk.kb_end; ++kb) {
+        if (lane == 0) ok = wait_bounded(empty_bar(stage), phase ^ 1u, &abort_flag, p);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        const uint32_t a_dst = smem_u32(stage_base + stage * C::STAGE_BYTES);
+        const uint32_t b_dst = a_dst + A_STAGE_BYTES;
+        const int k0 = kb * BK;
+        if (lane == 0) {
+          mbar_expect_tx(full_bar(stage), C::STAGE_BYTES);
+          filled_parity[stage] = (int)phase;
+#pragma unroll
+          for (int c = 0; c < BN / 64; ++c) {
+            const CUtensorMap* m = (c < BN / 128) ? &tmB : &tmB2;
+            const int col = ti.n0 + (c % (BN / 128)) * 64;
+            tma_load_3d(b_dst + c * (64 * BK * 2), m, full_bar(stage), col, k0, ti.g);
+          }
+        }
+        __syncwarp();  // the byte count is set before any gather can complete
+        tma_gather4(a_dst + lane * (4 * BK * 2), &tmA, full_bar(stage), k0, src[0], src[1], src[2], src[3]);
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    // drain: every stage this warp filled must have landed before exit
+    if (lane == 0) {
+      for (int s = 0; s < STAGES; ++s) {
+        if (filled_parity[s] < 0) continue;
+        const long long t0 = clock64();
+        while (!mbar_try_wait(full_bar(s), (uint32_t)filled_parity[s])) {
+          if ((unsigned long long)(clock64() - t0) > DRAIN_LIMIT) { set_error(p.err, DEV_TIMEOUT); break; }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int stage = 0;
@@ -875,11 +951,19 @@ Params params(const int32_t* cu, int G, int M, int N, int K, void* out, long lon
 
 // act = silu(xs Wg[e]) * (xs Wu[e]);  h = act Wd[e]^T   (bf16, grouped by cu)
 int launch_expert_ffn_tc(const void* xs, const int32_t* cu, int rows, const void* wg, const void* wu,
-                         const void* wd, int E, int H, int Hp, void* act, void* gu, void* h, cudaStream_t s) {
+                         const void* wd, int E, int H, int Hp, void* act, void* gu, void* h, cudaStream_t s,
+                         const int32_t* gather, int gather_n) {
   using namespace tc;
   if (E > 1024) return MOE_ERR_UNSUPPORTED;
   CUtensorMap mA, mG, mU, mA2, mD;
-  if (!map_2d_as_3d(&mA, xs, H, rows, BK, BM)) return MOE_ERR_CUDA;
+  if (gather) {  // the source rows, one-row boxes for the four-row gathers
+    cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)gather_n};
+    cuuint64_t str[1] = {(cuuint64_t)H * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, 1};
+    if (!make_map(&mA, xs, 2, dims, str, box)) return MOE_ERR_CUDA;
+  } else if (!map_2d_as_3d(&mA, xs, H, rows, BK, BM)) {
+    return MOE_ERR_CUDA;
+  }
   if (!map_3d(&mG, wg, Hp, H, E, 64, BK)) return MOE_ERR_CUDA;
   if (!map_3d(&mU, wu, Hp, H, E, 64, BK)) return MOE_ERR_CUDA;
   if (!map_2d_as_3d(&mA2, act, Hp, rows, BK, BM)) return MOE_ERR_CUDA;
@@ -888,6 +972,8 @@ int launch_expert_ffn_tc(const void* xs, const int32_t* cu, int rows, const void
   Params p1 = params(cu, E, rows, Hp, H, act, Hp, nullptr);
   p1.aux = gu;  // nullable: g and u kept for the backward
   p1.ld_aux = 2LL * Hp;
+  p1.gather = gather;
+  p1.gather_n = gather_n;
   int st = launch<EPI_SWIGLU, false, true, 256, 4, 1, 1>(mA, mG, mU, p1, mtiles * ((Hp + 127) / 128), s);
   if (st != MOE_OK) return st;
   Params p2 = params(cu, E, rows, H, Hp, h, H, nullptr);

@@ -136,7 +136,7 @@ int moe_dispatch(const void* x, const int32_t* topk_idx, int T, int H, int E, in
   if (!valid_dtype(dtype) || T < 0 || H < 1 || E < 1 || E > 1024 || K < 1 || K > E || K > 16)
     return MOE_ERR_INVALID_ARG;
   if ((long long)T * K > 0x7fffffffll) return MOE_ERR_UNSUPPORTED;
-  if (!cu_seqlens || (T > 0 && (!x || !topk_idx || !dst_row || !src_tok || !xs)))
+  if (!cu_seqlens || (T > 0 && (!topk_idx || !dst_row || !src_tok || (xs && !x))))
     return MOE_ERR_INVALID_ARG;
   if (!all_aligned({x, topk_idx, cu_seqlens, dst_row, src_tok, xs, ws})) return MOE_ERR_MISALIGNED;
   if (H % vec_elems(dtype) != 0) return MOE_ERR_UNSUPPORTED;
@@ -151,7 +151,7 @@ int moe_dispatch_noalloc(const void* x, const int32_t* topk_idx, int T, int H, i
   if (!valid_dtype(dtype) || T < 0 || H < 1 || E < 1 || E > 1024 || K < 1 || K > E || K > 16)
     return MOE_ERR_INVALID_ARG;
   if ((long long)T * K > 0x7fffffffll) return MOE_ERR_UNSUPPORTED;
-  if (!cu_seqlens || (T > 0 && (!x || !topk_idx || !dst_row || !src_tok || !xs)))
+  if (!cu_seqlens || (T > 0 && (!topk_idx || !dst_row || !src_tok || (xs && !x))))
     return MOE_ERR_INVALID_ARG;
   if (!all_aligned({x, topk_idx, cu_seqlens, dst_row, src_tok, xs})) return MOE_ERR_MISALIGNED;
   if (H % vec_elems(dtype) != 0) return MOE_ERR_UNSUPPORTED;
@@ -181,6 +181,20 @@ int moe_expert_ffn_ex(const void* xs, const int32_t* cu_seqlens, int rows, const
   if (gu && dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   return launch_expert_ffn(xs, cu_seqlens, rows, w_gate, w_up, w_down, E, H, Hp, dtype, act, gu, h,
                            as_stream(stream));
+}
+
+int moe_expert_ffn_gather(const void* x, const int32_t* src_tok, int T, const int32_t* cu_seqlens, int rows,
+                          const void* w_gate, const void* w_up, const void* w_down, int E, int H, int Hp, int dtype,
+                          void* act, void* gu, void* h, void* ws, size_t ws_bytes, void* stream) {
+  (void)ws; (void)ws_bytes;
+  if (T < 0) return MOE_ERR_INVALID_ARG;
+  int st = check_expert_ffn(x, cu_seqlens, rows, w_gate, w_up, w_down, E, H, Hp, dtype);
+  if (st != MOE_OK) return st;
+  if (rows > 0 && (!act || !h || !src_tok || T < 1)) return MOE_ERR_INVALID_ARG;
+  if (!all_aligned({act, gu, h, src_tok})) return MOE_ERR_MISALIGNED;
+  if (gu && dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  return launch_expert_ffn(x, cu_seqlens, rows, w_gate, w_up, w_down, E, H, Hp, dtype, act, gu, h,
+                           as_stream(stream), src_tok, T);
 }
 
 int moe_expert_ffn(const void* xs, const int32_t* cu_seqlens, int rows, const void* w_gate,

@@ -155,9 +155,11 @@ int launch_permute_bwd(const void* dy, const void* h, const float* gate, const i
                        cudaStream_t s);
 
 // expert FFN
+// gather (nullable): row r of the FFN input is row gather[r] of xs [gather_n, H]
+// (the dispatch gather fused into the gate/up operand load)
 int launch_expert_ffn(const void* xs, const int32_t* cu, int rows, const void* wg, const void* wu,
                       const void* wd, int E, int H, int Hp, int dtype, void* act, void* gu, void* h,
-                      cudaStream_t s);
+                      cudaStream_t s, const int32_t* gather = nullptr, int gather_n = 0);
 int launch_expert_ffn_bwd(const void* xs, const int32_t* cu, int rows, const void* wg, const void* wu,
                           const void* wd, int E, int H, int Hp, const void* gu, const void* act, const void* dh,
                           void* dxs, float* dwg, float* dwu, float* dwd, void* ws, cudaStream_t s);
@@ -185,6 +187,7 @@ struct SimtGemmArgs {
   int M, N, K, groups;
   int epilogue;
   bool swiglu;
+  const int32_t* a_rows = nullptr;  // when set, row m of A is row a_rows[m] of the A matrix
 };
 int launch_simt_gemm(const SimtGemmArgs& a, int in_dtype_a, int in_dtype_b, int out_dtype,
                      cudaStream_t s);

@@ -5,6 +5,8 @@ the layer runs in libmoe's kernels.  Nothing here synchronises the host with the
 device: the row split per expert stays on the device (cu_seqlens).
 
     MoE forward:  moe_route -> moe_dispatch -> moe_expert_ffn -> moe_combine
+                  (or moe_dispatch writing index maps only -> moe_expert_ffn_gather,
+                  whose gate/up GEMM reads the rows of x itself)
     backward:     moe_permute_bwd (dh, d_gate, dx from dxs) -> moe_route_bwd
     MoD front:    mod_select (scores, capacity top-C, gather, skip copy) -> MoE on the
                   selected tokens -> moe_combine(row_scale = score, residual = x,
@@ -69,15 +71,27 @@ class MoEBuffers:
 
 
 def moe_forward(b: MoEBuffers, x, w_router, logit_bias, w_gate, w_up, w_down, stream=None,
-                row_scale=None, residual=None, out_row=None, y=None, route_flags=0):
+                row_scale=None, residual=None, out_row=None, y=None, route_flags=0, fused_gather=None):
     """One MoE forward pass into the buffers of ``b`` (y defaults to ``b.y``);
-    ``route_flags``: MOE_ROUTE_RENORM / MOE_ROUTE_BIAS_SELECT gate options."""
+    ``route_flags``: MOE_ROUTE_RENORM / MOE_ROUTE_BIAS_SELECT gate options.
+    ``fused_gather``: dispatch writes only the index maps and the expert FFN
+    reads the rows of x itself (moe_expert_ffn_gather); off by default (the
+    row-by-row operand fetch measured slower than the gather kernel plus the
+    FFN on the dispatched rows), and never with train=True buffers (the expert
+    backward reads the dispatched rows)."""
     T, H, E, K, Hp, dt = b.T, b.H, b.E, b.K, b.Hp, b.cdt
+    if fused_gather is None or b.gu is not None:
+        fused_gather = False
     L.moe_route_ex(x, w_router, logit_bias, T, H, E, K, dt, route_flags, b.logits, b.idx, b.gate, b.ws_route,
                    b.ws_route_bytes, stream=stream)
-    L.moe_dispatch(x, b.idx, T, H, E, K, dt, b.cu, b.dst_row, b.src_tok, b.xs, b.ws_dispatch,
-                   b.ws_dispatch_bytes, stream=stream)
-    L.moe_expert_ffn_ex(b.xs, b.cu, T * K, w_gate, w_up, w_down, E, H, Hp, dt, b.act, b.gu, b.h, stream=stream)
+    L.moe_dispatch(x, b.idx, T, H, E, K, dt, b.cu, b.dst_row, b.src_tok, None if fused_gather else b.xs,
+                   b.ws_dispatch, b.ws_dispatch_bytes, stream=stream)
+    if fused_gather:
+        L.moe_expert_ffn_gather(x, b.src_tok, T, b.cu, T * K, w_gate, w_up, w_down, E, H, Hp, dt, b.act, b.gu, b.h,
+                                stream=stream)
+    else:
+        L.moe_expert_ffn_ex(b.xs, b.cu, T * K, w_gate, w_up, w_down, E, H, Hp, dt, b.act, b.gu, b.h,
+                            stream=stream)
     L.moe_combine(b.h, b.gate, b.dst_row, row_scale, residual, out_row, T, H, K, dt,
                   b.y if y is None else y, stream=stream)
 
