@@ -220,10 +220,11 @@ MOE_API int moe_expert_ffn(const void* xs, const int32_t* cu_seqlens, int rows,
  *                      [FW "What's in the box": dispatch reads the buffers
  *                       directly; EP "Step-by-step": rows addressed by index]
  *
- *   moe_expert_ffn_ex with xs[r,:] = x[src_tok[r],:] read straight from x: the
- *   gate/up GEMM's producer copies the rows of each 128-row tile from x by
- *   src_tok (as written by moe_dispatch) into its operand stages, so the
- *   expert-sorted copy of the input is never written or read.
+ *   moe_expert_ffn_ex with xs[r,:] = x[src_tok[r],:] read straight from x: in
+ *   the gate/up GEMM eight extra warps copy the rows of each 128-row tile from
+ *   x by src_tok (as written by moe_dispatch) into its operand stages, so the
+ *   expert-sorted copy of the input is never written or read.  The results
+ *   are bit-identical to moe_expert_ffn_ex on the rows moe_dispatch writes.
  *   x [T,H] dtype; src_tok [rows] int32 in [0,T) (an index outside sets
  *   MOE_ERR_DEVICE_BOUNDS and reads row 0); the rest as moe_expert_ffn_ex.
  *   Workspace: none.

@@ -49,6 +49,17 @@ namespace tc {
 constexpr int BM = 128;
 constexpr int BK = 64;            // 64 bf16 = 128 bytes: one swizzle row
 constexpr int NUM_THREADS = 192;  // 6 warps
+constexpr int GATHER_WARPS = 8;   // extra warps copying gathered A rows (the gate/up GEMM)
+
+// the gate/up GEMM can take its A rows gathered from another matrix
+template <int EPI, bool A_MN, int NA, int NB, int KSUB>
+__host__ __device__ constexpr bool can_gather() {
+  return EPI == 0 && NA == 1 && NB == 1 && KSUB == 1 && !A_MN;
+}
+template <int EPI, bool A_MN, int NA, int NB, int KSUB>
+__host__ __device__ constexpr int max_threads() {
+  return can_gather<EPI, A_MN, NA, NB, KSUB>() ? NUM_THREADS + 32 * GATHER_WARPS : NUM_THREADS;
+}
 constexpr int A_STAGE_BYTES = BM * BK * 2;
 
 // EPI_SWIGLU_BWD: the accumulator is da; with g, u read back from p.aux it
@@ -84,10 +95,11 @@ struct Params {
   int gk = 0;
   int b_col_off = 0;  // added to the N coordinate of MN-major B loads
   // K-major A rows gathered from another matrix: row r of A is row gather[r]
-  // of the source [gather_n, K] (bf16) that tmA maps with a 64 x 1 box; the
-  // producer warp loads them with four-row TMA gathers (the dispatch gather
+  // of gather_src [gather_n, K] (bf16), copied into the swizzled stages by
+  // four extra warps with 16-byte asynchronous copies (the dispatch gather
   // fused into the operand load)
   const int32_t* gather = nullptr;
+  const bf16* gather_src = nullptr;
   int gather_n = 0;
 };
 
@@ -150,15 +162,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
-      : "memory");
-}
-// Four rows of a 2D map (box: 64 columns x 1 row) into four consecutive
-// 128-byte rows of shared memory, swizzled like a 4-row box
-__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int r0,
-                                            int r1, int r2, int r3) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5, %6, %7}], [%2];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3)
       : "memory");
 }
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
@@ -264,7 +267,7 @@ __device__ __forceinline__ TileInfo decode(int t, const int* mt_pre, const int* 
 // slices of K (a stage covers 64*KSUB of K), so each row of a streamed operand
 // is requested as 128*KSUB contiguous bytes at once.
 template <int EPI, bool A_MN, bool B_MN, int BN, int STAGES, int NA, int NB, int KSUB = 1>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__((max_threads<EPI, A_MN, NA, NB, KSUB>()), 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmB2, const Params p) {
   using C = Cfg<BN, EPI, NA, NB>;
@@ -285,8 +288,8 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = p.G;
-  // A rows gathered by the producer warp (the gate/up GEMM only)
-  constexpr bool CAN_GATHER = EPI == EPI_SWIGLU && NA == 1 && NB == 1 && KSUB == 1 && !A_MN;
+  // A rows gathered by the extra warps (the gate/up GEMM only)
+  constexpr bool CAN_GATHER = can_gather<EPI, A_MN, NA, NB, KSUB>();
   const bool gathered = CAN_GATHER && p.gather != nullptr;
   const int n_tiles = (p.N + C::OUT_BN - 1) / C::OUT_BN;
 
@@ -299,7 +302,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), gathered ? 1 + 32 * GATHER_WARPS : 1);  // + a copy-completion arrival per gather lane
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -412,39 +415,21 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   };
 
   if (warp == 0 && gathered) {
-    // ------------------------------------------------ producer, gathered A
-    // Lane 0 waits for free stages, sets the stage's byte count and loads B;
-    // lane l gathers rows 4l .. 4l+3 of the A tile with one four-row TMA
-    // gather (a 64-column, one-row box of the source rows, swizzled as a
-    // 4-row box).  Rows past the matrix read row 0 (their outputs are masked).
-    int stage = 0;
-    uint32_t phase = 0;
-    int filled_parity[STAGES];
-    for (int s = 0; s < STAGES; ++s) filled_parity[s] = -1;
-    bool ok = true;
-    for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-      const Work wk = work(t);
-      const TileInfo& ti = wk.ti;
-      int src[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int r = ti.row0 + 4 * lane + i;
-        int v = r < p.M ? __ldg(p.gather + r) : 0;
-        if (v < 0 || v >= p.gather_n) {
-          set_error(p.err, DEV_BOUNDS);
-          v = 0;
-        }
-        src[i] = v;
-      }
-      for (int kb = wk.kb_begin; kb < wk.kb_end; ++kb) {
-        if (lane == 0) ok = wait_bounded(empty_bar(stage), phase ^ 1u, &abort_flag, p);
-        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        const uint32_t a_dst = smem_u32(stage_base + stage * C::STAGE_BYTES);
-        const uint32_t b_dst = a_dst + A_STAGE_BYTES;
-        const int k0 = kb * BK;
-        if (lane == 0) {
-          mbar_expect_tx(full_bar(stage), C::STAGE_BYTES);
+    // ------------------------------------------------ producer of B (A gathered)
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int filled_parity[STAGES];
+      for (int s = 0; s < STAGES; ++s) filled_parity[s] = -1;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+        const Work wk = work(t);
+        const TileInfo& ti = wk.ti;
+        for (int kb = wk.kb_begin; kb < wk.kb_end; ++kb) {
+          if (!wait_bounded(empty_bar(stage), phase ^ 1u, &abort_flag, p)) { ok = false; break; }
+          const uint32_t b_dst = smem_u32(stage_base + stage * C::STAGE_BYTES) + A_STAGE_BYTES;
+          const int k0 = kb * BK;
+          mbar_expect_tx(full_bar(stage), C::STAGE_BYTES - A_STAGE_BYTES);
           filled_parity[stage] = (int)phase;
 #pragma unroll
           for (int c = 0; c < BN / 64; ++c) {
@@ -452,14 +437,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int col = ti.n0 + (c % (BN / 128)) * 64;
             tma_load_3d(b_dst + c * (64 * BK * 2), m, full_bar(stage), col, k0, ti.g);
           }
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
-        __syncwarp();  // the byte count is set before any gather can complete
-        tma_gather4(a_dst + lane * (4 * BK * 2), &tmA, full_bar(stage), k0, src[0], src[1], src[2], src[3]);
-        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
-    }
-    // drain: every stage this warp filled must have landed before exit
-    if (lane == 0) {
+      // drain: every stage filled must have landed (B and the gathered A rows)
       for (int s = 0; s < STAGES; ++s) {
         if (filled_parity[s] < 0) continue;
         const long long t0 = clock64();
@@ -468,7 +449,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
       }
     }
-    __syncwarp();
   } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -552,6 +532,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int kb = kb_begin; kb < kb_end; ++kb) {
           if (!wait_bounded(full_bar(stage), phase, &abort_flag, p)) { ok = false; break; }
           tc_fence_after();
+          // gathered A rows were written by the generic proxy (asynchronous
+          // copies): make them visible to the MMA's reads
+          if (gathered) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           const uint32_t a_addr = smem_u32(stage_base + stage * C::STAGE_BYTES);
           const uint32_t b_addr = a_addr + NA * A_STAGE_BYTES;
           if (A_MN && kb == kb_end - 1 && wk.last_valid < BK) {
@@ -598,6 +581,51 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if ((unsigned long long)(clock64() - t0) > DRAIN_LIMIT) { set_error(p.err, DEV_TIMEOUT); break; }
         }
       }
+    }
+  } else if (warp >= NUM_THREADS / 32) {
+    // ------------------------------------------------ gathered A rows
+    // Warp 6 + w copies rows RW*w .. RW*w + RW-1 of every A tile (RW = 128 /
+    // GATHER_WARPS): instruction j takes 4 rows, 8 lanes per row, one 16-byte
+    // chunk each (whole 128-byte row segments), to the chunk's
+    // 128-byte-swizzled place.  Rows past the matrix read row 0 (their outputs
+    // are masked).
+    if (gathered) {
+      constexpr int RW = BM / GATHER_WARPS;
+      const int gw = warp - NUM_THREADS / 32;
+      const int crow = lane >> 3, chunk = lane & 7;
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
+        const Work wk = work(t);
+        const TileInfo& ti = wk.ti;
+        const int r_own = ti.row0 + RW * gw + (lane % RW);
+        int src = r_own < p.M ? __ldg(p.gather + r_own) : 0;
+        if (src < 0 || src >= p.gather_n) {
+          set_error(p.err, DEV_BOUNDS);
+          src = 0;
+        }
+        for (int kb = wk.kb_begin; kb < wk.kb_end; ++kb) {
+          if (lane == 0) ok = wait_bounded(empty_bar(stage), phase ^ 1u, &abort_flag, p);
+          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+          if (!ok) break;
+          const uint32_t a_dst = smem_u32(stage_base + stage * C::STAGE_BYTES);
+          const int k0 = kb * BK;
+#pragma unroll
+          for (int j = 0; j < RW / 4; ++j) {
+            const int rr = 4 * j + crow;  // row inside this warp's RW
+            const int r = RW * gw + rr;   // row inside the tile
+            const int srow = __shfl_sync(0xffffffffu, src, rr);
+            const bf16* g = p.gather_src + (long long)srow * p.K + k0 + chunk * 8;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(a_dst + r * 128 + ((chunk ^ (r & 7)) << 4)),
+                         "l"(g)
+                         : "memory");
+          }
+          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(full_bar(stage)) : "memory");
+          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      asm volatile("cp.async.wait_all;" ::: "memory");
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -922,7 +950,9 @@ int launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, co
   long long grid = sm_count();
   if (tiles_upper < grid) grid = tiles_upper;
   if (grid < 1) return MOE_OK;
-  k<<<(unsigned)grid, NUM_THREADS, smem, s>>>(a, b, b2, p);
+  const int threads = (can_gather<EPI, A_MN, NA, NB, KSUB>() && p.gather) ? NUM_THREADS + 32 * GATHER_WARPS
+                                                                           : NUM_THREADS;
+  k<<<(unsigned)grid, threads, smem, s>>>(a, b, b2, p);
   return launch_status();
 }
 
@@ -956,14 +986,8 @@ int launch_expert_ffn_tc(const void* xs, const int32_t* cu, int rows, const void
   using namespace tc;
   if (E > 1024) return MOE_ERR_UNSUPPORTED;
   CUtensorMap mA, mG, mU, mA2, mD;
-  if (gather) {  // the source rows, one-row boxes for the four-row gathers
-    cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)gather_n};
-    cuuint64_t str[1] = {(cuuint64_t)H * 2};
-    cuuint32_t box[2] = {(cuuint32_t)BK, 1};
-    if (!make_map(&mA, xs, 2, dims, str, box)) return MOE_ERR_CUDA;
-  } else if (!map_2d_as_3d(&mA, xs, H, rows, BK, BM)) {
-    return MOE_ERR_CUDA;
-  }
+  // gathered rows: the A map is not read (the gather warps copy rows themselves)
+  if (!map_2d_as_3d(&mA, xs, H, gather ? gather_n : rows, BK, BM)) return MOE_ERR_CUDA;
   if (!map_3d(&mG, wg, Hp, H, E, 64, BK)) return MOE_ERR_CUDA;
   if (!map_3d(&mU, wu, Hp, H, E, 64, BK)) return MOE_ERR_CUDA;
   if (!map_2d_as_3d(&mA2, act, Hp, rows, BK, BM)) return MOE_ERR_CUDA;
@@ -973,6 +997,7 @@ int launch_expert_ffn_tc(const void* xs, const int32_t* cu, int rows, const void
   p1.aux = gu;  // nullable: g and u kept for the backward
   p1.ld_aux = 2LL * Hp;
   p1.gather = gather;
+  p1.gather_src = static_cast<const bf16*>(xs);
   p1.gather_n = gather_n;
   int st = launch<EPI_SWIGLU, false, true, 256, 4, 1, 1>(mA, mG, mU, p1, mtiles * ((Hp + 127) / 128), s);
   if (st != MOE_OK) return st;
