@@ -50,9 +50,13 @@ L2_FLUSH_BYTES = 512 << 20  # > 129 MB L2
 # moe_expert_ffn call, both GEMM launches, from one ncu capture per workload of
 # the kernels as they stand; a workload without a capture reports null
 FFN_DRAM_BYTES = {
-    # (workload, rows gathered by the FFN): bytes
-    # Mixtral-shaped layer, T=8192, rows read from xs: 2.472 GB (gate/up) + 2.355 GB (down)
-    ("mixtral_bf16_T8192_H4096_E8_K2_Hp14336", False): 4826546944,
+    # (workload, rows gathered by the FFN): DRAM bytes read + written by the
+    # gate/up and down GEMMs of one moe_expert_ffn call (ncu dram__bytes_read.sum
+    # + dram__bytes_write.sum of the two kernels, one launch each, full size)
+    ("mixtral_bf16_T8192_H4096_E8_K2_Hp14336", False): 2013782272 + 456965376 + 2228715008 + 125932800,
+    ("finegrained_bf16_T16384_H2048_E64_K6_Hp1408", False): 1140968960 + 260407808 + 646142976 + 368247296,
+    ("epbench_bf16_T8192_H7168_E384_K8_Hp2048", False): 23813588736 + 269010944 + 11565326592 + 929113856,
+    ("mod_bf16_B4_L2048_C1024_H2048_E16_K2_Hp5632", False): 771887872 + 81952768 + 486998784 + 25858816,
 }
 DEFAULT_WORKLOAD = "mixtral_bf16_T8192_H4096_E8_K2_Hp14336"
 
