@@ -184,6 +184,13 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
 }
 
 // 32 lanes x 32 consecutive 32-bit columns
+// Order-preserving integer key of a float: a > b iff key(a) > key(b); -0 and
+// +0 give the same key.  Keys of real values are >= 0x007fffff (that of -inf).
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = __float_as_uint(f == 0.f ? 0.f : f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
   asm volatile(
@@ -232,7 +239,7 @@ struct Cfg {
   // bf16 epilogue: per warp a [32 rows][33] fp32 staging tile, so the global
   // stores (and the reads of the old values) go out row-contiguous
   static constexpr int STG_LD = 33;
-  static constexpr int EPI_BYTES = (EPI == EPI_BF16 || EPI == EPI_F32_GK) ? 4 * 32 * STG_LD * 4 : 0;
+  static constexpr int EPI_BYTES = (EPI == EPI_BF16 || EPI == EPI_F32_GK || EPI == EPI_ROUTER) ? 4 * 32 * STG_LD * 4 : 0;
 };
 
 struct TileInfo {
@@ -812,52 +819,114 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
       } else if (EPI == EPI_ROUTER) {
         // one thread = one token: its BN logits (E valid) come out of TMEM, get
-        // the bias, are stored, and the softmax / top-k are taken in registers
-        // (value descending, lowest expert first on ties)
+        // the bias and are stored; the softmax and the top-k (value descending,
+        // lowest expert first on ties) run in registers as balanced trees, so
+        // every level is BN/2^l independent operations instead of one chain
+        // of BN dependent ones
         float v[BN];
 #pragma unroll
         for (int c = 0; c < BN / 32; ++c) tmem_ld32(tbase + c * 32, *reinterpret_cast<float(*)[32]>(v + c * 32));
-        if (row_ok) {
-          float* out = static_cast<float*>(p.out) + grow * p.ldo;
+        if (p.bias) {
 #pragma unroll
           for (int j = 0; j < BN; j += 4) {
             if (j < p.N) {
-              if (p.bias) {
-                const float4 bb = __ldg(reinterpret_cast<const float4*>(p.bias + j));
-                v[j] += bb.x; v[j + 1] += bb.y; v[j + 2] += bb.z; v[j + 3] += bb.w;
-              }
-              *reinterpret_cast<float4*>(out + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+              const float4 bb = __ldg(reinterpret_cast<const float4*>(p.bias + j));
+              v[j] += bb.x; v[j + 1] += bb.y; v[j + 2] += bb.z; v[j + 3] += bb.w;
             }
           }
-          float m = -INFINITY;
+        }
+        {
+          // logits through this warp's staging tile, 32 columns at a time: each
+          // store instruction writes 4 rows x 128 contiguous bytes (a row per
+          // thread would touch 32 lines per instruction)
+          float* out = static_cast<float*>(p.out);
+          float* stg = epi_stage + q * 32 * C::STG_LD;
+          const int seg = (lane & 7) * 4;
 #pragma unroll
-          for (int j = 0; j < BN; ++j) if (j < p.N) m = fmaxf(m, v[j]);
-          float sum = 0.f;
+          for (int c = 0; c < BN / 32; ++c) {
 #pragma unroll
-          for (int j = 0; j < BN; ++j) if (j < p.N) sum += expf(v[j] - m);
-          // selection values: the logits, plus the selection-only bias when given
-          float sv[BN];
+            for (int j = 0; j < 32; ++j) stg[lane * C::STG_LD + j] = v[c * 32 + j];
+            __syncwarp();
+#pragma unroll
+            for (int ps = 0; ps < 8; ++ps) {
+              const int rw = ps * 4 + (lane >> 3);
+              const int rr = q * 32 + rw;
+              const long long gr = (long long)ti.row0 + rr;
+              const int col = c * 32 + seg;
+              if (rr < ti.rows && gr < p.M && col < p.N) {
+                const float* sp = stg + rw * C::STG_LD + seg;
+                *reinterpret_cast<float4*>(out + gr * p.ldo + col) = make_float4(sp[0], sp[1], sp[2], sp[3]);
+              }
+            }
+            __syncwarp();
+          }
+        }
+        if (row_ok) {
+          // selection keys: the logits (plus the selection-only bias when
+          // given) as order-preserving integers, -0 folded onto +0 (equal
+          // values are equal keys); 0 marks a column past E or an expert
+          // already chosen (every real value has a larger key)
+          uint32_t key[BN];
 #pragma unroll
           for (int j = 0; j < BN; j += 4) {
-            sv[j] = v[j]; sv[j + 1] = v[j + 1]; sv[j + 2] = v[j + 2]; sv[j + 3] = v[j + 3];
-            if (p.sel_bias && j < p.N) {
-              const float4 bb = __ldg(reinterpret_cast<const float4*>(p.sel_bias + j));
-              sv[j] += bb.x; sv[j + 1] += bb.y; sv[j + 2] += bb.z; sv[j + 3] += bb.w;
-            }
+            float4 sb = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (p.sel_bias && j < p.N) sb = __ldg(reinterpret_cast<const float4*>(p.sel_bias + j));
+            const float sv[4] = {v[j] + sb.x, v[j + 1] + sb.y, v[j + 2] + sb.z, v[j + 3] + sb.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) key[j + u] = j < p.N ? order_key(sv[u]) : 0u;
           }
-          unsigned long long taken = 0;
+          float m[BN / 2];
+#pragma unroll
+          for (int j = 0; j < BN / 2; ++j) {
+            const float a = j < p.N ? v[j] : -INFINITY, b = j + BN / 2 < p.N ? v[j + BN / 2] : -INFINITY;
+            m[j] = fmaxf(a, b);
+          }
+#pragma unroll
+          for (int w = BN / 4; w >= 1; w >>= 1)
+#pragma unroll
+            for (int j = 0; j < w; ++j) m[j] = fmaxf(m[j], m[j + w]);
+          // exp(v - max) = 2^(v log2(e) - max log2(e)): one fused multiply-add
+          // and the base-2 exponential per expert
+          const float mx = m[0];
+          const float mxl = mx * 1.4426950408889634f;
+          float e[BN], sm[BN / 2];
+#pragma unroll
+          for (int j = 0; j < BN; ++j) e[j] = j < p.N ? exp2f(fmaf(v[j], 1.4426950408889634f, -mxl)) : 0.f;
+#pragma unroll
+          for (int j = 0; j < BN / 2; ++j) sm[j] = e[j] + e[j + BN / 2];
+#pragma unroll
+          for (int w = BN / 4; w >= 1; w >>= 1)
+#pragma unroll
+            for (int j = 0; j < w; ++j) sm[j] += sm[j + w];
+          const float sum = sm[0];
           float chosen = 0.f;
           for (int k = 0; k < p.topk; ++k) {
-            float bv = -INFINITY;
-            int be = -1;
+            // arg-max tree over adjacent pairs: the left operand always holds
+            // the lower expert ids, so a tie keeps the left one; the winner's
+            // exp value rides along
+            uint32_t tk[BN / 2];
+            int ti_[BN / 2];
+            float te[BN / 2];
 #pragma unroll
-            for (int j = 0; j < BN; ++j)
-              if (j < p.N && !((taken >> j) & 1ull) && (be < 0 || sv[j] > bv)) { bv = sv[j]; be = j; }
-            taken |= 1ull << be;
-            float vb = 0.f;
+            for (int j = 0; j < BN / 2; ++j) {
+              const bool r = key[2 * j + 1] > key[2 * j];
+              tk[j] = r ? key[2 * j + 1] : key[2 * j];
+              ti_[j] = r ? 2 * j + 1 : 2 * j;
+              te[j] = r ? e[2 * j + 1] : e[2 * j];
+            }
 #pragma unroll
-            for (int j = 0; j < BN; ++j) if (j == be) vb = v[j];
-            const float pk = expf(vb - m) / sum;
+            for (int w = BN / 4; w >= 1; w >>= 1)
+#pragma unroll
+              for (int j = 0; j < w; ++j) {
+                const bool r = tk[2 * j + 1] > tk[2 * j];
+                tk[j] = r ? tk[2 * j + 1] : tk[2 * j];
+                ti_[j] = r ? ti_[2 * j + 1] : ti_[2 * j];
+                te[j] = r ? te[2 * j + 1] : te[2 * j];
+              }
+            const int be = ti_[0];
+#pragma unroll
+            for (int j = 0; j < BN; ++j) key[j] = j == be ? 0u : key[j];
+            const float pk = te[0] / sum;
             chosen += pk;
             p.topk_idx[grow * p.topk + k] = be;
             p.topk_gate[grow * p.topk + k] = pk;
