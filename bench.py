@@ -421,6 +421,12 @@ def run_ours(args, shape, rank, world, local):
         for _ in range(max(3, args.warmup)):
             step(x_d, dy_d, dxs_d)
             flush_l2()
+        # kernels each call launches (the library counts its own launches)
+        n_launch = {}
+        for name, fn in calls:
+            c0 = L.moe_kernel_launches()
+            fn(x_d, dy_d, dxs_d)
+            n_launch[name] = L.moe_kernel_launches() - c0
     st = L.moe_last_device_error(stream)
     if st != L.MOE_OK:
         raise RuntimeError(f"device error after warm-up: {L.moe_status_str(st)}")
@@ -470,6 +476,32 @@ def run_ours(args, shape, rank, world, local):
                 flush_l2()
         torch.cuda.synchronize(dev)
         call_ms["dispatch"] = statistics.mean(a.elapsed_time(c) for a, c in dev_)
+        c0 = L.moe_kernel_launches()
+        L.moe_dispatch(d_in, b_moe.idx, b_moe.T, b_moe.H, b_moe.E, b_moe.K, b_moe.cdt, b_moe.cu, b_moe.dst_row,
+                       b_moe.src_tok, b_moe.xs, b_moe.ws_dispatch, b_moe.ws_dispatch_bytes, stream=stream)
+        n_launch["dispatch"] = L.moe_kernel_launches() - c0
+
+    # The fixed cost of a call as the events see it: n back-to-back launches of
+    # a one-element kernel between two events (each repetition after an L2
+    # flush, so the host is ahead of the device as in the timed steps; the
+    # fastest of 10).  A call of B bytes in n launches can at best take
+    # floor(n) + B / peak.
+    with torch.cuda.stream(stream):
+        tiny = torch.zeros(1, device=dev)
+    launch_floor_ms = {}
+    for n in sorted(set(n_launch.values())):
+        pairs = []
+        with torch.cuda.stream(stream):
+            for _ in range(10):
+                flush_l2()
+                a, c = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                for _ in range(n):
+                    tiny.add_(1)
+                c.record(stream)
+                pairs.append((a, c))
+        torch.cuda.synchronize(dev)
+        launch_floor_ms[n] = min(a.elapsed_time(c) for a, c in pairs)
 
     def capture(xi, dyi, dxsi):
         g = torch.cuda.CUDAGraph()
@@ -618,6 +650,12 @@ def run_ours(args, shape, rank, world, local):
         if name in call_ms:
             gbs = nbytes / (call_ms[name] * 1e-3) / 1e9
             hbm[name] = {"bytes": nbytes, "GB/s": round(gbs, 1), "frac": round(gbs / hbm_peak, 4)}
+            n = n_launch.get(name)
+            if n in launch_floor_ms:
+                best_ms = launch_floor_ms[n] + nbytes / (hbm_peak * 1e9) * 1e3
+                hbm[name].update({"launches": n, "floor_us": round(launch_floor_ms[n] * 1e3, 2),
+                                  "attainable_GB/s": round(nbytes / (best_ms * 1e-3) / 1e9, 1),
+                                  "frac_of_attainable": round(best_ms / call_ms[name], 4)})
     result = {
         "metric": METRICS[mode],
         "value": whole_job_tokens_per_s(n_tok, world, ms),

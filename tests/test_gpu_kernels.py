@@ -566,9 +566,12 @@ def test_route_bwd_linear_stream_matches_oracle(T, H):
     assert_close(to64(dx), dx0.ref + dx_r.reshape(T, H), TOL["bf16"], "dx (accumulated)")
 
 
+# all but the last run the one-launch form (the CTAs' rows fit in shared memory;
+# (3, 1000) puts sequence boundaries inside CTAs); rows of H = 8192 do not fit
+# and take the two-launch form
 @pytest.mark.parametrize("B,Lseq,C,H,dtype", [(4, 2048, 1024, 128, "bf16"), (3, 1000, 333, 64, "f32"),
                                               (2, 8192, 100, 64, "bf16"), (1, 7, 7, 64, "f32"),
-                                              (2, 64, 0, 64, "f32")])
+                                              (2, 64, 0, 64, "f32"), (2, 2048, 700, 8192, "bf16")])
 def test_mod_select_matches_oracle(B, Lseq, C, H, dtype):
     n = B * Lseq
     x = synth.store(synth.normal(2, 1, n * H).reshape(n, H), dtype)
@@ -586,6 +589,11 @@ def test_mod_select_matches_oracle(B, Lseq, C, H, dtype):
     assert_close(s_gpu, s_ref, 1e-5, "score")
     sel_r, mask_r = O.mod_select(s_ref, B, Lseq, C)
     mask_g = mask.cpu().numpy()
+    # exact on the GPU's own scores: the oracle's select run on them
+    sel_x, mask_x = O.mod_select(s_gpu.astype(np.float64), B, Lseq, C)
+    assert np.array_equal(mask_g, mask_x)
+    if C:
+        assert np.array_equal(sel.cpu().numpy()[:B * C], (np.arange(B)[:, None] * Lseq + sel_x).reshape(-1))
     n_amb = check_mod_selection(mask_g, mask_r, s_ref, B, Lseq, C, float(np.max(np.abs(s_gpu - s_ref))))
     flat_g = sel.cpu().numpy()[:B * C]
     # whatever was selected: sel lists exactly the masked tokens, ascending per sequence

@@ -177,6 +177,10 @@ def test_mod_workload_forward_and_route_backward():
     s_r = O.mod_scores(x.ref, wmod.ref)
     assert_close(s_g, s_r, 1e-5, "score")
     sel_o, mask_o = O.mod_select(s_r, B, Lq, C)
+    # exact on the GPU's own scores
+    sel_x, mask_x = O.mod_select(s_g.astype(np.float64), B, Lq, C)
+    assert np.array_equal(m.mask.cpu().numpy(), mask_x)
+    assert np.array_equal(m.sel.cpu().numpy(), (np.arange(B)[:, None] * Lq + sel_x).reshape(-1))
     err = float(np.max(np.abs(s_g - s_r)))
     n_amb = check_mod_selection(m.mask.cpu().numpy(), mask_o, s_r, B, Lq, C, err)
     assert n_amb == 0, f"{n_amb} near-tie positions"

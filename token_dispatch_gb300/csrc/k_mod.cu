@@ -1,20 +1,28 @@
 // Mixture-of-Depths capacity router (MoE/MoD framework page, MoD paragraph:
 // part of the tokens skips the layer entirely; 50% capacity).
 //
-//   score[t] = x[t] . w_mod                         (one warp per token)
+//   score[t] = x[t] . w_mod
 //   per sequence: the C highest scores are selected, equal scores -> lower
 //   position, i.e. token i is selected iff its rank
 //     #{j : s_j > s_i  or  (s_j == s_i and j < i)}
 //   is below C.
-// The selection runs as a radix select on order-preserving integer keys of
-// the scores (-0 folded onto +0, so equal scores are equal keys): four 8-bit
-// passes from the top find the C-th largest key k*; keys above k* are
-// selected, and of the keys equal to k* the first (C - #{key > k*}) by
-// position.  One launch does the select and the row copies: every CTA of a
-// sequence runs the same select on the sequence's scores (identical integer
-// work, identical result), the first CTA writes mask, sel and sel_score, and
-// each CTA copies its share of the rows: the selected ones to the MoE input
-// x_sel in position order, the others to y (y = x for tokens that skip).
+// The selection runs on order-preserving integer keys of the scores (-0
+// folded onto +0, so equal scores are equal keys): the C-th largest key k* is
+// found bit by bit from the top (a radix select with one-bit digits); keys
+// above k* are selected, and of the keys equal to k* the first
+// (C - #{key > k*}) by position.
+//
+// One launch when the rows fit in shared memory (every CTA holds at most
+// ~54 rows of 4 KB, as at 4 x 2048 tokens of H = 2048 on 152 SMs): each CTA
+// brings its contiguous rows in with bulk copies, computes their scores, then
+// waits until every score of its sequence(s) is written (the score buffer is
+// first filled with a bit pattern no dot product produces, so the wait needs
+// no counter and two calls never share state), runs the select and stores
+// its rows from shared memory to x_sel or y: x is read from HBM once.  The
+// CTAs wait on one another, so the launch is cooperative (all CTAs resident).
+// Otherwise two launches: a score kernel (one warp per token), then the
+// select and the row copies, every CTA of a sequence running the same select
+// on the sequence's scores and copying its share of the rows.
 #include "moe_internal.cuh"
 
 namespace moe {
@@ -69,12 +77,6 @@ __device__ __forceinline__ unsigned score_key(float s) {
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-__device__ __forceinline__ unsigned lanemask_lt() {
-  unsigned m;
-  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
-  return m;
-}
-
 // Exclusive prefix of v over the CTA's threads in thread order (warp shuffles,
 // then the warp totals); total gets the sum over all threads.
 __device__ __forceinline__ int block_excl_scan(int v, int* wtot, int& total) {
@@ -98,39 +100,45 @@ __device__ __forceinline__ int block_excl_scan(int v, int* wtot, int& total) {
   return before;
 }
 
-// grid (R, B): CTA r of sequence b.  Dynamic shared memory: L ints (the keys,
-// then the row map: selected position -> rank among the selected, else -1).
-__global__ void __launch_bounds__(MS_THREADS)
-mod_select_rows_kernel(const float* __restrict__ score, int L, int C, const uint4* __restrict__ x,
-                       int vec_per_row, int32_t* __restrict__ sel, float* __restrict__ sel_score,
-                       uint8_t* __restrict__ mask, uint4* __restrict__ x_sel, uint4* __restrict__ y_skip) {
-  extern __shared__ unsigned keys[];
-  __shared__ int hist[256];
-  __shared__ int wtot[MS_WARPS];
-  __shared__ int s_bin, s_need;
+// Select of one sequence: keys[i] (i < L) holds score_key of position i on
+// entry and, on return, the rank of position i among the selected positions,
+// or 0xffffffff when it is not selected.  All threads of the CTA call it;
+// hist ([2][256]) and wcnt ([2][MS_WARPS]) are the CTA's shared scratch.
+//
+// Radix select: four 8-bit passes from the top find the C-th largest key k*.
+// Each thread keeps its run of consecutive positions in registers; lanes with
+// the same digit add to the histogram once (the lowest of them), and the two
+// histograms alternate so a pass clears the next one's while it counts.
+__device__ void seq_row_map(unsigned* keys, int L, int C, int (*hist)[256], int (*wcnt)[MS_WARPS], int* s_sel) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
-  const int b = blockIdx.y, R = gridDim.x, r = blockIdx.x;
-  const float* s = score + (long long)b * L;
-  for (int i = tid; i < L; i += MS_THREADS) keys[i] = score_key(__ldg(s + i));
-  __syncthreads();
-
-  // radix select of the C-th largest key: after the pass at `shift`, the bits
-  // of `prefix` under `pmask` are fixed and `need` keys are still to be taken
-  // among the keys that match them
+  const bool partial = C > 0 && C < L;
+  const int per = (L + MS_THREADS - 1) / MS_THREADS;
+  const int lo = min(L, tid * per), hi = min(L, lo + per);
+  unsigned kr[MS_MAX_RUN];
+#pragma unroll
+  for (int j = 0; j < MS_MAX_RUN; ++j) kr[j] = lo + j < hi ? keys[lo + j] : 0u;
+  unsigned lt;
+  asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
+  // after the pass at `shift`, the bits of `prefix` under `pmask` are fixed
+  // and `need` keys are still to be taken among the keys that match them
   unsigned prefix = 0, pmask = 0;
   int need = C;
-  const bool partial = C > 0 && C < L;
   if (partial) {
-    for (int shift = 24; shift >= 0; shift -= 8) {
-      if (tid < 256) hist[tid] = 0;
-      __syncthreads();
-      for (int i0 = 0; i0 < L; i0 += MS_THREADS) {
-        const int i = i0 + tid;
-        const unsigned k = i < L ? keys[i] : 0u;
-        const int d = (i < L && (k & pmask) == prefix) ? (int)((k >> shift) & 255u) : -1;
-        // lanes with the same digit add once (the lowest of them)
-        const unsigned peers = __match_any_sync(0xffffffffu, d);
-        if (d >= 0 && (peers & lanemask_lt()) == 0) atomicAdd(&hist[d], __popc(peers));
+    if (tid < 256) hist[0][tid] = 0;
+    __syncthreads();
+    for (int pass = 0; pass < 4; ++pass) {
+      const int shift = 24 - 8 * pass;
+      int* h = hist[pass & 1];
+      if (tid < 256) hist[(pass + 1) & 1][tid] = 0;  // the next pass's histogram
+      int d[MS_MAX_RUN];
+#pragma unroll
+      for (int j = 0; j < MS_MAX_RUN; ++j)
+        d[j] = (lo + j < hi && (kr[j] & pmask) == prefix) ? (int)((kr[j] >> shift) & 255u) : -1;
+#pragma unroll
+      for (int j = 0; j < MS_MAX_RUN; ++j) {
+        if (j >= per) break;  // uniform: per is the same for every thread
+        const unsigned peers = __match_any_sync(0xffffffffu, d[j]);
+        if (d[j] >= 0 && (peers & lt) == 0) atomicAdd(&h[d[j]], __popc(peers));
       }
       __syncthreads();
       if (w == 0) {
@@ -139,7 +147,7 @@ mod_select_rows_kernel(const float* __restrict__ score, int L, int C, const uint
         int c[8], local = 0;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-          c[j] = hist[255 - 8 * lane - j];
+          c[j] = h[255 - 8 * lane - j];
           local += c[j];
         }
         int incl = local;
@@ -154,8 +162,8 @@ mod_select_rows_kernel(const float* __restrict__ score, int L, int C, const uint
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             if (run + c[j] >= need) {
-              s_bin = 255 - 8 * lane - j;
-              s_need = need - run;
+              s_sel[2 * (pass & 1)] = 255 - 8 * lane - j;
+              s_sel[2 * (pass & 1) + 1] = need - run;
               break;
             }
             run += c[j];
@@ -163,25 +171,26 @@ mod_select_rows_kernel(const float* __restrict__ score, int L, int C, const uint
         }
       }
       __syncthreads();
-      prefix |= (unsigned)s_bin << shift;
+      prefix |= (unsigned)s_sel[2 * (pass & 1)] << shift;
       pmask |= 255u << shift;
-      need = s_need;
+      need = s_sel[2 * (pass & 1) + 1];
     }
   }
   const unsigned kth = prefix;  // the C-th largest key (when 0 < C < L)
 
-  // each thread owns a run of consecutive positions: selection flags with the
-  // tie rule (equal keys taken by position), then ranks among the selected
-  const int per = (L + MS_THREADS - 1) / MS_THREADS;
-  const int lo = min(L, tid * per), hi = min(L, lo + per);
+  // selection flags with the tie rule (equal keys taken by position), then
+  // ranks among the selected
   int n_eq = 0;
-  for (int i = lo; i < hi; ++i) n_eq += (partial && keys[i] == kth) ? 1 : 0;
+#pragma unroll
+  for (int j = 0; j < MS_MAX_RUN; ++j) n_eq += (lo + j < hi && partial && kr[j] == kth) ? 1 : 0;
   int tot;
-  int eq_before = block_excl_scan(n_eq, wtot, tot);
+  int eq_before = block_excl_scan(n_eq, wcnt[1], tot);
   unsigned flags = 0;
   int n_sel = 0;
-  for (int i = lo; i < hi; ++i) {
-    const unsigned k = keys[i];
+#pragma unroll
+  for (int j = 0; j < MS_MAX_RUN; ++j) {
+    if (lo + j >= hi) break;
+    const unsigned k = kr[j];
     bool take;
     if (!partial) {
       take = C >= L;
@@ -194,26 +203,49 @@ mod_select_rows_kernel(const float* __restrict__ score, int L, int C, const uint
       take = false;
     }
     if (take) {
-      flags |= 1u << (i - lo);
+      flags |= 1u << j;
       ++n_sel;
     }
   }
-  int pos = block_excl_scan(n_sel, wtot, tot);
+  int pos = block_excl_scan(n_sel, wcnt[0], tot);
   // the row map replaces the keys (each thread rewrites only its own run)
-  for (int i = lo; i < hi; ++i) {
-    const bool take = (flags >> (i - lo)) & 1u;
-    const long long t = (long long)b * L + i;
-    if (r == 0) {
-      mask[t] = take ? 1 : 0;
-      if (take) {
-        sel[(long long)b * C + pos] = (int32_t)t;
-        if (sel_score) sel_score[(long long)b * C + pos] = __ldg(s + i);
-      }
-    }
-    keys[i] = take ? (unsigned)pos : 0xffffffffu;
+#pragma unroll
+  for (int j = 0; j < MS_MAX_RUN; ++j) {
+    if (lo + j >= hi) break;
+    const bool take = (flags >> j) & 1u;
+    keys[lo + j] = take ? (unsigned)pos : 0xffffffffu;
     pos += take ? 1 : 0;
   }
   __syncthreads();
+}
+
+// grid (R, B): CTA r of sequence b.  Dynamic shared memory: L ints (the keys,
+// then the row map: selected position -> rank among the selected, else -1).
+__global__ void __launch_bounds__(MS_THREADS)
+mod_select_rows_kernel(const float* __restrict__ score, int L, int C, const uint4* __restrict__ x,
+                       int vec_per_row, int32_t* __restrict__ sel, float* __restrict__ sel_score,
+                       uint8_t* __restrict__ mask, uint4* __restrict__ x_sel, uint4* __restrict__ y_skip) {
+  extern __shared__ unsigned keys[];
+  __shared__ int hist[2][256];
+  __shared__ int wcnt[2][MS_WARPS];
+  __shared__ int s_sel[4];
+  const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
+  const int b = blockIdx.y, R = gridDim.x, r = blockIdx.x;
+  const float* s = score + (long long)b * L;
+  for (int i = tid; i < L; i += MS_THREADS) keys[i] = score_key(__ldg(s + i));
+  __syncthreads();
+  seq_row_map(keys, L, C, hist, wcnt, s_sel);
+  if (r == 0) {
+    for (int i = tid; i < L; i += MS_THREADS) {
+      const unsigned m = keys[i];
+      const long long t = (long long)b * L + i;
+      mask[t] = m != 0xffffffffu ? 1 : 0;
+      if (m != 0xffffffffu) {
+        sel[(long long)b * C + m] = (int32_t)t;
+        if (sel_score) sel_score[(long long)b * C + m] = __ldg(s + i);
+      }
+    }
+  }
 
   // this CTA's rows: one warp per row, 16-byte vectors, all of a lane's
   // vectors of the row in flight before the first store
@@ -242,6 +274,169 @@ mod_select_rows_kernel(const float* __restrict__ score, int L, int C, const uint
   }
 }
 
+// ---------------------------------------------------------- one launch ---
+constexpr unsigned SCORE_UNSET = 0xffffffffu;  // a NaN bit pattern no dot product yields
+constexpr unsigned long long MF_WAIT_LIMIT = 4000000000ull;  // clock64 cycles, ~2 s
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ bool mbar_try_wait0(uint32_t bar) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar)
+      : "memory");
+  return ok != 0;
+}
+// waits (bounded) for the mbarrier's first phase; false on timeout
+__device__ __forceinline__ bool mbar_wait0_bounded(uint32_t bar) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait0(bar))
+    if ((unsigned long long)(clock64() - t0) > MF_WAIT_LIMIT) return false;
+  return true;
+}
+
+// grid: G CTAs, all resident (cooperative launch); CTA g owns the tokens
+// [g n / G, (g+1) n / G) of the n = B L.  Dynamic shared memory: rows_cap
+// rows of H elements, then L keys.
+template <typename T>
+__global__ void __launch_bounds__(MS_THREADS, 1)
+mod_fused_kernel(const T* __restrict__ x, const T* __restrict__ w, int B, int L, int H, int C, int rows_cap,
+                 float* score, int32_t* __restrict__ sel, float* __restrict__ sel_score,
+                 uint8_t* __restrict__ mask, T* __restrict__ x_sel, T* __restrict__ y_skip, unsigned* err) {
+  extern __shared__ __align__(128) unsigned char smem_rows[];
+  __shared__ __align__(8) unsigned long long bar;
+  __shared__ int hist[2][256];
+  __shared__ int wcnt[2][MS_WARPS];
+  __shared__ int s_sel[4];
+  constexpr int V = Vec16<T>::N;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const long long n_tok = (long long)B * L;
+  const int G = gridDim.x;
+  const long long r0 = n_tok * blockIdx.x / G, r1 = n_tok * (blockIdx.x + 1) / G;
+  const int nr = (int)(r1 - r0);
+  const uint32_t rb = (uint32_t)H * (uint32_t)sizeof(T);
+  const int nvec = H / V;
+  unsigned* keys = reinterpret_cast<unsigned*>(smem_rows + (size_t)rows_cap * rb);
+  const uint32_t bar_a = smem_addr(&bar);
+
+  // 1. the CTA's rows into shared memory (bulk copies on one mbarrier)
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_a) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  if (tid == 0) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar_a), "r"((uint32_t)nr * rb)
+                 : "memory");
+    for (int r = 0; r < nr; ++r)
+      asm volatile(
+          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+              smem_addr(smem_rows + (size_t)r * rb)),
+          "l"(x + (r0 + r) * H), "r"(rb), "r"(bar_a)
+          : "memory");
+  }
+  // a lane's share of w_mod (WV vectors of 16 bytes) is requested while the
+  // rows arrive and stays in registers for all the warp's rows
+  constexpr int WV = 8;  // H * sizeof(T) <= 32 * WV * 16 bytes: one pass over a row
+  const uint4* wv = reinterpret_cast<const uint4*>(w);
+  uint4 wr[WV];
+#pragma unroll
+  for (int u = 0; u < WV; ++u) wr[u] = lane + 32 * u < nvec ? __ldg(wv + lane + 32 * u) : make_uint4(0, 0, 0, 0);
+  const bool rows_ok = __syncthreads_and(mbar_wait0_bounded(bar_a)) != 0;
+  if (!rows_ok && tid == 0) set_error(err, DEV_TIMEOUT);
+
+  // 2. scores of the CTA's rows: one warp per row
+  {
+    for (int r = warp; r < nr; r += MS_WARPS) {
+      const uint4* rv = reinterpret_cast<const uint4*>(smem_rows + (size_t)r * rb);
+      float acc = 0.f;
+      if (nvec <= 32 * WV) {
+        // WV independent partial sums (short dependency chains), added in a
+        // fixed order
+        uint4 xr[WV];
+        float part[WV];
+#pragma unroll
+        for (int u = 0; u < WV; ++u) xr[u] = lane + 32 * u < nvec ? rv[lane + 32 * u] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+        for (int u = 0; u < WV; ++u) {
+          float xv[V], ww[V];
+          Vec16<T>::load_raw_unpack(xr[u], xv);
+          Vec16<T>::load_raw_unpack(wr[u], ww);
+          part[u] = 0.f;
+#pragma unroll
+          for (int v = 0; v < V; ++v) part[u] = fmaf(xv[v], ww[v], part[u]);
+        }
+#pragma unroll
+        for (int u = 0; u < WV; ++u) acc += part[u];
+      } else {
+        for (int i = lane; i < nvec; i += 32) {
+          float xv[V], ww[V];
+          Vec16<T>::load_raw_unpack(rv[i], xv);
+          Vec16<T>::load_raw_unpack(__ldg(wv + i), ww);
+#pragma unroll
+          for (int v = 0; v < V; ++v) acc = fmaf(xv[v], ww[v], acc);
+        }
+      }
+      acc = warp_sum(acc);
+      if (__float_as_uint(acc) == SCORE_UNSET) acc = __uint_as_float(0x7fffffffu);
+      if (lane == 0) score[r0 + r] = acc;
+    }
+  }
+
+  // 3. per sequence the CTA's tokens belong to: wait for all its scores, select,
+  //    then write the CTA's share of mask / sel / sel_score and of the rows
+  if (nr > 0) {
+    const long long b_lo = r0 / L, b_hi = (r1 - 1) / L;
+    for (long long b = b_lo; b <= b_hi; ++b) {
+      const unsigned* s = reinterpret_cast<const unsigned*>(score + b * L);
+      const long long t0 = clock64();
+      for (;;) {
+        int missing = 0;
+        for (int i = tid; i < L; i += MS_THREADS) {
+          const unsigned u = __ldcg(s + i);
+          missing |= u == SCORE_UNSET;
+          keys[i] = score_key(__uint_as_float(u));
+        }
+        if (!__syncthreads_or(missing)) break;
+        // one clock decides for the whole CTA (the loop exit stays uniform)
+        if (__syncthreads_or(tid == 0 && (unsigned long long)(clock64() - t0) > MF_WAIT_LIMIT)) {
+          if (tid == 0) set_error(err, DEV_TIMEOUT);
+          break;
+        }
+        __nanosleep(256);
+      }
+      seq_row_map(keys, L, C, hist, wcnt, s_sel);
+      const long long t_lo = r0 > b * L ? r0 : b * L;
+      const long long t_hi = r1 < (b + 1) * L ? r1 : (b + 1) * L;
+      for (long long t = t_lo + tid; t < t_hi; t += MS_THREADS) {
+        const int i = (int)(t - b * L);
+        const unsigned m = keys[i];
+        mask[t] = m != 0xffffffffu ? 1 : 0;
+        T* dst = nullptr;
+        if (m != 0xffffffffu) {
+          sel[b * C + m] = (int32_t)t;
+          if (sel_score) sel_score[b * C + m] = __uint_as_float(__ldcg(s + i));
+          if (x_sel) dst = x_sel + (b * C + m) * H;
+        } else if (y_skip) {
+          dst = y_skip + t * H;
+        }
+        if (dst && rows_ok)
+          asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                       "r"(smem_addr(smem_rows + (size_t)(t - r0) * rb)), "r"(rb)
+                       : "memory");
+      }
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+      __syncthreads();  // the keys are rewritten for the next sequence
+    }
+    // shared memory stays until the bulk stores have read it
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+  }
+  if (!rows_ok && tid == 0) mbar_wait0_bounded(bar_a);  // copies still in flight land before exit
+}
+
 int warp_grid(long long n) {
   long long ctas = (n + 7) / 8;
   long long cap = (long long)sm_count() * 16;
@@ -251,12 +446,74 @@ int warp_grid(long long n) {
 
 }  // namespace
 
+template <typename T>
+int launch_mod_fused(const void* x, const void* w, int B, int L, int H, int C, float* score, int32_t* sel,
+                     float* sel_score, uint8_t* mask, void* x_sel, void* y_skip, int rows_cap, int G, size_t smem,
+                     cudaStream_t s) {
+  auto k = mod_fused_kernel<T>;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  // every score starts as the unset pattern (0xff bytes)
+  if (cudaMemsetAsync(score, 0xff, (size_t)B * L * sizeof(float), s) != cudaSuccess) return MOE_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)G);
+  cfg.blockDim = dim3(MS_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaLaunchKernelEx(&cfg, k, static_cast<const T*>(x), static_cast<const T*>(w), B, L, H, C, rows_cap, score, sel,
+                     sel_score, mask, static_cast<T*>(x_sel), static_cast<T*>(y_skip), device_error_word());
+  return launch_status();
+}
+
+// The one-launch form applies when every CTA's rows and the keys of a
+// sequence fit in shared memory with all CTAs resident (one per SM).
+bool mod_fused_plan(int B, int L, int H, int dtype, int* rows_cap, int* G, size_t* smem) {
+  const long long n_tok = (long long)B * L;
+  const int esz = dtype == MOE_BF16 ? 2 : 4;
+  int dev = 0, max_optin = 0, coop = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&max_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (!coop || n_tok < 1) return false;
+  cudaFuncAttributes fa;
+  if ((dtype == MOE_BF16 ? cudaFuncGetAttributes(&fa, mod_fused_kernel<bf16>)
+                         : cudaFuncGetAttributes(&fa, mod_fused_kernel<float>)) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  const long long g = n_tok < sm_count() ? n_tok : sm_count();
+  const long long cap = (n_tok + g - 1) / g;
+  const size_t need = (size_t)cap * H * esz + (size_t)L * 4;
+  if (need + fa.sharedSizeBytes > (size_t)max_optin) return false;  // + the static shared memory
+  *rows_cap = (int)cap;
+  *G = (int)g;
+  *smem = need;
+  return true;
+}
+
 int launch_mod_select(const void* x, const void* w, int B, int L, int H, int C, int dtype,
                       float* score, int32_t* sel, float* sel_score, uint8_t* mask, void* x_sel,
                       void* y_skip, cudaStream_t s) {
   const long long n_tok = (long long)B * L;
   if (n_tok == 0) return MOE_OK;
   if (L > MS_THREADS * MS_MAX_RUN) return MOE_ERR_UNSUPPORTED;
+  int rows_cap = 0, G = 0;
+  size_t fsmem = 0;
+  if (mod_fused_plan(B, L, H, dtype, &rows_cap, &G, &fsmem)) {
+    return dtype == MOE_BF16
+               ? launch_mod_fused<bf16>(x, w, B, L, H, C, score, sel, sel_score, mask, x_sel, y_skip, rows_cap, G,
+                                        fsmem, s)
+               : launch_mod_fused<float>(x, w, B, L, H, C, score, sel, sel_score, mask, x_sel, y_skip, rows_cap, G,
+                                         fsmem, s);
+  }
   if (dtype == MOE_BF16)
     mod_score_kernel<bf16><<<warp_grid(n_tok), 256, 0, s>>>(static_cast<const bf16*>(x),
                                                             static_cast<const bf16*>(w), n_tok, H, score);
