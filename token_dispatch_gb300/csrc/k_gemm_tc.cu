@@ -61,6 +61,7 @@ __host__ __device__ constexpr int max_threads() {
   return can_gather<EPI, A_MN, NA, NB, KSUB>() ? NUM_THREADS + 32 * GATHER_WARPS : NUM_THREADS;
 }
 constexpr int A_STAGE_BYTES = BM * BK * 2;
+constexpr int STG_LD = 33;  // row stride (floats) of an epilogue staging tile
 
 // EPI_SWIGLU_BWD: the accumulator is da; with g, u read back from p.aux it
 // writes dg and du (bf16) side by side.  EPI_F32_GK: fp32 tile of a grouped-K
@@ -238,7 +239,7 @@ struct Cfg {
                                    : (2 * BN <= 256) ? 256 : 512;
   // bf16 epilogue: per warp a [32 rows][33] fp32 staging tile, so the global
   // stores (and the reads of the old values) go out row-contiguous
-  static constexpr int STG_LD = 33;
+  static constexpr int STG_LD = tc::STG_LD;
   static constexpr int EPI_BYTES = (EPI == EPI_BF16 || EPI == EPI_F32_GK || EPI == EPI_ROUTER) ? 4 * 32 * STG_LD * 4 : 0;
 };
 
@@ -268,6 +269,119 @@ __device__ __forceinline__ TileInfo decode(int t, const int* mt_pre, const int* 
   ti.rows = min(BM, end - ti.row0);
   ti.n0 = n * out_bn;
   return ti;
+}
+
+// ------------------------------------------------------------ epilogues ---
+// The thread owns TMEM lane (row) q*32 + lane of the tile's accumulator at
+// tbase; grow is that row's index in the output, row_ok whether it exists.
+
+// EPI_SWIGLU: columns [0, OUT_BN) hold g, [OUT_BN, 2 OUT_BN) hold u; act =
+// silu(g) * u goes out as bf16 (and g, u to p.aux when set).
+template <int OUT_BN>
+__device__ __forceinline__ void epi_swiglu(const Params& p, uint32_t tbase, const TileInfo& ti, bool row_ok,
+                                           long long grow) {
+  bf16* out = static_cast<bf16*>(p.out);
+#pragma unroll 1
+  for (int c = 0; c < OUT_BN / 32; ++c) {
+    float gv[32], uv[32];
+    tmem_ld32(tbase + c * 32, gv);
+    tmem_ld32(tbase + OUT_BN + c * 32, uv);
+    const int col = ti.n0 + c * 32;
+    if (row_ok && col < p.N) {
+      uint4 pk[4];
+      __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(pk);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        float a0 = gv[2 * j] / (1.0f + __expf(-gv[2 * j])) * uv[2 * j];
+        float a1 = gv[2 * j + 1] / (1.0f + __expf(-gv[2 * j + 1])) * uv[2 * j + 1];
+        h2[j] = __floats2bfloat162_rn(a0, a1);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(out + grow * p.ldo + col);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) dst[j] = pk[j];
+      if (p.aux) {  // keep g and u for the backward
+        uint4 gp[4], up[4];
+        __nv_bfloat162* g2 = reinterpret_cast<__nv_bfloat162*>(gp);
+        __nv_bfloat162* u2 = reinterpret_cast<__nv_bfloat162*>(up);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          g2[j] = __floats2bfloat162_rn(gv[2 * j], gv[2 * j + 1]);
+          u2[j] = __floats2bfloat162_rn(uv[2 * j], uv[2 * j + 1]);
+        }
+        bf16* ax = static_cast<bf16*>(p.aux) + grow * p.ld_aux;
+        uint4* gd = reinterpret_cast<uint4*>(ax + col);
+        uint4* ud = reinterpret_cast<uint4*>(ax + p.N + col);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          gd[j] = gp[j];
+          ud[j] = up[j];
+        }
+      }
+    }
+  }
+}
+
+// EPI_BF16: the fp32 tile rounded to bf16 (plus the old values with
+// p.accumulate), through the warp's [32][STG_LD] staging tile.
+template <int OUT_BN>
+__device__ __forceinline__ void epi_bf16(const Params& p, uint32_t tbase, const TileInfo& ti, float* epi_stage,
+                                         int q, int lane) {
+  // TMEM row per thread -> this warp's staging tile -> 8 rows x 64 bytes
+  // per store instruction (4 lanes per row segment of 32 columns).  With
+  // accumulate, every old value the warp will add is requested first.
+  bf16* out = static_cast<bf16*>(p.out);
+  constexpr int NCH = OUT_BN / 32;
+  float* stg = epi_stage + q * 32 * STG_LD;
+  const int seg = (lane & 3) * 8;
+  uint4 old[NCH][4];
+  if (p.accumulate) {
+#pragma unroll
+    for (int c = 0; c < NCH; ++c) {
+#pragma unroll
+      for (int ps = 0; ps < 4; ++ps) {
+        const int rr = q * 32 + ps * 8 + (lane >> 2);
+        const long long gr = (long long)ti.row0 + rr;
+        const int col = ti.n0 + c * 32 + seg;
+        const bool ok = rr < ti.rows && gr < p.M && col < p.N;
+        old[c][ps] = ok ? *reinterpret_cast<const uint4*>(out + gr * p.ldo + col) : make_uint4(0, 0, 0, 0);
+      }
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < NCH; ++c) {
+    float v[32];
+    tmem_ld32(tbase + c * 32, v);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) stg[lane * STG_LD + j] = v[j];
+    __syncwarp();
+#pragma unroll
+    for (int ps = 0; ps < 4; ++ps) {
+      const int rw = ps * 8 + (lane >> 2);
+      const int rr = q * 32 + rw;
+      const long long gr = (long long)ti.row0 + rr;
+      const int col = ti.n0 + c * 32 + seg;
+      if (rr < ti.rows && gr < p.M && col < p.N) {
+        float a[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) a[j] = stg[rw * STG_LD + seg + j];
+        if (p.accumulate) {
+          const __nv_bfloat162* oh = reinterpret_cast<const __nv_bfloat162*>(&old[c][ps]);
+#pragma unroll
+          for (int q2 = 0; q2 < 4; ++q2) {
+            const float2 f = __bfloat1622float2(oh[q2]);
+            a[2 * q2] += f.x;
+            a[2 * q2 + 1] += f.y;
+          }
+        }
+        uint4 pk;
+        __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&pk);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) h2[j] = __floats2bfloat162_rn(a[2 * j], a[2 * j + 1]);
+        *reinterpret_cast<uint4*>(out + gr * p.ldo + col) = pk;
+      }
+    }
+    __syncwarp();
+  }
 }
 
 // KSUB > 1: the NA = NB = KSUB tile pairs of a stage are consecutive 64-wide
@@ -650,45 +764,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const bool row_ok = r_local < ti.rows && grow >= 0 && grow < p.M;
       const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
       if (EPI == EPI_SWIGLU) {
-        bf16* out = static_cast<bf16*>(p.out);
-#pragma unroll 1
-        for (int c = 0; c < C::OUT_BN / 32; ++c) {
-          float gv[32], uv[32];
-          tmem_ld32(tbase + c * 32, gv);
-          tmem_ld32(tbase + C::OUT_BN + c * 32, uv);
-          const int col = ti.n0 + c * 32;
-          if (row_ok && col < p.N) {
-            uint4 pk[4];
-            __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(pk);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              float a0 = gv[2 * j] / (1.0f + __expf(-gv[2 * j])) * uv[2 * j];
-              float a1 = gv[2 * j + 1] / (1.0f + __expf(-gv[2 * j + 1])) * uv[2 * j + 1];
-              h2[j] = __floats2bfloat162_rn(a0, a1);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(out + grow * p.ldo + col);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) dst[j] = pk[j];
-            if (p.aux) {  // keep g and u for the backward
-              uint4 gp[4], up[4];
-              __nv_bfloat162* g2 = reinterpret_cast<__nv_bfloat162*>(gp);
-              __nv_bfloat162* u2 = reinterpret_cast<__nv_bfloat162*>(up);
-#pragma unroll
-              for (int j = 0; j < 16; ++j) {
-                g2[j] = __floats2bfloat162_rn(gv[2 * j], gv[2 * j + 1]);
-                u2[j] = __floats2bfloat162_rn(uv[2 * j], uv[2 * j + 1]);
-              }
-              bf16* ax = static_cast<bf16*>(p.aux) + grow * p.ld_aux;
-              uint4* gd = reinterpret_cast<uint4*>(ax + col);
-              uint4* ud = reinterpret_cast<uint4*>(ax + p.N + col);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                gd[j] = gp[j];
-                ud[j] = up[j];
-              }
-            }
-          }
-        }
+        epi_swiglu<C::OUT_BN>(p, tbase, ti, row_ok, grow);
       } else if (EPI == EPI_SWIGLU_BWD) {
         // da for 32 columns at a time; g and u of the same columns come from
         // p.aux ([g | u] per row); dg and du go to p.out ([dg | du] per row)
@@ -761,62 +837,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           __syncwarp();
         }
       } else if (EPI == EPI_BF16) {
-        // TMEM row per thread -> this warp's staging tile -> 8 rows x 64 bytes
-        // per store instruction (4 lanes per row segment of 32 columns).  With
-        // accumulate, every old value the warp will add is requested first.
-        bf16* out = static_cast<bf16*>(p.out);
-        constexpr int NCH = C::OUT_BN / 32;
-        float* stg = epi_stage + q * 32 * C::STG_LD;
-        const int seg = (lane & 3) * 8;
-        uint4 old[NCH][4];
-        if (p.accumulate) {
-#pragma unroll
-          for (int c = 0; c < NCH; ++c) {
-#pragma unroll
-            for (int ps = 0; ps < 4; ++ps) {
-              const int rr = q * 32 + ps * 8 + (lane >> 2);
-              const long long gr = (long long)ti.row0 + rr;
-              const int col = ti.n0 + c * 32 + seg;
-              const bool ok = rr < ti.rows && gr < p.M && col < p.N;
-              old[c][ps] = ok ? *reinterpret_cast<const uint4*>(out + gr * p.ldo + col) : make_uint4(0, 0, 0, 0);
-            }
-          }
-        }
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-          float v[32];
-          tmem_ld32(tbase + c * 32, v);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) stg[lane * C::STG_LD + j] = v[j];
-          __syncwarp();
-#pragma unroll
-          for (int ps = 0; ps < 4; ++ps) {
-            const int rw = ps * 8 + (lane >> 2);
-            const int rr = q * 32 + rw;
-            const long long gr = (long long)ti.row0 + rr;
-            const int col = ti.n0 + c * 32 + seg;
-            if (rr < ti.rows && gr < p.M && col < p.N) {
-              float a[8];
-#pragma unroll
-              for (int j = 0; j < 8; ++j) a[j] = stg[rw * C::STG_LD + seg + j];
-              if (p.accumulate) {
-                const __nv_bfloat162* oh = reinterpret_cast<const __nv_bfloat162*>(&old[c][ps]);
-#pragma unroll
-                for (int q2 = 0; q2 < 4; ++q2) {
-                  const float2 f = __bfloat1622float2(oh[q2]);
-                  a[2 * q2] += f.x;
-                  a[2 * q2 + 1] += f.y;
-                }
-              }
-              uint4 pk;
-              __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(&pk);
-#pragma unroll
-              for (int j = 0; j < 4; ++j) h2[j] = __floats2bfloat162_rn(a[2 * j], a[2 * j + 1]);
-              *reinterpret_cast<uint4*>(out + gr * p.ldo + col) = pk;
-            }
-          }
-          __syncwarp();
-        }
+        epi_bf16<C::OUT_BN>(p, tbase, ti, epi_stage, q, lane);
       } else if (EPI == EPI_ROUTER) {
         // one thread = one token: its BN logits (E valid) come out of TMEM, get
         // the bias and are stored; the softmax and the top-k (value descending,
@@ -963,6 +984,342 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
 }
 
+// ------------------------------------------------------ CTA-pair GEMM ---
+// The expert FFN's gate/up (SwiGLU epilogue) and down (bf16 epilogue) GEMMs
+// on pairs of SMs with the 5th-generation tensor core's two-CTA MMA
+// (tcgen05 cta_group::2): one 256 x 256 tile per pair, each CTA holding 128
+// rows of A and half of the B columns in its own shared memory, each CTA's
+// tensor memory holding the accumulator rows of its A rows.  Per SM a stage is
+// 32 KB instead of 48 KB (B is not duplicated), so shared-memory traffic per
+// MMA falls by a third and six stages fit where four did.
+//
+// Protocol (barriers at the same offsets in both CTAs):
+//   full[s]   leader's only: its producer expects both CTAs' bytes; the two
+//             producers' loads (cta_group::2 form) complete on it;
+//   empty[s]  each CTA's own: the leader's MMA commit arrives on both;
+//   accf[a]   each CTA's own: the leader's accumulator commit arrives on both;
+//   acce[a]   leader's only: 128 epilogue threads of each CTA arrive (the
+//             peer's remotely) before the leader reuses accumulator a.
+// Tensor memory is allocated and freed by both CTAs together (the same
+// columns in each); cluster barriers after set-up and before the release.
+constexpr int PAIR_STAGES = 6;
+constexpr int PAIR_BN = 256;
+
+template <int EPI>
+struct PairCfg {
+  static constexpr int B_HALF_BYTES = (PAIR_BN / 2) * BK * 2;
+  static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_HALF_BYTES;
+  static constexpr int OUT_BN = EPI == EPI_SWIGLU ? PAIR_BN / 2 : PAIR_BN;
+  static constexpr int TMEM_COLS = 2 * PAIR_BN;
+  static constexpr int EPI_BYTES = EPI == EPI_BF16 ? 4 * 32 * STG_LD * 4 : 0;
+  static constexpr size_t SMEM = (size_t)PAIR_STAGES * STAGE_BYTES + EPI_BYTES + (2 * PAIR_STAGES + 5) * 8 + 1024;
+};
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+// the shared::cluster address of the same offset in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// TMA load into this CTA's shared memory, completing on an mbarrier of
+// either CTA of the pair (a shared::cluster address)
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, uint32_t bar, int c0, int c1,
+                                                 int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%3, %4, "
+      "%5}], [%2];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+__device__ __forceinline__ void tc_mma_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate));
+}
+// arrive (once the MMAs issued so far complete) on the mbarrier at this
+// offset in every CTA of ctaMask
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t mask) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   bar),
+               "h"(mask)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// bounded wait with cluster-scope acquire (for arrivals from the peer CTA)
+__device__ __forceinline__ bool wait_bounded_cluster(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                                     const Params& p) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (*abort_flag) return false;
+      if ((unsigned long long)(clock64() - t0) > p.wait_limit) {
+        *abort_flag = 1;
+        set_error(p.err, DEV_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Pair tile t -> (group, this CTA's 128 rows, first output column): m-tiles of
+// 256 rows per group (mt_pre counts them), CTA `rank` takes rows 128 rank ..
+template <int OUT_BN>
+__device__ __forceinline__ TileInfo decode_pair(int t, const int* mt_pre, const int* cu, int G, int n_tiles,
+                                                uint32_t rank) {
+  int lo = 0, hi = G - 1;
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (mt_pre[mid] * n_tiles <= t) lo = mid;
+    else hi = mid - 1;
+  }
+  const int g = lo;
+  const int mt_g = mt_pre[g + 1] - mt_pre[g];
+  const int local = t - mt_pre[g] * n_tiles;
+  const int m = local % mt_g, n = local / mt_g;
+  TileInfo ti;
+  ti.g = g;
+  ti.row0 = cu[g] + m * 2 * BM + (int)rank * BM;
+  ti.rows = max(0, min(BM, cu[g + 1] - ti.row0));
+  ti.n0 = n * OUT_BN;
+  return ti;
+}
+
+template <int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1) __cluster_dims__(2, 1, 1)
+tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const __grid_constant__ CUtensorMap tmB2, const Params p) {
+  static_assert(EPI == EPI_SWIGLU || EPI == EPI_BF16, "pair kernel: the expert FFN's two GEMMs");
+  using C = PairCfg<EPI>;
+  constexpr bool B_MN = EPI == EPI_SWIGLU;  // Wg / Wu [H][H'] are N-contiguous; Wd [H][H'] is K-contiguous
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stage_base = smem;
+  float* epi_stage = reinterpret_cast<float*>(smem + PAIR_STAGES * C::STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + PAIR_STAGES * C::STAGE_BYTES + C::EPI_BYTES);
+  __shared__ uint32_t tmem_base_slot;
+  __shared__ int abort_flag;
+  __shared__ int mt_pre[1025];
+  __shared__ int cu_s[1025];
+  __shared__ int total_tiles_s;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int G = p.G;
+  const uint32_t rank = cluster_rank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+  const int n_tiles = (p.N + C::OUT_BN - 1) / C::OUT_BN;
+
+  auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty_bar = [&](int s) { return smem_u32(&bars[PAIR_STAGES + s]); };
+  auto accf_bar = [&](int a) { return smem_u32(&bars[2 * PAIR_STAGES + a]); };
+  auto acce_bar = [&](int a) { return smem_u32(&bars[2 * PAIR_STAGES + 2 + a]); };
+  const uint32_t drain_bar = smem_u32(&bars[2 * PAIR_STAGES + 4]);
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < PAIR_STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(accf_bar(a), 1);
+      mbar_init(acce_bar(a), 2 * 128);  // the epilogue threads of both CTAs
+    }
+    mbar_init(drain_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+    if (EPI == EPI_SWIGLU) prefetch_tmap(&tmB2);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base_slot)),
+                 "r"((uint32_t)C::TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
+  }
+  if (warp == 2) {
+    for (int base = 0; base <= G; base += 32 * 8) {
+      int v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = base + u * 32 + lane;
+        v[u] = i <= G ? p.cu[i] : 0;
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const int i = base + u * 32 + lane;
+        if (i <= G) cu_s[i] = v[u];
+      }
+    }
+    __syncwarp();
+    // pair m-tiles (256 rows) per group, prefix over groups
+    const int per = (G + 31) / 32;
+    int sum = 0;
+    for (int g = lane * per; g < min(G, lane * per + per); ++g) sum += (max(0, cu_s[g + 1] - cu_s[g]) + 2 * BM - 1) / (2 * BM);
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - sum;
+    for (int g = lane * per; g < min(G, lane * per + per); ++g) {
+      mt_pre[g] = run;
+      run += (max(0, cu_s[g + 1] - cu_s[g]) + 2 * BM - 1) / (2 * BM);
+    }
+    if (lane == 0 && (cu_s[0] != 0 || cu_s[G] != p.M)) set_error(p.err, DEV_BOUNDS);
+    if (lane == 31) {
+      mt_pre[G] = incl;
+      total_tiles_s = incl * n_tiles;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the peer's barriers are initialised before anything arrives on them
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_slot;
+  const int total_tiles = total_tiles_s;
+  const int KB_ALL = (p.K + BK - 1) / BK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int filled_parity[PAIR_STAGES];
+      for (int s = 0; s < PAIR_STAGES; ++s) filled_parity[s] = -1;
+      bool ok = true;
+      for (int t = pair; ok && t < total_tiles; t += n_pairs) {
+        const TileInfo ti = decode_pair<C::OUT_BN>(t, mt_pre, cu_s, G, n_tiles, rank);
+        for (int kb = 0; kb < KB_ALL; ++kb) {
+          if (!wait_bounded(empty_bar(stage), phase ^ 1u, &abort_flag, p)) { ok = false; break; }
+          const uint32_t a_dst = smem_u32(stage_base + stage * C::STAGE_BYTES);
+          const uint32_t b_dst = a_dst + A_STAGE_BYTES;
+          const int k0 = kb * BK;
+          if (leader) {
+            mbar_expect_tx(full_bar(stage), 2 * C::STAGE_BYTES);  // this CTA's bytes and the peer's
+            filled_parity[stage] = (int)phase;
+          }
+          const uint32_t fb = cluster_addr(full_bar(stage), 0);
+          tma_load_3d_pair(a_dst, &tmA, fb, k0, ti.row0, 0);
+          if constexpr (B_MN) {
+            // the leader stages the gate columns, the peer the up columns
+            const CUtensorMap* m = leader ? &tmB : &tmB2;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) tma_load_3d_pair(b_dst + c * (64 * BK * 2), m, fb, ti.n0 + c * 64, k0, ti.g);
+          } else {
+            tma_load_3d_pair(b_dst, &tmB, fb, k0, ti.n0 + (int)rank * (PAIR_BN / 2), ti.g);
+          }
+          if (++stage == PAIR_STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+      // drain (leader): every stage filled must have landed, both CTAs' bytes
+      if (leader) {
+        for (int s = 0; s < PAIR_STAGES; ++s) {
+          if (filled_parity[s] < 0) continue;
+          const long long t0 = clock64();
+          while (!mbar_try_wait(full_bar(s), (uint32_t)filled_parity[s])) {
+            if ((unsigned long long)(clock64() - t0) > DRAIN_LIMIT) { set_error(p.err, DEV_TIMEOUT); break; }
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------- MMA issuer (leader only)
+    if (lane == 0 && leader) {
+      constexpr uint32_t IDESC = instr_desc(2 * BM, PAIR_BN, false, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      bool issued = false;
+      int i = 0;
+      for (int t = pair; ok && t < total_tiles; t += n_pairs, ++i) {
+        const int acc = i & 1;
+        if (!wait_bounded_cluster(acce_bar(acc), (((uint32_t)i >> 1) & 1u) ^ 1u, &abort_flag, p)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * PAIR_BN;
+        for (int kb = 0; kb < KB_ALL; ++kb) {
+          if (!wait_bounded(full_bar(stage), phase, &abort_flag, p)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_t = smem_u32(stage_base + stage * C::STAGE_BYTES);
+          const uint32_t b_t = a_t + A_STAGE_BYTES;
+#pragma unroll
+          for (int k = 0; k < BK / 16; ++k) {
+            const uint64_t adesc = smem_desc(a_t + k * 32, 16, 1024);
+            const uint64_t bdesc = B_MN ? smem_desc(b_t + k * 16 * 128, 64 * BK * 2, 1024) : smem_desc(b_t + k * 32, 16, 1024);
+            tc_mma_pair(d_tmem, adesc, bdesc, IDESC, (kb > 0 || k > 0) ? 1u : 0u);
+          }
+          issued = true;
+          tc_commit_pair(empty_bar(stage), 3);
+          if (++stage == PAIR_STAGES) { stage = 0; phase ^= 1u; }
+        }
+        if (!ok) break;
+        tc_commit_pair(accf_bar(acc), 3);
+      }
+      if (issued) {
+        tc_commit_pair(drain_bar, 1);
+        const long long t0 = clock64();
+        while (!mbar_try_wait(drain_bar, 0)) {
+          if ((unsigned long long)(clock64() - t0) > DRAIN_LIMIT) { set_error(p.err, DEV_TIMEOUT); break; }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int r_local = q * 32 + lane;
+    int i = 0;
+    for (int t = pair; t < total_tiles; t += n_pairs, ++i) {
+      const int acc = i & 1;
+      if (!wait_bounded(accf_bar(acc), ((uint32_t)i >> 1) & 1u, &abort_flag, p)) break;
+      tc_fence_after();
+      const TileInfo ti = decode_pair<C::OUT_BN>(t, mt_pre, cu_s, G, n_tiles, rank);
+      const long long grow = (long long)ti.row0 + r_local;
+      const bool row_ok = r_local < ti.rows && grow < p.M;
+      const uint32_t tbase = tmem_base + acc * PAIR_BN + ((uint32_t)(q * 32) << 16);
+      if constexpr (EPI == EPI_SWIGLU) epi_swiglu<C::OUT_BN>(p, tbase, ti, row_ok, grow);
+      else epi_bf16<C::OUT_BN>(p, tbase, ti, epi_stage, q, lane);
+      tc_fence_before();
+      if (leader) mbar_arrive(acce_bar(acc));
+      else mbar_arrive_remote(cluster_addr(acce_bar(acc), 0));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs are done with tensor memory and with each other's barriers
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"((uint32_t)C::TMEM_COLS));
+  }
+}
+
 // Failure-detection probe: one thread waits on an mbarrier that nothing ever
 // arrives at, with the bounded wait of the pipelined kernels above; it gives up
 // after p.wait_limit cycles and records DEV_TIMEOUT, as a stalled pipeline would.
@@ -1025,6 +1382,52 @@ int launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, co
   return launch_status();
 }
 
+// Pairs resident at once for the pair kernel (cached per device and kernel):
+// clusters of two SMs with one CTA each.
+template <int EPI>
+int pair_slots() {
+  static int cached[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    cudaGetLastError();
+    return sm_count() / 2;
+  }
+  if (cached[dev] > 0) return cached[dev];
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = PairCfg<EPI>::SMEM;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<EPI>, &cfg) != cudaSuccess || n < 1) {
+    cudaGetLastError();
+    n = sm_count() / 2;
+  }
+  cached[dev] = n;
+  return n;
+}
+
+template <int EPI>
+int launch_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const Params& p,
+                long long pair_tiles_upper, cudaStream_t s) {
+  using C = PairCfg<EPI>;
+  static_assert(C::SMEM + 8500 <= 227 * 1024, "smem (dynamic + static)");
+  auto k = tc_gemm_pair_kernel<EPI>;
+  if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  long long pairs = pair_slots<EPI>();
+  if (pair_tiles_upper < pairs) pairs = pair_tiles_upper;
+  if (pairs < 1) return MOE_OK;
+  k<<<(unsigned)(2 * pairs), NUM_THREADS, C::SMEM, s>>>(a, b, b2, p);
+  return launch_status();
+}
+
 // [rows, inner] bf16 matrix as a 3D map {inner, rows, 1}
 bool map_2d_as_3d(CUtensorMap* m, const void* base, long long inner, long long rows, int box_inner, int box_rows) {
   cuuint64_t dims[3] = {(cuuint64_t)inner, (cuuint64_t)rows, 1};
@@ -1065,12 +1468,21 @@ int launch_expert_ffn_tc(const void* xs, const int32_t* cu, int rows, const void
   Params p1 = params(cu, E, rows, Hp, H, act, Hp, nullptr);
   p1.aux = gu;  // nullable: g and u kept for the backward
   p1.ld_aux = 2LL * Hp;
+  Params p2 = params(cu, E, rows, H, Hp, h, H, nullptr);
+  if (!gather) {
+    // CTA pairs: 256-row tiles, each CTA staging half of the B columns
+    CUtensorMap mDh;
+    if (!map_3d(&mDh, wd, Hp, H, E, BK, PAIR_BN / 2)) return MOE_ERR_CUDA;
+    const long long ptiles = (rows + 2 * BM - 1) / (2 * BM) + E;
+    int st = launch_pair<EPI_SWIGLU>(mA, mG, mU, p1, ptiles * ((Hp + 127) / 128), s);
+    if (st != MOE_OK) return st;
+    return launch_pair<EPI_BF16>(mA2, mDh, mDh, p2, ptiles * ((H + 255) / 256), s);
+  }
   p1.gather = gather;
   p1.gather_src = static_cast<const bf16*>(xs);
   p1.gather_n = gather_n;
   int st = launch<EPI_SWIGLU, false, true, 256, 4, 1, 1>(mA, mG, mU, p1, mtiles * ((Hp + 127) / 128), s);
   if (st != MOE_OK) return st;
-  Params p2 = params(cu, E, rows, H, Hp, h, H, nullptr);
   return launch<EPI_BF16, false, false, 256, 4, 1, 1>(mA2, mD, mD, p2, mtiles * ((H + 255) / 256), s);
 }
 
