@@ -1232,7 +1232,8 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             // the leader stages the gate columns, the peer the up columns
             const CUtensorMap* m = leader ? &tmB : &tmB2;
 #pragma unroll
-            for (int c = 0; c < 2; ++c) tma_load_3d_pair(b_dst + c * (64 * BK * 2), m, fb, ti.n0 + c * 64, k0, ti.g);
+            for (int c = 0; c < 2; ++c)
+              tma_load_3d_pair(b_dst + c * (64 * BK * 2), m, fb, ti.n0 + c * 64, k0, ti.g);
           } else {
             tma_load_3d_pair(b_dst, &tmB, fb, k0, ti.n0 + (int)rank * (PAIR_BN / 2), ti.g);
           }
@@ -1463,7 +1464,8 @@ int launch_expert_ffn_tc(const void* xs, const int32_t* cu, int rows, const void
   if (!map_3d(&mG, wg, Hp, H, E, 64, BK)) return MOE_ERR_CUDA;
   if (!map_3d(&mU, wu, Hp, H, E, 64, BK)) return MOE_ERR_CUDA;
   if (!map_2d_as_3d(&mA2, act, Hp, rows, BK, BM)) return MOE_ERR_CUDA;
-  if (!map_3d(&mD, wd, Hp, H, E, BK, 256)) return MOE_ERR_CUDA;
+  // down-projection B: 256-row boxes for one CTA, 128-row halves for a pair
+  if (!map_3d(&mD, wd, Hp, H, E, BK, gather ? 256 : PAIR_BN / 2)) return MOE_ERR_CUDA;
   const long long mtiles = (rows + BM - 1) / BM + E;
   Params p1 = params(cu, E, rows, Hp, H, act, Hp, nullptr);
   p1.aux = gu;  // nullable: g and u kept for the backward
@@ -1471,12 +1473,10 @@ int launch_expert_ffn_tc(const void* xs, const int32_t* cu, int rows, const void
   Params p2 = params(cu, E, rows, H, Hp, h, H, nullptr);
   if (!gather) {
     // CTA pairs: 256-row tiles, each CTA staging half of the B columns
-    CUtensorMap mDh;
-    if (!map_3d(&mDh, wd, Hp, H, E, BK, PAIR_BN / 2)) return MOE_ERR_CUDA;
     const long long ptiles = (rows + 2 * BM - 1) / (2 * BM) + E;
     int st = launch_pair<EPI_SWIGLU>(mA, mG, mU, p1, ptiles * ((Hp + 127) / 128), s);
     if (st != MOE_OK) return st;
-    return launch_pair<EPI_BF16>(mA2, mDh, mDh, p2, ptiles * ((H + 255) / 256), s);
+    return launch_pair<EPI_BF16>(mA2, mD, mD, p2, ptiles * ((H + 255) / 256), s);
   }
   p1.gather = gather;
   p1.gather_src = static_cast<const bf16*>(xs);
