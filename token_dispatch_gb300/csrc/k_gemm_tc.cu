@@ -321,6 +321,70 @@ __device__ __forceinline__ void epi_swiglu(const Params& p, uint32_t tbase, cons
   }
 }
 
+// EPI_SWIGLU_BWD: the accumulator is da; with g, u read back from p.aux it
+// writes dg and du (bf16) side by side.
+template <int OUT_BN>
+__device__ __forceinline__ void epi_swiglu_bwd(const Params& p, uint32_t tbase, const TileInfo& ti, bool row_ok,
+                                               long long grow) {
+  // da for 32 columns at a time; g and u of the same columns come from
+  // p.aux ([g | u] per row); dg and du go to p.out ([dg | du] per row)
+  //   dg = da * u * s(g) * (1 + g * (1 - s(g))),  du = da * g * s(g)
+  // The g, u loads of chunk c + 1 are issued before chunk c is computed (the
+  // loop stays rolled: the next chunk's registers move into the current's).
+  bf16* out = static_cast<bf16*>(p.out);
+  const bf16* ax = static_cast<const bf16*>(p.aux);
+  uint4 gq[4], uq[4], gn[4], un[4];
+  auto load = [&](int c, uint4 (&g)[4], uint4 (&u)[4]) {
+    const int col = ti.n0 + c * 32;
+    if (row_ok && col < p.N) {
+      const uint4* gs = reinterpret_cast<const uint4*>(ax + grow * p.ld_aux + col);
+      const uint4* us = reinterpret_cast<const uint4*>(ax + grow * p.ld_aux + p.N + col);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        g[j] = gs[j];
+        u[j] = us[j];
+      }
+    }
+  };
+  load(0, gq, uq);
+#pragma unroll 1
+  for (int c = 0; c < OUT_BN / 32; ++c) {
+    if (c + 1 < OUT_BN / 32) load(c + 1, gn, un);
+    float da[32];
+    tmem_ld32(tbase + c * 32, da);
+    const int col = ti.n0 + c * 32;
+    if (row_ok && col < p.N) {
+      uint4 dgp[4], dup[4];
+      const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(gq);
+      const __nv_bfloat162* u2 = reinterpret_cast<const __nv_bfloat162*>(uq);
+      __nv_bfloat162* dg2 = reinterpret_cast<__nv_bfloat162*>(dgp);
+      __nv_bfloat162* du2 = reinterpret_cast<__nv_bfloat162*>(dup);
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float2 g = __bfloat1622float2(g2[j]);
+        const float2 u = __bfloat1622float2(u2[j]);
+        const float s0 = 1.0f / (1.0f + __expf(-g.x)), s1 = 1.0f / (1.0f + __expf(-g.y));
+        const float a0 = da[2 * j], a1 = da[2 * j + 1];
+        dg2[j] = __floats2bfloat162_rn(a0 * u.x * s0 * (1.0f + g.x * (1.0f - s0)),
+                                       a1 * u.y * s1 * (1.0f + g.y * (1.0f - s1)));
+        du2[j] = __floats2bfloat162_rn(a0 * g.x * s0, a1 * g.y * s1);
+      }
+      uint4* dgd = reinterpret_cast<uint4*>(out + grow * p.ldo + col);
+      uint4* dud = reinterpret_cast<uint4*>(out + grow * p.ldo + p.N + col);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        dgd[j] = dgp[j];
+        dud[j] = dup[j];
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      gq[j] = gn[j];
+      uq[j] = un[j];
+    }
+  }
+}
+
 // EPI_BF16: the fp32 tile rounded to bf16 (plus the old values with
 // p.accumulate), through the warp's [32][STG_LD] staging tile.
 template <int OUT_BN>
@@ -766,49 +830,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       if (EPI == EPI_SWIGLU) {
         epi_swiglu<C::OUT_BN>(p, tbase, ti, row_ok, grow);
       } else if (EPI == EPI_SWIGLU_BWD) {
-        // da for 32 columns at a time; g and u of the same columns come from
-        // p.aux ([g | u] per row); dg and du go to p.out ([dg | du] per row)
-        //   dg = da * u * s(g) * (1 + g * (1 - s(g))),  du = da * g * s(g)
-        bf16* out = static_cast<bf16*>(p.out);
-        const bf16* ax = static_cast<const bf16*>(p.aux);
-#pragma unroll 1
-        for (int c = 0; c < C::OUT_BN / 32; ++c) {
-          float da[32];
-          tmem_ld32(tbase + c * 32, da);
-          const int col = ti.n0 + c * 32;
-          if (row_ok && col < p.N) {
-            const uint4* gs = reinterpret_cast<const uint4*>(ax + grow * p.ld_aux + col);
-            const uint4* us = reinterpret_cast<const uint4*>(ax + grow * p.ld_aux + p.N + col);
-            uint4 gq[4], uq[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              gq[j] = gs[j];
-              uq[j] = us[j];
-            }
-            uint4 dgp[4], dup[4];
-            const __nv_bfloat162* g2 = reinterpret_cast<const __nv_bfloat162*>(gq);
-            const __nv_bfloat162* u2 = reinterpret_cast<const __nv_bfloat162*>(uq);
-            __nv_bfloat162* dg2 = reinterpret_cast<__nv_bfloat162*>(dgp);
-            __nv_bfloat162* du2 = reinterpret_cast<__nv_bfloat162*>(dup);
-#pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float2 g = __bfloat1622float2(g2[j]);
-              const float2 u = __bfloat1622float2(u2[j]);
-              const float s0 = 1.0f / (1.0f + __expf(-g.x)), s1 = 1.0f / (1.0f + __expf(-g.y));
-              const float a0 = da[2 * j], a1 = da[2 * j + 1];
-              dg2[j] = __floats2bfloat162_rn(a0 * u.x * s0 * (1.0f + g.x * (1.0f - s0)),
-                                             a1 * u.y * s1 * (1.0f + g.y * (1.0f - s1)));
-              du2[j] = __floats2bfloat162_rn(a0 * g.x * s0, a1 * g.y * s1);
-            }
-            uint4* dgd = reinterpret_cast<uint4*>(out + grow * p.ldo + col);
-            uint4* dud = reinterpret_cast<uint4*>(out + grow * p.ldo + p.N + col);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              dgd[j] = dgp[j];
-              dud[j] = dup[j];
-            }
-          }
-        }
+        epi_swiglu_bwd<C::OUT_BN>(p, tbase, ti, row_ok, grow);
       } else if (EPI == EPI_F32_GK) {
         // fp32 tile of group wk.slab through this warp's staging tile: 4 rows x
         // 128 bytes per store instruction; a group without rows gets zeros
@@ -1010,6 +1032,9 @@ struct PairCfg {
   static constexpr int B_HALF_BYTES = (PAIR_BN / 2) * BK * 2;
   static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_HALF_BYTES;
   static constexpr int OUT_BN = EPI == EPI_SWIGLU ? PAIR_BN / 2 : PAIR_BN;
+  // B N-contiguous (MN-major: Wg / Wu / Wd read as [K = H][N = H']) or
+  // K-contiguous (Wd, or Wg / Wu in the backward, read as [N = H][K = H'])
+  static constexpr bool B_MN = EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD;
   static constexpr int TMEM_COLS = 2 * PAIR_BN;
   static constexpr int EPI_BYTES = EPI == EPI_BF16 ? 4 * 32 * STG_LD * 4 : 0;
   static constexpr size_t SMEM = (size_t)PAIR_STAGES * STAGE_BYTES + EPI_BYTES + (2 * PAIR_STAGES + 5) * 8 + 1024;
@@ -1114,9 +1139,10 @@ template <int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1) __cluster_dims__(2, 1, 1)
 tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmB2, const Params p) {
-  static_assert(EPI == EPI_SWIGLU || EPI == EPI_BF16, "pair kernel: the expert FFN's two GEMMs");
+  static_assert(EPI == EPI_SWIGLU || EPI == EPI_BF16 || EPI == EPI_SWIGLU_BWD,
+                "pair kernel: the expert FFN's GEMMs with a row-major output");
   using C = PairCfg<EPI>;
-  constexpr bool B_MN = EPI == EPI_SWIGLU;  // Wg / Wu [H][H'] are N-contiguous; Wd [H][H'] is K-contiguous
+  constexpr bool B_MN = C::B_MN;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_base = smem;
@@ -1156,7 +1182,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
-    if (EPI == EPI_SWIGLU) prefetch_tmap(&tmB2);
+    if (EPI == EPI_SWIGLU || p.kcat) prefetch_tmap(&tmB2);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base_slot)),
@@ -1228,12 +1254,21 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           }
           const uint32_t fb = cluster_addr(full_bar(stage), 0);
           tma_load_3d_pair(a_dst, &tmA, fb, k0, ti.row0, 0);
-          if constexpr (B_MN) {
+          if constexpr (EPI == EPI_SWIGLU) {
             // the leader stages the gate columns, the peer the up columns
             const CUtensorMap* m = leader ? &tmB : &tmB2;
 #pragma unroll
             for (int c = 0; c < 2; ++c)
               tma_load_3d_pair(b_dst + c * (64 * BK * 2), m, fb, ti.n0 + c * 64, k0, ti.g);
+          } else if constexpr (B_MN) {
+            // each CTA stages its half of the 256 output columns
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+              tma_load_3d_pair(b_dst + c * (64 * BK * 2), &tmB, fb, ti.n0 + (int)rank * (PAIR_BN / 2) + c * 64, k0,
+                               ti.g);
+          } else if (p.kcat && k0 >= p.kcat) {
+            // K concatenated from two tensors: k >= kcat reads the second
+            tma_load_3d_pair(b_dst, &tmB2, fb, k0 - p.kcat, ti.n0 + (int)rank * (PAIR_BN / 2), ti.g);
           } else {
             tma_load_3d_pair(b_dst, &tmB, fb, k0, ti.n0 + (int)rank * (PAIR_BN / 2), ti.g);
           }
@@ -1305,6 +1340,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       const bool row_ok = r_local < ti.rows && grow < p.M;
       const uint32_t tbase = tmem_base + acc * PAIR_BN + ((uint32_t)(q * 32) << 16);
       if constexpr (EPI == EPI_SWIGLU) epi_swiglu<C::OUT_BN>(p, tbase, ti, row_ok, grow);
+      else if constexpr (EPI == EPI_SWIGLU_BWD) epi_swiglu_bwd<C::OUT_BN>(p, tbase, ti, row_ok, grow);
       else epi_bf16<C::OUT_BN>(p, tbase, ti, epi_stage, q, lane);
       tc_fence_before();
       if (leader) mbar_arrive(acce_bar(acc));
@@ -1495,7 +1531,8 @@ int launch_expert_ffn_bwd_tc(const void* xs, const int32_t* cu, int rows, const 
                              void* dgu, void* dxs, float* dwg, float* dwu, float* dwd, cudaStream_t s) {
   using namespace tc;
   if (E > 1024) return MOE_ERR_UNSUPPORTED;
-  const long long mtiles = (rows + BM - 1) / BM + E;
+  // da and dxs on CTA pairs (256-row tiles)
+  const long long ptiles = (rows + 2 * BM - 1) / (2 * BM) + E;
   int st;
   {  // dgu: A = dh (K-major, K = H), B = Wd[e] read as [K = H, N = H'] (MN-major)
     CUtensorMap mA, mB;
@@ -1504,17 +1541,17 @@ int launch_expert_ffn_bwd_tc(const void* xs, const int32_t* cu, int rows, const 
     Params p = params(cu, E, rows, Hp, H, dgu, 2LL * Hp, nullptr);
     p.aux = const_cast<void*>(gu);
     p.ld_aux = 2LL * Hp;
-    st = launch<EPI_SWIGLU_BWD, false, true, 256, 4, 1, 1>(mA, mB, mB, p, mtiles * ((Hp + 255) / 256), s);
+    st = launch_pair<EPI_SWIGLU_BWD>(mA, mB, mB, p, ptiles * ((Hp + 255) / 256), s);
     if (st != MOE_OK) return st;
   }
   if (dxs) {  // A = dgu (K-major, K = 2H'), B = Wg[e] then Wu[e], each [N = H rows, K = H'] (K-major)
     CUtensorMap mA, mG, mU;
     if (!map_2d_as_3d(&mA, dgu, 2LL * Hp, rows, BK, BM)) return MOE_ERR_CUDA;
-    if (!map_3d(&mG, wg, Hp, H, E, BK, 256)) return MOE_ERR_CUDA;
-    if (!map_3d(&mU, wu, Hp, H, E, BK, 256)) return MOE_ERR_CUDA;
+    if (!map_3d(&mG, wg, Hp, H, E, BK, PAIR_BN / 2)) return MOE_ERR_CUDA;
+    if (!map_3d(&mU, wu, Hp, H, E, BK, PAIR_BN / 2)) return MOE_ERR_CUDA;
     Params p = params(cu, E, rows, H, 2 * Hp, dxs, H, nullptr);
     p.kcat = Hp;
-    st = launch<EPI_BF16, false, false, 256, 4, 1, 1>(mA, mG, mU, p, mtiles * ((H + 255) / 256), s);
+    st = launch_pair<EPI_BF16>(mA, mG, mU, p, ptiles * ((H + 255) / 256), s);
     if (st != MOE_OK) return st;
   }
   // weight gradients: M = H (A = an [rows, H] matrix read transposed, MN-major),
