@@ -27,8 +27,13 @@ SHAPES = [
     S("bf16_T777_H256_E64_K6_Hp192", 777, 256, 64, 6, 192, "bf16"),
     S("f32_T300_H64_E12_K3_Hp96", 300, 64, 12, 3, 96, "f32"),
 ]
+# many experts: split over H into partials when the token tiles are few (T=300),
+# one pass on CTA pairs of 256 x 256 tiles otherwise (ragged T=6600 with a
+# half-empty last expert tile at E=384; E=1024)
 ROUTE_ONLY = [S("bf16_T300_H128_E384_K8", 300, 128, 384, 8, 64, "bf16"),
-              S("f32_T129_H32_E1024_K16", 129, 32, 1024, 16, 32, "f32")]
+              S("f32_T129_H32_E1024_K16", 129, 32, 1024, 16, 32, "f32"),
+              S("bf16_T6600_H128_E384_K8", 6600, 128, 384, 8, 64, "bf16"),
+              S("bf16_T4000_H256_E1024_K8", 4000, 256, 1024, 8, 64, "bf16")]
 # bf16 routers with 8 or 16 experts and H a multiple of 512 take the one-launch
 # streaming router: ragged token blocks of 8 to 64 tokens, fewer blocks than
 # SMs, slices of H from 32 to 256 columns per warp

@@ -385,6 +385,40 @@ __device__ __forceinline__ void epi_swiglu_bwd(const Params& p, uint32_t tbase, 
   }
 }
 
+// EPI_F32_BIAS (CTA pairs): the fp32 tile plus the bias of its columns,
+// 32 columns at a time through the warp's staging tile: 4 rows x 128 bytes per
+// store instruction; columns at or past N are not stored.
+template <int OUT_BN>
+__device__ __forceinline__ void epi_f32_bias(const Params& p, uint32_t tbase, const TileInfo& ti, float* epi_stage,
+                                             int q, int lane) {
+  float* out = static_cast<float*>(p.out);
+  float* stg = epi_stage + q * 32 * STG_LD;
+  const int seg = (lane & 7) * 4;
+#pragma unroll 1
+  for (int c = 0; c < OUT_BN / 32; ++c) {
+    float v[32];
+    tmem_ld32(tbase + c * 32, v);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) stg[lane * STG_LD + j] = v[j];
+    __syncwarp();
+    const int col = ti.n0 + c * 32 + seg;
+    float4 bb = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (p.bias && col < p.N) bb = __ldg(reinterpret_cast<const float4*>(p.bias + col));
+#pragma unroll
+    for (int ps = 0; ps < 8; ++ps) {
+      const int rw = ps * 4 + (lane >> 3);
+      const int rr = q * 32 + rw;
+      const long long gr = (long long)ti.row0 + rr;
+      if (rr < ti.rows && gr < p.M && col < p.N) {
+        const float* sp = stg + rw * STG_LD + seg;
+        *reinterpret_cast<float4*>(out + gr * p.ldo + col) =
+            make_float4(sp[0] + bb.x, sp[1] + bb.y, sp[2] + bb.z, sp[3] + bb.w);
+      }
+    }
+    __syncwarp();
+  }
+}
+
 // EPI_BF16: the fp32 tile rounded to bf16 (plus the old values with
 // p.accumulate), through the warp's [32][STG_LD] staging tile.
 template <int OUT_BN>
@@ -1032,11 +1066,12 @@ struct PairCfg {
   static constexpr int B_HALF_BYTES = (PAIR_BN / 2) * BK * 2;
   static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_HALF_BYTES;
   static constexpr int OUT_BN = EPI == EPI_SWIGLU ? PAIR_BN / 2 : PAIR_BN;
-  // B N-contiguous (MN-major: Wg / Wu / Wd read as [K = H][N = H']) or
-  // K-contiguous (Wd, or Wg / Wu in the backward, read as [N = H][K = H'])
-  static constexpr bool B_MN = EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD;
+  // B N-contiguous (MN-major: Wg / Wu / Wd read as [K = H][N = H'], W_r as
+  // [K = H][N = E]) or K-contiguous (Wd, or Wg / Wu in the backward, read as
+  // [N = H][K = H'])
+  static constexpr bool B_MN = EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD || EPI == EPI_F32_BIAS;
   static constexpr int TMEM_COLS = 2 * PAIR_BN;
-  static constexpr int EPI_BYTES = EPI == EPI_BF16 ? 4 * 32 * STG_LD * 4 : 0;
+  static constexpr int EPI_BYTES = (EPI == EPI_BF16 || EPI == EPI_F32_BIAS) ? 4 * 32 * STG_LD * 4 : 0;
   static constexpr size_t SMEM = (size_t)PAIR_STAGES * STAGE_BYTES + EPI_BYTES + (2 * PAIR_STAGES + 5) * 8 + 1024;
 };
 
@@ -1139,8 +1174,8 @@ template <int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1) __cluster_dims__(2, 1, 1)
 tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmB2, const Params p) {
-  static_assert(EPI == EPI_SWIGLU || EPI == EPI_BF16 || EPI == EPI_SWIGLU_BWD,
-                "pair kernel: the expert FFN's GEMMs with a row-major output");
+  static_assert(EPI == EPI_SWIGLU || EPI == EPI_BF16 || EPI == EPI_SWIGLU_BWD || EPI == EPI_F32_BIAS,
+                "pair kernel: GEMMs with a row-major output");
   using C = PairCfg<EPI>;
   constexpr bool B_MN = C::B_MN;
   extern __shared__ uint8_t smem_raw[];
@@ -1190,12 +1225,13 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;");
   }
   if (warp == 2) {
+    // group boundaries (no cu: one group of M rows)
     for (int base = 0; base <= G; base += 32 * 8) {
       int v[8];
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
         const int i = base + u * 32 + lane;
-        v[u] = i <= G ? p.cu[i] : 0;
+        v[u] = i <= G ? (p.cu ? p.cu[i] : (i == 0 ? 0 : p.M)) : 0;
       }
 #pragma unroll
       for (int u = 0; u < 8; ++u) {
@@ -1341,6 +1377,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       const uint32_t tbase = tmem_base + acc * PAIR_BN + ((uint32_t)(q * 32) << 16);
       if constexpr (EPI == EPI_SWIGLU) epi_swiglu<C::OUT_BN>(p, tbase, ti, row_ok, grow);
       else if constexpr (EPI == EPI_SWIGLU_BWD) epi_swiglu_bwd<C::OUT_BN>(p, tbase, ti, row_ok, grow);
+      else if constexpr (EPI == EPI_F32_BIAS) epi_f32_bias<C::OUT_BN>(p, tbase, ti, epi_stage, q, lane);
       else epi_bf16<C::OUT_BN>(p, tbase, ti, epi_stage, q, lane);
       tc_fence_before();
       if (leader) mbar_arrive(acce_bar(acc));
@@ -1627,6 +1664,12 @@ int launch_router_tc(const void* x, const void* w, const float* bias, const floa
   // request 512 (256) contiguous bytes of every row at a time
   if (E <= 64) return launch<EPI_F32_BIAS, false, true, 64, 2, 4, 4, 4>(mA, mB, mB, p, tiles, s);
   if (E <= 128) return launch<EPI_F32_BIAS, false, true, 128, 3, 2, 2, 2>(mA, mB, mB, p, tiles, s);
+  if (S == 1) {
+    // CTA pairs: 256 tokens x 256 experts per tile (columns past E read as
+    // zeros and are not stored)
+    const long long ptiles = (T + 2 * BM - 1) / (2 * BM) * ((E + PAIR_BN - 1) / PAIR_BN);
+    return launch_pair<EPI_F32_BIAS>(mA, mB, mB, p, ptiles, s);
+  }
   if (E % 192 == 0) return launch<EPI_F32_BIAS, false, true, 192, 5, 1, 1>(mA, mB, mB, p, tiles * (E / 192), s);
   return launch<EPI_F32_BIAS, false, true, 256, 4, 1, 1>(mA, mB, mB, p, tiles * ((E + 255) / 256), s);
 }
