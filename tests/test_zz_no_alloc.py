@@ -7,8 +7,9 @@ table dispatch needs (per-chunk expert counts) in a static device array.  This
 file checks, through the C ABI, that the variant gives exactly the results of
 moe_dispatch with a caller workspace, on two calls in a row with different
 sizes (the shared array keeps the previous call's contents), at the largest
-table the array holds, for fp32 rows and for an empty batch, and that sizes
-past the array's capacity are refused before anything runs.
+table the array holds, for fp32 rows, for an empty batch and when captured in
+a CUDA graph and replayed on new inputs, and that sizes past the array's
+capacity are refused before anything runs.
 
 The file name sorts last so that a run stopping at the first failure has run
 every other test before this one."""
@@ -94,3 +95,51 @@ def test_noalloc_refuses_sizes_past_the_static_scratch():
     # one token past the largest table that fits: 64 * 1024 + 1024 > 65536
     st = raw.moe_dispatch_noalloc(A, A, 63 * 256 + 1, 64, 1024, 2, L.MOE_BF16, A, A, A, A, None)
     assert st == L.MOE_ERR_WORKSPACE
+
+
+def test_noalloc_replays_in_a_cuda_graph_on_new_inputs():
+    # one eager call first (it resolves the static array's address), then the
+    # call captured once on a side stream and replayed after the inputs are
+    # overwritten in place: every replay must equal moe_dispatch on the same
+    # inputs, bit for bit
+    raw = L.lib()
+    T, H, E, K = 3000, 128, 64, 6
+    x = torch.empty((T, H), dtype=torch.bfloat16, device=DEV)
+    idx = torch.empty((T, K), dtype=torch.int32, device=DEV)
+    cu = torch.empty((E + 1,), dtype=torch.int32, device=DEV)
+    dst = torch.empty((T * K,), dtype=torch.int32, device=DEV)
+    src = torch.empty((T * K,), dtype=torch.int32, device=DEV)
+    xs = torch.empty((T * K, H), dtype=torch.bfloat16, device=DEV)
+
+    def fill(seed):
+        g = torch.Generator().manual_seed(seed)
+        x.copy_(torch.randn((T, H), generator=g).to(torch.bfloat16))
+        idx.copy_(torch.from_numpy(idx_for(T, E, K, seed)))
+
+    def call(stream):
+        return raw.moe_dispatch_noalloc(x.data_ptr(), idx.data_ptr(), T, H, E, K, L.MOE_BF16, cu.data_ptr(),
+                                        dst.data_ptr(), src.data_ptr(), xs.data_ptr(), stream)
+
+    fill(10)
+    assert call(torch.cuda.current_stream().cuda_stream) == L.MOE_OK
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        st = call(side.cuda_stream)
+    assert st == L.MOE_OK
+    for seed in (11, 12):
+        fill(seed)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert raw.moe_last_device_error(None) == L.MOE_OK
+        ref = (torch.empty_like(cu), torch.empty_like(dst), torch.empty_like(src), torch.empty_like(xs))
+        nbytes = raw.moe_workspace_bytes(L.MOE_OP_DISPATCH, T, H, E, K, 0)
+        ws = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=DEV)
+        st = raw.moe_dispatch(x.data_ptr(), idx.data_ptr(), T, H, E, K, L.MOE_BF16, ref[0].data_ptr(),
+                              ref[1].data_ptr(), ref[2].data_ptr(), ref[3].data_ptr(), ws.data_ptr(), nbytes, None)
+        assert st == L.MOE_OK
+        torch.cuda.synchronize()
+        for a, b in zip(ref[:3], (cu, dst, src)):
+            assert torch.equal(a, b)
+        assert torch.equal(ref[3].view(torch.int16), xs.view(torch.int16))
