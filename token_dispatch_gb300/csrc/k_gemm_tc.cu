@@ -1523,6 +1523,246 @@ Params params(const int32_t* cu, int G, int M, int N, int K, void* out, long lon
   return Params{cu, G, M, N, K, out, ldo, bias, device_error_word(), g_wait_limit, 1, 0, 0};
 }
 
+// ---------------------------------------------- router backward, one pass ---
+// Router backward for bf16 routers with 32..64 experts (E % 8 == 0, padded to
+// 64 by TMA zero fill) in one launch after the softmax backward: with the
+// logit gradient split exactly into three bf16 parts dl = hi + mid + lo,
+//   dW_r[h, e] = sum_t x[t, h] dl[t, e]        (fp32 partials per token range)
+//   dx[t, h]  (+)= sum_e dl[t, e] W_r[h, e]    (bf16, read-modify-write)
+// A CTA owns a 128-column slice of H and a range of 128-token blocks.  Per
+// block one TMA stage brings the x tile (128 tokens x 128 columns, two
+// M-contiguous boxes) and the three dl parts (128 tokens x 64 experts each);
+// the same dl boxes are the N-contiguous B operand of dW (N = 192: the three
+// parts side by side) and the K-major A operand of dx (M = 128 tokens, K = 3 x
+// 64), so dl is read once for both products and x once.  dW accumulates in
+// tensor memory over the CTA's whole token range (columns [0, 192)); dx uses two
+// accumulators (columns [256, 384) and [384, 512)) so the epilogue of one block
+// overlaps the next block's MMAs.  W_r's slice (128 x 64) is loaded once.
+constexpr int RB_STAGES = 2;
+constexpr int RB_TB = 128;                               // tokens per block
+constexpr int RB_HS = 128;                               // H columns per CTA
+constexpr int RB_X_BYTES = RB_TB * RB_HS * 2;            // 32 KB: two 64-column boxes
+constexpr int RB_DL_BYTES = 3 * RB_TB * 64 * 2;          // 48 KB: three parts
+constexpr int RB_STAGE_BYTES = RB_X_BYTES + RB_DL_BYTES;
+constexpr int RB_W_BYTES = RB_HS * 64 * 2;               // 16 KB
+// two epilogue warp groups, one per dx accumulator: consecutive blocks'
+// read-modify-write round trips overlap
+constexpr int RB_THREADS = 64 + 2 * 128;
+constexpr int RB_STG_BYTES = 8 * 32 * STG_LD * 4;
+constexpr size_t RB_SMEM = (size_t)RB_STAGES * RB_STAGE_BYTES + RB_W_BYTES + RB_STG_BYTES + 16 * 8 + 1024;
+
+__global__ void __launch_bounds__(RB_THREADS, 1)
+router_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmDL,
+                     const __grid_constant__ CUtensorMap tmW, const Params p, int n_slices, int splits,
+                     int n_blocks, float* part, int E) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* stage_base = smem;
+  uint8_t* w_tile = smem + RB_STAGES * RB_STAGE_BYTES;
+  float* epi_stage = reinterpret_cast<float*>(w_tile + RB_W_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(epi_stage) + RB_STG_BYTES);
+  // bars: full[2], empty[2], accf[2], acce[2], w_full, dw_full, drain
+  __shared__ uint32_t tmem_base_slot;
+  __shared__ int abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
+  auto empty_bar = [&](int s) { return smem_u32(&bars[RB_STAGES + s]); };
+  auto accf_bar = [&](int a) { return smem_u32(&bars[2 * RB_STAGES + a]); };
+  auto acce_bar = [&](int a) { return smem_u32(&bars[2 * RB_STAGES + 2 + a]); };
+  const uint32_t w_bar = smem_u32(&bars[2 * RB_STAGES + 4]);
+  const uint32_t dw_bar = smem_u32(&bars[2 * RB_STAGES + 5]);
+  const uint32_t drain_bar = smem_u32(&bars[2 * RB_STAGES + 6]);
+  // this CTA's slice of H and range of token blocks
+  const int slice = blockIdx.x % n_slices, split = blockIdx.x / n_slices;
+  const int h0 = slice * RB_HS;
+  const int b_lo = (int)((long long)split * n_blocks / splits), b_hi = (int)((long long)(split + 1) * n_blocks / splits);
+  const bool do_dw = part != nullptr, do_dx = p.out != nullptr;
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < RB_STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(accf_bar(a), 1);
+      mbar_init(acce_bar(a), 128);
+    }
+    mbar_init(w_bar, 1);
+    mbar_init(dw_bar, 1);
+    mbar_init(drain_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    prefetch_tmap(&tmX);
+    prefetch_tmap(&tmDL);
+    prefetch_tmap(&tmW);
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base_slot)),
+                 "r"(512u));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int filled_parity[RB_STAGES];
+      for (int s = 0; s < RB_STAGES; ++s) filled_parity[s] = -1;
+      if (do_dx) {
+        mbar_expect_tx(w_bar, RB_W_BYTES);
+        tma_load_3d(smem_u32(w_tile), &tmW, w_bar, 0, h0, 0);
+      }
+      for (int b = b_lo; b < b_hi; ++b) {
+        if (!wait_bounded(empty_bar(stage), phase ^ 1u, &abort_flag, p)) break;
+        const uint32_t xs = smem_u32(stage_base + stage * RB_STAGE_BYTES), ds = xs + RB_X_BYTES;
+        const int t0 = b * RB_TB;
+        mbar_expect_tx(full_bar(stage), (do_dw ? RB_X_BYTES : 0) + RB_DL_BYTES);
+        filled_parity[stage] = (int)phase;
+        if (do_dw) {  // x tile: columns h0.. and h0 + 64.. of 128 token rows
+          tma_load_3d(xs, &tmX, full_bar(stage), h0, t0, 0);
+          tma_load_3d(xs + RB_TB * 128, &tmX, full_bar(stage), h0 + 64, t0, 0);
+        }
+#pragma unroll
+        for (int q = 0; q < 3; ++q) tma_load_3d(ds + q * (RB_TB * 128), &tmDL, full_bar(stage), 0, t0, q);
+        if (++stage == RB_STAGES) { stage = 0; phase ^= 1u; }
+      }
+      // drain: every copy this thread started has landed before exit
+      for (int s = 0; s < RB_STAGES; ++s) {
+        if (filled_parity[s] < 0) continue;
+        const long long t0 = clock64();
+        while (!mbar_try_wait(full_bar(s), (uint32_t)filled_parity[s])) {
+          if ((unsigned long long)(clock64() - t0) > DRAIN_LIMIT) { set_error(p.err, DEV_TIMEOUT); break; }
+        }
+      }
+      if (do_dx) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(w_bar, 0)) {
+          if ((unsigned long long)(clock64() - t0) > DRAIN_LIMIT) { set_error(p.err, DEV_TIMEOUT); break; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      // dW: M = 128 columns of H (x^T, M-contiguous), N = 192 (the three dl
+      // parts, N-contiguous), K = 128 tokens per block
+      constexpr uint32_t IDW = instr_desc(128, 192, true, true);
+      // dx: M = 128 tokens (dl part, K-major), N = 128 columns of H (W_r slice,
+      // K-major), K = 64 experts per part
+      constexpr uint32_t IDX = instr_desc(128, 128, false, false);
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = !do_dx || wait_bounded(w_bar, 0, &abort_flag, p);
+      bool issued = false;
+      tc_fence_after();
+      const uint32_t wt = smem_u32(w_tile);
+      int i = 0;
+      for (int b = b_lo; ok && b < b_hi; ++b, ++i) {
+        const int acc = i & 1;
+        if (do_dx && !wait_bounded(acce_bar(acc), (((uint32_t)i >> 1) & 1u) ^ 1u, &abort_flag, p)) { ok = false; break; }
+        if (!wait_bounded(full_bar(stage), phase, &abort_flag, p)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t xs = smem_u32(stage_base + stage * RB_STAGE_BYTES), ds = xs + RB_X_BYTES;
+        if (do_dw) {
+#pragma unroll
+          for (int k = 0; k < RB_TB / 16; ++k) {
+            // 16 token rows per step; 64-wide atoms one 16 KB box apart
+            const uint64_t adesc = smem_desc(xs + k * 16 * 128, RB_TB * 128, 1024);
+            const uint64_t bdesc = smem_desc(ds + k * 16 * 128, RB_TB * 128, 1024);
+            tc_mma(tmem_base, adesc, bdesc, IDW, (b > b_lo || k > 0) ? 1u : 0u);
+          }
+        }
+        if (do_dx) {
+          const uint32_t d = tmem_base + 256 + acc * 128;
+#pragma unroll
+          for (int q = 0; q < 3; ++q)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              const uint64_t adesc = smem_desc(ds + q * (RB_TB * 128) + k * 32, 16, 1024);
+              const uint64_t bdesc = smem_desc(wt + k * 32, 16, 1024);
+              tc_mma(d, adesc, bdesc, IDX, (q > 0 || k > 0) ? 1u : 0u);
+            }
+        }
+        issued = true;
+        tc_commit(empty_bar(stage));
+        if (do_dx) tc_commit(accf_bar(acc));
+        if (++stage == RB_STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (ok && do_dw) tc_commit(dw_bar);
+      if (issued) {
+        tc_commit(drain_bar);
+        const long long t0 = clock64();
+        while (!mbar_try_wait(drain_bar, 0)) {
+          if ((unsigned long long)(clock64() - t0) > DRAIN_LIMIT) { set_error(p.err, DEV_TIMEOUT); break; }
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    // group eg (warps 2-5 or 6-9) takes the blocks of accumulator eg
+    const int q = warp & 3;  // TMEM lane quadrant this warp may access
+    const int eg = (warp - 2) >> 2;
+    float* stg_g = epi_stage + eg * 4 * 32 * STG_LD;
+    if (do_dx) {
+      for (int b = b_lo + eg, i = eg; b < b_hi; b += 2, i += 2) {
+        const int acc = eg;
+        if (!wait_bounded(accf_bar(acc), ((uint32_t)i >> 1) & 1u, &abort_flag, p)) break;
+        tc_fence_after();
+        TileInfo ti;
+        ti.g = 0;
+        ti.row0 = b * RB_TB;
+        ti.rows = min(RB_TB, p.M - ti.row0);
+        ti.n0 = h0;
+        const uint32_t tbase = tmem_base + 256 + acc * 128 + ((uint32_t)(q * 32) << 16);
+        epi_bf16<RB_HS>(p, tbase, ti, stg_g, q, lane);
+        tc_fence_before();
+        mbar_arrive(acce_bar(acc));
+      }
+    }
+    if (do_dw && wait_bounded(dw_bar, 0, &abort_flag, p)) {
+      // TMEM lane = column h of W_r; dW[h, e] = hi + mid + lo (fixed order);
+      // group eg writes experts 32 eg .. 32 eg + 31; a CTA without tokens
+      // writes zeros
+      tc_fence_after();
+      const bool empty = b_hi <= b_lo;
+      const int h = h0 + q * 32 + lane;
+      const uint32_t tb = tmem_base + ((uint32_t)(q * 32) << 16);
+      float* out = part + ((long long)split * p.N + h) * E;
+      {
+        const int c = eg;
+        float hi[32], mid[32], lo[32];
+        if (!empty) {
+          tmem_ld32(tb + c * 32, hi);
+          tmem_ld32(tb + 64 + c * 32, mid);
+          tmem_ld32(tb + 128 + c * 32, lo);
+        }
+#pragma unroll
+        for (int j = 0; j < 32; j += 4) {
+          if (c * 32 + j < E) {
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (!empty)
+              v = make_float4(hi[j] + mid[j] + lo[j], hi[j + 1] + mid[j + 1] + lo[j + 1],
+                              hi[j + 2] + mid[j + 2] + lo[j + 2], hi[j + 3] + mid[j + 3] + lo[j + 3]);
+            *reinterpret_cast<float4*>(out + c * 32 + j) = v;
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(512u));
+  }
+}
+
 }  // namespace tc
 
 // act = silu(xs Wg[e]) * (xs Wu[e]);  h = act Wd[e]^T   (bf16, grouped by cu)
@@ -1675,21 +1915,23 @@ int launch_router_tc(const void* x, const void* w, const float* bias, const floa
 }
 
 // Split count for the router weight gradient on tensor cores: the (h tile x
-// token split) work items should fill whole waves of the GPU's SMs; among
-// split counts up to 64 (each split at least one 64-token block) a larger
-// count is taken only when it raises the wave efficiency by more than 2%.
+// token split) work items run in ceil(items / SMs) rounds, and a round costs a
+// fixed part (the first stage's latency, the fp32 partial tile's epilogue:
+// about 12 K blocks' worth) plus its K blocks; the split count (up to 64, each
+// split at least one 64-token block) with the smallest estimate wins, the
+// smaller count on ties.
 int router_dw_tc_splits(int T, int H, int E) {
   const long long tiles = ((H + tc::BM - 1) / tc::BM) * (long long)(E <= 64 ? 1 : (E + 127) / 128);
   const long long kb = (T + tc::BK - 1) / tc::BK;
   const long long sms = sm_count();
-  long long best = 1;
-  double best_eff = 0.0;
+  constexpr long long FIXED = 12;
+  long long best = 1, best_cost = -1;
   for (long long s = 1; s <= 64 && s <= kb; ++s) {
-    const long long work = tiles * s;
-    const double eff = (double)work / (double)(((work + sms - 1) / sms) * sms);
-    if (eff > best_eff * 1.02) {
+    const long long rounds = (tiles * s + sms - 1) / sms;
+    const long long cost = rounds * (FIXED + (kb + s - 1) / s);
+    if (best_cost < 0 || cost < best_cost) {
       best = s;
-      best_eff = eff;
+      best_cost = cost;
     }
   }
   return (int)best;
@@ -1712,6 +1954,45 @@ int launch_router_dw_tc(const void* x, const void* dl3, int T, int H, int E, flo
 }
 
 // dx[t,h] (+)= sum_e (hi+mid+lo)[t,e] W_r[h,e]; dx bf16 [T,H], H % 64 == 0
+// One-pass router backward (dW partials and dx) for 32..64 experts: one CTA per
+// (128-column slice of H, range of token blocks), the token ranges sized so
+// that all CTAs run in one wave.
+bool router_bwd_tc_applies(int H, int E) { return E % 8 == 0 && E > 16 && E <= 64 && H % tc::RB_HS == 0; }
+
+int router_bwd_tc_splits(int T, int H, int E) {
+  const long long n_slices = H / tc::RB_HS, n_blocks = (T + tc::RB_TB - 1) / tc::RB_TB;
+  long long sp = sm_count() / (n_slices > 0 ? n_slices : 1);
+  if (sp > n_blocks) sp = n_blocks;
+  if (sp > 64) sp = 64;
+  return sp < 1 ? 1 : (int)sp;
+}
+
+int launch_router_bwd_tc(const void* x, const void* dl3, const void* w, int T, int H, int E, float* part, bool write,
+                         void* dx, cudaStream_t s) {
+  using namespace tc;
+  CUtensorMap mX, mDL, mW;
+  if (!map_3d(&mDL, dl3, E, T, 3, 64, RB_TB)) return MOE_ERR_CUDA;
+  if (part) {
+    if (!map_2d_as_3d(&mX, x, H, T, 64, RB_TB)) return MOE_ERR_CUDA;
+  } else {
+    mX = mDL;  // not read
+  }
+  if (dx) {
+    if (!map_2d_as_3d(&mW, w, E, H, 64, RB_HS)) return MOE_ERR_CUDA;
+  } else {
+    mW = mDL;  // not read
+  }
+  Params p = params(nullptr, 1, T, H, E, dx, H, nullptr);
+  p.accumulate = write ? 0 : 1;
+  const int n_slices = H / RB_HS, n_blocks = (T + RB_TB - 1) / RB_TB, splits = router_bwd_tc_splits(T, H, E);
+  if (cudaFuncSetAttribute(router_bwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)RB_SMEM) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  router_bwd_tc_kernel<<<n_slices * splits, RB_THREADS, RB_SMEM, s>>>(mX, mDL, mW, p, n_slices, splits, n_blocks,
+                                                                      part, E);
+  return launch_status();
+}
+
 int launch_router_dx_tc(const void* dl3, const void* w, int T, int H, int E, bool write, void* dx, cudaStream_t s) {
   using namespace tc;
   CUtensorMap mA, mB;

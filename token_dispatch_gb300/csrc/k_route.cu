@@ -692,6 +692,10 @@ int launch_route(const void* x, const void* w, const float* bias, int T, int H, 
 
 int router_dw_tc_splits(int T, int H, int E);
 int launch_router_dw_tc(const void* x, const void* dl3, int T, int H, int E, float* part, cudaStream_t s);
+bool router_bwd_tc_applies(int H, int E);
+int router_bwd_tc_splits(int T, int H, int E);
+int launch_router_bwd_tc(const void* x, const void* dl3, const void* w, int T, int H, int E, float* part, bool write,
+                         void* dx, cudaStream_t s);
 int launch_router_dx_tc(const void* dl3, const void* w, int T, int H, int E, bool write, void* dx, cudaStream_t s);
 
 // The tensor-core router backward serves bf16 layers whose W_r rows are
@@ -709,6 +713,8 @@ static BwdWs bwd_ws(int T, int H, int E) {
   long long splits = pl.splits;
   const long long tcs = router_dw_tc_splits(T, H, E);
   if (tcs > splits) splits = tcs;
+  const long long fused = router_bwd_tc_applies(H, E) ? router_bwd_tc_splits(T, H, E) : 0;
+  if (fused > splits) splits = fused;
   const long long sts = (E == 1 || E == 8 || E == 16) ? router_bwd_stream_splits(T, H, E) : 0;
   if (sts > splits) splits = sts;
   return BwdWs{align256((size_t)splits * H * E * 4), align256((size_t)T * E * 4), align256((size_t)3 * T * E * 2)};
@@ -789,6 +795,12 @@ int launch_route_bwd(int mode, const float* d_gate, const float* logits, const i
   int st = (mode == MOE_ROUTE_SOFTMAX_TOPK || d_logits) ? launch_status() : MOE_OK;
   if (st != MOE_OK) return st;
 
+  if (tc && router_bwd_tc_applies(H, E) && (dw || dx)) {
+    // dW partials and dx in one pass over x and dx, then the partials' reduction
+    st = launch_router_bwd_tc(x, dl3, w, T, H, E, dw ? part : nullptr, dx_write, dx, s);
+    if (st == MOE_OK && dw) st = launch_reduce(part, router_bwd_tc_splits(T, H, E), H, E, dw, s);
+    return st;
+  }
   if (dw) {
     if (tc) {
       st = launch_router_dw_tc(x, dl3, T, H, E, part, s);
