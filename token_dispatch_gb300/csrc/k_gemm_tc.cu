@@ -419,6 +419,37 @@ __device__ __forceinline__ void epi_f32_bias(const Params& p, uint32_t tbase, co
   }
 }
 
+// EPI_F32_GK: fp32 tile of group `slab` (a grouped-K product, one output slab
+// per group) through the warp's staging tile: 4 rows x 128 bytes per store
+// instruction; a group without rows gets zeros.
+template <int OUT_BN>
+__device__ __forceinline__ void epi_f32_gk(const Params& p, uint32_t tbase, const TileInfo& ti, int slab, bool empty,
+                                           float* epi_stage, int q, int lane) {
+  float* out = static_cast<float*>(p.out) + (long long)slab * p.part_stride;
+  float* stg = epi_stage + q * 32 * STG_LD;
+  const int seg = (lane & 7) * 4;
+#pragma unroll 1
+  for (int c = 0; c < OUT_BN / 32; ++c) {
+    float v[32];
+    if (!empty) tmem_ld32(tbase + c * 32, v);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) stg[lane * STG_LD + j] = empty ? 0.f : v[j];
+    __syncwarp();
+#pragma unroll
+    for (int ps = 0; ps < 8; ++ps) {
+      const int rw = ps * 4 + (lane >> 3);
+      const int rr = q * 32 + rw;
+      const long long gr = (long long)ti.row0 + rr;
+      const int col = ti.n0 + c * 32 + seg;
+      if (rr < ti.rows && gr < p.M && col < p.N) {
+        const float* sp = stg + rw * STG_LD + seg;
+        *reinterpret_cast<float4*>(out + gr * p.ldo + col) = make_float4(sp[0], sp[1], sp[2], sp[3]);
+      }
+    }
+    __syncwarp();
+  }
+}
+
 // EPI_BF16: the fp32 tile rounded to bf16 (plus the old values with
 // p.accumulate), through the warp's [32][STG_LD] staging tile.
 template <int OUT_BN>
@@ -866,32 +897,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       } else if (EPI == EPI_SWIGLU_BWD) {
         epi_swiglu_bwd<C::OUT_BN>(p, tbase, ti, row_ok, grow);
       } else if (EPI == EPI_F32_GK) {
-        // fp32 tile of group wk.slab through this warp's staging tile: 4 rows x
-        // 128 bytes per store instruction; a group without rows gets zeros
-        float* out = static_cast<float*>(p.out) + (long long)wk.slab * p.part_stride;
-        float* stg = epi_stage + q * 32 * C::STG_LD;
-        const bool empty = wk.kb_end <= wk.kb_begin;
-        const int seg = (lane & 7) * 4;
-#pragma unroll 1
-        for (int c = 0; c < C::OUT_BN / 32; ++c) {
-          float v[32];
-          if (!empty) tmem_ld32(tbase + c * 32, v);
-#pragma unroll
-          for (int j = 0; j < 32; ++j) stg[lane * C::STG_LD + j] = empty ? 0.f : v[j];
-          __syncwarp();
-#pragma unroll
-          for (int ps = 0; ps < 8; ++ps) {
-            const int rw = ps * 4 + (lane >> 3);
-            const int rr = q * 32 + rw;
-            const long long gr = (long long)ti.row0 + rr;
-            const int col = ti.n0 + c * 32 + seg;
-            if (rr < ti.rows && gr < p.M && col < p.N) {
-              const float* sp = stg + rw * C::STG_LD + seg;
-              *reinterpret_cast<float4*>(out + gr * p.ldo + col) = make_float4(sp[0], sp[1], sp[2], sp[3]);
-            }
-          }
-          __syncwarp();
-        }
+        epi_f32_gk<C::OUT_BN>(p, tbase, ti, wk.slab, wk.kb_end <= wk.kb_begin, epi_stage, q, lane);
       } else if (EPI == EPI_BF16) {
         epi_bf16<C::OUT_BN>(p, tbase, ti, epi_stage, q, lane);
       } else if (EPI == EPI_ROUTER) {
@@ -1069,9 +1075,12 @@ struct PairCfg {
   // B N-contiguous (MN-major: Wg / Wu / Wd read as [K = H][N = H'], W_r as
   // [K = H][N = E]) or K-contiguous (Wd, or Wg / Wu in the backward, read as
   // [N = H][K = H'])
-  static constexpr bool B_MN = EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD || EPI == EPI_F32_BIAS;
+  static constexpr bool B_MN = EPI == EPI_SWIGLU || EPI == EPI_SWIGLU_BWD || EPI == EPI_F32_BIAS || EPI == EPI_F32_GK;
+  // grouped K (weight gradients): A read transposed from a row-major [rows, M]
+  // matrix, M-contiguous
+  static constexpr bool A_MN = EPI == EPI_F32_GK;
   static constexpr int TMEM_COLS = 2 * PAIR_BN;
-  static constexpr int EPI_BYTES = (EPI == EPI_BF16 || EPI == EPI_F32_BIAS) ? 4 * 32 * STG_LD * 4 : 0;
+  static constexpr int EPI_BYTES = (EPI == EPI_BF16 || EPI == EPI_F32_BIAS || EPI == EPI_F32_GK) ? 4 * 32 * STG_LD * 4 : 0;
   static constexpr size_t SMEM = (size_t)PAIR_STAGES * STAGE_BYTES + EPI_BYTES + (2 * PAIR_STAGES + 5) * 8 + 1024;
 };
 
@@ -1085,6 +1094,22 @@ __device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) 
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
   return r;
+}
+// the pipeline stage n K blocks after stage s
+__device__ __forceinline__ int pair_stage(int s, int n) { return (s + n) % PAIR_STAGES; }
+// Zero K rows [from, BK) of both 64-column halves of a grouped-K A stage in
+// both CTAs of the pair.  In the MN-major boxes each K row is one 128-byte
+// line, so the swizzle does not matter; the 32 lanes of a warp take one K row
+// (8 chunks x 2 halves x 2 CTAs) per step, then fence their generic writes
+// against the MMAs' async-proxy reads.
+__device__ __forceinline__ void clear_rows_pair(uint32_t a_stage, int from, int lane) {
+  const int n = (BK - from) * 32;
+  for (int idx = lane; idx < n; idx += 32) {
+    const int j = idx & 7, half = (idx >> 3) & 1, cta = (idx >> 4) & 1, r = from + (idx >> 5);
+    const uint32_t a = cluster_addr(a_stage + half * (64 * BK * 2) + r * 128 + j * 16, cta);
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
+  }
+  asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
@@ -1174,10 +1199,13 @@ template <int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1) __cluster_dims__(2, 1, 1)
 tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmB2, const Params p) {
-  static_assert(EPI == EPI_SWIGLU || EPI == EPI_BF16 || EPI == EPI_SWIGLU_BWD || EPI == EPI_F32_BIAS,
+  static_assert(EPI == EPI_SWIGLU || EPI == EPI_BF16 || EPI == EPI_SWIGLU_BWD || EPI == EPI_F32_BIAS ||
+                    EPI == EPI_F32_GK,
                 "pair kernel: GEMMs with a row-major output");
   using C = PairCfg<EPI>;
   constexpr bool B_MN = C::B_MN;
+  constexpr bool A_MN = C::A_MN;
+  constexpr bool GK = EPI == EPI_F32_GK;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_base = smem;
@@ -1255,10 +1283,11 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       mt_pre[g] = run;
       run += (max(0, cu_s[g + 1] - cu_s[g]) + 2 * BM - 1) / (2 * BM);
     }
-    if (lane == 0 && (cu_s[0] != 0 || cu_s[G] != p.M)) set_error(p.err, DEV_BOUNDS);
+    if (lane == 0 && (cu_s[0] != 0 || cu_s[G] != (GK ? p.K : p.M))) set_error(p.err, DEV_BOUNDS);
     if (lane == 31) {
       mt_pre[G] = incl;
-      total_tiles_s = incl * n_tiles;
+      // grouped K: every group has all (M / 256) x (N / 256) output tiles
+      total_tiles_s = GK ? G * ((p.M + 2 * BM - 1) / (2 * BM)) * n_tiles : incl * n_tiles;
     }
   }
   tc_fence_before();
@@ -1268,6 +1297,37 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   const uint32_t tmem_base = tmem_base_slot;
   const int total_tiles = total_tiles_s;
   const int KB_ALL = (p.K + BK - 1) / BK;
+  // One pair tile: this CTA's output rows, its K blocks, the first K row of
+  // block 0, the output slab (group) and the valid K rows of its last block.
+  struct PairWork {
+    TileInfo ti;
+    int kb_end, k_base, slab, last_valid;
+  };
+  const int gk_mt = (p.M + 2 * BM - 1) / (2 * BM);
+  auto pair_work = [&](int t) {
+    PairWork w;
+    if constexpr (GK) {
+      const int per_g = gk_mt * n_tiles;
+      const int g = t / per_g, rem = t - g * per_g;
+      const int m = rem % gk_mt, n = rem / gk_mt;
+      w.ti.g = g;
+      w.ti.row0 = m * 2 * BM + (int)rank * BM;
+      w.ti.rows = max(0, min(BM, p.M - w.ti.row0));
+      w.ti.n0 = n * C::OUT_BN;
+      const int beg = cu_s[g], rows = max(0, cu_s[g + 1] - beg);
+      w.kb_end = (rows + BK - 1) / BK;
+      w.k_base = beg;
+      w.slab = g;
+      w.last_valid = rows - (w.kb_end - 1) * BK;
+    } else {
+      w.ti = decode_pair<C::OUT_BN>(t, mt_pre, cu_s, G, n_tiles, rank);
+      w.kb_end = KB_ALL;
+      w.k_base = 0;
+      w.slab = 0;
+      w.last_valid = BK;
+    }
+    return w;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -1278,18 +1338,26 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       for (int s = 0; s < PAIR_STAGES; ++s) filled_parity[s] = -1;
       bool ok = true;
       for (int t = pair; ok && t < total_tiles; t += n_pairs) {
-        const TileInfo ti = decode_pair<C::OUT_BN>(t, mt_pre, cu_s, G, n_tiles, rank);
-        for (int kb = 0; kb < KB_ALL; ++kb) {
+        const PairWork wk = pair_work(t);
+        const TileInfo& ti = wk.ti;
+        for (int kb = 0; kb < wk.kb_end; ++kb) {
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, &abort_flag, p)) { ok = false; break; }
           const uint32_t a_dst = smem_u32(stage_base + stage * C::STAGE_BYTES);
           const uint32_t b_dst = a_dst + A_STAGE_BYTES;
-          const int k0 = kb * BK;
+          const int k0 = wk.k_base + kb * BK;
           if (leader) {
             mbar_expect_tx(full_bar(stage), 2 * C::STAGE_BYTES);  // this CTA's bytes and the peer's
             filled_parity[stage] = (int)phase;
           }
           const uint32_t fb = cluster_addr(full_bar(stage), 0);
-          tma_load_3d_pair(a_dst, &tmA, fb, k0, ti.row0, 0);
+          if constexpr (A_MN) {
+            // [64 K rows x 64 M] boxes, the two M halves 8 KB apart (a
+            // group's last block is cleared past the group before its MMAs)
+            tma_load_3d_pair(a_dst, &tmA, fb, ti.row0, k0, 0);
+            tma_load_3d_pair(a_dst + 64 * BK * 2, &tmA, fb, ti.row0 + 64, k0, 0);
+          } else {
+            tma_load_3d_pair(a_dst, &tmA, fb, k0, ti.row0, 0);
+          }
           if constexpr (EPI == EPI_SWIGLU) {
             // the leader stages the gate columns, the peer the up columns
             const CUtensorMap* m = leader ? &tmB : &tmB2;
@@ -1297,11 +1365,12 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             for (int c = 0; c < 2; ++c)
               tma_load_3d_pair(b_dst + c * (64 * BK * 2), m, fb, ti.n0 + c * 64, k0, ti.g);
           } else if constexpr (B_MN) {
-            // each CTA stages its half of the 256 output columns
+            // each CTA stages its half of the 256 output columns (grouped K:
+            // rows k0.. of one [rows, .] matrix, columns from b_col_off)
 #pragma unroll
             for (int c = 0; c < 2; ++c)
-              tma_load_3d_pair(b_dst + c * (64 * BK * 2), &tmB, fb, ti.n0 + (int)rank * (PAIR_BN / 2) + c * 64, k0,
-                               ti.g);
+              tma_load_3d_pair(b_dst + c * (64 * BK * 2), &tmB, fb,
+                               ti.n0 + (int)rank * (PAIR_BN / 2) + c * 64 + p.b_col_off, k0, GK ? 0 : ti.g);
           } else if (p.kcat && k0 >= p.kcat) {
             // K concatenated from two tensors: k >= kcat reads the second
             tma_load_3d_pair(b_dst, &tmB2, fb, k0 - p.kcat, ti.n0 + (int)rank * (PAIR_BN / 2), ti.g);
@@ -1324,37 +1393,74 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
   } else if (warp == 1) {
     // ---------------------------------------------- MMA issuer (leader only)
-    if (lane == 0 && leader) {
-      constexpr uint32_t IDESC = instr_desc(2 * BM, PAIR_BN, false, B_MN);
+    // Lane 0 waits and issues.  Grouped K: the other lanes follow the same
+    // tile sequence and meet lane 0 only in a group's last, partial K block,
+    // whose rows past the group (the next group's) they clear to zeros in
+    // both CTAs' A stages before its MMAs.  After a failed wait lane 0 keeps
+    // walking the tiles without issuing, so the meetings still happen.
+    if (leader && (lane == 0 || GK)) {
+      constexpr uint32_t IDESC = instr_desc(2 * BM, PAIR_BN, A_MN, B_MN);
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
       bool issued = false;
       int i = 0;
-      for (int t = pair; ok && t < total_tiles; t += n_pairs, ++i) {
+      for (int t = pair; t < total_tiles; t += n_pairs, ++i) {
         const int acc = i & 1;
-        if (!wait_bounded_cluster(acce_bar(acc), (((uint32_t)i >> 1) & 1u) ^ 1u, &abort_flag, p)) { ok = false; break; }
+        int kb_end = KB_ALL, last_valid = BK;
+        if constexpr (GK) {
+          const PairWork wk = pair_work(t);
+          kb_end = wk.kb_end;
+          last_valid = wk.last_valid;
+        }
+        const bool clear = GK && kb_end > 0 && last_valid < BK;
+        if (lane != 0) {
+          // follower: the clearing of this tile's last block
+          if (clear) {
+            __syncwarp();
+            const uint32_t a_t = smem_u32(stage_base + pair_stage(stage, kb_end - 1) * C::STAGE_BYTES);
+            clear_rows_pair(a_t, last_valid, lane);
+            __syncwarp();
+          }
+          stage = pair_stage(stage, kb_end);
+          continue;
+        }
+        if (ok && !wait_bounded_cluster(acce_bar(acc), (((uint32_t)i >> 1) & 1u) ^ 1u, &abort_flag, p)) ok = false;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * PAIR_BN;
-        for (int kb = 0; kb < KB_ALL; ++kb) {
-          if (!wait_bounded(full_bar(stage), phase, &abort_flag, p)) { ok = false; break; }
+        for (int kb = 0; kb < kb_end; ++kb) {
+          const bool last_clear = clear && kb == kb_end - 1;
+          if (ok && !(last_clear ? wait_bounded_cluster(full_bar(stage), phase, &abort_flag, p)
+                                 : wait_bounded(full_bar(stage), phase, &abort_flag, p)))
+            ok = false;
           tc_fence_after();
           const uint32_t a_t = smem_u32(stage_base + stage * C::STAGE_BYTES);
           const uint32_t b_t = a_t + A_STAGE_BYTES;
-#pragma unroll
-          for (int k = 0; k < BK / 16; ++k) {
-            const uint64_t adesc = smem_desc(a_t + k * 32, 16, 1024);
-            const uint64_t bdesc = B_MN ? smem_desc(b_t + k * 16 * 128, 64 * BK * 2, 1024) : smem_desc(b_t + k * 32, 16, 1024);
-            tc_mma_pair(d_tmem, adesc, bdesc, IDESC, (kb > 0 || k > 0) ? 1u : 0u);
+          if (last_clear) {
+            __syncwarp();
+            clear_rows_pair(a_t, last_valid, lane);
+            __syncwarp();
           }
-          issued = true;
-          tc_commit_pair(empty_bar(stage), 3);
+          if (ok) {
+#pragma unroll
+            for (int k = 0; k < BK / 16; ++k) {
+              // K-major: +32 bytes per 16-element K step in the 128-byte row;
+              // MN-major: +16 rows of 128 bytes, 64-wide atoms 8 KB apart
+              const uint64_t adesc =
+                  A_MN ? smem_desc(a_t + k * 16 * 128, 64 * BK * 2, 1024) : smem_desc(a_t + k * 32, 16, 1024);
+              const uint64_t bdesc =
+                  B_MN ? smem_desc(b_t + k * 16 * 128, 64 * BK * 2, 1024) : smem_desc(b_t + k * 32, 16, 1024);
+              tc_mma_pair(d_tmem, adesc, bdesc, IDESC, (kb > 0 || k > 0) ? 1u : 0u);
+            }
+            issued = true;
+            tc_commit_pair(empty_bar(stage), 3);
+          }
           if (++stage == PAIR_STAGES) { stage = 0; phase ^= 1u; }
         }
-        if (!ok) break;
-        tc_commit_pair(accf_bar(acc), 3);
+        if (ok) tc_commit_pair(accf_bar(acc), 3);
+        else if (!GK) break;
       }
-      if (issued) {
+      if (lane == 0 && issued) {
         tc_commit_pair(drain_bar, 1);
         const long long t0 = clock64();
         while (!mbar_try_wait(drain_bar, 0)) {
@@ -1371,13 +1477,15 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       const int acc = i & 1;
       if (!wait_bounded(accf_bar(acc), ((uint32_t)i >> 1) & 1u, &abort_flag, p)) break;
       tc_fence_after();
-      const TileInfo ti = decode_pair<C::OUT_BN>(t, mt_pre, cu_s, G, n_tiles, rank);
+      const PairWork wk = pair_work(t);
+      const TileInfo& ti = wk.ti;
       const long long grow = (long long)ti.row0 + r_local;
       const bool row_ok = r_local < ti.rows && grow < p.M;
       const uint32_t tbase = tmem_base + acc * PAIR_BN + ((uint32_t)(q * 32) << 16);
       if constexpr (EPI == EPI_SWIGLU) epi_swiglu<C::OUT_BN>(p, tbase, ti, row_ok, grow);
       else if constexpr (EPI == EPI_SWIGLU_BWD) epi_swiglu_bwd<C::OUT_BN>(p, tbase, ti, row_ok, grow);
       else if constexpr (EPI == EPI_F32_BIAS) epi_f32_bias<C::OUT_BN>(p, tbase, ti, epi_stage, q, lane);
+      else if constexpr (GK) epi_f32_gk<C::OUT_BN>(p, tbase, ti, wk.slab, wk.kb_end == 0, epi_stage, q, lane);
       else epi_bf16<C::OUT_BN>(p, tbase, ti, epi_stage, q, lane);
       tc_fence_before();
       if (leader) mbar_arrive(acce_bar(acc));
@@ -1833,7 +1941,8 @@ int launch_expert_ffn_bwd_tc(const void* xs, const int32_t* cu, int rows, const 
   }
   // weight gradients: M = H (A = an [rows, H] matrix read transposed, MN-major),
   // N = H' (B = an [rows, .] matrix, MN-major), K = the rows of each expert
-  const long long gk_tiles = (long long)E * ((H + BM - 1) / BM) * ((Hp + 255) / 256);
+  // (CTA pairs: 256 x 256 output tiles)
+  const long long gk_tiles = (long long)E * ((H + 2 * BM - 1) / (2 * BM)) * ((Hp + 255) / 256);
   auto wgrad = [&](const void* a_rows, const void* b_rows, long long b_ld, int b_off, float* out) {
     CUtensorMap mA, mB;
     if (!map_2d_as_3d(&mA, a_rows, H, rows, 64, BK)) return (int)MOE_ERR_CUDA;
@@ -1842,7 +1951,7 @@ int launch_expert_ffn_bwd_tc(const void* xs, const int32_t* cu, int rows, const 
     p.gk = 1;
     p.b_col_off = b_off;
     p.part_stride = (long long)H * Hp;
-    return launch<EPI_F32_GK, true, true, 256, 4, 1, 1>(mA, mB, mB, p, gk_tiles, s);
+    return launch_pair<EPI_F32_GK>(mA, mB, mB, p, gk_tiles, s);
   };
   if (dwd && (st = wgrad(dh, act, Hp, 0, dwd)) != MOE_OK) return st;
   if (dwg && (st = wgrad(xs, dgu, 2LL * Hp, 0, dwg)) != MOE_OK) return st;
