@@ -95,6 +95,10 @@ struct Params {
   // grouped K: group g reduces over rows [cu[g], cu[g+1]) of K (M, N fixed)
   int gk = 0;
   int b_col_off = 0;  // added to the N coordinate of MN-major B loads
+  // grouped K on CTA pairs: fp32 tiles stored through the tensor map passed
+  // in place of the second B map (set when the output's rows are 16-byte
+  // aligned)
+  int tma_out = 0;
   // K-major A rows gathered from another matrix: row r of A is row gather[r]
   // of gather_src [gather_n, K] (bf16), copied into the swizzled stages by
   // four extra warps with 16-byte asynchronous copies (the dispatch gather
@@ -447,6 +451,55 @@ __device__ __forceinline__ void epi_f32_gk(const Params& p, uint32_t tbase, cons
       }
     }
     __syncwarp();
+  }
+}
+
+// EPI_F32_GK through tensor stores: each 32-column chunk of the warp's 32
+// TMEM lanes goes to one of the warp's GK_OUT_BUFS 4 KB staging tiles in the
+// 128-byte swizzled layout (16-byte piece j of row r at j ^ (r & 7): the
+// lanes' writes fall in distinct banks) and leaves as one [32 x 32] fp32 store
+// into slab `slab` of the map's [G][M][N] output, which clips rows and columns
+// past the output.  Lane 0 issues one bulk group per chunk; `chunk` counts the
+// warp's chunks across tiles, and a staging tile is refilled GK_OUT_BUFS
+// chunks later, once the store from it has read it (the stores in flight are
+// what keeps the fp32 output streaming).
+constexpr int GK_OUT_BUFS = 2;
+template <int OUT_BN>
+__device__ __forceinline__ void epi_f32_gk_tma(const CUtensorMap* tmO, const Params& p, uint32_t tbase,
+                                               const TileInfo& ti, int slab, bool empty, float* stage_w, int q,
+                                               int lane, int& chunk) {
+  if (ti.rows <= q * 32) return;  // none of this warp's rows is an output row
+  const uint32_t buf = smem_u32(stage_w);
+#pragma unroll 1
+  for (int c = 0; c < OUT_BN / 32; ++c) {
+    const int col = ti.n0 + c * 32;
+    if (col >= p.N) break;
+    float v[32];
+    if (!empty) {
+      tmem_ld32(tbase + c * 32, v);
+    } else {
+#pragma unroll
+      for (int j = 0; j < 32; ++j) v[j] = 0.f;
+    }
+    const uint32_t dst = buf + (chunk % GK_OUT_BUFS) * 4096;
+    ++chunk;
+    if (lane == 0) asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(GK_OUT_BUFS - 1) : "memory");
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const uint32_t a = dst + lane * 128 + ((j ^ (lane & 7)) << 4);
+      asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(a), "f"(v[4 * j]), "f"(v[4 * j + 1]),
+                   "f"(v[4 * j + 2]), "f"(v[4 * j + 3])
+                   : "memory");
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    if (lane == 0) {
+      asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(tmO),
+                   "r"(col), "r"(ti.row0 + q * 32), "r"(slab), "r"(dst)
+                   : "memory");
+      asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+    }
   }
 }
 
@@ -1069,6 +1122,10 @@ constexpr int PAIR_BN = 256;
 
 template <int EPI>
 struct PairCfg {
+  // grouped K keeps GK_OUT_BUFS 4 KB staging tiles per epilogue warp for its
+  // tensor stores, in place of pipeline stages
+  static constexpr int STAGES = EPI == EPI_F32_GK ? (GK_OUT_BUFS <= 3 ? PAIR_STAGES - 1 : PAIR_STAGES - 2)
+                                                 : PAIR_STAGES;
   static constexpr int B_HALF_BYTES = (PAIR_BN / 2) * BK * 2;
   static constexpr int STAGE_BYTES = A_STAGE_BYTES + B_HALF_BYTES;
   static constexpr int OUT_BN = EPI == EPI_SWIGLU ? PAIR_BN / 2 : PAIR_BN;
@@ -1080,8 +1137,9 @@ struct PairCfg {
   // matrix, M-contiguous
   static constexpr bool A_MN = EPI == EPI_F32_GK;
   static constexpr int TMEM_COLS = 2 * PAIR_BN;
-  static constexpr int EPI_BYTES = (EPI == EPI_BF16 || EPI == EPI_F32_BIAS || EPI == EPI_F32_GK) ? 4 * 32 * STG_LD * 4 : 0;
-  static constexpr size_t SMEM = (size_t)PAIR_STAGES * STAGE_BYTES + EPI_BYTES + (2 * PAIR_STAGES + 5) * 8 + 1024;
+  static constexpr int EPI_BYTES =
+      EPI == EPI_F32_GK ? 4 * GK_OUT_BUFS * 32 * 32 * 4 : (EPI == EPI_BF16 || EPI == EPI_F32_BIAS) ? 4 * 32 * STG_LD * 4 : 0;
+  static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + EPI_BYTES + (2 * STAGES + 5) * 8 + 1024;
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -1096,7 +1154,8 @@ __device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) 
   return r;
 }
 // the pipeline stage n K blocks after stage s
-__device__ __forceinline__ int pair_stage(int s, int n) { return (s + n) % PAIR_STAGES; }
+template <int STAGES>
+__device__ __forceinline__ int pair_stage(int s, int n) { return (s + n) % STAGES; }
 // Zero K rows [from, BK) of both 64-column halves of a grouped-K A stage in
 // both CTAs of the pair.  In the MN-major boxes each K row is one 128-byte
 // line, so the swizzle does not matter; the 32 lanes of a warp take one K row
@@ -1209,8 +1268,8 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* stage_base = smem;
-  float* epi_stage = reinterpret_cast<float*>(smem + PAIR_STAGES * C::STAGE_BYTES);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + PAIR_STAGES * C::STAGE_BYTES + C::EPI_BYTES);
+  float* epi_stage = reinterpret_cast<float*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES + C::EPI_BYTES);
   __shared__ uint32_t tmem_base_slot;
   __shared__ int abort_flag;
   __shared__ int mt_pre[1025];
@@ -1226,14 +1285,14 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   const int n_tiles = (p.N + C::OUT_BN - 1) / C::OUT_BN;
 
   auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
-  auto empty_bar = [&](int s) { return smem_u32(&bars[PAIR_STAGES + s]); };
-  auto accf_bar = [&](int a) { return smem_u32(&bars[2 * PAIR_STAGES + a]); };
-  auto acce_bar = [&](int a) { return smem_u32(&bars[2 * PAIR_STAGES + 2 + a]); };
-  const uint32_t drain_bar = smem_u32(&bars[2 * PAIR_STAGES + 4]);
+  auto empty_bar = [&](int s) { return smem_u32(&bars[C::STAGES + s]); };
+  auto accf_bar = [&](int a) { return smem_u32(&bars[2 * C::STAGES + a]); };
+  auto acce_bar = [&](int a) { return smem_u32(&bars[2 * C::STAGES + 2 + a]); };
+  const uint32_t drain_bar = smem_u32(&bars[2 * C::STAGES + 4]);
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int s = 0; s < PAIR_STAGES; ++s) {
+    for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
@@ -1334,8 +1393,8 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
-      int filled_parity[PAIR_STAGES];
-      for (int s = 0; s < PAIR_STAGES; ++s) filled_parity[s] = -1;
+      int filled_parity[C::STAGES];
+      for (int s = 0; s < C::STAGES; ++s) filled_parity[s] = -1;
       bool ok = true;
       for (int t = pair; ok && t < total_tiles; t += n_pairs) {
         const PairWork wk = pair_work(t);
@@ -1377,12 +1436,12 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           } else {
             tma_load_3d_pair(b_dst, &tmB, fb, k0, ti.n0 + (int)rank * (PAIR_BN / 2), ti.g);
           }
-          if (++stage == PAIR_STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
       }
       // drain (leader): every stage filled must have landed, both CTAs' bytes
       if (leader) {
-        for (int s = 0; s < PAIR_STAGES; ++s) {
+        for (int s = 0; s < C::STAGES; ++s) {
           if (filled_parity[s] < 0) continue;
           const long long t0 = clock64();
           while (!mbar_try_wait(full_bar(s), (uint32_t)filled_parity[s])) {
@@ -1418,11 +1477,11 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           // follower: the clearing of this tile's last block
           if (clear) {
             __syncwarp();
-            const uint32_t a_t = smem_u32(stage_base + pair_stage(stage, kb_end - 1) * C::STAGE_BYTES);
+            const uint32_t a_t = smem_u32(stage_base + pair_stage<C::STAGES>(stage, kb_end - 1) * C::STAGE_BYTES);
             clear_rows_pair(a_t, last_valid, lane);
             __syncwarp();
           }
-          stage = pair_stage(stage, kb_end);
+          stage = pair_stage<C::STAGES>(stage, kb_end);
           continue;
         }
         if (ok && !wait_bounded_cluster(acce_bar(acc), (((uint32_t)i >> 1) & 1u) ^ 1u, &abort_flag, p)) ok = false;
@@ -1455,7 +1514,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             issued = true;
             tc_commit_pair(empty_bar(stage), 3);
           }
-          if (++stage == PAIR_STAGES) { stage = 0; phase ^= 1u; }
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
         }
         if (ok) tc_commit_pair(accf_bar(acc), 3);
         else if (!GK) break;
@@ -1473,6 +1532,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int r_local = q * 32 + lane;
     int i = 0;
+    int out_chunk = 0;  // grouped K: this warp's output chunks so far (staging tile rotation)
     for (int t = pair; t < total_tiles; t += n_pairs, ++i) {
       const int acc = i & 1;
       if (!wait_bounded(accf_bar(acc), ((uint32_t)i >> 1) & 1u, &abort_flag, p)) break;
@@ -1485,12 +1545,23 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       if constexpr (EPI == EPI_SWIGLU) epi_swiglu<C::OUT_BN>(p, tbase, ti, row_ok, grow);
       else if constexpr (EPI == EPI_SWIGLU_BWD) epi_swiglu_bwd<C::OUT_BN>(p, tbase, ti, row_ok, grow);
       else if constexpr (EPI == EPI_F32_BIAS) epi_f32_bias<C::OUT_BN>(p, tbase, ti, epi_stage, q, lane);
-      else if constexpr (GK) epi_f32_gk<C::OUT_BN>(p, tbase, ti, wk.slab, wk.kb_end == 0, epi_stage, q, lane);
-      else epi_bf16<C::OUT_BN>(p, tbase, ti, epi_stage, q, lane);
+      else if constexpr (GK) {
+        if (p.tma_out)
+          epi_f32_gk_tma<C::OUT_BN>(&tmB2, p, tbase, ti, wk.slab, wk.kb_end == 0,
+                                    epi_stage + q * GK_OUT_BUFS * 32 * 32, q, lane, out_chunk);
+        else
+          epi_f32_gk<C::OUT_BN>(p, tbase, ti, wk.slab, wk.kb_end == 0, epi_stage, q, lane);
+      } else {
+        epi_bf16<C::OUT_BN>(p, tbase, ti, epi_stage, q, lane);
+      }
       tc_fence_before();
       if (leader) mbar_arrive(acce_bar(acc));
       else mbar_arrive_remote(cluster_addr(acce_bar(acc), 0));
     }
+    // the tensor stores are complete (and done reading shared memory) before
+    // the CTA exits
+    if constexpr (GK)
+      if (lane == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
   }
 
   tc_fence_before();
@@ -1533,11 +1604,11 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // bf16 tensor map, 128-byte swizzle; dims/strides innermost first (strides in
 // bytes for dims 1..rank-1).
 bool make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-              const cuuint32_t* box) {
+              const cuuint32_t* box, CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint32_t es[3] = {1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, es,
+  CUresult r = fn(m, dt, rank, const_cast<void*>(base), dims, strides, box, es,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -1951,7 +2022,17 @@ int launch_expert_ffn_bwd_tc(const void* xs, const int32_t* cu, int rows, const 
     p.gk = 1;
     p.b_col_off = b_off;
     p.part_stride = (long long)H * Hp;
-    return launch_pair<EPI_F32_GK>(mA, mB, mB, p, gk_tiles, s);
+    // fp32 [E][H][H'] output as a map of [32 x 32] store boxes (rows of
+    // 16-byte multiples, a 16-byte aligned base)
+    CUtensorMap mO = mB;
+    if (Hp % 4 == 0 && ((uintptr_t)out & 15) == 0) {
+      cuuint64_t dims[3] = {(cuuint64_t)Hp, (cuuint64_t)H, (cuuint64_t)E};
+      cuuint64_t str[2] = {(cuuint64_t)Hp * 4, (cuuint64_t)H * Hp * 4};
+      cuuint32_t box[3] = {32, 32, 1};
+      if (!make_map(&mO, out, 3, dims, str, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32)) return (int)MOE_ERR_CUDA;
+      p.tma_out = 1;
+    }
+    return launch_pair<EPI_F32_GK>(mA, mB, mO, p, gk_tiles, s);
   };
   if (dwd && (st = wgrad(dh, act, Hp, 0, dwd)) != MOE_OK) return st;
   if (dwg && (st = wgrad(xs, dgu, 2LL * Hp, 0, dwg)) != MOE_OK) return st;
