@@ -670,6 +670,14 @@ def run_ours(args, shape, rank, world, local):
         roof = {"bound": "hbm", "achieved": ffn_bytes / ffn_s / 1e9, "peak": hbm_peak, "unit": "GB/s",
                 "peak_source": f"{peak_src} hbm_gbs"}
     roof["frac"] = roof["achieved"] / roof["peak"] if roof["peak"] else None
+    if roof["bound"] == "tensor" and mode != "train" and not fused:
+        # the CTA-pair GEMMs compute whole 256-row tiles per expert (gate/up:
+        # 128 SwiGLU columns per tile, down: 256 columns): the share of the
+        # FLOP they issue that the routed rows need
+        m_pad = float(np.sum((counts + 255) // 256 * 256))
+        hp128, h256, hp64 = -(-Hp // 128) * 128, -(-H // 256) * 256, -(-Hp // 64) * 64
+        issued = 2.0 * m_pad * H * 2 * hp128 + 2.0 * m_pad * hp64 * h256
+        roof["tile_fill"] = round(6.0 * R * H * Hp / issued, 4)
     roof["traffic"] = None if mode == "train" else FFN_DRAM_BYTES.get((shape.name, fused))
     roof["algorithmic"] = {"flops": ffn_flops, "bytes": ffn_bytes}
     hbm = {}
