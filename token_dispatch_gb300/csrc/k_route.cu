@@ -657,8 +657,7 @@ int launch_route(const void* x, const void* w, const float* bias, int T, int H, 
     S = router_tc_splits(T, H, E);
     part = S > 1 ? static_cast<float*>(ws) : nullptr;
     if (S == 1 && E <= 64) {  // the whole expert row is one tile: one launch
-      st = launch_router_tc(x, w, gemm_bias, sel_bias, renorm, T, H, E, logits, 1, K, idx, gate, s);
-      return st != MOE_OK ? st : launch_status();
+      return launch_router_tc(x, w, gemm_bias, sel_bias, renorm, T, H, E, logits, 1, K, idx, gate, s);
     }
     st = launch_router_tc(x, w, gemm_bias, nullptr, false, T, H, E, S > 1 ? part : logits, S, 0, nullptr, nullptr,
                           s);
