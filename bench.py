@@ -84,6 +84,8 @@ def parse():
     p.add_argument("--route-flags", type=int, default=0,
                    help="moe_route_ex gate options: 1 renormalise the top-k gates, 2 bias for selection only")
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-tail-split", action="store_true",
+                   help="run the down projection's last round as whole tiles (no expert FFN workspace)")
     p.add_argument("--fused-gather", action="store_true",
                    help="the forward's dispatch writes only the index maps and the gate/up GEMM gathers the rows "
                         "of x itself (moe_expert_ffn_gather) instead of reading the rows dispatch wrote")
@@ -266,7 +268,7 @@ def build_inputs(shape, dev, rank, bias_np):
     return inp
 
 
-def make_step(shape, inp, dev, stream, route_flags=0, fused=True):
+def make_step(shape, inp, dev, stream, route_flags=0, fused=True, tail_split=True):
     """(call names, step(x, dy, dxs, marks) -> None, buffers, outputs for the host).
     fused: the forward's dispatch writes only the index maps and the expert FFN
     gathers the rows of x in its gate/up operand load (not for the training
@@ -284,6 +286,7 @@ def make_step(shape, inp, dev, stream, route_flags=0, fused=True):
 
     if mode in ("fwd_bwd", "fwd", "train"):
         b = layer.MoEBuffers(T, H, E, K, Hp, shape.dtype, dev, backward=(mode != "fwd"), train=(mode == "train"))
+        fws, fwsb = (b.ws_ffn, b.ws_ffn_bytes) if tail_split else (None, 0)
         calls = [
             ("route", lambda xi, dyi, dxsi: L.moe_route_ex(xi, wr_d, bias_d, T, H, E, K, b.cdt, route_flags, b.logits,
                                                           b.idx, b.gate, b.ws_route, b.ws_route_bytes,
@@ -296,14 +299,14 @@ def make_step(shape, inp, dev, stream, route_flags=0, fused=True):
                                                                          Hp, b.cdt, b.act, None, b.h, stream=stream))
              if fused else
              (lambda xi, dyi, dxsi: L.moe_expert_ffn(b.xs, b.cu, R, wg, wu, wd, E, H, Hp, b.cdt, b.act, b.h,
-                                                     stream=stream))),
+                                                     fws, fwsb, stream=stream))),
             ("combine", lambda xi, dyi, dxsi: L.moe_combine(b.h, b.gate, b.dst_row, None, None, None, T, H, K, b.cdt,
                                                            b.y, stream=stream)),
         ]
         outs = [b.y]
         if mode == "train":
             calls[2] = ("expert_ffn", lambda xi, dyi, dxsi: L.moe_expert_ffn_ex(b.xs, b.cu, R, wg, wu, wd, E, H, Hp,
-                                                                              b.cdt, b.act, b.gu, b.h,
+                                                                              b.cdt, b.act, b.gu, b.h, fws, fwsb,
                                                                               stream=stream))
             calls += [
                 ("permute_bwd", lambda xi, dyi, dxsi: L.moe_permute_bwd(dyi, b.h, b.gate, b.dst_row, None, None,
@@ -339,6 +342,7 @@ def make_step(shape, inp, dev, stream, route_flags=0, fused=True):
     Bq, Lq, C = shape.mod_B, shape.mod_L, shape.mod_C
     m = layer.MoDBuffers(Bq, Lq, C, H, E, K, Hp, shape.dtype, dev)
     b = m.moe
+    fws, fwsb = (b.ws_ffn, b.ws_ffn_bytes) if tail_split else (None, 0)
     wmod_d = inp["wmod"].host.to(dev)
     calls = [
         ("mod_select", lambda xi, dyi, dxsi: L.mod_select(xi, wmod_d, Bq, Lq, H, C, m.cdt, m.score, m.sel,
@@ -353,7 +357,7 @@ def make_step(shape, inp, dev, stream, route_flags=0, fused=True):
                                                                      H, Hp, b.cdt, b.act, None, b.h, stream=stream))
          if fused else
          (lambda xi, dyi, dxsi: L.moe_expert_ffn(b.xs, b.cu, R, wg, wu, wd, E, H, Hp, b.cdt, b.act, b.h,
-                                                 stream=stream))),
+                                                 fws, fwsb, stream=stream))),
         ("combine", lambda xi, dyi, dxsi: L.moe_combine(b.h, b.gate, b.dst_row, m.sel_score, xi, m.sel, T, H, K,
                                                        b.cdt, m.y, stream=stream)),
         ("permute_bwd", lambda xi, dyi, dxsi: L.moe_permute_bwd(dyi, b.h, b.gate, b.dst_row, m.sel_score, m.sel,
@@ -396,7 +400,7 @@ def run_ours(args, shape, rank, world, local):
     dy_d, dxs_d = inp.get("dy"), inp.get("dxs")
     stream = torch.cuda.Stream(device=dev)
     fused = args.fused_gather and mode != "train"
-    calls, bufs, outs, cu = make_step(shape, inp, dev, stream, args.route_flags, fused)
+    calls, bufs, outs, cu = make_step(shape, inp, dev, stream, args.route_flags, fused, not args.no_tail_split)
     names = [n for n, _ in calls]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     flush_rd = torch.zeros(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
@@ -710,7 +714,7 @@ def run_ours(args, shape, rank, world, local):
                    "expert0_logit_bias": None if bias_entry is None else bias_entry["beta"],
                    "l2": "flushed between timed steps (512 MB write, then 512 MB read)", "parallelism": f"replicas{world}",
                    "route_flags": args.route_flags, "train": bool(args.train), "graph": not args.eager,
-                   "fused_gather": fused},
+                   "fused_gather": fused, "tail_split": not fused and not args.no_tail_split},
         "calls_ms": {k: round(v, 4) for k, v in call_ms.items()},
         "roofline": {"kernel": ("moe_expert_ffn + moe_expert_ffn_bwd (grouped tcgen05 GEMMs, forward and backward)"
                                 if mode == "train" else

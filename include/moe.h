@@ -87,7 +87,8 @@ MOE_API int moe_version(void);
 MOE_API unsigned long long moe_kernel_launches(void);
 
 /* Bytes of device workspace `op` needs for these sizes (0 = none; `ws` may then be
- * NULL).  Sizes not used by `op` are ignored.  Returns 0 for invalid sizes. */
+ * NULL).  Sizes not used by `op` are ignored.  Returns 0 for invalid sizes.
+ * MOE_OP_EXPERT_FFN: the workspace is optional (see moe_expert_ffn). */
 MOE_API size_t moe_workspace_bytes(int op, int T, int H, int E, int K, int Hp);
 
 /* Synchronises `stream`, then returns and clears the current device's error word:
@@ -208,7 +209,18 @@ MOE_API int moe_dispatch_noalloc(const void* x, const int32_t* topk_idx, int T, 
  *   act [rows,Hp] and h [rows,H] dtype out.  Accumulation is fp32; bf16 outputs
  *   are rounded to nearest-even.  The row split is read on the device from
  *   cu_seqlens (no host synchronisation); cu_seqlens[E] must equal `rows`.
- *   bf16 needs H % 64 == 0 and Hp % 64 == 0.  Workspace: none.
+ *   bf16 needs H % 64 == 0 and Hp % 64 == 0.
+ *   Workspace (optional, bf16): with ws 16-byte aligned and ws_bytes >=
+ *   moe_workspace_bytes(MOE_OP_EXPERT_FFN, ...) (about 32 MB, independent of the
+ *   sizes), when the down projection's last round of 256 x 256 tiles holds at
+ *   most half as many tiles as the GPU runs CTA pairs, each of those tiles is
+ *   computed as two K halves on two pairs whose fp32 partials are added (once,
+ *   in fp32) before the bf16 rounding; the workspace holds the partials and
+ *   arrival counters (the gate/up kernel of the same call zeroes them; no
+ *   state carries between calls).  h then differs from a call without the
+ *   workspace by that one extra fp32 rounding in those tiles; for the same
+ *   inputs on the same GPU model it is deterministic.  NULL or fewer bytes:
+ *   whole tiles only.  Concurrent calls need distinct workspaces.
  */
 MOE_API int moe_expert_ffn(const void* xs, const int32_t* cu_seqlens, int rows,
                    const void* w_gate, const void* w_up, const void* w_down,

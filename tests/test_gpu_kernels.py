@@ -274,6 +274,45 @@ def test_expert_ffn_matches_oracle(shape):
     assert_close(to64(h), h_ref, TOL[shape.dtype], "h")
 
 
+SPLIT_SHAPES = [S("bf16_T1000_H320_E4_K2_Hp320", 1000, 320, 4, 2, 320, "bf16"),
+                S("bf16_T3000_H256_E8_K2_Hp1408", 3000, 256, 8, 2, 1408, "bf16")]
+
+
+@pytest.mark.parametrize("shape", SPLIT_SHAPES, ids=ids(SPLIT_SHAPES))
+def test_expert_ffn_tail_split_matches_oracle(shape):
+    """With its workspace the down projection runs its last round of tiles as
+    two K halves on two CTA pairs whose fp32 partials meet in the workspace
+    (at these sizes every tile: there are fewer tiles than half the pairs; K =
+    H' of 5 and 22 blocks, split 2 + 3 and 11 + 11).  The workspace starts
+    as garbage (the call zeroes its counters itself); h matches the oracle and
+    comes out bit for bit the same on a second call; act does not depend on
+    the workspace (only the down projection splits); h without the workspace
+    agrees within the bf16 tolerance."""
+    x, wr, wg, wu, wd = host_layer_inputs(shape)
+    idx = O.topk_experts(O.router_logits(x.ref, wr.ref), shape.K)
+    cu, dst, src, xs_ref = O.dispatch(x.ref, idx, shape.E)
+    act_ref, h_ref = O.expert_ffn(xs_ref, cu, wg.ref, wu.ref, wd.ref)
+    R, H, Hp, E = shape.R, shape.H, shape.Hp, shape.E
+    xs, cu_d = dev(synth.store(xs_ref, shape.dtype)), torch.from_numpy(cu).to(DEV)
+    n = L.moe_workspace_bytes(L.MOE_OP_EXPERT_FFN, shape.T, H, E, shape.K, Hp)
+    ws = torch.full((n,), 0x7F, dtype=torch.uint8, device=DEV)
+    outs = []
+    for use_ws in (True, True, False):
+        act = torch.empty((R, Hp), dtype=TDT[shape.dtype], device=DEV)
+        h = torch.empty((R, H), dtype=TDT[shape.dtype], device=DEV)
+        L.moe_expert_ffn(xs, cu_d, R, dev(wg), dev(wu), dev(wd), E, H, Hp, CDT[shape.dtype], act, h,
+                         ws if use_ws else None, n if use_ws else 0)
+        outs.append((act, h))
+    torch.cuda.synchronize()
+    assert L.moe_last_device_error() == L.MOE_OK
+    (act1, h1), (act2, h2), (act3, h3) = outs
+    assert_close(to64(act1), act_ref, TOL[shape.dtype], "act")
+    assert_close(to64(h1), h_ref, TOL[shape.dtype], "h (split)")
+    assert torch.equal(h1, h2) and torch.equal(act1, act2)
+    assert torch.equal(act1, act3)
+    assert_close(to64(h3), h_ref, TOL[shape.dtype], "h (whole tiles)")
+
+
 GATHER_SHAPES = [S("bf16_T1000_H384_E16_K4_Hp320", 1000, 384, 16, 4, 320, "bf16"),
                  S("bf16_T777_H256_E64_K6_Hp192", 777, 256, 64, 6, 192, "bf16"),
                  S("bf16_T3_H128_E8_K2_Hp64", 3, 128, 8, 2, 64, "bf16"),

@@ -10,7 +10,7 @@ namespace moe {
 
 int launch_expert_ffn_tc(const void* xs, const int32_t* cu, int rows, const void* wg, const void* wu,
                          const void* wd, int E, int H, int Hp, void* act, void* gu, void* h, cudaStream_t s,
-                         const int32_t* gather, int gather_n);
+                         const int32_t* gather, int gather_n, void* ws, size_t ws_bytes);
 int launch_expert_ffn_bwd_tc(const void* xs, const int32_t* cu, int rows, const void* wg, const void* wu,
                              const void* wd, int E, int H, int Hp, const void* gu, const void* act, const void* dh,
                              void* dgu, void* dxs, float* dwg, float* dwu, float* dwd, cudaStream_t s);
@@ -19,10 +19,10 @@ int launch_expert_ffn_bwd_tc(const void* xs, const int32_t* cu, int rows, const 
 // is out of reach of the tf32 tensor-core path).
 int launch_expert_ffn(const void* xs, const int32_t* cu, int rows, const void* wg, const void* wu,
                       const void* wd, int E, int H, int Hp, int dtype, void* act, void* gu, void* h,
-                      cudaStream_t s, const int32_t* gather, int gather_n) {
+                      cudaStream_t s, const int32_t* gather, int gather_n, void* ws, size_t ws_bytes) {
   if (rows == 0) return MOE_OK;
   if (dtype == MOE_BF16)
-    return launch_expert_ffn_tc(xs, cu, rows, wg, wu, wd, E, H, Hp, act, gu, h, s, gather, gather_n);
+    return launch_expert_ffn_tc(xs, cu, rows, wg, wu, wd, E, H, Hp, act, gu, h, s, gather, gather_n, ws, ws_bytes);
   // act = silu(xs . Wg[e]) * (xs . Wu[e])
   SimtGemmArgs a{};
   a.A = xs; a.a_sm = H; a.a_sk = 1;

@@ -99,6 +99,15 @@ struct Params {
   // in place of the second B map (set when the output's rows are 16-byte
   // aligned)
   int tma_out = 0;
+  // CTA pairs, bf16 output: when the last round holds at most half as many
+  // tiles as there are pairs, its tiles run as two K halves on two pairs,
+  // whose fp32 partials meet in split_ws; split_cnt holds one arrival counter
+  // per (tile slot, CTA, epilogue warp), zeroed by the previous kernel on the
+  // stream (zero_cnt / zero_n: the counters this kernel zeroes for the next)
+  float* split_ws = nullptr;
+  int* split_cnt = nullptr;
+  int* zero_cnt = nullptr;
+  int zero_n = 0;
   // K-major A rows gathered from another matrix: row r of A is row gather[r]
   // of gather_src [gather_n, K] (bf16), copied into the swizzled stages by
   // four extra warps with 16-byte asynchronous copies (the dispatch gather
@@ -507,7 +516,7 @@ __device__ __forceinline__ void epi_f32_gk_tma(const CUtensorMap* tmO, const Par
 // p.accumulate), through the warp's [32][STG_LD] staging tile.
 template <int OUT_BN>
 __device__ __forceinline__ void epi_bf16(const Params& p, uint32_t tbase, const TileInfo& ti, float* epi_stage,
-                                         int q, int lane) {
+                                         int q, int lane, const float* addp = nullptr) {
   // TMEM row per thread -> this warp's staging tile -> 8 rows x 64 bytes
   // per store instruction (4 lanes per row segment of 32 columns).  With
   // accumulate, every old value the warp will add is requested first.
@@ -533,6 +542,17 @@ __device__ __forceinline__ void epi_bf16(const Params& p, uint32_t tbase, const 
   for (int c = 0; c < NCH; ++c) {
     float v[32];
     tmem_ld32(tbase + c * 32, v);
+    if (addp) {
+      // the other K half's partial of this thread's row (split tiles)
+#pragma unroll
+      for (int j4 = 0; j4 < 8; ++j4) {
+        const float4 o = __ldcg(reinterpret_cast<const float4*>(addp) + (c * 8 + j4) * 32 + lane);
+        v[4 * j4] += o.x;
+        v[4 * j4 + 1] += o.y;
+        v[4 * j4 + 2] += o.z;
+        v[4 * j4 + 3] += o.w;
+      }
+    }
 #pragma unroll
     for (int j = 0; j < 32; ++j) stg[lane * STG_LD + j] = v[j];
     __syncwarp();
@@ -564,6 +584,44 @@ __device__ __forceinline__ void epi_bf16(const Params& p, uint32_t tbase, const 
     }
     __syncwarp();
   }
+}
+
+// Tail split (CTA pairs): tile slots, and the fp32 partial of one K half of one
+// epilogue warp's 32 rows x 256 columns, stored so that every store and load
+// instruction covers 512 contiguous bytes (float4 j of chunk c of lane l at
+// (c * 8 + j) * 32 + l).
+constexpr int SPLIT_SLOTS = 64;
+constexpr long long SPLIT_WARP_ELEMS = 32LL * 256;
+constexpr size_t SPLIT_PART_BYTES = (size_t)SPLIT_SLOTS * 2 * 4 * 2 * SPLIT_WARP_ELEMS * 4;
+constexpr int SPLIT_COUNTERS = SPLIT_SLOTS * 2 * 4;
+
+// EPI_BF16 of a split tile, first part: each epilogue warp stores its partial,
+// then counts itself in with a device-scope fence before the atomic.  Returns
+// the other half's partial when this warp arrived second (it then adds that
+// partial, in epi_bf16, and writes the bf16 rows; fp32 addition commutes, so
+// the result does not depend on which half finishes first), else nullptr: the
+// warp is done once its partial is out.  Nothing waits.
+template <int OUT_BN>
+__device__ __forceinline__ const float* split_partial(const Params& p, uint32_t tbase, int slot, int half,
+                                                      uint32_t rank, int q, int lane) {
+  static_assert(32LL * OUT_BN == SPLIT_WARP_ELEMS, "one warp's partial is 32 rows x 256 columns");
+  float* base = p.split_ws + (((long long)slot * 2 + rank) * 4 + q) * 2 * SPLIT_WARP_ELEMS;
+  float4* mine = reinterpret_cast<float4*>(base + half * SPLIT_WARP_ELEMS);
+#pragma unroll 1
+  for (int c = 0; c < OUT_BN / 32; ++c) {
+    float v[32];
+    tmem_ld32(tbase + c * 32, v);
+#pragma unroll
+    for (int j4 = 0; j4 < 8; ++j4)
+      __stcg(mine + (c * 8 + j4) * 32 + lane, make_float4(v[4 * j4], v[4 * j4 + 1], v[4 * j4 + 2], v[4 * j4 + 3]));
+  }
+  __threadfence();
+  __syncwarp();
+  int first = 0;
+  if (lane == 0) first = atomicAdd(p.split_cnt + ((slot * 2 + (int)rank) * 4 + q), 1) == 0;
+  if (__shfl_sync(0xffffffffu, first, 0)) return nullptr;
+  __threadfence();
+  return base + (half ^ 1) * SPLIT_WARP_ELEMS;
 }
 
 // KSUB > 1: the NA = NB = KSUB tile pairs of a stage are consecutive 64-wide
@@ -1274,7 +1332,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   __shared__ int abort_flag;
   __shared__ int mt_pre[1025];
   __shared__ int cu_s[1025];
-  __shared__ int total_tiles_s;
+  __shared__ int total_tiles_s, full_tiles_s;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -1346,21 +1404,36 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     if (lane == 31) {
       mt_pre[G] = incl;
       // grouped K: every group has all (M / 256) x (N / 256) output tiles
-      total_tiles_s = GK ? G * ((p.M + 2 * BM - 1) / (2 * BM)) * n_tiles : incl * n_tiles;
+      int total = GK ? G * ((p.M + 2 * BM - 1) / (2 * BM)) * n_tiles : incl * n_tiles;
+      int full = total;
+      if (EPI == EPI_BF16 && p.split_ws && (p.K + BK - 1) / BK >= 2) {
+        // tail split: the last round's tiles become two K halves each
+        const int P = gridDim.x >> 1, rem = total % P;
+        if (rem > 0 && 2 * rem <= P && rem <= SPLIT_SLOTS) {
+          full = total - rem;
+          total = full + 2 * rem;
+        }
+      }
+      total_tiles_s = total;
+      full_tiles_s = full;
     }
   }
+  // counters of the next kernel on the stream (its split tiles' arrivals)
+  if (p.zero_cnt && blockIdx.x == 0)
+    for (int i = threadIdx.x; i < p.zero_n; i += blockDim.x) p.zero_cnt[i] = 0;
   tc_fence_before();
   __syncthreads();
   cluster_sync();  // the peer's barriers are initialised before anything arrives on them
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_slot;
-  const int total_tiles = total_tiles_s;
+  const int total_tiles = total_tiles_s, full_tiles = full_tiles_s;
   const int KB_ALL = (p.K + BK - 1) / BK;
   // One pair tile: this CTA's output rows, its K blocks, the first K row of
   // block 0, the output slab (group) and the valid K rows of its last block.
   struct PairWork {
     TileInfo ti;
     int kb_end, k_base, slab, last_valid;
+    int slot, half;  // split tiles: the tile's slot and K half (slot -1: a whole tile)
   };
   const int gk_mt = (p.M + 2 * BM - 1) / (2 * BM);
   auto pair_work = [&](int t) {
@@ -1378,12 +1451,26 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       w.k_base = beg;
       w.slab = g;
       w.last_valid = rows - (w.kb_end - 1) * BK;
+      w.slot = -1;
+      w.half = 0;
     } else {
-      w.ti = decode_pair<C::OUT_BN>(t, mt_pre, cu_s, G, n_tiles, rank);
-      w.kb_end = KB_ALL;
-      w.k_base = 0;
       w.slab = 0;
       w.last_valid = BK;
+      if (t < full_tiles) {
+        w.ti = decode_pair<C::OUT_BN>(t, mt_pre, cu_s, G, n_tiles, rank);
+        w.kb_end = KB_ALL;
+        w.k_base = 0;
+        w.slot = -1;
+        w.half = 0;
+      } else {
+        // units full, full + 1 are the two K halves of tile full, and so on
+        const int v = t - full_tiles, kb_mid = KB_ALL / 2;
+        w.ti = decode_pair<C::OUT_BN>(full_tiles + (v >> 1), mt_pre, cu_s, G, n_tiles, rank);
+        w.slot = v >> 1;
+        w.half = v & 1;
+        w.k_base = w.half ? kb_mid * BK : 0;
+        w.kb_end = w.half ? KB_ALL - kb_mid : kb_mid;
+      }
     }
     return w;
   };
@@ -1466,12 +1553,8 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       int i = 0;
       for (int t = pair; t < total_tiles; t += n_pairs, ++i) {
         const int acc = i & 1;
-        int kb_end = KB_ALL, last_valid = BK;
-        if constexpr (GK) {
-          const PairWork wk = pair_work(t);
-          kb_end = wk.kb_end;
-          last_valid = wk.last_valid;
-        }
+        const PairWork wk_m = pair_work(t);
+        const int kb_end = wk_m.kb_end, last_valid = wk_m.last_valid;
         const bool clear = GK && kb_end > 0 && last_valid < BK;
         if (lane != 0) {
           // follower: the clearing of this tile's last block
@@ -1552,7 +1635,9 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         else
           epi_f32_gk<C::OUT_BN>(p, tbase, ti, wk.slab, wk.kb_end == 0, epi_stage, q, lane);
       } else {
-        epi_bf16<C::OUT_BN>(p, tbase, ti, epi_stage, q, lane);
+        const float* addp = nullptr;
+        if (wk.slot >= 0) addp = split_partial<C::OUT_BN>(p, tbase, wk.slot, wk.half, rank, q, lane);
+        if (wk.slot < 0 || addp) epi_bf16<C::OUT_BN>(p, tbase, ti, epi_stage, q, lane, addp);
       }
       tc_fence_before();
       if (leader) mbar_arrive(acce_bar(acc));
@@ -1945,9 +2030,11 @@ router_bwd_tc_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_const
 }  // namespace tc
 
 // act = silu(xs Wg[e]) * (xs Wu[e]);  h = act Wd[e]^T   (bf16, grouped by cu)
+size_t expert_ffn_ws_bytes() { return tc::SPLIT_PART_BYTES + (size_t)tc::SPLIT_COUNTERS * sizeof(int); }
+
 int launch_expert_ffn_tc(const void* xs, const int32_t* cu, int rows, const void* wg, const void* wu,
                          const void* wd, int E, int H, int Hp, void* act, void* gu, void* h, cudaStream_t s,
-                         const int32_t* gather, int gather_n) {
+                         const int32_t* gather, int gather_n, void* ws, size_t ws_bytes) {
   using namespace tc;
   if (E > 1024) return MOE_ERR_UNSUPPORTED;
   CUtensorMap mA, mG, mU, mA2, mD;
@@ -1964,7 +2051,15 @@ int launch_expert_ffn_tc(const void* xs, const int32_t* cu, int rows, const void
   p1.ld_aux = 2LL * Hp;
   Params p2 = params(cu, E, rows, H, Hp, h, H, nullptr);
   if (!gather) {
-    // CTA pairs: 256-row tiles, each CTA staging half of the B columns
+    // CTA pairs: 256-row tiles, each CTA staging half of the B columns.  With
+    // the workspace, the gate/up kernel zeroes the counters with which the
+    // down projection's split tiles (if its last round has any) meet.
+    if (ws && ws_bytes >= expert_ffn_ws_bytes()) {
+      p2.split_ws = static_cast<float*>(ws);
+      p2.split_cnt = reinterpret_cast<int*>(static_cast<char*>(ws) + SPLIT_PART_BYTES);
+      p1.zero_cnt = p2.split_cnt;
+      p1.zero_n = SPLIT_COUNTERS;
+    }
     const long long ptiles = (rows + 2 * BM - 1) / (2 * BM) + E;
     int st = launch_pair<EPI_SWIGLU>(mA, mG, mU, p1, ptiles * ((Hp + 127) / 128), s);
     if (st != MOE_OK) return st;

@@ -83,6 +83,7 @@ size_t moe_workspace_bytes(int op, int T, int H, int E, int K, int Hp) {
     case MOE_OP_ROUTE: return (E > 0 && H > 0) ? route_ws_bytes(T, H, E) : 0;
     case MOE_OP_DISPATCH: return E > 0 ? dispatch_ws_bytes(T, E, K) : 0;
     case MOE_OP_ROUTE_BWD: return (E > 0 && H > 0) ? route_bwd_ws_bytes(T, H, E) : 0;
+    case MOE_OP_EXPERT_FFN: return expert_ffn_ws_bytes();
     case MOE_OP_EXPERT_FFN_BWD: return Hp > 0 ? expert_ffn_bwd_ws_bytes((int)((long long)T * K), Hp) : 0;
     default: return 0;
   }
@@ -173,14 +174,13 @@ static int check_expert_ffn(const void* xs, const int32_t* cu_seqlens, int rows,
 int moe_expert_ffn_ex(const void* xs, const int32_t* cu_seqlens, int rows, const void* w_gate, const void* w_up,
                       const void* w_down, int E, int H, int Hp, int dtype, void* act, void* gu, void* h, void* ws,
                       size_t ws_bytes, void* stream) {
-  (void)ws; (void)ws_bytes;
   int st = check_expert_ffn(xs, cu_seqlens, rows, w_gate, w_up, w_down, E, H, Hp, dtype);
   if (st != MOE_OK) return st;
   if (rows > 0 && (!act || !h)) return MOE_ERR_INVALID_ARG;
-  if (!all_aligned({act, gu, h})) return MOE_ERR_MISALIGNED;
+  if (!all_aligned({act, gu, h, ws})) return MOE_ERR_MISALIGNED;
   if (gu && dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   return launch_expert_ffn(xs, cu_seqlens, rows, w_gate, w_up, w_down, E, H, Hp, dtype, act, gu, h,
-                           as_stream(stream));
+                           as_stream(stream), nullptr, 0, ws, ws_bytes);
 }
 
 int moe_expert_ffn_gather(const void* x, const int32_t* src_tok, int T, const int32_t* cu_seqlens, int rows,

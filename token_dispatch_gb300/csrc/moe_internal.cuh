@@ -156,10 +156,14 @@ int launch_permute_bwd(const void* dy, const void* h, const float* gate, const i
 
 // expert FFN
 // gather (nullable): row r of the FFN input is row gather[r] of xs [gather_n, H]
-// (the dispatch gather fused into the gate/up operand load)
+// (the dispatch gather fused into the gate/up operand load).  ws (nullable):
+// with expert_ffn_ws_bytes() bytes, the bf16 down projection may split its
+// last round of tiles along K (fp32 partials and arrival counters in ws)
 int launch_expert_ffn(const void* xs, const int32_t* cu, int rows, const void* wg, const void* wu,
                       const void* wd, int E, int H, int Hp, int dtype, void* act, void* gu, void* h,
-                      cudaStream_t s, const int32_t* gather = nullptr, int gather_n = 0);
+                      cudaStream_t s, const int32_t* gather = nullptr, int gather_n = 0, void* ws = nullptr,
+                      size_t ws_bytes = 0);
+size_t expert_ffn_ws_bytes();
 int launch_expert_ffn_bwd(const void* xs, const int32_t* cu, int rows, const void* wg, const void* wu,
                           const void* wd, int E, int H, int Hp, const void* gu, const void* act, const void* dh,
                           void* dxs, float* dwg, float* dwu, float* dwd, void* ws, cudaStream_t s);

@@ -51,6 +51,10 @@ class MoEBuffers:
         self.ws_dispatch = _ws(self.ws_dispatch_bytes, dev)
         self.ws_route_bytes = L.moe_workspace_bytes(L.MOE_OP_ROUTE, T, H, E, K, Hp)
         self.ws_route = _ws(self.ws_route_bytes, dev)
+        # the expert FFN's optional workspace (bf16: the down projection's
+        # last round split along K)
+        self.ws_ffn_bytes = L.moe_workspace_bytes(L.MOE_OP_EXPERT_FFN, T, H, E, K, Hp) if dtype == "bf16" else 0
+        self.ws_ffn = _ws(self.ws_ffn_bytes, dev)
         if backward:
             self.dh = torch.empty((R, H), dtype=tdt, device=dev)
             self.d_gate = torch.empty((T, K), dtype=f32, device=dev)
@@ -91,7 +95,7 @@ def moe_forward(b: MoEBuffers, x, w_router, logit_bias, w_gate, w_up, w_down, st
                                 stream=stream)
     else:
         L.moe_expert_ffn_ex(b.xs, b.cu, T * K, w_gate, w_up, w_down, E, H, Hp, dt, b.act, b.gu, b.h,
-                            stream=stream)
+                            b.ws_ffn, b.ws_ffn_bytes, stream=stream)
     L.moe_combine(b.h, b.gate, b.dst_row, row_scale, residual, out_row, T, H, K, dt,
                   b.y if y is None else y, stream=stream)
 
