@@ -14,7 +14,8 @@
 //
 // One launch when the rows fit in shared memory (every CTA holds at most
 // ~54 rows of 4 KB, as at 4 x 2048 tokens of H = 2048 on 152 SMs): each CTA
-// brings its contiguous rows in with bulk copies, computes their scores, then
+// brings its contiguous rows in with bulk copies (groups of 16 rows on their
+// own mbarriers, each row scored as soon as its group lands), then
 // waits until every score of its sequence(s) is written (the score buffer is
 // first filled with a bit pattern no dot product produces, so the wait needs
 // no counter and two calls never share state), runs the select and stores
@@ -105,10 +106,15 @@ __device__ __forceinline__ int block_excl_scan(int v, int* wtot, int& total) {
 // or 0xffffffff when it is not selected.  All threads of the CTA call it;
 // hist ([2][256]) and wcnt ([2][MS_WARPS]) are the CTA's shared scratch.
 //
-// Radix select: four 8-bit passes from the top find the C-th largest key k*.
-// Each thread keeps its run of consecutive positions in registers; lanes with
-// the same digit add to the histogram once (the lowest of them), and the two
-// histograms alternate so a pass clears the next one's while it counts.
+// Radix select: up to four 8-bit passes from the top find the C-th largest key
+// k*.  Each thread keeps its run of consecutive positions in registers; lanes
+// with the same digit add to the histogram once (the lowest of them), and the
+// two histograms alternate so a pass clears the next one's while it counts.
+// When the digit bucket holding the C-th key is taken whole (every key with
+// that prefix is among the C largest), the remaining passes are skipped: the
+// selection is then every key whose prefix is at least that bucket's, the
+// same set the full passes give (ties between equal keys can only fall inside
+// the bucket, all of which is taken).
 __device__ void seq_row_map(unsigned* keys, int L, int C, int (*hist)[256], int (*wcnt)[MS_WARPS], int* s_sel) {
   const int tid = threadIdx.x, lane = tid & 31, w = tid >> 5;
   const bool partial = C > 0 && C < L;
@@ -162,7 +168,8 @@ __device__ void seq_row_map(unsigned* keys, int L, int C, int (*hist)[256], int 
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             if (run + c[j] >= need) {
-              s_sel[2 * (pass & 1)] = 255 - 8 * lane - j;
+              // digit, and a flag (bit 8) when the bucket is taken whole
+              s_sel[2 * (pass & 1)] = (255 - 8 * lane - j) | (run + c[j] == need ? 256 : 0);
               s_sel[2 * (pass & 1) + 1] = need - run;
               break;
             }
@@ -171,18 +178,21 @@ __device__ void seq_row_map(unsigned* keys, int L, int C, int (*hist)[256], int 
         }
       }
       __syncthreads();
-      prefix |= (unsigned)s_sel[2 * (pass & 1)] << shift;
+      const int dsel = s_sel[2 * (pass & 1)];
+      prefix |= (unsigned)(dsel & 255) << shift;
       pmask |= 255u << shift;
       need = s_sel[2 * (pass & 1) + 1];
+      if (dsel & 256) break;  // uniform: every thread read the same flag
     }
   }
-  const unsigned kth = prefix;  // the C-th largest key (when 0 < C < L)
+  // the C-th largest key's prefix under pmask (the whole key after four passes)
+  const unsigned kth = prefix;
 
   // selection flags with the tie rule (equal keys taken by position), then
   // ranks among the selected
   int n_eq = 0;
 #pragma unroll
-  for (int j = 0; j < MS_MAX_RUN; ++j) n_eq += (lo + j < hi && partial && kr[j] == kth) ? 1 : 0;
+  for (int j = 0; j < MS_MAX_RUN; ++j) n_eq += (lo + j < hi && partial && (kr[j] & pmask) == kth) ? 1 : 0;
   int tot;
   int eq_before = block_excl_scan(n_eq, wcnt[1], tot);
   unsigned flags = 0;
@@ -190,7 +200,7 @@ __device__ void seq_row_map(unsigned* keys, int L, int C, int (*hist)[256], int 
 #pragma unroll
   for (int j = 0; j < MS_MAX_RUN; ++j) {
     if (lo + j >= hi) break;
-    const unsigned k = kr[j];
+    const unsigned k = kr[j] & pmask;
     bool take;
     if (!partial) {
       take = C >= L;
@@ -277,6 +287,7 @@ mod_select_rows_kernel(const float* __restrict__ score, int L, int C, const uint
 // ---------------------------------------------------------- one launch ---
 constexpr unsigned SCORE_UNSET = 0xffffffffu;  // a NaN bit pattern no dot product yields
 constexpr unsigned long long MF_WAIT_LIMIT = 4000000000ull;  // clock64 cycles, ~2 s
+constexpr int MF_GROUPS = 8;  // row groups (mbarriers) per CTA
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -307,7 +318,8 @@ mod_fused_kernel(const T* __restrict__ x, const T* __restrict__ w, int B, int L,
                  float* score, int32_t* __restrict__ sel, float* __restrict__ sel_score,
                  uint8_t* __restrict__ mask, T* __restrict__ x_sel, T* __restrict__ y_skip, unsigned* err) {
   extern __shared__ __align__(128) unsigned char smem_rows[];
-  __shared__ __align__(8) unsigned long long bar;
+  __shared__ __align__(8) unsigned long long bar[MF_GROUPS];
+  __shared__ int rows_bad;
   __shared__ int hist[2][256];
   __shared__ int wcnt[2][MS_WARPS];
   __shared__ int s_sel[4];
@@ -320,23 +332,32 @@ mod_fused_kernel(const T* __restrict__ x, const T* __restrict__ w, int B, int L,
   const uint32_t rb = (uint32_t)H * (uint32_t)sizeof(T);
   const int nvec = H / V;
   unsigned* keys = reinterpret_cast<unsigned*>(smem_rows + (size_t)rows_cap * rb);
-  const uint32_t bar_a = smem_addr(&bar);
+  // rows [MS_WARPS g, MS_WARPS (g + 1)) arrive on barrier g (the last one takes
+  // the rest): the warps score the first rows while the later ones land
+  const int n_groups = min(MF_GROUPS, (nr + MS_WARPS - 1) / MS_WARPS);
+  auto group_of = [&](int r) { return min(r / MS_WARPS, MF_GROUPS - 1); };
 
-  // 1. the CTA's rows into shared memory (bulk copies on one mbarrier)
+  // 1. the CTA's rows into shared memory (bulk copies, one mbarrier per group)
   if (tid == 0) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(bar_a) : "memory");
+    rows_bad = 0;
+    for (int g = 0; g < n_groups; ++g)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(smem_addr(&bar[g])) : "memory");
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
   if (tid == 0) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar_a), "r"((uint32_t)nr * rb)
-                 : "memory");
-    for (int r = 0; r < nr; ++r)
-      asm volatile(
-          "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-              smem_addr(smem_rows + (size_t)r * rb)),
-          "l"(x + (r0 + r) * H), "r"(rb), "r"(bar_a)
-          : "memory");
+    for (int g = 0; g < n_groups; ++g) {
+      const int ra = g * MS_WARPS, rz = g == MF_GROUPS - 1 ? nr : min(nr, ra + MS_WARPS);
+      const uint32_t bg = smem_addr(&bar[g]);
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bg), "r"((uint32_t)(rz - ra) * rb)
+                   : "memory");
+      for (int r = ra; r < rz; ++r)
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                smem_addr(smem_rows + (size_t)r * rb)),
+            "l"(x + (r0 + r) * H), "r"(rb), "r"(bg)
+            : "memory");
+    }
   }
   // a lane's share of w_mod (WV vectors of 16 bytes) is requested while the
   // rows arrive and stays in registers for all the warp's rows
@@ -345,12 +366,12 @@ mod_fused_kernel(const T* __restrict__ x, const T* __restrict__ w, int B, int L,
   uint4 wr[WV];
 #pragma unroll
   for (int u = 0; u < WV; ++u) wr[u] = lane + 32 * u < nvec ? __ldg(wv + lane + 32 * u) : make_uint4(0, 0, 0, 0);
-  const bool rows_ok = __syncthreads_and(mbar_wait0_bounded(bar_a)) != 0;
-  if (!rows_ok && tid == 0) set_error(err, DEV_TIMEOUT);
 
-  // 2. scores of the CTA's rows: one warp per row
+  // 2. scores of the CTA's rows: one warp per row, as its group lands (a row
+  //    whose copy timed out is still scored, so no CTA waits on it forever)
   {
     for (int r = warp; r < nr; r += MS_WARPS) {
+      if (!mbar_wait0_bounded(smem_addr(&bar[group_of(r)])) && lane == 0) rows_bad = 1;
       const uint4* rv = reinterpret_cast<const uint4*>(smem_rows + (size_t)r * rb);
       float acc = 0.f;
       if (nvec <= 32 * WV) {
@@ -385,6 +406,8 @@ mod_fused_kernel(const T* __restrict__ x, const T* __restrict__ w, int B, int L,
       if (lane == 0) score[r0 + r] = acc;
     }
   }
+  const bool rows_ok = !__syncthreads_or(rows_bad);
+  if (!rows_ok && tid == 0) set_error(err, DEV_TIMEOUT);
 
   // 3. per sequence the CTA's tokens belong to: wait for all its scores, select,
   //    then write the CTA's share of mask / sel / sel_score and of the rows
@@ -434,7 +457,8 @@ mod_fused_kernel(const T* __restrict__ x, const T* __restrict__ w, int B, int L,
     // shared memory stays until the bulk stores have read it
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
   }
-  if (!rows_ok && tid == 0) mbar_wait0_bounded(bar_a);  // copies still in flight land before exit
+  if (!rows_ok && tid == 0)  // copies still in flight land before exit
+    for (int g = 0; g < n_groups; ++g) mbar_wait0_bounded(smem_addr(&bar[g]));
 }
 
 int warp_grid(long long n) {
