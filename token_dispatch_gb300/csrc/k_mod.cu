@@ -107,9 +107,11 @@ __device__ __forceinline__ int block_excl_scan(int v, int* wtot, int& total) {
 // hist ([2][256]) and wcnt ([2][MS_WARPS]) are the CTA's shared scratch.
 //
 // Radix select: up to four 8-bit passes from the top find the C-th largest key
-// k*.  Each thread keeps its run of consecutive positions in registers; lanes
-// with the same digit add to the histogram once (the lowest of them), and the
-// two histograms alternate so a pass clears the next one's while it counts.
+// k*.  Each thread keeps its run of consecutive positions in registers; in the
+// first pass lanes with the same digit add to the histogram once (the lowest
+// of them), in later passes (only the keys under the chosen prefix) each key
+// adds itself; the two histograms alternate so a pass clears the next one's
+// while it counts.
 // When the digit bucket holding the C-th key is taken whole (every key with
 // that prefix is among the C largest), the remaining passes are skipped: the
 // selection is then every key whose prefix is at least that bucket's, the
@@ -140,11 +142,20 @@ __device__ void seq_row_map(unsigned* keys, int L, int C, int (*hist)[256], int 
 #pragma unroll
       for (int j = 0; j < MS_MAX_RUN; ++j)
         d[j] = (lo + j < hi && (kr[j] & pmask) == prefix) ? (int)((kr[j] >> shift) & 255u) : -1;
+      if (pass == 0) {
+        // all keys count, and scores crowd into few top digits: lanes with
+        // equal digits add once
 #pragma unroll
-      for (int j = 0; j < MS_MAX_RUN; ++j) {
-        if (j >= per) break;  // uniform: per is the same for every thread
-        const unsigned peers = __match_any_sync(0xffffffffu, d[j]);
-        if (d[j] >= 0 && (peers & lt) == 0) atomicAdd(&h[d[j]], __popc(peers));
+        for (int j = 0; j < MS_MAX_RUN; ++j) {
+          if (j >= per) break;  // uniform: per is the same for every thread
+          const unsigned peers = __match_any_sync(0xffffffffu, d[j]);
+          if (d[j] >= 0 && (peers & lt) == 0) atomicAdd(&h[d[j]], __popc(peers));
+        }
+      } else {
+        // only the keys under the chosen prefix count, spread over the digits
+#pragma unroll
+        for (int j = 0; j < MS_MAX_RUN; ++j)
+          if (d[j] >= 0) atomicAdd(&h[d[j]], 1);
       }
       __syncthreads();
       if (w == 0) {
