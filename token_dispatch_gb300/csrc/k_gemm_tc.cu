@@ -1,6 +1,16 @@
 // Grouped bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
 //
-// Serves the three dense contractions of the layer:
+// Two persistent, warp-specialised kernels: a one-CTA kernel (described below;
+// the router GEMMs of up to 128 experts, the router backward's dW and dx GEMMs,
+// and the expert FFN when the dispatch gather is fused into its gate/up operand
+// load), and a CTA-pair kernel (two-CTA MMA,
+// 256 x 256 tiles, each CTA staging half of B; its own section further down)
+// for the expert FFN forward and backward and the router logits of more than
+// 128 experts.  The backward of the expert FFN adds
+//   da = dh Wd[e] with the SwiGLU backward in the epilogue, dxs = [dg | du]
+//   [Wg[e] ; Wu[e]]^T, and the grouped-K weight gradients dW[e] = A_e^T B_e.
+//
+// The contractions of the layer:
 //   * gate/up projection of every expert with SwiGLU fused in the epilogue
 //       act[r, n] = silu(sum_k xs[r,k] Wg[e][k,n]) * (sum_k xs[r,k] Wu[e][k,n])
 //   * down projection  h[r, n] = sum_k act[r,k] Wd[e][n,k]
@@ -16,7 +26,7 @@
 // are [cu[e], cu[e+1]) of the expert-sorted activation buffer, read on the device
 // (no host synchronisation).
 //
-// Design (one persistent CTA per SM, warp-specialised):
+// Design of the one-CTA kernel (one persistent CTA per SM, warp-specialised):
 //   warp 0      TMA producer: A tile 128x64 (K-major) and B tile (MN-major
 //               [64 K x BN] chunks for W[e] stored [H, H'] or W_r [H, E];
 //               K-major [BN x 64 K] for Wd[e] stored [H, H']) into a STAGES-deep
@@ -92,9 +102,7 @@ struct Params {
   long long ld_aux = 0;
   // K-major B from two tensors along K: k < kcat from tmB, k >= kcat from tmB2
   int kcat = 0;
-  // grouped K: group g reduces over rows [cu[g], cu[g+1]) of K (M, N fixed)
-  int gk = 0;
-  int b_col_off = 0;  // added to the N coordinate of MN-major B loads
+  int b_col_off = 0;  // grouped K (CTA pairs): added to the N coordinate of the B loads
   // grouped K on CTA pairs: fp32 tiles stored through the tensor map passed
   // in place of the second B map (set when the output's rows are 16-byte
   // aligned)
@@ -253,7 +261,7 @@ struct Cfg {
   // bf16 epilogue: per warp a [32 rows][33] fp32 staging tile, so the global
   // stores (and the reads of the old values) go out row-contiguous
   static constexpr int STG_LD = tc::STG_LD;
-  static constexpr int EPI_BYTES = (EPI == EPI_BF16 || EPI == EPI_F32_GK || EPI == EPI_ROUTER) ? 4 * 32 * STG_LD * 4 : 0;
+  static constexpr int EPI_BYTES = (EPI == EPI_BF16 || EPI == EPI_ROUTER) ? 4 * 32 * STG_LD * 4 : 0;
 };
 
 struct TileInfo {
@@ -699,13 +707,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     __syncwarp();
   }
   const int* cu = p.cu ? cu_s : nullptr;
-  if (warp == 2 && p.gk) {
-    // grouped K: G x (M tiles) x (N tiles), all groups alike
-    if (lane == 0) {
-      total_tiles_s = G * ((p.M + BM - 1) / BM) * n_tiles;
-      if (cu_s[0] != 0 || cu_s[G] != p.K) set_error(p.err, DEV_BOUNDS);
-    }
-  } else if (warp == 2) {
+  if (warp == 2) {
     // m-tile prefix over groups: each lane owns a contiguous run of groups
     const int per = (G + 31) / 32;
     int sum = 0;
@@ -740,38 +742,17 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int KB_ALL = (p.K + KSTAGE - 1) / KSTAGE;
   // k-blocks [kb_lo, kb_hi) of split s (every split non-empty: ksplit <= KB_ALL)
   auto kb_lo = [&](int s) { return (int)((long long)s * KB_ALL / p.ksplit); };
-  // One work item: its output tile, its k-blocks, the first K row of block 0,
-  // the output slab (split or group) and the valid rows of its last k-block.
+  // One work item: its output tile, its k-blocks and its K split.
   struct Work {
     TileInfo ti;
-    int kb_begin, kb_end, k_base, slab, last_valid;
+    int kb_begin, kb_end, split;
   };
-  const int gk_mt = (p.M + BM - 1) / BM;
   auto work = [&](int t) {
     Work w;
-    if (p.gk) {
-      const int per_g = gk_mt * n_tiles;
-      const int g = t / per_g, rem = t - g * per_g;
-      const int m = rem % gk_mt, n = rem / gk_mt;
-      w.ti.g = g;
-      w.ti.row0 = m * BM;
-      w.ti.rows = min(BM, p.M - w.ti.row0);
-      w.ti.n0 = n * C::OUT_BN;
-      const int beg = cu[g], rows = max(0, cu[g + 1] - beg);
-      w.kb_begin = 0;
-      w.kb_end = (rows + BK - 1) / BK;
-      w.k_base = beg;
-      w.slab = g;
-      w.last_valid = rows - (w.kb_end - 1) * BK;
-    } else {
-      const int split = t / base_tiles;
-      w.ti = decode(t - split * base_tiles, mt_pre, cu, G, n_tiles, p, C::OUT_BN);
-      w.kb_begin = kb_lo(split);
-      w.kb_end = kb_lo(split + 1);
-      w.k_base = 0;
-      w.slab = split;
-      w.last_valid = BK;
-    }
+    w.split = t / base_tiles;
+    w.ti = decode(t - w.split * base_tiles, mt_pre, cu, G, n_tiles, p, C::OUT_BN);
+    w.kb_begin = kb_lo(w.split);
+    w.kb_end = kb_lo(w.split + 1);
     return w;
   };
 
@@ -794,8 +775,10 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           filled_parity[stage] = (int)phase;
 #pragma unroll
           for (int c = 0; c < BN / 64; ++c) {
-            const CUtensorMap* m = (c < BN / 128) ? &tmB : &tmB2;
-            const int col = ti.n0 + (c % (BN / 128)) * 64;
+            // gate columns in the first half of the tile, up columns in the second
+            constexpr int HALF = BN >= 128 ? BN / 128 : 1;
+            const CUtensorMap* m = (c < HALF) ? &tmB : &tmB2;
+            const int col = ti.n0 + (c % HALF) * 64;
             tma_load_3d(b_dst + c * (64 * BK * 2), m, full_bar(stage), col, k0, ti.g);
           }
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -825,7 +808,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if (!wait_bounded(empty_bar(stage), phase ^ 1u, &abort_flag, p)) { ok = false; break; }
           const uint32_t a_dst = smem_u32(stage_base + stage * C::STAGE_BYTES);
           const uint32_t b_dst = a_dst + NA * A_STAGE_BYTES;
-          const int k0 = wk.k_base + kb * KSTAGE;
+          const int k0 = kb * KSTAGE;
           mbar_expect_tx(full_bar(stage), C::STAGE_BYTES);
           filled_parity[stage] = (int)phase;
 #pragma unroll
@@ -852,10 +835,9 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 tma_load_3d(dst + c * (64 * BK * 2), m, full_bar(stage), col, k0, z);
               }
             } else if (B_MN) {
-              const int zb = p.gk ? 0 : z;
 #pragma unroll
               for (int c = 0; c < BN / 64; ++c)
-                tma_load_3d(dst + c * (64 * BK * 2), &tmB, full_bar(stage), ti.n0 + c * 64 + p.b_col_off, kb0, zb);
+                tma_load_3d(dst + c * (64 * BK * 2), &tmB, full_bar(stage), ti.n0 + c * 64, kb0, z);
             } else if (p.kcat && kb0 >= p.kcat) {
               tma_load_3d(dst, &tmB2, full_bar(stage), kb0 - p.kcat, ti.n0, z);
             } else {
@@ -898,19 +880,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if (gathered) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           const uint32_t a_addr = smem_u32(stage_base + stage * C::STAGE_BYTES);
           const uint32_t b_addr = a_addr + NA * A_STAGE_BYTES;
-          if (A_MN && kb == kb_end - 1 && wk.last_valid < BK) {
-            // grouped K: the last block's rows past the group belong to the next
-            // group; zero them in A (each K row of an MN-major box is one
-            // 128-byte line, so the swizzle does not matter) before the MMAs
-            uint8_t* a_gen = stage_base + stage * C::STAGE_BYTES;
-            for (int bx = 0; bx < 2; ++bx)
-              for (int r = wk.last_valid; r < BK; ++r) {
-                uint4* line = reinterpret_cast<uint4*>(a_gen + bx * (64 * BK * 2) + r * 128);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) line[j] = make_uint4(0, 0, 0, 0);
-              }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          }
 #pragma unroll
           for (int pp = 0; pp < C::NP; ++pp) {
             const uint32_t a_t = a_addr + (pp < NA ? pp : NA - 1) * A_STAGE_BYTES;
@@ -999,7 +968,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       tc_fence_after();
       const Work wk = work(t);
       const TileInfo& ti = wk.ti;
-      const int split = wk.slab;
+      const int split = wk.split;
       const long long grow = (long long)ti.row0 + r_local;
       const bool row_ok = r_local < ti.rows && grow >= 0 && grow < p.M;
       const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
@@ -1007,8 +976,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         epi_swiglu<C::OUT_BN>(p, tbase, ti, row_ok, grow);
       } else if (EPI == EPI_SWIGLU_BWD) {
         epi_swiglu_bwd<C::OUT_BN>(p, tbase, ti, row_ok, grow);
-      } else if (EPI == EPI_F32_GK) {
-        epi_f32_gk<C::OUT_BN>(p, tbase, ti, wk.slab, wk.kb_end <= wk.kb_begin, epi_stage, q, lane);
       } else if (EPI == EPI_BF16) {
         epi_bf16<C::OUT_BN>(p, tbase, ti, epi_stage, q, lane);
       } else if (EPI == EPI_ROUTER) {
@@ -2114,7 +2081,6 @@ int launch_expert_ffn_bwd_tc(const void* xs, const int32_t* cu, int rows, const 
     if (!map_2d_as_3d(&mA, a_rows, H, rows, 64, BK)) return (int)MOE_ERR_CUDA;
     if (!map_2d_as_3d(&mB, b_rows, b_ld, rows, 64, BK)) return (int)MOE_ERR_CUDA;
     Params p = params(cu, E, H, Hp, rows, out, Hp, nullptr);
-    p.gk = 1;
     p.b_col_off = b_off;
     p.part_stride = (long long)H * Hp;
     // fp32 [E][H][H'] output as a map of [32 x 32] store boxes (rows of
