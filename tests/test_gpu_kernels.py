@@ -384,6 +384,16 @@ def test_expert_ffn_empty_and_single_row_experts():
                      dev(wd), 8, 128, 128, L.MOE_BF16, act, h)
     torch.cuda.synchronize()
     assert_close(to64(h), h_ref, 2e-2, "h")
+    # with the workspace: the one tile of each non-empty expert splits along K
+    # (H' = 128: two K blocks, one per half)
+    n = L.moe_workspace_bytes(L.MOE_OP_EXPERT_FFN, 5, 128, 8, 1, 128)
+    ws = torch.full((n,), 0x5A, dtype=torch.uint8, device=DEV)
+    h2 = torch.empty_like(h)
+    L.moe_expert_ffn(dev(synth.store(xs_ref, "bf16")), torch.from_numpy(cu).to(DEV), 5, dev(wg), dev(wu),
+                     dev(wd), 8, 128, 128, L.MOE_BF16, act, h2, ws, n)
+    torch.cuda.synchronize()
+    assert L.moe_last_device_error() == L.MOE_OK
+    assert_close(to64(h2), h_ref, 2e-2, "h (split)")
 
 
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
