@@ -20,9 +20,10 @@ bias from tests/golden/skew_bias.json.
 the library's entry points (the host issues one launch per step); the per-call
 split comes from the same calls launched one by one, each bracketed by CUDA
 events, and that loop's step time is reported as `eager_ms_per_step`
-(`--eager` takes `value` from it instead).  The end-to-end figure replays the
-step as a CUDA graph between the per-step host copies (`--e2e-eager` launches
-it call by call instead).
+(`--eager` takes `value` from it instead).  The end-to-end figure replays one
+CUDA graph per iteration holding the next step's host-to-device copies, this
+step's calls and the previous step's device-to-host copies (`--e2e-eager`
+issues the copies and the calls from the host, call by call, instead).
 
 Multi-GPU runs (torchrun) are replicas: every rank processes its own batch with
 no data-path collective; `value` is all ranks' tokens over the slowest rank's
@@ -581,52 +582,100 @@ def run_ours(args, shape, rank, world, local):
             done.record(sub)
             lead.wait_event(done)
     e2e_steps = max(3, min(args.steps, 20))
-    # the step's calls are captured once per input slot as a CUDA graph (through
-    # the same public entry points) and replayed: no host launch work per kernel
-    graph_in = None if args.e2e_eager else [capture(*(b + [None, None])[:3]) for b in bufs_in]
-    loaded = [torch.cuda.Event() for _ in range(2)]
-    consumed = [torch.cuda.Event() for _ in range(2)]
-    staged = [torch.cuda.Event() for _ in range(2)]
-    read_back = [torch.cuda.Event() for _ in range(2)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
-    def load(i):
-        slot = i % 2
-        with torch.cuda.stream(copy_stream):
-            if i >= 2:
-                copy_stream.wait_event(consumed[slot])  # step i-2 no longer reads this slot
-            split_copy(list(zip(bufs_in[slot], srcs)), copy_stream, h2d_sub)
-            loaded[slot].record(copy_stream)
+    def join(side):
+        # the step's stream waits for everything issued so far on `side`
+        ev = torch.cuda.Event()
+        ev.record(side)
+        stream.wait_event(ev)
 
-    torch.cuda.synchronize(dev)
-    e0.record(stream)
-    copy_stream.wait_event(e0)
-    d2h_stream.wait_event(e0)
-    load(0)
-    for i in range(e2e_steps):
-        if i + 1 < e2e_steps:
-            load(i + 1)
-        slot = i % 2
-        stream.wait_event(loaded[slot])
-        with torch.cuda.stream(stream):
-            ins = bufs_in[slot] + [None, None]
-            if graph_in:
-                graph_in[slot].replay()
-            else:
+    if not args.e2e_eager:
+        # One CUDA graph per iteration (built once per input slot and position):
+        # the next step's inputs go up on the copy streams, this step's calls
+        # run through the public entry points and copy their results to the
+        # staging slot, and the previous step's staged results go down, all
+        # three concurrent inside the graph; consecutive graphs on the step's
+        # stream run one after the other, so step i+1 reads inputs loaded in
+        # iteration i and step i's results are read back in iteration i+1.
+        def iteration_graph(slot, load_next, read_prev):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
+                fork = torch.cuda.Event()
+                fork.record(stream)
+                if load_next:
+                    copy_stream.wait_event(fork)
+                    split_copy(list(zip(bufs_in[1 - slot], srcs)), copy_stream, h2d_sub)
+                if read_prev:
+                    d2h_stream.wait_event(fork)
+                    split_copy(list(zip(host_out[1 - slot], stage_out[1 - slot])), d2h_stream, d2h_sub)
+                ins = bufs_in[slot] + [None, None]
                 step(ins[0], ins[1], ins[2])
-            consumed[slot].record(stream)
-            if i >= 2:
-                stream.wait_event(read_back[slot])  # step i-2's results are on the host
-            for d, st in zip(outs, stage_out[slot]):
-                st.copy_(d, non_blocking=True)
-            staged[slot].record(stream)
-        with torch.cuda.stream(d2h_stream):
-            d2h_stream.wait_event(staged[slot])
-            split_copy(list(zip(host_out[slot], stage_out[slot])), d2h_stream, d2h_sub)
-            read_back[slot].record(d2h_stream)
-    stream.wait_event(read_back[(e2e_steps - 1) % 2])
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
+                for d, st in zip(outs, stage_out[slot]):
+                    st.copy_(d, non_blocking=True)
+                if load_next:
+                    join(copy_stream)
+                if read_prev:
+                    join(d2h_stream)
+            return g
+        keys = [(i % 2, i + 1 < e2e_steps, i >= 1) for i in range(e2e_steps)]
+        graphs = {k: iteration_graph(*k) for k in sorted(set(keys))}
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        copy_stream.wait_event(e0)
+        split_copy(list(zip(bufs_in[0], srcs)), copy_stream, h2d_sub)  # step 0's inputs
+        join(copy_stream)
+        with torch.cuda.stream(stream):
+            for k in keys:
+                graphs[k].replay()
+        last = (e2e_steps - 1) % 2
+        tail = torch.cuda.Event()
+        tail.record(stream)
+        d2h_stream.wait_event(tail)
+        split_copy(list(zip(host_out[last], stage_out[last])), d2h_stream, d2h_sub)  # the last results
+        join(d2h_stream)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+    else:
+        loaded = [torch.cuda.Event() for _ in range(2)]
+        consumed = [torch.cuda.Event() for _ in range(2)]
+        staged = [torch.cuda.Event() for _ in range(2)]
+        read_back = [torch.cuda.Event() for _ in range(2)]
+
+        def load(i):
+            slot = i % 2
+            with torch.cuda.stream(copy_stream):
+                if i >= 2:
+                    copy_stream.wait_event(consumed[slot])  # step i-2 no longer reads this slot
+                split_copy(list(zip(bufs_in[slot], srcs)), copy_stream, h2d_sub)
+                loaded[slot].record(copy_stream)
+
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        copy_stream.wait_event(e0)
+        d2h_stream.wait_event(e0)
+        load(0)
+        for i in range(e2e_steps):
+            if i + 1 < e2e_steps:
+                load(i + 1)
+            slot = i % 2
+            stream.wait_event(loaded[slot])
+            with torch.cuda.stream(stream):
+                ins = bufs_in[slot] + [None, None]
+                step(ins[0], ins[1], ins[2])
+                consumed[slot].record(stream)
+                if i >= 2:
+                    stream.wait_event(read_back[slot])  # step i-2's results are on the host
+                for d, st in zip(outs, stage_out[slot]):
+                    st.copy_(d, non_blocking=True)
+                staged[slot].record(stream)
+            with torch.cuda.stream(d2h_stream):
+                d2h_stream.wait_event(staged[slot])
+                split_copy(list(zip(host_out[slot], stage_out[slot])), d2h_stream, d2h_sub)
+                read_back[slot].record(d2h_stream)
+        stream.wait_event(read_back[(e2e_steps - 1) % 2])
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     clk = clocks.stop()
     h2d = sum(h.numel() * h.element_size() for h in srcs)
@@ -726,7 +775,9 @@ def run_ours(args, shape, rank, world, local):
         "hbm_roofline": {"peak_GB/s": hbm_peak, "peak_source": f"{peak_src} hbm_gbs", "calls": hbm},
         "e2e": {"value": whole_job_tokens_per_s(n_tok, world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "launch": "host, call by call" if graph_in is None else "CUDA graph of the step, one per input slot"},
+                "launch": ("host, call by call" if args.e2e_eager else
+                           "one CUDA graph per iteration: the next step's host-to-device copies, this step's "
+                           "calls and staging, the previous step's device-to-host copies")},
         "gpu_launches": launches,
         "clocks": clk,
     }
