@@ -103,10 +103,6 @@ struct Params {
   // K-major B from two tensors along K: k < kcat from tmB, k >= kcat from tmB2
   int kcat = 0;
   int b_col_off = 0;  // grouped K (CTA pairs): added to the N coordinate of the B loads
-  // grouped K on CTA pairs: fp32 tiles stored through the tensor map passed
-  // in place of the second B map (set when the output's rows are 16-byte
-  // aligned)
-  int tma_out = 0;
   // CTA pairs, bf16 output: when the last round holds at most half as many
   // tiles as there are pairs, its tiles run as two K halves on two pairs,
   // whose fp32 partials meet in split_ws; split_cnt holds one arrival counter
@@ -434,37 +430,6 @@ __device__ __forceinline__ void epi_f32_bias(const Params& p, uint32_t tbase, co
         const float* sp = stg + rw * STG_LD + seg;
         *reinterpret_cast<float4*>(out + gr * p.ldo + col) =
             make_float4(sp[0] + bb.x, sp[1] + bb.y, sp[2] + bb.z, sp[3] + bb.w);
-      }
-    }
-    __syncwarp();
-  }
-}
-
-// EPI_F32_GK: fp32 tile of group `slab` (a grouped-K product, one output slab
-// per group) through the warp's staging tile: 4 rows x 128 bytes per store
-// instruction; a group without rows gets zeros.
-template <int OUT_BN>
-__device__ __forceinline__ void epi_f32_gk(const Params& p, uint32_t tbase, const TileInfo& ti, int slab, bool empty,
-                                           float* epi_stage, int q, int lane) {
-  float* out = static_cast<float*>(p.out) + (long long)slab * p.part_stride;
-  float* stg = epi_stage + q * 32 * STG_LD;
-  const int seg = (lane & 7) * 4;
-#pragma unroll 1
-  for (int c = 0; c < OUT_BN / 32; ++c) {
-    float v[32];
-    if (!empty) tmem_ld32(tbase + c * 32, v);
-#pragma unroll
-    for (int j = 0; j < 32; ++j) stg[lane * STG_LD + j] = empty ? 0.f : v[j];
-    __syncwarp();
-#pragma unroll
-    for (int ps = 0; ps < 8; ++ps) {
-      const int rw = ps * 4 + (lane >> 3);
-      const int rr = q * 32 + rw;
-      const long long gr = (long long)ti.row0 + rr;
-      const int col = ti.n0 + c * 32 + seg;
-      if (rr < ti.rows && gr < p.M && col < p.N) {
-        const float* sp = stg + rw * STG_LD + seg;
-        *reinterpret_cast<float4*>(out + gr * p.ldo + col) = make_float4(sp[0], sp[1], sp[2], sp[3]);
       }
     }
     __syncwarp();
@@ -1596,11 +1561,9 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       else if constexpr (EPI == EPI_SWIGLU_BWD) epi_swiglu_bwd<C::OUT_BN>(p, tbase, ti, row_ok, grow);
       else if constexpr (EPI == EPI_F32_BIAS) epi_f32_bias<C::OUT_BN>(p, tbase, ti, epi_stage, q, lane);
       else if constexpr (GK) {
-        if (p.tma_out)
-          epi_f32_gk_tma<C::OUT_BN>(&tmB2, p, tbase, ti, wk.slab, wk.kb_end == 0,
-                                    epi_stage + q * GK_OUT_BUFS * 32 * 32, q, lane, out_chunk);
-        else
-          epi_f32_gk<C::OUT_BN>(p, tbase, ti, wk.slab, wk.kb_end == 0, epi_stage, q, lane);
+        // the fp32 output's tensor map comes in place of the second B map
+        epi_f32_gk_tma<C::OUT_BN>(&tmB2, p, tbase, ti, wk.slab, wk.kb_end == 0,
+                                  epi_stage + q * GK_OUT_BUFS * 32 * 32, q, lane, out_chunk);
       } else {
         const float* addp = nullptr;
         if (wk.slot >= 0) addp = split_partial<C::OUT_BN>(p, tbase, wk.slot, wk.half, rank, q, lane);
@@ -2082,17 +2045,14 @@ int launch_expert_ffn_bwd_tc(const void* xs, const int32_t* cu, int rows, const 
     if (!map_2d_as_3d(&mB, b_rows, b_ld, rows, 64, BK)) return (int)MOE_ERR_CUDA;
     Params p = params(cu, E, H, Hp, rows, out, Hp, nullptr);
     p.b_col_off = b_off;
-    p.part_stride = (long long)H * Hp;
-    // fp32 [E][H][H'] output as a map of [32 x 32] store boxes (rows of
-    // 16-byte multiples, a 16-byte aligned base)
-    CUtensorMap mO = mB;
-    if (Hp % 4 == 0 && ((uintptr_t)out & 15) == 0) {
-      cuuint64_t dims[3] = {(cuuint64_t)Hp, (cuuint64_t)H, (cuuint64_t)E};
-      cuuint64_t str[2] = {(cuuint64_t)Hp * 4, (cuuint64_t)H * Hp * 4};
-      cuuint32_t box[3] = {32, 32, 1};
-      if (!make_map(&mO, out, 3, dims, str, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32)) return (int)MOE_ERR_CUDA;
-      p.tma_out = 1;
-    }
+    // fp32 [E][H][H'] output as a map of [32 x 32] store boxes (the C ABI
+    // guarantees a 16-byte aligned base; H' % 64 == 0 makes every row a
+    // 16-byte multiple)
+    CUtensorMap mO;
+    cuuint64_t dims[3] = {(cuuint64_t)Hp, (cuuint64_t)H, (cuuint64_t)E};
+    cuuint64_t str[2] = {(cuuint64_t)Hp * 4, (cuuint64_t)H * Hp * 4};
+    cuuint32_t box[3] = {32, 32, 1};
+    if (!make_map(&mO, out, 3, dims, str, box, CU_TENSOR_MAP_DATA_TYPE_FLOAT32)) return (int)MOE_ERR_CUDA;
     return launch_pair<EPI_F32_GK>(mA, mB, mO, p, gk_tiles, s);
   };
   if (dwd && (st = wgrad(dh, act, Hp, 0, dwd)) != MOE_OK) return st;
