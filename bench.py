@@ -548,14 +548,14 @@ def run_ours(args, shape, rank, world, local):
     # End to end through the public API: every step copies its inputs from pinned
     # host memory and its results back.  Inputs are double-buffered: the next
     # step's host-to-device copies run on a copy stream while this step computes.
-    # Results are first copied on the device into a double-buffered staging area
-    # (so the next step may overwrite them), then read back to pinned host memory
-    # on a third stream while the next step computes; the timed region ends when
-    # the last step's results are on the host.
+    # Results are read back to pinned host memory on a third stream while the
+    # next step computes: from a second set of layer buffers used on alternate
+    # steps (graph iterations), or, issued from the host (--e2e-eager), after a
+    # device copy into a double-buffered staging area.  The timed region ends
+    # when the last step's results are on the host.
     srcs = [x_h] + ([dy_d.cpu().pin_memory()] if dy_d is not None else []) + \
         ([dxs_d.cpu().pin_memory()] if dxs_d is not None else [])
     bufs_in = [[torch.empty_like(h, device=dev) for h in srcs] for _ in range(2)]
-    stage_out = [[torch.empty_like(o) for o in outs] for _ in range(2)]
     host_out = [[torch.empty(o.shape, dtype=o.dtype).pin_memory() for o in outs] for _ in range(2)]
     copy_stream = torch.cuda.Stream(device=dev)
     d2h_stream = torch.cuda.Stream(device=dev)
@@ -593,11 +593,16 @@ def run_ours(args, shape, rank, world, local):
     if not args.e2e_eager:
         # One CUDA graph per iteration (built once per input slot and position):
         # the next step's inputs go up on the copy streams, this step's calls
-        # run through the public entry points and copy their results to the
-        # staging slot, and the previous step's staged results go down, all
-        # three concurrent inside the graph; consecutive graphs on the step's
-        # stream run one after the other, so step i+1 reads inputs loaded in
-        # iteration i and step i's results are read back in iteration i+1.
+        # run through the public entry points into the slot's own layer
+        # buffers, and the previous step's results go down from the other
+        # slot's buffers, all three concurrent inside the graph; consecutive
+        # graphs on the step's stream run one after the other, so step i+1
+        # reads inputs loaded in iteration i and step i's results are read back
+        # in iteration i+1, before iteration i+2 overwrites them.
+        calls_b, _, outs_b, _ = make_step(shape, inp, dev, stream, args.route_flags, fused,
+                                          not args.no_tail_split)
+        slot_calls, slot_outs = [calls, calls_b], [outs, outs_b]
+
         def iteration_graph(slot, load_next, read_prev):
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream, capture_error_mode="relaxed"):
@@ -608,11 +613,10 @@ def run_ours(args, shape, rank, world, local):
                     split_copy(list(zip(bufs_in[1 - slot], srcs)), copy_stream, h2d_sub)
                 if read_prev:
                     d2h_stream.wait_event(fork)
-                    split_copy(list(zip(host_out[1 - slot], stage_out[1 - slot])), d2h_stream, d2h_sub)
+                    split_copy(list(zip(host_out[1 - slot], slot_outs[1 - slot])), d2h_stream, d2h_sub)
                 ins = bufs_in[slot] + [None, None]
-                step(ins[0], ins[1], ins[2])
-                for d, st in zip(outs, stage_out[slot]):
-                    st.copy_(d, non_blocking=True)
+                for _, fn in slot_calls[slot]:
+                    fn(ins[0], ins[1], ins[2])
                 if load_next:
                     join(copy_stream)
                 if read_prev:
@@ -632,11 +636,12 @@ def run_ours(args, shape, rank, world, local):
         tail = torch.cuda.Event()
         tail.record(stream)
         d2h_stream.wait_event(tail)
-        split_copy(list(zip(host_out[last], stage_out[last])), d2h_stream, d2h_sub)  # the last results
+        split_copy(list(zip(host_out[last], slot_outs[last])), d2h_stream, d2h_sub)  # the last results
         join(d2h_stream)
         e1.record(stream)
         torch.cuda.synchronize(dev)
     else:
+        stage_out = [[torch.empty_like(o) for o in outs] for _ in range(2)]
         loaded = [torch.cuda.Event() for _ in range(2)]
         consumed = [torch.cuda.Event() for _ in range(2)]
         staged = [torch.cuda.Event() for _ in range(2)]
