@@ -443,8 +443,8 @@ __device__ __forceinline__ void epi_f32_bias(const Params& p, uint32_t tbase, co
 // into slab `slab` of the map's [G][M][N] output, which clips rows and columns
 // past the output.  Lane 0 issues one bulk group per chunk; `chunk` counts the
 // warp's chunks across tiles, and a staging tile is refilled GK_OUT_BUFS
-// chunks later, once the store from it has read it (the stores in flight are
-// what keeps the fp32 output streaming).
+// chunks later, once the store from it has read it (two tiles per warp: deeper
+// rotations measured the same).
 constexpr int GK_OUT_BUFS = 2;
 template <int OUT_BN>
 __device__ __forceinline__ void epi_f32_gk_tma(const CUtensorMap* tmO, const Params& p, uint32_t tbase,
