@@ -19,9 +19,10 @@
 //     its 8 warps owns 64 columns, and lane group g (lanes 4g..4g+3) owns 8
 //     consecutive columns of them.  Tokens go in groups of 16; lane (g, c)
 //     touches the rows of tokens 2c, 2c+1, 2c+8, 2c+9 of the group at its 8
-//     columns: it loads them from x and dx (16 bytes each: whole 128-byte lines
-//     per 8 lanes, two or three groups ahead) and writes dx back to the same
-//     places.
+//     columns: it copies them from x and dx (16 bytes each: whole 128-byte
+//     lines per 8 lanes) into its own slots of a shared-memory ring with
+//     cp.async, six groups ahead for 8 experts and four for 16, reads them
+//     back when the group comes up, and writes dx back to the same places.
 //   * dx: D[h, t] = W_r[h, :] . dl[t, :]^T per 8 tokens.  Row m of M tile i is
 //     column 8g + 2i (m = g) or 8g + 2i + 1 (m = g + 8), so after the four
 //     tiles each lane holds whole 8-column row pieces of its two tokens; the
@@ -59,11 +60,13 @@ template <int E> struct RmCfg {
   static constexpr int TPS = RM_CHUNK / 2 + 4;          // token pairs per expert row, padded
   static constexpr int DLP_WORDS = NPART * RM_CHUNK * EPS;
   static constexpr int DLT_WORDS = NPART * E * TPS;
-  static constexpr int SMEM = (DLP_WORDS + DLT_WORDS) * 4;
   static constexpr int DWM = E == 8 ? 2 : 3;           // dW MMAs per N tile
-  // groups whose loads are in flight ahead (16 experts need the registers for
-  // their dW sums)
-  static constexpr int D = E == 8 ? 3 : 2;
+  // groups whose x and dx pieces are in flight ahead, each thread's in its own
+  // slots of a shared-memory ring (filled by cp.async, read back by the same
+  // thread): 8 pieces of 16 bytes per thread and group
+  static constexpr int D = E == 8 ? 6 : 4;
+  static constexpr int RING_OFF = ((DLP_WORDS + DLT_WORDS) * 4 + 15) / 16 * 16;  // bytes
+  static constexpr int SMEM = RING_OFF + D * 8 * RM_THREADS * 16;
 };
 
 __device__ __forceinline__ void mma_k16(float (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3,
@@ -88,13 +91,10 @@ __device__ __forceinline__ unsigned pack2(float lo, float hi) {
   return *reinterpret_cast<unsigned*>(&h);
 }
 
-// 16 bytes of a row: predicated load (the register keeps its value when off)
-__device__ __forceinline__ void ld16(uint4& v, const bf16* p, bool ok) {
-  asm volatile(
-      "{\n .reg .pred q;\n setp.ne.b32 q, %4, 0;\n"
-      " @q ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%5];\n}"
-      : "+r"(v.x), "+r"(v.y), "+r"(v.z), "+r"(v.w)
-      : "r"((int)ok), "l"(p));
+// 16 bytes of a row into shared memory, through L2 only (zeros when !ok)
+__device__ __forceinline__ void cp16(void* smem, const bf16* p, bool ok) {
+  const unsigned dst = static_cast<unsigned>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(p), "r"(ok ? 16 : 0) : "memory");
 }
 __device__ __forceinline__ unsigned word(const uint4& v, int i) {
   return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
@@ -195,26 +195,27 @@ router_bwd_mma_kernel(const float* __restrict__ logits, const int32_t* __restric
 
   // rows of a group this lane touches: tokens 2c, 2c+1, 2c+8, 2c+9
   auto row_tok = [&](int grp, int r) { return t0 + grp * 16 + 2 * c + (r & 1) + (r >> 1) * 8; };
-  auto load_group = [&](uint4 (&xr)[4], uint4 (&dr)[4], int grp) {
+  // ring slot of group grp: piece j (x rows 0-3, then dx rows 0-3) of thread
+  // tid at [slot][j][tid] (consecutive lanes 16 bytes apart: no bank conflicts)
+  uint4* ring = reinterpret_cast<uint4*>(reinterpret_cast<unsigned char*>(rm_smem) + C::RING_OFF);
+  auto piece = [&](int grp, int j) { return ring + ((grp % C::D) * 8 + j) * RM_THREADS + tid; };
+  // every thread commits one copy group per ring group, copies or not, so the
+  // per-thread wait counts stay aligned
+  auto load_group = [&](int grp) {
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int t = row_tok(grp, r);
       const bool ok = grp < n_groups && t < t1;
       const long long off = (long long)(ok ? t : 0) * H + col;
-      if (do_dw) ld16(xr[r], x + off, ok);
-      // dx is written by this kernel: its loads take the coherent path (the
-      // non-coherent one measured 2.5x slower here)
-      if (load_dx && ok) dr[r] = *reinterpret_cast<const uint4*>(dx + off);
+      if (do_dw) cp16(piece(grp, r), x + off, ok);
+      // dx is written by this kernel (a piece is read groups before it is
+      // written back, by the same thread): the copies read through L2
+      if (load_dx) cp16(piece(grp, 4 + r), dx + off, ok);
     }
+    asm volatile("cp.async.commit_group;" ::: "memory");
   };
-
-  uint4 xb[C::D][4], db[C::D][4];
 #pragma unroll
-  for (int d = 0; d < C::D; ++d)
-#pragma unroll
-    for (int r = 0; r < 4; ++r) { xb[d][r] = make_uint4(0, 0, 0, 0); db[d][r] = make_uint4(0, 0, 0, 0); }
-#pragma unroll
-  for (int d = 0; d < C::D; ++d) load_group(xb[d], db[d], d);
+  for (int d = 0; d < C::D; ++d) load_group(d);
 
   auto process = [&](uint4 (&xr)[4], uint4 (&dr)[4], int grp) {
     const int lg = grp % RM_GROUPS;  // group inside the chunk
@@ -343,17 +344,23 @@ router_bwd_mma_kernel(const float* __restrict__ logits, const int32_t* __restric
         }
       }
     }
-    load_group(xr, dr, grp + C::D);
   };
 
-  for (int q = 0; q < n_groups; q += C::D) {
+  // every thread takes part in the chunk barriers: the group loop is uniform
+  for (int grp = 0; grp < n_groups; ++grp) {
+    // this thread's copies of group grp have landed (the D - 1 newer groups may
+    // still be in flight)
+    asm volatile("cp.async.wait_group %0;" ::"n"(C::D - 1) : "memory");
+    uint4 xr[4], dr[4];
 #pragma unroll
-    for (int d = 0; d < C::D; ++d) {
-      const int grp = q + d;
-      // every thread takes part in the chunk barriers: the group loop is uniform
-      if (grp < n_groups) process(xb[d], db[d], grp);
+    for (int r = 0; r < 4; ++r) {
+      xr[r] = do_dw ? *piece(grp, r) : make_uint4(0, 0, 0, 0);
+      dr[r] = load_dx ? *piece(grp, 4 + r) : make_uint4(0, 0, 0, 0);
     }
+    process(xr, dr, grp);
+    load_group(grp + C::D);  // into the slot just read
   }
+  asm volatile("cp.async.wait_group 0;" ::: "memory");
 
   if (do_dw) {
     // dW[h][e] of column h = col + j (N tile j, n = g of the lane group that
