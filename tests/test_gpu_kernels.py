@@ -621,11 +621,13 @@ def test_route_bwd_linear_stream_matches_oracle(T, H):
 
 
 # all but the last run the one-launch form (the CTAs' rows fit in shared memory;
-# (3, 1000) puts sequence boundaries inside CTAs); rows of H = 8192 do not fit
-# and take the two-launch form
+# (3, 1000) puts sequence boundaries inside CTAs; (4, 8192) gives a CTA 215-216
+# rows, more than its eight row groups of 16, so the last group takes the rest);
+# rows of H = 8192 do not fit and take the two-launch form
 @pytest.mark.parametrize("B,Lseq,C,H,dtype", [(4, 2048, 1024, 128, "bf16"), (3, 1000, 333, 64, "f32"),
-                                              (2, 8192, 100, 64, "bf16"), (1, 7, 7, 64, "f32"),
-                                              (2, 64, 0, 64, "f32"), (2, 2048, 700, 8192, "bf16")])
+                                              (2, 8192, 100, 64, "bf16"), (4, 8192, 3000, 64, "bf16"),
+                                              (1, 7, 7, 64, "f32"), (2, 64, 0, 64, "f32"),
+                                              (2, 2048, 700, 8192, "bf16")])
 def test_mod_select_matches_oracle(B, Lseq, C, H, dtype):
     n = B * Lseq
     x = synth.store(synth.normal(2, 1, n * H).reshape(n, H), dtype)
