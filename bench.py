@@ -299,7 +299,8 @@ def make_step(shape, inp, dev, stream, route_flags=0, fused=True, tail_split=Tru
                                                   None if fused else b.xs, b.ws_dispatch, b.ws_dispatch_bytes,
                                                   stream=stream)),
             ("expert_ffn", (lambda xi, dyi, dxsi: L.moe_expert_ffn_gather(xi, b.src_tok, T, b.cu, R, wg, wu, wd, E, H,
-                                                                         Hp, b.cdt, b.act, None, b.h, stream=stream))
+                                                                         Hp, b.cdt, b.act, None, b.h, fws, fwsb,
+                                                                         stream=stream))
              if fused else
              (lambda xi, dyi, dxsi: L.moe_expert_ffn(b.xs, b.cu, R, wg, wu, wd, E, H, Hp, b.cdt, b.act, b.h,
                                                      fws, fwsb, stream=stream))),
@@ -357,7 +358,8 @@ def make_step(shape, inp, dev, stream, route_flags=0, fused=True, tail_split=Tru
                                               None if fused else b.xs, b.ws_dispatch, b.ws_dispatch_bytes,
                                               stream=stream)),
         ("expert_ffn", (lambda xi, dyi, dxsi: L.moe_expert_ffn_gather(m.x_sel, b.src_tok, T, b.cu, R, wg, wu, wd, E,
-                                                                     H, Hp, b.cdt, b.act, None, b.h, stream=stream))
+                                                                     H, Hp, b.cdt, b.act, None, b.h, fws, fwsb,
+                                                                     stream=stream))
          if fused else
          (lambda xi, dyi, dxsi: L.moe_expert_ffn(b.xs, b.cu, R, wg, wu, wd, E, H, Hp, b.cdt, b.act, b.h,
                                                  fws, fwsb, stream=stream))),
@@ -770,7 +772,7 @@ def run_ours(args, shape, rank, world, local):
                    "expert0_logit_bias": None if bias_entry is None else bias_entry["beta"],
                    "l2": "flushed between timed steps (512 MB write, then 512 MB read)", "parallelism": f"replicas{world}",
                    "route_flags": args.route_flags, "train": bool(args.train), "graph": not args.eager,
-                   "fused_gather": fused, "tail_split": not fused and not args.no_tail_split},
+                   "fused_gather": fused, "tail_split": not args.no_tail_split},
         "calls_ms": {k: round(v, 4) for k, v in call_ms.items()},
         "roofline": {"kernel": ("moe_expert_ffn + moe_expert_ffn_bwd (grouped tcgen05 GEMMs, forward and backward)"
                                 if mode == "train" else

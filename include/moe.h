@@ -233,13 +233,15 @@ MOE_API int moe_expert_ffn(const void* xs, const int32_t* cu_seqlens, int rows,
  *                       directly; EP "Step-by-step": rows addressed by index]
  *
  *   moe_expert_ffn_ex with xs[r,:] = x[src_tok[r],:] read straight from x: in
- *   the gate/up GEMM eight extra warps copy the rows of each 128-row tile from
- *   x by src_tok (as written by moe_dispatch) into its operand stages, so the
- *   expert-sorted copy of the input is never written or read.  The results
- *   are bit-identical to moe_expert_ffn_ex on the rows moe_dispatch writes.
- *   x [T,H] dtype; src_tok [rows] int32 in [0,T) (an index outside sets
- *   MOE_ERR_DEVICE_BOUNDS and reads row 0); the rest as moe_expert_ffn_ex.
- *   Workspace: none.
+ *   the gate/up GEMM (CTA pairs, 256-row tiles) eight extra warps per CTA copy
+ *   the CTA's 128 rows of each tile from x by src_tok (as written by
+ *   moe_dispatch) into its operand stages, so the expert-sorted copy of the
+ *   input is never written or read.  The results are bit-identical to
+ *   moe_expert_ffn_ex on the rows moe_dispatch writes (with the same
+ *   workspace argument).  x [T,H] dtype; src_tok [rows] int32 in [0,T) (an
+ *   index outside sets MOE_ERR_DEVICE_BOUNDS and reads row 0); the rest as
+ *   moe_expert_ffn_ex.
+ *   Workspace: optional, as moe_expert_ffn (the down projection's tail split).
  */
 MOE_API int moe_expert_ffn_gather(const void* x, const int32_t* src_tok, int T, const int32_t* cu_seqlens,
                                   int rows, const void* w_gate, const void* w_up, const void* w_down, int E,

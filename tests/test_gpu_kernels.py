@@ -314,6 +314,7 @@ def test_expert_ffn_tail_split_matches_oracle(shape):
 
 
 GATHER_SHAPES = [S("bf16_T1000_H384_E16_K4_Hp320", 1000, 384, 16, 4, 320, "bf16"),
+                 S("bf16_T2048_H512_E8_K2_Hp768", 2048, 512, 8, 2, 768, "bf16"),
                  S("bf16_T777_H256_E64_K6_Hp192", 777, 256, 64, 6, 192, "bf16"),
                  S("bf16_T3_H128_E8_K2_Hp64", 3, 128, 8, 2, 64, "bf16"),
                  S("f32_T300_H64_E12_K3_Hp96", 300, 64, 12, 3, 96, "f32")]
@@ -323,9 +324,11 @@ GATHER_SHAPES = [S("bf16_T1000_H384_E16_K4_Hp320", 1000, 384, 16, 4, 320, "bf16"
 def test_expert_ffn_gather_equals_ffn_on_dispatched_rows(shape):
     """The gate/up GEMM reading the rows of x by src_tok gives bit for bit what
     the FFN gives on the expert-sorted rows dispatch writes (the same operands
-    in the same order), and matches the oracle; dispatch without xs writes the
-    same index maps.  Ragged experts and tiles (T not a multiple of 128, some
-    experts without rows for T=3)."""
+    in the same order; the saved [g | u] too, and the same split of the down
+    projection's last round when both get the workspace), and matches the
+    oracle; dispatch without xs writes the same index maps.  Ragged experts and
+    tiles (T not a multiple of 128, some experts without rows for T=3), several
+    rounds of pair tiles and more K blocks than pipeline stages (T=2048)."""
     x, wr, wg, wu, wd = host_layer_inputs(shape)
     T, H, E, K, Hp, R = shape.T, shape.H, shape.E, shape.K, shape.Hp, shape.R
     idx = O.topk_experts(O.router_logits(x.ref, wr.ref), K)
@@ -335,9 +338,14 @@ def test_expert_ffn_gather_equals_ffn_on_dispatched_rows(shape):
     xd, idx_d = dev(x), torch.from_numpy(idx).to(DEV)
     L.moe_dispatch(xd, idx_d, T, H, E, K, CDT[shape.dtype], b.cu, b.dst_row, b.src_tok, b.xs, b.ws_dispatch,
                    b.ws_dispatch_bytes)
+    bf = shape.dtype == "bf16"
     act1 = torch.empty((R, Hp), dtype=TDT[shape.dtype], device=DEV)
     h1 = torch.empty((R, H), dtype=TDT[shape.dtype], device=DEV)
-    L.moe_expert_ffn(b.xs, b.cu, R, dev(wg), dev(wu), dev(wd), E, H, Hp, CDT[shape.dtype], act1, h1)
+    gu1 = torch.empty((R, 2 * Hp), dtype=TDT[shape.dtype], device=DEV) if bf else None
+    nws = L.moe_workspace_bytes(L.MOE_OP_EXPERT_FFN, T, H, E, K, Hp) if bf else 0
+    ws = torch.full((max(nws, 1),), 0x7F, dtype=torch.uint8, device=DEV)
+    L.moe_expert_ffn_ex(b.xs, b.cu, R, dev(wg), dev(wu), dev(wd), E, H, Hp, CDT[shape.dtype], act1, gu1, h1,
+                        ws if bf else None, nws)
     cu2 = torch.full_like(b.cu, -9)
     dst2 = torch.full_like(b.dst_row, -9)
     src2 = torch.full_like(b.src_tok, -9)
@@ -345,13 +353,17 @@ def test_expert_ffn_gather_equals_ffn_on_dispatched_rows(shape):
                    b.ws_dispatch_bytes)
     act2 = torch.empty_like(act1)
     h2 = torch.empty_like(h1)
-    L.moe_expert_ffn_gather(xd, src2, T, cu2, R, dev(wg), dev(wu), dev(wd), E, H, Hp, CDT[shape.dtype], act2, None,
-                            h2)
+    gu2 = torch.empty_like(gu1) if bf else None
+    ws.fill_(0x7F)  # stale partials and counters: the call zeroes what it uses
+    L.moe_expert_ffn_gather(xd, src2, T, cu2, R, dev(wg), dev(wu), dev(wd), E, H, Hp, CDT[shape.dtype], act2, gu2,
+                            h2, ws if bf else None, nws)
     torch.cuda.synchronize()
     assert L.moe_last_device_error() == L.MOE_OK
     for a_, b_ in ((b.cu, cu2), (b.dst_row, dst2), (b.src_tok, src2)):
         assert torch.equal(a_, b_)
     assert torch.equal(act1, act2) and torch.equal(h1, h2)
+    if bf:
+        assert torch.equal(gu1, gu2)
     assert_close(to64(act2), act_ref, TOL[shape.dtype], "act")
     assert_close(to64(h2), h_ref, TOL[shape.dtype], "h")
 

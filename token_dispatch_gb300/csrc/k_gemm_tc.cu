@@ -1,12 +1,11 @@
 // Grouped bf16 GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA).
 //
 // Two persistent, warp-specialised kernels: a one-CTA kernel (described below;
-// the router GEMMs of up to 128 experts, the router backward's dW and dx GEMMs,
-// and the expert FFN when the dispatch gather is fused into its gate/up operand
-// load), and a CTA-pair kernel (two-CTA MMA,
-// 256 x 256 tiles, each CTA staging half of B; its own section further down)
-// for the expert FFN forward and backward and the router logits of more than
-// 128 experts.  The backward of the expert FFN adds
+// the router GEMMs of up to 128 experts and the router backward's dW and dx
+// GEMMs), and a CTA-pair kernel (two-CTA MMA, 256 x 256 tiles, each CTA staging
+// half of B; its own section further down) for the expert FFN forward (with
+// the dispatch gather optionally fused into its gate/up operand load) and
+// backward and the router logits of more than 128 experts.  The backward of the expert FFN adds
 //   da = dh Wd[e] with the SwiGLU backward in the epilogue, dxs = [dg | du]
 //   [Wg[e] ; Wu[e]]^T, and the grouped-K weight gradients dW[e] = A_e^T B_e.
 //
@@ -59,17 +58,7 @@ namespace tc {
 constexpr int BM = 128;
 constexpr int BK = 64;            // 64 bf16 = 128 bytes: one swizzle row
 constexpr int NUM_THREADS = 192;  // 6 warps
-constexpr int GATHER_WARPS = 8;   // extra warps copying gathered A rows (the gate/up GEMM)
-
-// the gate/up GEMM can take its A rows gathered from another matrix
-template <int EPI, bool A_MN, int NA, int NB, int KSUB>
-__host__ __device__ constexpr bool can_gather() {
-  return EPI == 0 && NA == 1 && NB == 1 && KSUB == 1 && !A_MN;
-}
-template <int EPI, bool A_MN, int NA, int NB, int KSUB>
-__host__ __device__ constexpr int max_threads() {
-  return can_gather<EPI, A_MN, NA, NB, KSUB>() ? NUM_THREADS + 32 * GATHER_WARPS : NUM_THREADS;
-}
+constexpr int GATHER_WARPS = 8;   // extra warps per CTA copying gathered A rows (the gate/up GEMM)
 constexpr int A_STAGE_BYTES = BM * BK * 2;
 constexpr int STG_LD = 33;  // row stride (floats) of an epilogue staging tile
 
@@ -112,10 +101,11 @@ struct Params {
   int* split_cnt = nullptr;
   int* zero_cnt = nullptr;
   int zero_n = 0;
-  // K-major A rows gathered from another matrix: row r of A is row gather[r]
-  // of gather_src [gather_n, K] (bf16), copied into the swizzled stages by
-  // four extra warps with 16-byte asynchronous copies (the dispatch gather
-  // fused into the operand load)
+  // K-major A rows gathered from another matrix (the gate/up GEMM on CTA
+  // pairs): row r of A is row gather[r] of gather_src [gather_n, K] (bf16),
+  // copied into the swizzled stages by GATHER_WARPS extra warps per CTA with
+  // 16-byte asynchronous copies (the dispatch gather fused into the operand
+  // load)
   const int32_t* gather = nullptr;
   const bf16* gather_src = nullptr;
   int gather_n = 0;
@@ -601,7 +591,7 @@ __device__ __forceinline__ const float* split_partial(const Params& p, uint32_t 
 // slices of K (a stage covers 64*KSUB of K), so each row of a streamed operand
 // is requested as 128*KSUB contiguous bytes at once.
 template <int EPI, bool A_MN, bool B_MN, int BN, int STAGES, int NA, int NB, int KSUB = 1>
-__global__ void __launch_bounds__((max_threads<EPI, A_MN, NA, NB, KSUB>()), 1)
+__global__ void __launch_bounds__(NUM_THREADS, 1)
 tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                const __grid_constant__ CUtensorMap tmB2, const Params p) {
   using C = Cfg<BN, EPI, NA, NB>;
@@ -622,9 +612,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int G = p.G;
-  // A rows gathered by the extra warps (the gate/up GEMM only)
-  constexpr bool CAN_GATHER = can_gather<EPI, A_MN, NA, NB, KSUB>();
-  const bool gathered = CAN_GATHER && p.gather != nullptr;
   const int n_tiles = (p.N + C::OUT_BN - 1) / C::OUT_BN;
 
   auto full_bar = [&](int s) { return smem_u32(&bars[s]); };
@@ -636,7 +623,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), gathered ? 1 + 32 * GATHER_WARPS : 1);  // + a copy-completion arrival per gather lane
+      mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -721,44 +708,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     return w;
   };
 
-  if (warp == 0 && gathered) {
-    // ------------------------------------------------ producer of B (A gathered)
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      int filled_parity[STAGES];
-      for (int s = 0; s < STAGES; ++s) filled_parity[s] = -1;
-      bool ok = true;
-      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-        const Work wk = work(t);
-        const TileInfo& ti = wk.ti;
-        for (int kb = wk.kb_begin; kb < wk.kb_end; ++kb) {
-          if (!wait_bounded(empty_bar(stage), phase ^ 1u, &abort_flag, p)) { ok = false; break; }
-          const uint32_t b_dst = smem_u32(stage_base + stage * C::STAGE_BYTES) + A_STAGE_BYTES;
-          const int k0 = kb * BK;
-          mbar_expect_tx(full_bar(stage), C::STAGE_BYTES - A_STAGE_BYTES);
-          filled_parity[stage] = (int)phase;
-#pragma unroll
-          for (int c = 0; c < BN / 64; ++c) {
-            // gate columns in the first half of the tile, up columns in the second
-            constexpr int HALF = BN >= 128 ? BN / 128 : 1;
-            const CUtensorMap* m = (c < HALF) ? &tmB : &tmB2;
-            const int col = ti.n0 + (c % HALF) * 64;
-            tma_load_3d(b_dst + c * (64 * BK * 2), m, full_bar(stage), col, k0, ti.g);
-          }
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        }
-      }
-      // drain: every stage filled must have landed (B and the gathered A rows)
-      for (int s = 0; s < STAGES; ++s) {
-        if (filled_parity[s] < 0) continue;
-        const long long t0 = clock64();
-        while (!mbar_try_wait(full_bar(s), (uint32_t)filled_parity[s])) {
-          if ((unsigned long long)(clock64() - t0) > DRAIN_LIMIT) { set_error(p.err, DEV_TIMEOUT); break; }
-        }
-      }
-    }
-  } else if (warp == 0) {
+  if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       int stage = 0;
@@ -840,9 +790,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int kb = kb_begin; kb < kb_end; ++kb) {
           if (!wait_bounded(full_bar(stage), phase, &abort_flag, p)) { ok = false; break; }
           tc_fence_after();
-          // gathered A rows were written by the generic proxy (asynchronous
-          // copies): make them visible to the MMA's reads
-          if (gathered) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
           const uint32_t a_addr = smem_u32(stage_base + stage * C::STAGE_BYTES);
           const uint32_t b_addr = a_addr + NA * A_STAGE_BYTES;
 #pragma unroll
@@ -876,51 +823,6 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if ((unsigned long long)(clock64() - t0) > DRAIN_LIMIT) { set_error(p.err, DEV_TIMEOUT); break; }
         }
       }
-    }
-  } else if (warp >= NUM_THREADS / 32) {
-    // ------------------------------------------------ gathered A rows
-    // Warp 6 + w copies rows RW*w .. RW*w + RW-1 of every A tile (RW = 128 /
-    // GATHER_WARPS): instruction j takes 4 rows, 8 lanes per row, one 16-byte
-    // chunk each (whole 128-byte row segments), to the chunk's
-    // 128-byte-swizzled place.  Rows past the matrix read row 0 (their outputs
-    // are masked).
-    if (gathered) {
-      constexpr int RW = BM / GATHER_WARPS;
-      const int gw = warp - NUM_THREADS / 32;
-      const int crow = lane >> 3, chunk = lane & 7;
-      int stage = 0;
-      uint32_t phase = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; ok && t < total_tiles; t += gridDim.x) {
-        const Work wk = work(t);
-        const TileInfo& ti = wk.ti;
-        const int r_own = ti.row0 + RW * gw + (lane % RW);
-        int src = r_own < p.M ? __ldg(p.gather + r_own) : 0;
-        if (src < 0 || src >= p.gather_n) {
-          set_error(p.err, DEV_BOUNDS);
-          src = 0;
-        }
-        for (int kb = wk.kb_begin; kb < wk.kb_end; ++kb) {
-          if (lane == 0) ok = wait_bounded(empty_bar(stage), phase ^ 1u, &abort_flag, p);
-          ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-          if (!ok) break;
-          const uint32_t a_dst = smem_u32(stage_base + stage * C::STAGE_BYTES);
-          const int k0 = kb * BK;
-#pragma unroll
-          for (int j = 0; j < RW / 4; ++j) {
-            const int rr = 4 * j + crow;  // row inside this warp's RW
-            const int r = RW * gw + rr;   // row inside the tile
-            const int srow = __shfl_sync(0xffffffffu, src, rr);
-            const bf16* g = p.gather_src + (long long)srow * p.K + k0 + chunk * 8;
-            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(a_dst + r * 128 + ((chunk ^ (r & 7)) << 4)),
-                         "l"(g)
-                         : "memory");
-          }
-          asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(full_bar(stage)) : "memory");
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
-        }
-      }
-      asm volatile("cp.async.wait_all;" ::: "memory");
     }
   } else {
     // ------------------------------------------------------------ epilogue
@@ -1129,7 +1031,8 @@ struct PairCfg {
   static constexpr int TMEM_COLS = 2 * PAIR_BN;
   static constexpr int EPI_BYTES =
       EPI == EPI_F32_GK ? 4 * GK_OUT_BUFS * 32 * 32 * 4 : (EPI == EPI_BF16 || EPI == EPI_F32_BIAS) ? 4 * 32 * STG_LD * 4 : 0;
-  static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + EPI_BYTES + (2 * STAGES + 5) * 8 + 1024;
+  // barriers: full, empty, gathered [STAGES] each; accf, acce [2] each; drain
+  static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + EPI_BYTES + (3 * STAGES + 5) * 8 + 1024;
 };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -1244,13 +1147,25 @@ __device__ __forceinline__ TileInfo decode_pair(int t, const int* mt_pre, const 
   return ti;
 }
 
-template <int EPI>
-__global__ void __launch_bounds__(NUM_THREADS, 1) __cluster_dims__(2, 1, 1)
+// GATHER (gate/up only): the A rows are gathered from p.gather_src by
+// GATHER_WARPS extra warps per CTA instead of loaded by TMA, each CTA copying
+// its own 128 rows (rows past the group's end are not copied: their outputs
+// are masked, and an accumulator row depends on its own A row only).  Every
+// gather lane's copies complete on its CTA's `gathered` barrier; one more warp
+// per CTA relays each completed stage to the leader's full barrier: it fences
+// the copies (generic proxy) against the MMA's reads (async proxy) and sends
+// 16 bytes to the leader by a bulk copy that completes on that barrier, like
+// the TMA loads (a plain remote arrival at cluster scope, measured, made the
+// MMA's waits about twice as long).
+constexpr int PAIR_GATHER_THREADS = NUM_THREADS + 32 * (GATHER_WARPS + 1);
+template <int EPI, bool GATHER = false>
+__global__ void __launch_bounds__(GATHER ? PAIR_GATHER_THREADS : NUM_THREADS, 1) __cluster_dims__(2, 1, 1)
 tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmB2, const Params p) {
   static_assert(EPI == EPI_SWIGLU || EPI == EPI_BF16 || EPI == EPI_SWIGLU_BWD || EPI == EPI_F32_BIAS ||
                     EPI == EPI_F32_GK,
                 "pair kernel: GEMMs with a row-major output");
+  static_assert(!GATHER || EPI == EPI_SWIGLU, "gathered A rows: the gate/up GEMM only");
   using C = PairCfg<EPI>;
   constexpr bool B_MN = C::B_MN;
   constexpr bool A_MN = C::A_MN;
@@ -1265,6 +1180,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   __shared__ int mt_pre[1025];
   __shared__ int cu_s[1025];
   __shared__ int total_tiles_s, full_tiles_s;
+  __shared__ alignas(16) uint32_t relay_buf[8 * PAIR_STAGES];
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -1279,12 +1195,14 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
   auto accf_bar = [&](int a) { return smem_u32(&bars[2 * C::STAGES + a]); };
   auto acce_bar = [&](int a) { return smem_u32(&bars[2 * C::STAGES + 2 + a]); };
   const uint32_t drain_bar = smem_u32(&bars[2 * C::STAGES + 4]);
+  auto gath_bar = [&](int s) { return smem_u32(&bars[2 * C::STAGES + 5 + s]); };
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
+      if (GATHER) mbar_init(gath_bar(s), 32 * GATHER_WARPS);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(accf_bar(a), 1);
@@ -1424,11 +1342,15 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
           const uint32_t b_dst = a_dst + A_STAGE_BYTES;
           const int k0 = wk.k_base + kb * BK;
           if (leader) {
-            mbar_expect_tx(full_bar(stage), 2 * C::STAGE_BYTES);  // this CTA's bytes and the peer's
+            // this CTA's bytes and the peer's (gathered A: B and the two
+            // relays' 16 bytes)
+            mbar_expect_tx(full_bar(stage), GATHER ? 2 * C::B_HALF_BYTES + 32 : 2 * C::STAGE_BYTES);
             filled_parity[stage] = (int)phase;
           }
           const uint32_t fb = cluster_addr(full_bar(stage), 0);
-          if constexpr (A_MN) {
+          if constexpr (GATHER) {
+            // A rows: the gather warps
+          } else if constexpr (A_MN) {
             // [64 K rows x 64 M] boxes, the two M halves 8 KB apart (a
             // group's last block is cleared past the group before its MMAs)
             tma_load_3d_pair(a_dst, &tmA, fb, ti.row0, k0, 0);
@@ -1542,6 +1464,72 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
       }
     }
+  } else if (GATHER && warp == NUM_THREADS / 32 + GATHER_WARPS) {
+    // ------------------------------------- relay of the gathered A rows
+    // Per stage, once every gather lane's copies have landed: fence them
+    // against the async proxy, then 16 bytes from this CTA's relay slot to the
+    // leader's by a bulk copy completing on the leader's full barrier.
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = pair; ok && t < total_tiles; t += n_pairs) {
+        const int kb_end = pair_work(t).kb_end;
+        for (int kb = 0; kb < kb_end; ++kb) {
+          if (!wait_bounded(gath_bar(stage), phase, &abort_flag, p)) { ok = false; break; }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          const uint32_t slot = smem_u32(&relay_buf[8 * stage + 4 * rank]);
+          asm volatile(
+              "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], 16, [%2];" ::"r"(
+                  cluster_addr(slot, 0)),
+              "r"(slot), "r"(cluster_addr(full_bar(stage), 0))
+              : "memory");
+          if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+        }
+      }
+    }
+  } else if (GATHER && warp >= NUM_THREADS / 32) {
+    // ------------------------------------------------ gathered A rows
+    // Warp 6 + w copies rows RW*w .. RW*w + RW-1 of this CTA's 128 A rows
+    // (RW = 128 / GATHER_WARPS): instruction j takes 4 rows, 8 lanes per row,
+    // one 16-byte chunk each (whole 128-byte row segments), to the chunk's
+    // 128-byte-swizzled place.  Rows past the group's end are skipped.
+    constexpr int RW = BM / GATHER_WARPS;
+    const int gw = warp - NUM_THREADS / 32;
+    const int crow = lane >> 3, chunk = lane & 7;
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int t = pair; ok && t < total_tiles; t += n_pairs) {
+      const PairWork wk = pair_work(t);
+      const int r_own = wk.ti.row0 + RW * gw + (lane % RW);
+      int src = r_own < p.M ? __ldg(p.gather + r_own) : 0;
+      if (src < 0 || src >= p.gather_n) {
+        set_error(p.err, DEV_BOUNDS);
+        src = 0;
+      }
+      for (int kb = 0; kb < wk.kb_end; ++kb) {
+        if (lane == 0) ok = wait_bounded(empty_bar(stage), phase ^ 1u, &abort_flag, p);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        const uint32_t a_dst = smem_u32(stage_base + stage * C::STAGE_BYTES);
+        const int k0 = wk.k_base + kb * BK;
+#pragma unroll
+        for (int j = 0; j < RW / 4; ++j) {
+          const int rr = 4 * j + crow;  // row inside this warp's RW
+          const int r = RW * gw + rr;   // row inside the CTA's 128
+          const int srow = __shfl_sync(0xffffffffu, src, rr);
+          const bf16* g = p.gather_src + (long long)srow * p.K + k0 + chunk * 8;
+          if (r < wk.ti.rows)
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(a_dst + r * 128 + ((chunk ^ (r & 7)) << 4)),
+                         "l"(g)
+                         : "memory");
+        }
+        asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(gath_bar(stage)) : "memory");
+        if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
@@ -1644,15 +1632,13 @@ int launch(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, co
   long long grid = sm_count();
   if (tiles_upper < grid) grid = tiles_upper;
   if (grid < 1) return MOE_OK;
-  const int threads = (can_gather<EPI, A_MN, NA, NB, KSUB>() && p.gather) ? NUM_THREADS + 32 * GATHER_WARPS
-                                                                           : NUM_THREADS;
-  k<<<(unsigned)grid, threads, smem, s>>>(a, b, b2, p);
+  k<<<(unsigned)grid, NUM_THREADS, smem, s>>>(a, b, b2, p);
   return launch_status();
 }
 
 // Pairs resident at once for the pair kernel (cached per device and kernel):
 // clusters of two SMs with one CTA each.
-template <int EPI>
+template <int EPI, bool GATHER = false>
 int pair_slots() {
   static int cached[64] = {0};
   int dev = 0;
@@ -1663,7 +1649,7 @@ int pair_slots() {
   if (cached[dev] > 0) return cached[dev];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2);
-  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.blockDim = dim3(GATHER ? PAIR_GATHER_THREADS : NUM_THREADS);
   cfg.dynamicSmemBytes = PairCfg<EPI>::SMEM;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1673,7 +1659,7 @@ int pair_slots() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<EPI>, &cfg) != cudaSuccess || n < 1) {
+  if (cudaOccupancyMaxActiveClusters(&n, tc_gemm_pair_kernel<EPI, GATHER>, &cfg) != cudaSuccess || n < 1) {
     cudaGetLastError();
     n = sm_count() / 2;
   }
@@ -1681,18 +1667,18 @@ int pair_slots() {
   return n;
 }
 
-template <int EPI>
+template <int EPI, bool GATHER = false>
 int launch_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b2, const Params& p,
                 long long pair_tiles_upper, cudaStream_t s) {
   using C = PairCfg<EPI>;
   static_assert(C::SMEM + 8500 <= 227 * 1024, "smem (dynamic + static)");
-  auto k = tc_gemm_pair_kernel<EPI>;
+  auto k = tc_gemm_pair_kernel<EPI, GATHER>;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::SMEM) != cudaSuccess)
     return MOE_ERR_CUDA;
-  long long pairs = pair_slots<EPI>();
+  long long pairs = pair_slots<EPI, GATHER>();
   if (pair_tiles_upper < pairs) pairs = pair_tiles_upper;
   if (pairs < 1) return MOE_OK;
-  k<<<(unsigned)(2 * pairs), NUM_THREADS, C::SMEM, s>>>(a, b, b2, p);
+  k<<<(unsigned)(2 * pairs), GATHER ? PAIR_GATHER_THREADS : NUM_THREADS, C::SMEM, s>>>(a, b, b2, p);
   return launch_status();
 }
 
@@ -1973,34 +1959,33 @@ int launch_expert_ffn_tc(const void* xs, const int32_t* cu, int rows, const void
   if (!map_3d(&mG, wg, Hp, H, E, 64, BK)) return MOE_ERR_CUDA;
   if (!map_3d(&mU, wu, Hp, H, E, 64, BK)) return MOE_ERR_CUDA;
   if (!map_2d_as_3d(&mA2, act, Hp, rows, BK, BM)) return MOE_ERR_CUDA;
-  // down-projection B: 256-row boxes for one CTA, 128-row halves for a pair
-  if (!map_3d(&mD, wd, Hp, H, E, BK, gather ? 256 : PAIR_BN / 2)) return MOE_ERR_CUDA;
-  const long long mtiles = (rows + BM - 1) / BM + E;
+  // down-projection B: 128-row halves, one per CTA of a pair
+  if (!map_3d(&mD, wd, Hp, H, E, BK, PAIR_BN / 2)) return MOE_ERR_CUDA;
   Params p1 = params(cu, E, rows, Hp, H, act, Hp, nullptr);
   p1.aux = gu;  // nullable: g and u kept for the backward
   p1.ld_aux = 2LL * Hp;
   Params p2 = params(cu, E, rows, H, Hp, h, H, nullptr);
-  if (!gather) {
-    // CTA pairs: 256-row tiles, each CTA staging half of the B columns.  With
-    // the workspace, the gate/up kernel zeroes the counters with which the
-    // down projection's split tiles (if its last round has any) meet.
-    if (ws && ws_bytes >= expert_ffn_ws_bytes()) {
-      p2.split_ws = static_cast<float*>(ws);
-      p2.split_cnt = reinterpret_cast<int*>(static_cast<char*>(ws) + SPLIT_PART_BYTES);
-      p1.zero_cnt = p2.split_cnt;
-      p1.zero_n = SPLIT_COUNTERS;
-    }
-    const long long ptiles = (rows + 2 * BM - 1) / (2 * BM) + E;
-    int st = launch_pair<EPI_SWIGLU>(mA, mG, mU, p1, ptiles * ((Hp + 127) / 128), s);
-    if (st != MOE_OK) return st;
-    return launch_pair<EPI_BF16>(mA2, mD, mD, p2, ptiles * ((H + 255) / 256), s);
+  // CTA pairs: 256-row tiles, each CTA staging half of the B columns.  With
+  // the workspace, the gate/up kernel zeroes the counters with which the
+  // down projection's split tiles (if its last round has any) meet.
+  if (ws && ws_bytes >= expert_ffn_ws_bytes()) {
+    p2.split_ws = static_cast<float*>(ws);
+    p2.split_cnt = reinterpret_cast<int*>(static_cast<char*>(ws) + SPLIT_PART_BYTES);
+    p1.zero_cnt = p2.split_cnt;
+    p1.zero_n = SPLIT_COUNTERS;
   }
-  p1.gather = gather;
-  p1.gather_src = static_cast<const bf16*>(xs);
-  p1.gather_n = gather_n;
-  int st = launch<EPI_SWIGLU, false, true, 256, 4, 1, 1>(mA, mG, mU, p1, mtiles * ((Hp + 127) / 128), s);
+  const long long ptiles = (rows + 2 * BM - 1) / (2 * BM) + E;
+  int st;
+  if (gather) {
+    p1.gather = gather;
+    p1.gather_src = static_cast<const bf16*>(xs);
+    p1.gather_n = gather_n;
+    st = launch_pair<EPI_SWIGLU, true>(mA, mG, mU, p1, ptiles * ((Hp + 127) / 128), s);
+  } else {
+    st = launch_pair<EPI_SWIGLU>(mA, mG, mU, p1, ptiles * ((Hp + 127) / 128), s);
+  }
   if (st != MOE_OK) return st;
-  return launch<EPI_BF16, false, false, 256, 4, 1, 1>(mA2, mD, mD, p2, mtiles * ((H + 255) / 256), s);
+  return launch_pair<EPI_BF16>(mA2, mD, mD, p2, ptiles * ((H + 255) / 256), s);
 }
 
 // Backward of the grouped SwiGLU FFN (bf16, tcgen05), given dh [rows, H]:

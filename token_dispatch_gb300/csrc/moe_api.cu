@@ -186,15 +186,14 @@ int moe_expert_ffn_ex(const void* xs, const int32_t* cu_seqlens, int rows, const
 int moe_expert_ffn_gather(const void* x, const int32_t* src_tok, int T, const int32_t* cu_seqlens, int rows,
                           const void* w_gate, const void* w_up, const void* w_down, int E, int H, int Hp, int dtype,
                           void* act, void* gu, void* h, void* ws, size_t ws_bytes, void* stream) {
-  (void)ws; (void)ws_bytes;
   if (T < 0) return MOE_ERR_INVALID_ARG;
   int st = check_expert_ffn(x, cu_seqlens, rows, w_gate, w_up, w_down, E, H, Hp, dtype);
   if (st != MOE_OK) return st;
   if (rows > 0 && (!act || !h || !src_tok || T < 1)) return MOE_ERR_INVALID_ARG;
-  if (!all_aligned({act, gu, h, src_tok})) return MOE_ERR_MISALIGNED;
+  if (!all_aligned({act, gu, h, src_tok, ws})) return MOE_ERR_MISALIGNED;
   if (gu && dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   return launch_expert_ffn(x, cu_seqlens, rows, w_gate, w_up, w_down, E, H, Hp, dtype, act, gu, h,
-                           as_stream(stream), src_tok, T);
+                           as_stream(stream), src_tok, T, ws, ws_bytes);
 }
 
 int moe_expert_ffn(const void* xs, const int32_t* cu_seqlens, int rows, const void* w_gate,
