@@ -3,7 +3,9 @@
 against the oracle's expert_ffn / expert_ffn_bwd on the same bf16-rounded
 inputs.  Row counts per expert are ragged: empty experts, a single row, exact
 and inexact multiples of the 64-row K block of the weight-gradient GEMMs, H'
-that is not a multiple of the 256-wide N tile."""
+that is not a multiple of the 256-wide N tile, and experts whose last 256-row
+tile of a CTA pair holds at most 128 rows (the peer CTA's rows all past the
+expert's end, 64 or 128 exactly)."""
 import numpy as np
 import pytest
 import torch
@@ -22,6 +24,8 @@ CASES = [
     (3, 256, 128, [1, 64, 200]),
     (8, 128, 256, [0, 0, 0, 300, 0, 0, 0, 5]),
     (2, 192, 320, [129, 127]),
+    (6, 128, 320, [1, 63, 64, 65, 128, 356]),
+    (2, 256, 192, [384, 200]),
 ]
 
 

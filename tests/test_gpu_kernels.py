@@ -275,7 +275,10 @@ def test_expert_ffn_matches_oracle(shape):
 
 
 SPLIT_SHAPES = [S("bf16_T1000_H320_E4_K2_Hp320", 1000, 320, 4, 2, 320, "bf16"),
-                S("bf16_T3000_H256_E8_K2_Hp1408", 3000, 256, 8, 2, 1408, "bf16")]
+                S("bf16_T3000_H256_E8_K2_Hp1408", 3000, 256, 8, 2, 1408, "bf16"),
+                # ~300 rows per expert: the last pair tile of every expert holds
+                # rows of the leader CTA only
+                S("bf16_T1200_H256_E8_K2_Hp320", 1200, 256, 8, 2, 320, "bf16")]
 
 
 @pytest.mark.parametrize("shape", SPLIT_SHAPES, ids=ids(SPLIT_SHAPES))
