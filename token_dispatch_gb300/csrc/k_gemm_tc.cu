@@ -286,10 +286,10 @@ __device__ __forceinline__ TileInfo decode(int t, const int* mt_pre, const int* 
 // silu(g) * u goes out as bf16 (and g, u to p.aux when set).
 template <int OUT_BN>
 __device__ __forceinline__ void epi_swiglu(const Params& p, uint32_t tbase, const TileInfo& ti, bool row_ok,
-                                           long long grow) {
+                                           long long grow, int c_begin = 0, int c_end = OUT_BN / 32) {
   bf16* out = static_cast<bf16*>(p.out);
 #pragma unroll 1
-  for (int c = 0; c < OUT_BN / 32; ++c) {
+  for (int c = c_begin; c < c_end; ++c) {
     float gv[32], uv[32];
     tmem_ld32(tbase + c * 32, gv);
     tmem_ld32(tbase + OUT_BN + c * 32, uv);
@@ -332,7 +332,7 @@ __device__ __forceinline__ void epi_swiglu(const Params& p, uint32_t tbase, cons
 // writes dg and du (bf16) side by side.
 template <int OUT_BN>
 __device__ __forceinline__ void epi_swiglu_bwd(const Params& p, uint32_t tbase, const TileInfo& ti, bool row_ok,
-                                               long long grow) {
+                                               long long grow, int c_begin = 0, int c_end = OUT_BN / 32) {
   // da for 32 columns at a time; g and u of the same columns come from
   // p.aux ([g | u] per row); dg and du go to p.out ([dg | du] per row)
   //   dg = da * u * s(g) * (1 + g * (1 - s(g))),  du = da * g * s(g)
@@ -353,10 +353,10 @@ __device__ __forceinline__ void epi_swiglu_bwd(const Params& p, uint32_t tbase, 
       }
     }
   };
-  load(0, gq, uq);
+  load(c_begin, gq, uq);
 #pragma unroll 1
-  for (int c = 0; c < OUT_BN / 32; ++c) {
-    if (c + 1 < OUT_BN / 32) load(c + 1, gn, un);
+  for (int c = c_begin; c < c_end; ++c) {
+    if (c + 1 < c_end) load(c + 1, gn, un);
     float da[32];
     tmem_ld32(tbase + c * 32, da);
     const int col = ti.n0 + c * 32;
@@ -1158,8 +1158,22 @@ __device__ __forceinline__ TileInfo decode_pair(int t, const int* mt_pre, const 
 // the TMA loads (a plain remote arrival at cluster scope, measured, made the
 // MMA's waits about twice as long).
 constexpr int PAIR_GATHER_THREADS = NUM_THREADS + 32 * (GATHER_WARPS + 1);
+// Epilogue warps of the pair kernel: the SwiGLU backward keeps two warps per
+// TMEM lane quadrant, each taking half of the tile's columns.  Its epilogue
+// (g and u read, dg and du written, a row per lane) takes about twice as long
+// as a tile's MMAs at K = 2048; the second warp per quadrant took the
+// fine-grained layer's expert backward from 2.90 to 2.80 ms (measured), while
+// the forward SwiGLU epilogue with g and u stored ran slower with it.
+template <int EPI, bool GATHER>
+__host__ __device__ constexpr int pair_epi_warps() {
+  return EPI == EPI_SWIGLU_BWD && !GATHER ? 8 : 4;
+}
+template <int EPI, bool GATHER>
+__host__ __device__ constexpr int pair_threads() {
+  return GATHER ? PAIR_GATHER_THREADS : 64 + 32 * pair_epi_warps<EPI, GATHER>();
+}
 template <int EPI, bool GATHER = false>
-__global__ void __launch_bounds__(GATHER ? PAIR_GATHER_THREADS : NUM_THREADS, 1) __cluster_dims__(2, 1, 1)
+__global__ void __launch_bounds__(pair_threads<EPI, GATHER>(), 1) __cluster_dims__(2, 1, 1)
 tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                     const __grid_constant__ CUtensorMap tmB2, const Params p) {
   static_assert(EPI == EPI_SWIGLU || EPI == EPI_BF16 || EPI == EPI_SWIGLU_BWD || EPI == EPI_F32_BIAS ||
@@ -1206,7 +1220,7 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(accf_bar(a), 1);
-      mbar_init(acce_bar(a), 2 * 128);  // the epilogue threads of both CTAs
+      mbar_init(acce_bar(a), 2 * 32 * pair_epi_warps<EPI, GATHER>());  // the epilogue threads of both CTAs
     }
     mbar_init(drain_bar, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -1534,6 +1548,10 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quadrant this warp may access
     const int r_local = q * 32 + lane;
+    // with two warps per quadrant, each takes half of the 32-column chunks
+    constexpr int EPI_H = pair_epi_warps<EPI, GATHER>() / 4;
+    constexpr int NCH = C::OUT_BN / 32;
+    const int c_begin = ((warp - 2) >> 2) * (NCH / EPI_H), c_end = c_begin + NCH / EPI_H;
     int i = 0;
     int out_chunk = 0;  // grouped K: this warp's output chunks so far (staging tile rotation)
     for (int t = pair; t < total_tiles; t += n_pairs, ++i) {
@@ -1545,8 +1563,8 @@ tc_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
       const long long grow = (long long)ti.row0 + r_local;
       const bool row_ok = r_local < ti.rows && grow < p.M;
       const uint32_t tbase = tmem_base + acc * PAIR_BN + ((uint32_t)(q * 32) << 16);
-      if constexpr (EPI == EPI_SWIGLU) epi_swiglu<C::OUT_BN>(p, tbase, ti, row_ok, grow);
-      else if constexpr (EPI == EPI_SWIGLU_BWD) epi_swiglu_bwd<C::OUT_BN>(p, tbase, ti, row_ok, grow);
+      if constexpr (EPI == EPI_SWIGLU) epi_swiglu<C::OUT_BN>(p, tbase, ti, row_ok, grow, c_begin, c_end);
+      else if constexpr (EPI == EPI_SWIGLU_BWD) epi_swiglu_bwd<C::OUT_BN>(p, tbase, ti, row_ok, grow, c_begin, c_end);
       else if constexpr (EPI == EPI_F32_BIAS) epi_f32_bias<C::OUT_BN>(p, tbase, ti, epi_stage, q, lane);
       else if constexpr (GK) {
         // the fp32 output's tensor map comes in place of the second B map
@@ -1649,7 +1667,7 @@ int pair_slots() {
   if (cached[dev] > 0) return cached[dev];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2);
-  cfg.blockDim = dim3(GATHER ? PAIR_GATHER_THREADS : NUM_THREADS);
+  cfg.blockDim = dim3(pair_threads<EPI, GATHER>());
   cfg.dynamicSmemBytes = PairCfg<EPI>::SMEM;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1678,7 +1696,7 @@ int launch_pair(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& b
   long long pairs = pair_slots<EPI, GATHER>();
   if (pair_tiles_upper < pairs) pairs = pair_tiles_upper;
   if (pairs < 1) return MOE_OK;
-  k<<<(unsigned)(2 * pairs), GATHER ? PAIR_GATHER_THREADS : NUM_THREADS, C::SMEM, s>>>(a, b, b2, p);
+  k<<<(unsigned)(2 * pairs), pair_threads<EPI, GATHER>(), C::SMEM, s>>>(a, b, b2, p);
   return launch_status();
 }
 
