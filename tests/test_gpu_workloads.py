@@ -5,7 +5,9 @@ benchmark shapes on one GPU (T=8192, E=384, H=7168, K=8, H'=2048) and the
 MoD + MoE layer (4 x 2048 tokens, 50% capacity, E=16, K=2, H'=5632).
 
 Checked exactly: top-k indices (up to genuine near-ties), cu_seqlens, the
-permutation, the dispatched rows, the MoD selection.  Checked on every output
+permutation, the dispatched rows, the MoD selection, and the expert FFN with
+the dispatch gather fused into its operand load against the FFN on the
+dispatched rows (bit for bit).  Checked on every output
 element: router logits and gates, combine, gate/dispatch backward.  Checked on
 sampled rows (the oracle computes them one by one): the expert FFN (first, last
 and random rows of sampled experts) and the layer output y of sampled tokens."""
@@ -111,6 +113,20 @@ def test_full_workload_forward_and_backward(shape):
         act_r[sel], h_r[sel] = O.expert_swiglu(x.ref[src[rows[sel]]], *we)
     assert_close(act_g, act_r, 2e-2, "act (sampled rows)")
     assert_close(h_g, h_r, 2e-2, "h (sampled rows)")
+    # the dispatch gather fused into the gate/up operand load (index maps only,
+    # rows read from x by src_tok): bit for bit the FFN on the dispatched rows
+    cu3 = torch.empty_like(b2.cu)
+    dst3 = torch.empty_like(b2.dst_row)
+    src3 = torch.empty_like(b2.src_tok)
+    L.moe_dispatch(xd, torch.from_numpy(r_idx).to(DEV), T, H, E, K, L.MOE_BF16, cu3, dst3, src3, None,
+                   b2.ws_dispatch, b2.ws_dispatch_bytes)
+    act3 = torch.empty_like(b2.act)
+    h3 = torch.empty_like(b2.h)
+    L.moe_expert_ffn_gather(xd, src3, T, cu3, R, wg, wu, wd, E, H, Hp, L.MOE_BF16, act3, None, h3)
+    torch.cuda.synchronize()
+    assert L.moe_last_device_error() == L.MOE_OK
+    assert torch.equal(act3, b2.act) and torch.equal(h3, b2.h)
+    del act3, h3
 
     # ---- layer output y of sampled tokens: sum_k gate * expert(x)
     toks = rng.choice(np.nonzero(same)[0], size=24 if E <= 64 else 6, replace=False)
