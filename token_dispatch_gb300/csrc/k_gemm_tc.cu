@@ -26,15 +26,16 @@
 // (no host synchronisation).
 //
 // Design of the one-CTA kernel (one persistent CTA per SM, warp-specialised):
-//   warp 0      TMA producer: A tile 128x64 (K-major) and B tile (MN-major
-//               [64 K x BN] chunks for W[e] stored [H, H'] or W_r [H, E];
-//               K-major [BN x 64 K] for Wd[e] stored [H, H']) into a STAGES-deep
-//               shared-memory ring, 128-byte swizzled.
+//   warp 0      TMA producer: A tile 128x64 (K-major x, or x^T read MN-major)
+//               and B tile (MN-major [64 K x BN] chunks for W_r [H, E] or the
+//               logit gradient; K-major [BN x 64 K] for W_r read as [E, H])
+//               into a STAGES-deep shared-memory ring, 128-byte swizzled.
 //   warp 1      allocates TMEM and issues tcgen05.mma (M=128, N=BN, K=16) from one
 //               thread into one of two fp32 TMEM accumulators, committing each
 //               stage back to the producer and each finished tile to the epilogue.
 //   warps 2..5  epilogue: tcgen05.ld the accumulator (warp w reads TMEM lanes
-//               32*(w%4)..+31 = tile rows), apply SwiGLU / bias, convert, store;
+//               32*(w%4)..+31 = tile rows), apply the bias / softmax and top-K,
+//               convert, store;
 //               the next tile's mainloop runs meanwhile in the other accumulator.
 // Tiles are (expert, m-tile, n-tile) with m fastest inside an expert so the CTAs
 // running at the same time share weight columns in L2.  Rows past an expert's
@@ -634,7 +635,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     prefetch_tmap(&tmA);
     prefetch_tmap(&tmB);
-    if (EPI == EPI_SWIGLU || p.kcat) prefetch_tmap(&tmB2);
+    if (p.kcat) prefetch_tmap(&tmB2);
   }
   if (warp == 1) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_base_slot)),
@@ -742,14 +743,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const uint32_t dst = b_dst + ib * C::B_TILE_BYTES;
             const int z = (NB > 1 && KSUB == 1) ? ib : ti.g;
             const int kb0 = KSUB > 1 ? k0 + ib * BK : k0;
-            if constexpr (EPI == EPI_SWIGLU) {
-#pragma unroll
-              for (int c = 0; c < BN / 64; ++c) {
-                const CUtensorMap* m = (c < BN / 128) ? &tmB : &tmB2;
-                const int col = ti.n0 + (c % (BN / 128)) * 64;
-                tma_load_3d(dst + c * (64 * BK * 2), m, full_bar(stage), col, k0, z);
-              }
-            } else if (B_MN) {
+            if (B_MN) {
 #pragma unroll
               for (int c = 0; c < BN / 64; ++c)
                 tma_load_3d(dst + c * (64 * BK * 2), &tmB, full_bar(stage), ti.n0 + c * 64, kb0, z);
@@ -839,11 +833,7 @@ tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const long long grow = (long long)ti.row0 + r_local;
       const bool row_ok = r_local < ti.rows && grow >= 0 && grow < p.M;
       const uint32_t tbase = tmem_base + acc * BN + ((uint32_t)(q * 32) << 16);
-      if (EPI == EPI_SWIGLU) {
-        epi_swiglu<C::OUT_BN>(p, tbase, ti, row_ok, grow);
-      } else if (EPI == EPI_SWIGLU_BWD) {
-        epi_swiglu_bwd<C::OUT_BN>(p, tbase, ti, row_ok, grow);
-      } else if (EPI == EPI_BF16) {
+      if (EPI == EPI_BF16) {
         epi_bf16<C::OUT_BN>(p, tbase, ti, epi_stage, q, lane);
       } else if (EPI == EPI_ROUTER) {
         // one thread = one token: its BN logits (E valid) come out of TMEM, get
