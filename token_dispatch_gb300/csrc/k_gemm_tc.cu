@@ -298,11 +298,23 @@ __device__ __forceinline__ void epi_swiglu(const Params& p, uint32_t tbase, cons
     if (row_ok && col < p.N) {
       uint4 pk[4];
       __nv_bfloat162* h2 = reinterpret_cast<__nv_bfloat162*>(pk);
+      if (p.aux) {
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        float a0 = gv[2 * j] / (1.0f + __expf(-gv[2 * j])) * uv[2 * j];
-        float a1 = gv[2 * j + 1] / (1.0f + __expf(-gv[2 * j + 1])) * uv[2 * j + 1];
-        h2[j] = __floats2bfloat162_rn(a0, a1);
+        for (int j = 0; j < 16; ++j) {
+          float a0 = gv[2 * j] / (1.0f + __expf(-gv[2 * j])) * uv[2 * j];
+          float a1 = gv[2 * j + 1] / (1.0f + __expf(-gv[2 * j + 1])) * uv[2 * j + 1];
+          h2[j] = __floats2bfloat162_rn(a0, a1);
+        }
+      } else {
+        // without g and u to store: the approximate divide (2 ulp; silu of
+        // g < -87 comes out 0), measured 1.5-1.8% faster at the short-K shapes;
+        // with the stores it measured slower, so that path keeps the IEEE one
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          float a0 = __fdividef(gv[2 * j], 1.0f + __expf(-gv[2 * j])) * uv[2 * j];
+          float a1 = __fdividef(gv[2 * j + 1], 1.0f + __expf(-gv[2 * j + 1])) * uv[2 * j + 1];
+          h2[j] = __floats2bfloat162_rn(a0, a1);
+        }
       }
       uint4* dst = reinterpret_cast<uint4*>(out + grow * p.ldo + col);
 #pragma unroll
