@@ -207,7 +207,9 @@ MOE_API int moe_dispatch_noalloc(const void* x, const int32_t* topk_idx, int T, 
  *     h[r,:]   = act[r,:] . w_down[e]^T
  *   xs [rows,H]; w_gate, w_up, w_down each one contiguous [E,H,Hp] tensor (dtype);
  *   act [rows,Hp] and h [rows,H] dtype out.  Accumulation is fp32; bf16 outputs
- *   are rounded to nearest-even.  The row split is read on the device from
+ *   are rounded to nearest-even (silu in fp32 with exp and divide of a few ulp;
+ *   moe_expert_ffn_ex with gu divides exactly, so its act may differ from this
+ *   call's in the last bit).  The row split is read on the device from
  *   cu_seqlens (no host synchronisation); cu_seqlens[E] must equal `rows`.
  *   bf16 needs H % 64 == 0 and Hp % 64 == 0.
  *   Workspace (optional, bf16): with ws 16-byte aligned and ws_bytes >=
