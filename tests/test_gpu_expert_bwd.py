@@ -86,6 +86,36 @@ def test_expert_ffn_backward_matches_oracle(E, H, Hp, counts):
         assert_close(g, ref, TOL, name)
 
 
+def test_expert_ffn_backward_alignment_of_saved_activations():
+    """[g | u] and the workspace at 16-byte but not 32-byte aligned addresses
+    (the SwiGLU backward then moves them as 16-byte vectors instead of 32-byte
+    ones): the same bits as with 256-byte aligned buffers."""
+    E, H, Hp, counts = 4, 128, 192, [70, 0, 130, 33]
+    R, cu, xs, wg, wu, wd, dh = inputs(E, H, Hp, counts, seed=11)
+    cu_d = torch.from_numpy(cu).to(DEV)
+    nbytes = L.moe_workspace_bytes(L.MOE_OP_EXPERT_FFN_BWD, R, H, E, 1, Hp)
+    outs = []
+    for off in (0, 8):  # bf16 elements: 0 or 16 bytes past a 256-byte aligned base
+        act = torch.empty((R, Hp), dtype=torch.bfloat16, device=DEV)
+        gu_buf = torch.empty(R * 2 * Hp + 16, dtype=torch.bfloat16, device=DEV)
+        gu = gu_buf[off:off + R * 2 * Hp].view(R, 2 * Hp)
+        h = torch.empty((R, H), dtype=torch.bfloat16, device=DEV)
+        L.moe_expert_ffn_ex(dev(xs), cu_d, R, dev(wg), dev(wu), dev(wd), E, H, Hp, L.MOE_BF16, act, gu, h)
+        ws_buf = torch.empty(nbytes + 64, dtype=torch.uint8, device=DEV)
+        ws = ws_buf[2 * off:2 * off + nbytes]
+        dxs = torch.empty((R, H), dtype=torch.bfloat16, device=DEV)
+        dws = [torch.empty((E, H, Hp), dtype=torch.float32, device=DEV) for _ in range(3)]
+        L.moe_expert_ffn_bwd(dev(xs), cu_d, R, dev(wg), dev(wu), dev(wd), E, H, Hp, L.MOE_BF16, gu, act, dev(dh),
+                             dxs, dws[0], dws[1], dws[2], ws, nbytes)
+        torch.cuda.synchronize()
+        assert L.moe_last_device_error() == L.MOE_OK
+        outs.append((dxs, dws))
+    (dxs0, dws0), (dxs1, dws1) = outs
+    assert torch.equal(dxs0, dxs1)
+    for a_, b_ in zip(dws0, dws1):
+        assert torch.equal(a_, b_)
+
+
 def test_expert_ffn_backward_without_rows_zeroes_weight_gradients():
     E, H, Hp = 3, 128, 128
     z = torch.zeros(1, dtype=torch.bfloat16, device=DEV)

@@ -110,6 +110,9 @@ struct Params {
   const int32_t* gather = nullptr;
   const bf16* gather_src = nullptr;
   int gather_n = 0;
+  // EPI_SWIGLU_BWD: p.aux and p.out are 32-byte aligned (their row strides are
+  // multiples of 256 bytes), so g, u, dg and du move as 32-byte vectors
+  int vec32 = 0;
 };
 
 // Waits for copies and MMAs already in flight when a role stops always use
@@ -341,6 +344,18 @@ __device__ __forceinline__ void epi_swiglu(const Params& p, uint32_t tbase, cons
   }
 }
 
+// 32 bytes (two uint4) from or to a 32-byte aligned global address
+__device__ __forceinline__ void ld_v8(uint4& a, uint4& b, const void* p) {
+  asm volatile("ld.global.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+               : "l"(p));
+}
+__device__ __forceinline__ void st_v8(void* p, const uint4& a, const uint4& b) {
+  asm volatile("st.global.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z),
+               "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+
 // EPI_SWIGLU_BWD: the accumulator is da; with g, u read back from p.aux it
 // writes dg and du (bf16) side by side.
 template <int OUT_BN>
@@ -357,12 +372,20 @@ __device__ __forceinline__ void epi_swiglu_bwd(const Params& p, uint32_t tbase, 
   auto load = [&](int c, uint4 (&g)[4], uint4 (&u)[4]) {
     const int col = ti.n0 + c * 32;
     if (row_ok && col < p.N) {
-      const uint4* gs = reinterpret_cast<const uint4*>(ax + grow * p.ld_aux + col);
-      const uint4* us = reinterpret_cast<const uint4*>(ax + grow * p.ld_aux + p.N + col);
+      const bf16* gs = ax + grow * p.ld_aux + col;
+      const bf16* us = gs + p.N;
+      if (p.vec32) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        g[j] = gs[j];
-        u[j] = us[j];
+        for (int j = 0; j < 2; ++j) {
+          ld_v8(g[2 * j], g[2 * j + 1], gs + 16 * j);
+          ld_v8(u[2 * j], u[2 * j + 1], us + 16 * j);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          g[j] = reinterpret_cast<const uint4*>(gs)[j];
+          u[j] = reinterpret_cast<const uint4*>(us)[j];
+        }
       }
     }
   };
@@ -389,12 +412,20 @@ __device__ __forceinline__ void epi_swiglu_bwd(const Params& p, uint32_t tbase, 
                                        a1 * u.y * s1 * (1.0f + g.y * (1.0f - s1)));
         du2[j] = __floats2bfloat162_rn(a0 * g.x * s0, a1 * g.y * s1);
       }
-      uint4* dgd = reinterpret_cast<uint4*>(out + grow * p.ldo + col);
-      uint4* dud = reinterpret_cast<uint4*>(out + grow * p.ldo + p.N + col);
+      bf16* dgd = out + grow * p.ldo + col;
+      bf16* dud = dgd + p.N;
+      if (p.vec32) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        dgd[j] = dgp[j];
-        dud[j] = dup[j];
+        for (int j = 0; j < 2; ++j) {
+          st_v8(dgd + 16 * j, dgp[2 * j], dgp[2 * j + 1]);
+          st_v8(dud + 16 * j, dup[2 * j], dup[2 * j + 1]);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          reinterpret_cast<uint4*>(dgd)[j] = dgp[j];
+          reinterpret_cast<uint4*>(dud)[j] = dup[j];
+        }
       }
     }
 #pragma unroll
@@ -2027,6 +2058,8 @@ int launch_expert_ffn_bwd_tc(const void* xs, const int32_t* cu, int rows, const 
     Params p = params(cu, E, rows, Hp, H, dgu, 2LL * Hp, nullptr);
     p.aux = const_cast<void*>(gu);
     p.ld_aux = 2LL * Hp;
+    // rows of [g | u] and [dg | du] are 4 H' bytes apart (H' % 64 == 0)
+    p.vec32 = (reinterpret_cast<uintptr_t>(gu) | reinterpret_cast<uintptr_t>(dgu)) % 32 == 0;
     st = launch_pair<EPI_SWIGLU_BWD>(mA, mB, mB, p, ptiles * ((Hp + 255) / 256), s);
     if (st != MOE_OK) return st;
   }
