@@ -110,8 +110,9 @@ struct Params {
   const int32_t* gather = nullptr;
   const bf16* gather_src = nullptr;
   int gather_n = 0;
-  // EPI_SWIGLU_BWD: p.aux and p.out are 32-byte aligned (their row strides are
-  // multiples of 256 bytes), so g, u, dg and du move as 32-byte vectors
+  // EPI_SWIGLU / EPI_SWIGLU_BWD: p.out and p.aux (when set) are 32-byte
+  // aligned (their row strides are multiples of 128 bytes), so the epilogue
+  // moves 64-byte row pieces as two 32-byte vectors
   int vec32 = 0;
 };
 
@@ -286,6 +287,29 @@ __device__ __forceinline__ TileInfo decode(int t, const int* mt_pre, const int* 
 // The thread owns TMEM lane (row) q*32 + lane of the tile's accumulator at
 // tbase; grow is that row's index in the output, row_ok whether it exists.
 
+// 32 bytes (two uint4) from or to a 32-byte aligned global address
+__device__ __forceinline__ void ld_v8(uint4& a, uint4& b, const void* p) {
+  asm volatile("ld.global.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+               : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
+               : "l"(p));
+}
+__device__ __forceinline__ void st_v8(void* p, const uint4& a, const uint4& b) {
+  asm volatile("st.global.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z),
+               "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
+}
+
+// 64 bytes of one row: two 32-byte vector stores when p.vec32, else four 16-byte
+__device__ __forceinline__ void st_row64(const Params& p, bf16* dst, const uint4 (&v)[4]) {
+  if (p.vec32) {
+    st_v8(dst, v[0], v[1]);
+    st_v8(dst + 16, v[2], v[3]);
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) reinterpret_cast<uint4*>(dst)[j] = v[j];
+  }
+}
+
 // EPI_SWIGLU: columns [0, OUT_BN) hold g, [OUT_BN, 2 OUT_BN) hold u; act =
 // silu(g) * u goes out as bf16 (and g, u to p.aux when set).
 template <int OUT_BN>
@@ -319,9 +343,7 @@ __device__ __forceinline__ void epi_swiglu(const Params& p, uint32_t tbase, cons
           h2[j] = __floats2bfloat162_rn(a0, a1);
         }
       }
-      uint4* dst = reinterpret_cast<uint4*>(out + grow * p.ldo + col);
-#pragma unroll
-      for (int j = 0; j < 4; ++j) dst[j] = pk[j];
+      st_row64(p, out + grow * p.ldo + col, pk);
       if (p.aux) {  // keep g and u for the backward
         uint4 gp[4], up[4];
         __nv_bfloat162* g2 = reinterpret_cast<__nv_bfloat162*>(gp);
@@ -332,28 +354,11 @@ __device__ __forceinline__ void epi_swiglu(const Params& p, uint32_t tbase, cons
           u2[j] = __floats2bfloat162_rn(uv[2 * j], uv[2 * j + 1]);
         }
         bf16* ax = static_cast<bf16*>(p.aux) + grow * p.ld_aux;
-        uint4* gd = reinterpret_cast<uint4*>(ax + col);
-        uint4* ud = reinterpret_cast<uint4*>(ax + p.N + col);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          gd[j] = gp[j];
-          ud[j] = up[j];
-        }
+        st_row64(p, ax + col, gp);
+        st_row64(p, ax + p.N + col, up);
       }
     }
   }
-}
-
-// 32 bytes (two uint4) from or to a 32-byte aligned global address
-__device__ __forceinline__ void ld_v8(uint4& a, uint4& b, const void* p) {
-  asm volatile("ld.global.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
-               : "=r"(a.x), "=r"(a.y), "=r"(a.z), "=r"(a.w), "=r"(b.x), "=r"(b.y), "=r"(b.z), "=r"(b.w)
-               : "l"(p));
-}
-__device__ __forceinline__ void st_v8(void* p, const uint4& a, const uint4& b) {
-  asm volatile("st.global.v8.u32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(a.x), "r"(a.y), "r"(a.z),
-               "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
-               : "memory");
 }
 
 // EPI_SWIGLU_BWD: the accumulator is da; with g, u read back from p.aux it
@@ -2015,6 +2020,7 @@ int launch_expert_ffn_tc(const void* xs, const int32_t* cu, int rows, const void
   Params p1 = params(cu, E, rows, Hp, H, act, Hp, nullptr);
   p1.aux = gu;  // nullable: g and u kept for the backward
   p1.ld_aux = 2LL * Hp;
+  p1.vec32 = (reinterpret_cast<uintptr_t>(act) | reinterpret_cast<uintptr_t>(gu)) % 32 == 0;
   Params p2 = params(cu, E, rows, H, Hp, h, H, nullptr);
   // CTA pairs: 256-row tiles, each CTA staging half of the B columns.  With
   // the workspace, the gate/up kernel zeroes the counters with which the
