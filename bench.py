@@ -58,10 +58,10 @@ FFN_DRAM_BYTES = {
     # + dram__bytes_write.sum of the two CTA-pair kernels, one launch each, full
     # size, with the tail-split workspace; at the Mixtral shape the figure moves
     # by +-5% between captures with the L2 hit rate)
-    ("mixtral_bf16_T8192_H4096_E8_K2_Hp14336", False): 2669724160 + 464089856 + 3097517824 + 128461568,
-    ("finegrained_bf16_T16384_H2048_E64_K6_Hp1408", False): 1143140608 + 265617408 + 646779904 + 372601088,
-    ("epbench_bf16_T8192_H7168_E384_K8_Hp2048", False): 24718538752 + 269722112 + 11550785024 + 930037248,
-    ("mod_bf16_B4_L2048_C1024_H2048_E16_K2_Hp5632", False): 771882752 + 83438336 + 486555136 + 23230720,
+    ("mixtral_bf16_T8192_H4096_E8_K2_Hp14336", False): 3252134912 + 463967488 + 3088918016 + 128402432,
+    ("finegrained_bf16_T16384_H2048_E64_K6_Hp1408", False): 1157933568 + 266742016 + 646429952 + 372195840,
+    ("epbench_bf16_T8192_H7168_E384_K8_Hp2048", False): 25055941632 + 269882368 + 11618349824 + 934911232,
+    ("mod_bf16_B4_L2048_C1024_H2048_E16_K2_Hp5632", False): 772024064 + 84482304 + 486685952 + 23238400,
 }
 DEFAULT_WORKLOAD = "mixtral_bf16_T8192_H4096_E8_K2_Hp14336"
 
